@@ -1,0 +1,270 @@
+/*
+ * zero_gb300.h -- C ABI of the ZeRO sharded mixed-precision Adam step on one
+ * GB300 (sm_103a).
+ *
+ * What the library computes
+ * -------------------------
+ * ZeRO-DP partitions a data-parallel job's model states -- optimizer state
+ * (stage 1, P_os), gradients (stage 2, P_os+g) and parameters (stage 3,
+ * P_os+g+p) -- across the N_d data-parallel ranks, each rank keeping 1/N_d
+ * ("ZeRO：大模型训练的内存优化革命" 3.1.1-3.1.3; ZeRO visual reading, stage
+ * list).  In mixed precision each parameter carries a 16-bit copy, a 16-bit
+ * gradient and 12 bytes of fp32 optimizer state (master weight, momentum,
+ * variance) ("AI论文陪读·ZeRO" section 01; ZeRO visual reading, 16Ψ account).
+ * One optimizer step of a stage-2 rank is: reduce-scatter the gradients of
+ * each constant-size bucket to their owners, update the owned fp32 shard with
+ * Adam, cast it to 16 bits and all-gather the new parameters to every rank
+ * (ZeRO visual reading, communication accounting; SC-2020 ZeRO notes, "Deep
+ * Dive into ZeRO-R / C_B" for the fixed-size fusion buffers).
+ *
+ * Here the N_d ranks are simulated: each rank's buffers are separate regions
+ * of one GPU's memory, and each collective is the memory traffic of the fused
+ * kernels.  Per bucket, one kernel reads the N_d ranks' 16-bit gradients,
+ * sums them in rank order in fp32, rounds once to 16 bits, checks for inf/NaN
+ * (loss-scale overflow), unscales by 1/(S*N_d), applies Adam (Kingma & Ba,
+ * Algorithm 1: bias correction, eps outside the square root, no weight decay)
+ * to the owned fp32 state and writes the 16-bit cast to every rank (stages
+ * 0-2) or to the owner's shard (stage 3).  The partition does not change the
+ * step's result: every stage gives the same numbers as one unpartitioned step.
+ *
+ * Layout
+ * ------
+ *   Psi  = n_params; N = n_ranks; A = align_elems (default 2048).
+ *   P    = ceil(Psi / N) rounded up to a multiple of A; rank r owns flat
+ *          indices [r*P, (r+1)*P).  padded = N*P.
+ *   Buckets are consecutive windows of bucket_elems elements over [0, Psi),
+ *   in parameter order; the last one may be shorter.  Padding elements
+ *   [Psi, padded) are never read or written by a step (keep them zero).
+ *   16-bit buffers hold IEEE binary16 or bfloat16 bit patterns (dtype).
+ *   Per rank r (device memory, caller-owned):
+ *     grads[r]    16-bit gradient, grad16_elems = padded elements, flat index
+ *                 order (loss-scaled).  Stages 0 and 1 overwrite it with the
+ *                 reduced gradient (the all-reduce result).
+ *     params16[r] 16-bit parameters: the full vector (padded elements) in
+ *                 stages 0-2; only rank r's shard (P elements) in stage 3.
+ *   fp32 state w, m, v: state_elems floats each.  Stages 1-3: the N shards
+ *   concatenated, i.e. flat index order (padded elements).  Stage 0: N full
+ *   replicas, replica r at offset r*padded.  Two copies of each may be given:
+ *   [cur] holds the current state; [1-cur] is the shadow that a fused step
+ *   writes the new state into (the step is speculative until the global
+ *   overflow flag is known; a clean step then flips cur).
+ *   reduced: 16-bit reduced gradient, padded elements in flat order (each
+ *   owner's shard), needed by the two-pass path in stages 2 and 3.
+ *   workspace: workspace_bytes of device memory, 16-byte aligned; contents
+ *   are scratch owned by the library during a step.
+ *
+ * Paths
+ * -----
+ *   fused     (no clipping and shadow state given): one kernel per bucket,
+ *             state read from [cur] and written to [1-cur].  On overflow the
+ *             step is discarded and each written 16-bit parameter is restored
+ *             to the cast of the unchanged master weights.
+ *   two-pass  (clipping, or no shadow): pass 1 per bucket reduces and checks
+ *             the gradient, materialises it (grads[] in stages 0/1, reduced
+ *             in stages 2/3) and accumulates the exact sum of squares; a
+ *             one-thread kernel forms the global norm and clip coefficient;
+ *             pass 2 per bucket updates the state in place, or does nothing
+ *             when the flag is set.
+ *
+ * Conventions
+ * -----------
+ *   The caller owns all memory; the library allocates nothing, keeps no
+ *   state between calls and never throws.  Every function returns a
+ *   zero_status_t; on failure zero_last_error() gives a message
+ *   (thread-local).  Kernels run asynchronously on the caller's stream
+ *   (a cudaStream_t passed as void*; NULL = legacy default stream).  The
+ *   end of a step synchronises that stream once to read the overflow flag.
+ *   Device pointers must be 16-byte aligned (ZERO_EALIGN otherwise).
+ *   Pointer arrays (grads, params16, dst) are host arrays of device
+ *   pointers, read during the call only.
+ */
+#ifndef ZERO_GB300_H
+#define ZERO_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZERO_GB300_VERSION 1
+#define ZERO_MAX_RANKS 64
+#define ZERO_DEFAULT_ALIGN 2048
+
+typedef enum {
+    ZERO_OK = 0,
+    ZERO_EINVAL = 1,         /* bad argument, inconsistent plan or call order */
+    ZERO_EALIGN = 2,         /* a device pointer is not 16-byte aligned */
+    ZERO_ENOMEM = 3,         /* a caller-provided buffer is missing or too small */
+    ZERO_ECUDA = 4,          /* a CUDA runtime call failed (message has the CUDA error) */
+    ZERO_ETIMEOUT = 5,       /* reserved: no kernel here waits on another */
+    ZERO_EUNSUPPORTED = 6    /* n_ranks outside 1..64, or another unsupported size */
+} zero_status_t;
+
+typedef enum { ZERO_FP16 = 0, ZERO_BF16 = 1 } zero_dtype_t;
+
+/* Job description.  48 bytes. */
+typedef struct zero_config {
+    int64_t n_params;            /* Psi >= 0 */
+    int64_t bucket_elems;        /* B > 0, multiple of 8 (gradient bucket, C_B) */
+    int64_t align_elems;         /* A: shard alignment in elements; 0 -> 2048; multiple of 8 */
+    const int64_t* layer_sizes;  /* stage-3 gather units in parameter order (sum = Psi); NULL -> one */
+    int32_t n_layers;            /* entries in layer_sizes (0 when NULL) */
+    int32_t stage;               /* ZeRO-DP stage 0..3 */
+    int32_t n_ranks;             /* N_d, 1..64 */
+    int32_t dtype;               /* zero_dtype_t of parameters and gradients */
+} zero_config_t;
+
+/* Partition and sizes derived from a config by zero_plan.  128 bytes. */
+typedef struct zero_plan {
+    int64_t shard_elems;         /* P */
+    int64_t padded_elems;        /* N*P */
+    int64_t n_buckets;           /* ceil(Psi / B) */
+    int64_t n_layers;
+    int64_t max_layer_elems;     /* capacity of a stage-3 gather destination */
+    int64_t state_elems;         /* floats in each of w, m, v: N*P, or N*N*P in stage 0 */
+    int64_t param16_elems;       /* per rank: N*P in stages 0-2, P in stage 3 */
+    int64_t grad16_elems;        /* per rank: N*P */
+    int64_t reduced_elems;       /* N*P in stages 2-3 (two-pass path), else 0 */
+    int64_t workspace_bytes;
+    int64_t hbm_bytes_fused;     /* algorithmic HBM bytes of one fused step (below) */
+    int64_t hbm_bytes_two_pass;  /* algorithmic HBM bytes of one two-pass step */
+    int64_t comm_counted_bytes;  /* bytes crossing simulated rank boundaries per step, all ranks */
+    double comm_paper_bytes;     /* per rank per step: 2*Psi*2 (stages 0-2), 3*Psi*2 (stage 3) */
+    double mem_total_bytes;      /* per rank, paper formula (b = 2, K = 12), see zero_model_state_bytes */
+    double reserved;
+} zero_plan_t;
+
+/* Adam hyper-parameters (Kingma & Ba): 24 bytes. */
+typedef struct zero_adam {
+    float lr, beta1, beta2, eps;
+    float max_grad_norm;         /* > 0: clip the global L2 norm of the unscaled gradient; <= 0: off */
+    int32_t reserved;
+} zero_adam_t;
+
+/* Host-side step state, read and updated by a step.  32 bytes. */
+typedef struct zero_state {
+    int64_t t;                   /* Adam steps applied so far; a clean step applies t+1 */
+    float loss_scale;            /* S: gradients arrive multiplied by S */
+    float min_loss_scale;        /* dynamic scaling never halves below this */
+    int32_t dynamic;             /* 0 static scale; 1 halve on overflow, double after growth_interval clean steps */
+    int32_t growth_interval;     /* 0: never grow */
+    int32_t good_steps;          /* consecutive clean steps (dynamic scaling) */
+    int32_t reserved;
+} zero_state_t;
+
+/* Caller-owned device buffers (layout above).  88 bytes. */
+typedef struct zero_buffers {
+    void* const* grads;          /* [N] */
+    void* const* params16;       /* [N] */
+    float* w[2];
+    float* m[2];
+    float* v[2];
+    void* reduced;
+    void* workspace;
+    int32_t cur;                 /* 0 or 1; the fused path flips it after a clean step */
+    int32_t reserved;
+} zero_buffers_t;
+
+/* Outcome of one step.  64 bytes. */
+typedef struct zero_step_result {
+    int64_t t;                   /* step count after the step */
+    int64_t hbm_bytes;           /* algorithmic HBM bytes moved */
+    int64_t comm_counted_bytes;  /* bytes crossing simulated rank boundaries */
+    double grad_norm;            /* clipping on: ||g||_2 (+inf on overflow); off: -1 */
+    uint32_t overflow;           /* 1 if any reduced gradient element was inf or NaN */
+    int32_t skipped;             /* 1 if the update was discarded (overflow) */
+    float clip_coef;             /* min(1, max_grad_norm/(||g||+1e-6)); 1 when off or skipped */
+    float loss_scale_used;
+    float new_loss_scale;
+    int32_t kernel_launches;     /* kernels this step launched */
+    int32_t path;                /* 0 fused, 1 two-pass */
+    int32_t reserved;
+} zero_step_result_t;
+
+/* ---- planning (host only, no CUDA calls) ------------------------------ */
+
+/* Partition, bucket table sizes, buffer sizes and the paper's accounting for
+ * cfg.  Errors: ZERO_EINVAL (bad field), ZERO_EUNSUPPORTED (n_ranks). */
+zero_status_t zero_plan(const zero_config_t* cfg, zero_plan_t* out);
+
+/* Segments of bucket b: for each rank owning part of it, in rank order,
+ * seg[3k] = rank, seg[3k+1] = offset inside that rank's shard, seg[3k+2] =
+ * length.  seg must hold 3*n_ranks entries; *n_seg receives the count. */
+zero_status_t zero_plan_bucket(const zero_config_t* cfg, int64_t b, int64_t* seg, int32_t* n_seg);
+
+/* Flat start and length of stage-3 layer `layer`. */
+zero_status_t zero_plan_layer(const zero_config_t* cfg, int32_t layer, int64_t* start, int64_t* len);
+
+/* Per-rank model-state bytes of the paper's accounting (ZeRO visual reading,
+ * stage formulas; Table 1): out[0] parameters, out[1] gradients, out[2]
+ * optimizer state, out[3] total.  param_bytes b (2 mixed precision, 4 fp32),
+ * optim_K K (12 mixed-precision Adam; the page's calculator also uses 4 for
+ * fp32 SGD with momentum, 0 for SGD).  Stage 0: (2b+K)Psi; 1: 2b*Psi +
+ * K*Psi/N; 2: b*Psi + (b+K)*Psi/N; 3: (2b+K)*Psi/N. */
+zero_status_t zero_model_state_bytes(int64_t n_params, int32_t n_ranks, int32_t stage,
+                                     int32_t param_bytes, int32_t optim_K, double out[4]);
+
+/* Communication per step.  *paper_per_rank: the paper's volume, 2*Psi*b for
+ * stages 0-2 and 3*Psi*b for stage 3 ("AI论文陪读·ZeRO" section 04; ZeRO
+ * visual reading, communication accounting).  *counted_all_ranks: bytes that
+ * cross simulated rank boundaries, k*(N-1)*Psi*b with k = 2 (stages 0, 2),
+ * 3 (stage 1, counting its end-of-step parameter all-gather; stage 3, two
+ * parameter all-gathers and one reduce-scatter). */
+zero_status_t zero_comm_bytes(int64_t n_params, int32_t n_ranks, int32_t stage, int32_t param_bytes,
+                              double* paper_per_rank, int64_t* counted_all_ranks);
+
+/* ---- the step (device) --------------------------------------------------- */
+
+/* One complete optimizer step over all buckets: begin, every bucket, end.
+ * zero_step dispatches on cfg->stage; zero_step_stageK requires stage K. */
+zero_status_t zero_step(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                        const zero_adam_t* adam, zero_state_t* state, void* stream,
+                        zero_step_result_t* out);
+zero_status_t zero_step_stage0(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                               const zero_adam_t* adam, zero_state_t* state, void* stream,
+                               zero_step_result_t* out);
+zero_status_t zero_step_stage1(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                               const zero_adam_t* adam, zero_state_t* state, void* stream,
+                               zero_step_result_t* out);
+zero_status_t zero_step_stage2(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                               const zero_adam_t* adam, zero_state_t* state, void* stream,
+                               zero_step_result_t* out);
+zero_status_t zero_step_stage3(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                               const zero_adam_t* adam, zero_state_t* state, void* stream,
+                               zero_step_result_t* out);
+
+/* The same step, bucket by bucket, for gradients that arrive one bucket at a
+ * time (backward hooks filling a constant-size bucket).  Call begin, then
+ * zero_step_bucket exactly once for every bucket b in any order, then end,
+ * all on one stream with unchanged arguments.
+ * bucket_grads: NULL to read bufs->grads, or (stages 2 and 3 only) a host
+ * array of N device pointers, each to this bucket's gradient window (bucket
+ * length, element 0 = the bucket's first flat index); it may be reused for
+ * the next bucket once this bucket's kernel has run on the stream. */
+zero_status_t zero_step_begin(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                              const zero_adam_t* adam, const zero_state_t* state, void* stream);
+zero_status_t zero_step_bucket(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                               const zero_adam_t* adam, const zero_state_t* state, int64_t bucket,
+                               void* const* bucket_grads, void* stream);
+zero_status_t zero_step_end(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                            const zero_adam_t* adam, zero_state_t* state, void* stream,
+                            zero_step_result_t* out);
+
+/* Stage 3: copy layer `layer`'s 16-bit parameters from the owners' shards
+ * (param_shards[r], P elements each) into each of the n_dst destination
+ * buffers dst[d] (capacity max_layer_elems; element j = flat index
+ * layer_start + j).  The parameter all-gather that runs before a layer's
+ * forward and again before its backward (ZeRO visual reading, communication
+ * accounting; "ZeRO：大模型训练的内存优化革命" 3.1.3).  n_dst 1..64. */
+zero_status_t zero_gather_layer(const zero_config_t* cfg, const zero_plan_t* plan, int32_t layer,
+                                void* const* param_shards, void* const* dst, int32_t n_dst, void* stream);
+
+/* Thread-local message of the last failed call ("" if none). */
+const char* zero_last_error(void);
+int32_t zero_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,336 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs.
+
+Bar: 16-bit parameters, the overflow flag, the reduced gradient and the
+partition offsets bit-exact; fp32 master weights, momentum and variance within
+1e-6 relative -- in fact required bit-identical here, since both sides
+evaluate the same IEEE operations in the same order (and a single differing
+fp32 ulp would flip 16-bit roundings).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import zero_sharded_mixed_bucket_gb300 as zg
+from tests.gpu_harness import Job, as_u16, as_u32
+
+pytestmark = pytest.mark.gpu
+
+FP16, BF16 = oracle.FP16, oracle.BF16
+
+
+def test_first_config_stage2_exact():
+    """Stage 2, 2^20 parameters, N_d = 4, grads N(0,1e-3) x 1024 loss scale,
+    Adam lr 1e-4, betas (0.9, 0.999), eps 1e-8, t = 1, m = v = 0."""
+    job = Job(1 << 20, 4, 2, 1 << 24, loss_scale=1024.0)
+    res, ref = job.step(job.make_grads(1))
+    assert res.path == 0 and res.kernel_launches == 1
+    job.check(res, ref)
+
+
+@pytest.mark.parametrize("stage", [0, 1, 2, 3])
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("shadow", [True, False])
+def test_stages_ragged_multi_step(stage, dtype, shadow):
+    """Three buckets with a ragged tail, N_d = 3 (not a power of two), three
+    steps, both paths (fused with shadow state; two-pass in place)."""
+    n = 3 * 8192 + 37
+    job = Job(n, 3, stage, 8192, 64, dtype=dtype, shadow=shadow, loss_scale=8.0)
+    for t in range(1, 4):
+        res, ref = job.step(job.make_grads(t))
+        assert res.path == (0 if shadow else 1)
+        job.check(res, ref)
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("sigma", [1e-3, 0.3])
+def test_clipped_steps(dtype, sigma):
+    """Global-norm clipping at 1.0: the exact integer sum of squares must give
+    the oracle's fp64 norm bit for bit, hence the same clip coefficient."""
+    n = (1 << 18) + 5
+    job = Job(n, 8, 2, 1 << 16, dtype=dtype, max_norm=1.0, sigma=sigma)
+    clipped = []
+    for t in range(1, 4):
+        res, ref = job.step(job.make_grads(t))
+        job.check(res, ref)
+        clipped.append(ref["clip"] < 1.0)
+    assert all(clipped) == (sigma > 0.1)
+
+
+@pytest.mark.parametrize("stage", [0, 1, 2, 3])
+def test_clipped_all_stages(stage):
+    job = Job(20_000 + 3, 4, stage, 4096, 16, max_norm=0.05, sigma=1e-2, loss_scale=4.0)
+    for t in range(1, 3):
+        res, ref = job.step(job.make_grads(t))
+        job.check(res, ref)
+
+
+@pytest.mark.parametrize("shadow", [True, False])
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+def test_overflow_skips_and_halves(shadow, dtype):
+    """An inf in one rank's gradient: flag set, state bit-identical, 16-bit
+    parameters unchanged, loss scale halved, t unchanged; the next clean step
+    proceeds from the unchanged state."""
+    n = 5 * 4096 + 11
+    job = Job(n, 4, 2, 4096, dtype=dtype, shadow=shadow, loss_scale=1024.0, dynamic=True)
+    res, ref = job.step(job.make_grads(1))
+    job.check(res, ref)
+    w_before = as_u32(job.bufs.state()[0][:n]).copy()
+    p_before = as_u16(job.bufs.params16[2][:n]).copy()
+    inf = synth.inf_bits(dtype)
+    res, ref = job.step(job.make_grads(2, inject=[(3, n - 2, inf)]))
+    assert res.overflow == 1 and res.skipped == 1 and res.new_loss_scale == 512.0 and res.t == 1
+    job.check(res, ref)
+    assert np.array_equal(as_u32(job.bufs.state()[0][:n]), w_before)
+    assert np.array_equal(as_u16(job.bufs.params16[2][:n]), p_before)
+    res, ref = job.step(job.make_grads(3))
+    assert res.overflow == 0 and res.t == 2
+    job.check(res, ref)
+
+
+@pytest.mark.parametrize("stage", [0, 1, 3])
+def test_overflow_other_stages(stage):
+    n = 3 * 2048 + 5
+    job = Job(n, 2, stage, 2048, 8, loss_scale=64.0, dynamic=True)
+    res, ref = job.step(job.make_grads(1, inject=[(0, 17, 0x7E00)]))   # NaN
+    assert res.overflow == 1
+    job.check(res, ref)
+    res, ref = job.step(job.make_grads(2))
+    job.check(res, ref)
+
+
+def test_overflow_by_sum():
+    """Finite gradients whose rank sum overflows binary16."""
+    n = 1000
+    job = Job(n, 2, 2, 512, 8, loss_scale=1.0, dynamic=True)
+    g = job.make_grads(1)
+    g[0][5] = g[1][5] = 0x7BFF   # 65504 + 65504
+    res, ref = job.step(g)
+    assert res.overflow == 1 == ref["overflow"]
+    job.check(res, ref)
+
+
+def test_dynamic_scale_sequence():
+    """Overflow on steps 2 and 3, growth after 2 clean steps."""
+    n = 4096 + 8
+    job = Job(n, 2, 2, 1024, 8, loss_scale=256.0, dynamic=True, growth=2, min_scale=1.0)
+    scales = []
+    for t in range(1, 8):
+        inj = [(1, t * 13, 0x7C00)] if t in (2, 3) else []
+        res, ref = job.step(job.make_grads(t, inject=inj))
+        job.check(res, ref)
+        scales.append(res.new_loss_scale)
+    assert scales == [256.0, 128.0, 64.0, 64.0, 128.0, 128.0, 256.0]
+
+
+@pytest.mark.parametrize("n,N,B", [(1, 1, 8), (7, 1, 8), (8, 2, 8), (9, 3, 8), (1, 64, 8), (100, 64, 16),
+                                   (5000, 64, 1024)])
+@pytest.mark.parametrize("stage", [0, 2, 3])
+def test_edge_sizes(n, N, B, stage):
+    job = Job(n, N, stage, B, 8)
+    for t in (1, 2):
+        res, ref = job.step(job.make_grads(t))
+        job.check(res, ref)
+
+
+def test_empty_model():
+    job = Job(0, 4, 2, 64)
+    res, ref = job.step(job.make_grads(1))
+    assert res.kernel_launches == 0 and res.overflow == 0 and res.t == 1
+
+
+@pytest.mark.parametrize("stage", [2, 3])
+@pytest.mark.parametrize("shadow", [True, False])
+def test_per_bucket_protocol(stage, shadow):
+    """begin / bucket / end gives the same result as the one-call step."""
+    n = 4 * 4096 + 100
+    job = Job(n, 4, stage, 4096, 16, shadow=shadow)
+    for t in (1, 2):
+        res, ref = job.step(job.make_grads(t), per_bucket=True)
+        job.check(res, ref)
+
+
+@pytest.mark.parametrize("stage", [2, 3])
+def test_bucket_staging_buffers(stage):
+    """Gradients arriving one bucket at a time in a constant-size staging
+    buffer per rank (reused for every bucket)."""
+    n, N, B = 5 * 2048 + 77, 4, 2048
+    job = Job(n, N, stage, B, 8, max_norm=1.0 if stage == 3 else 0.0)
+    grads = job.make_grads(1)
+    staging = [torch.zeros(B, dtype=torch.int16, device="cuda") for _ in range(N)]
+    s = torch.cuda.current_stream()
+    zg.zero_step_begin(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
+    for b in range(job.plan.n_buckets):
+        lo, hi = b * B, min((b + 1) * B, n)
+        for r in range(N):
+            staging[r][:hi - lo].copy_(torch.from_numpy(grads[r][lo:hi].view(np.int16)))
+        zg.zero_step_bucket(job.cfg, job.plan, job.bufs, job.adam, job.state, b,
+                            [t.data_ptr() for t in staging], s)
+    res = zg.zero_step_end(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
+    torch.cuda.synchronize()
+    ref = oracle.step(grads, job.w, job.m, job.v, dtype=FP16, t=0, loss_scale=1.0, max_grad_norm=job.max_norm,
+                      **job.hp)
+    job.p16, job.h, job.o["t"] = ref["p16"], ref["h"], ref["t"]
+    job.check(res, ref)
+
+
+def test_partition_invariance():
+    """Stage, bucket size and alignment do not change the step's numbers."""
+    n = 50_000 + 3
+    outs = []
+    for stage, B, A in [(0, 4096, 0), (1, 8192, 64), (2, 1 << 20, 8), (3, 2048, 2048), (2, 8, 8)]:
+        job = Job(n, 4, stage, B, A)
+        job.step(job.make_grads(1))
+        res, ref = job.step(job.make_grads(2))
+        job.check(res, ref)
+        w = as_u32(job.bufs.state()[0][:n])
+        if stage == 3:
+            P = job.plan.shard_elems
+            p = np.concatenate([as_u16(job.bufs.params16[r][:P]) for r in range(4)])[:n]
+        else:
+            p = as_u16(job.bufs.params16[1][:n])
+        outs.append((w, p))
+    for w, p in outs[1:]:
+        assert np.array_equal(w, outs[0][0]) and np.array_equal(p, outs[0][1])
+
+
+def test_replicas_identical_stage0():
+    n = 10_000
+    job = Job(n, 5, 0, 2048, 8)
+    res, ref = job.step(job.make_grads(1))
+    job.check(res, ref)
+    w = job.bufs.state()[0]
+    pad = job.plan.padded_elems
+    for r in range(1, 5):
+        assert torch.equal(w[r * pad:r * pad + n], w[:n])
+        assert torch.equal(job.bufs.params16[r], job.bufs.params16[0])
+
+
+def test_max_ranks_and_rejects_65():
+    job = Job(3000, 64, 2, 1024, 8)
+    res, ref = job.step(job.make_grads(1))
+    job.check(res, ref)
+    with pytest.raises(zg.ZeroError) as e:
+        zg.zero_plan(zg.Config(3000, 65, 2, 1024))
+    assert e.value.status == zg.ZERO_EUNSUPPORTED
+
+
+def test_deterministic_repeat():
+    n = 70_000
+    outs = []
+    for _ in range(2):
+        job = Job(n, 8, 2, 16384, max_norm=1.0)
+        res, _ = job.step(job.make_grads(1))
+        outs.append((res.grad_norm, as_u32(job.bufs.state()[0][:n])))
+    assert outs[0][0] == outs[1][0] and np.array_equal(outs[0][1], outs[1][1])
+
+
+# --- stage-3 layer gather ------------------------------------------------------
+@pytest.mark.parametrize("A", [8, 2048])
+def test_gather_layers(A):
+    layers = [1001, 4096, 7, 20_000, 3333]
+    n = sum(layers)
+    N = 6
+    job = Job(n, N, 3, 2048, A, layers=layers)
+    plan = job.plan
+    assert plan.max_layer_elems == 20_000
+    n_dst = 3
+    dst = [torch.full((plan.max_layer_elems,), -1, dtype=torch.int16, device="cuda") for _ in range(n_dst)]
+    shards = [t.data_ptr() for t in job.bufs.params16]
+    for step in range(2):
+        if step:
+            res, ref = job.step(job.make_grads(1))
+            job.check(res, ref)
+        start = 0
+        for l, ln in enumerate(layers):
+            zg.zero_gather_layer(job.cfg, plan, l, shards, [d.data_ptr() for d in dst])
+            torch.cuda.synchronize()
+            for d in dst:
+                got = as_u16(d[:ln])
+                assert np.array_equal(got, job.p16[start:start + ln]), (step, l)
+            start += ln
+
+
+def test_gather_max_destinations():
+    layers = [5000, 5000]
+    job = Job(10_000, 4, 3, 1024, 8, layers=layers)
+    dst = [torch.zeros(5000, dtype=torch.int16, device="cuda") for _ in range(64)]
+    zg.zero_gather_layer(job.cfg, job.plan, 1, [t.data_ptr() for t in job.bufs.params16],
+                         [d.data_ptr() for d in dst])
+    torch.cuda.synchronize()
+    for d in dst:
+        assert np.array_equal(as_u16(d), job.p16[5000:])
+
+
+# --- input generator: device == host ---------------------------------------------
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("offset,n", [(0, 100_000), (1, 99_999), (12_345, 7)])
+def test_synth_device_matches_host(dtype, offset, n):
+    t = torch.zeros(n, dtype=torch.int16, device="cuda")
+    synth.dev_normal16(t.data_ptr(), n, dtype, 1e-3, seed=3, stream=1, step=5, rank=7, offset=offset)
+    f = torch.zeros(n, dtype=torch.float32, device="cuda")
+    synth.dev_normal32(f.data_ptr(), n, 0.02, seed=3, stream=2, step=0, rank=1, offset=offset)
+    torch.cuda.synchronize()
+    h = synth.host_normal16(n, dtype, 1e-3, seed=3, stream=1, step=5, rank=7, offset=offset)
+    assert np.array_equal(as_u16(t), h)
+    hf = synth.host_normal32(n, 0.02, seed=3, stream=2, step=0, rank=1, offset=offset)
+    assert np.array_equal(as_u32(f), as_u32(hf))
+
+
+# --- the benchmark's workload at full size, sampled -------------------------------
+def _transformer_params(vocab, d, layers):
+    return vocab * d + layers * (12 * d * d + 4 * d)
+
+
+@pytest.mark.parametrize("stage", [2, 0])
+def test_full_size_sampled(stage):
+    """The 12-layer d=768 parameter list (123,568,896 params), N_d = 8, bucket
+    2^24, inputs generated on the device; 2^16 sampled elements recomputed by
+    the oracle from the host generator, every rank checked at those indices."""
+    n = _transformer_params(50257, 768, 12)
+    assert n == 123_568_896
+    N, B = 8, 1 << 24
+    cfg = zg.Config(n, N, stage, B)
+    plan = zg.zero_plan(cfg)
+    bufs = zg.DeviceBuffers(cfg, plan, device="cuda")
+    s = torch.cuda.current_stream()
+    reps = N if stage == 0 else 1
+    for r in range(reps):
+        off = r * plan.padded_elems
+        synth.dev_normal32(bufs.w[0].data_ptr() + 4 * off, n, 0.02, seed=0, stream=synth.STREAM_WEIGHT,
+                           cuda_stream=s.cuda_stream)
+    w0_dev = bufs.w[0][:n]
+    # 16-bit copy = cast of the master weights, made on the host for a sample only;
+    # the device copy is produced by one clean step from zero learning rate
+    for r in range(N):
+        synth.dev_normal16(bufs.grads[r].data_ptr(), n, FP16, 1e-3, seed=0, stream=synth.STREAM_GRAD, step=1,
+                           rank=r, cuda_stream=s.cuda_stream)
+    adam = zg.zero_adam_t(**{**dict(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8), "max_grad_norm": 0.0})
+    state = zg.zero_state_t(t=0, loss_scale=1.0, min_loss_scale=1.0)
+    fn = zg.zero_step_stage2 if stage == 2 else zg.zero_step_stage0
+    res = fn(cfg, plan, bufs, adam, state, s)
+    torch.cuda.synchronize()
+    assert res.overflow == 0 and res.t == 1 and res.kernel_launches == plan.n_buckets
+
+    rng = np.random.default_rng(99)
+    idx = np.unique(np.concatenate([rng.integers(0, n, 1 << 16), [0, 1, n - 1, n - 2, B - 1, B, 7 * B - 1]]))
+    grads = [synth.host_normal16_at(idx, FP16, 1e-3, seed=0, stream=synth.STREAM_GRAD, step=1, rank=r)
+             for r in range(N)]
+    w = synth.host_normal32_at(idx, 0.02, seed=0, stream=synth.STREAM_WEIGHT)
+    m = np.zeros_like(w)
+    v = np.zeros_like(w)
+    ref = oracle.step(grads, w, m, v, dtype=FP16, lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, t=0, loss_scale=1.0)
+    assert ref["overflow"] == 0
+    ti = torch.from_numpy(idx).cuda()
+    gw, gm, gv = (t.index_select(0, ti) for t in bufs.state())
+    assert np.array_equal(as_u32(gw), as_u32(w)) and np.array_equal(as_u32(gm), as_u32(m))
+    assert np.array_equal(as_u32(gv), as_u32(v))
+    for r in range(N):
+        assert np.array_equal(as_u16(bufs.params16[r].index_select(0, ti)), ref["p16"])
+    if stage == 0:
+        pad = plan.padded_elems
+        for r in range(1, N):
+            assert torch.equal(bufs.state()[0][r * pad:r * pad + n], bufs.state()[0][:n])
+    del w0_dev

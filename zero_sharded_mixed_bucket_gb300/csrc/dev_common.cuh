@@ -1,0 +1,259 @@
+// Device helpers shared by the step kernels: 16-bit formats, vector memory
+// access with streaming cache hints, the Adam element update and the exact
+// sum-of-squares accumulator.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "zero_internal.h"
+
+namespace zg {
+
+enum { kF16 = ZERO_FP16, kBF16 = ZERO_BF16 };
+
+// ---- 16-bit formats --------------------------------------------------------
+template <int DT>
+__device__ __forceinline__ float to_f32(uint32_t bits)
+{
+    if constexpr (DT == kBF16)
+        return __uint_as_float(bits << 16);
+    else
+        return __half2float(__ushort_as_half((unsigned short)bits));
+}
+
+// Round to nearest even.
+template <int DT>
+__device__ __forceinline__ uint32_t from_f32(float x)
+{
+    if constexpr (DT == kBF16)
+        return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+    else
+        return __half_as_ushort(__float2half_rn(x));
+}
+
+template <int DT>
+__device__ __forceinline__ bool nonfinite16(uint32_t bits)
+{
+    if constexpr (DT == kBF16)
+        return (bits & 0x7f80u) == 0x7f80u;
+    else
+        return (bits & 0x7c00u) == 0x7c00u;
+}
+
+// ---- groups of 8 elements --------------------------------------------------
+// A group is 8 consecutive flat elements starting at a multiple of 8.  Full
+// groups use one 16-byte access per 16-bit array and two per fp32 array;
+// the ragged last group of a bucket uses scalar accesses for its `cnt` < 8
+// elements.
+
+struct H8 {
+    uint32_t w[4];   // 8 x 16-bit, little-endian pairs
+    __device__ __forceinline__ uint32_t get(int j) const { return (w[j >> 1] >> ((j & 1) * 16)) & 0xffffu; }
+    __device__ __forceinline__ void set(int j, uint32_t b)
+    {
+        const int s = (j & 1) * 16;
+        w[j >> 1] = (w[j >> 1] & ~(0xffffu << s)) | ((b & 0xffffu) << s);
+    }
+};
+
+__device__ __forceinline__ H8 ld_h8(const void* base, int64_t idx, int cnt)
+{
+    const uint16_t* p = static_cast<const uint16_t*>(base) + idx;
+    H8 r;
+    if (cnt == kVec) {
+        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(p));
+        r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
+    } else {
+        r.w[0] = r.w[1] = r.w[2] = r.w[3] = 0;
+#pragma unroll
+        for (int j = 0; j < kVec; j++)
+            if (j < cnt) r.set(j, p[j]);
+    }
+    return r;
+}
+
+__device__ __forceinline__ void st_h8(void* base, int64_t idx, const H8& h, int cnt)
+{
+    uint16_t* p = static_cast<uint16_t*>(base) + idx;
+    if (cnt == kVec) {
+        __stcs(reinterpret_cast<uint4*>(p), make_uint4(h.w[0], h.w[1], h.w[2], h.w[3]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < kVec; j++)
+            if (j < cnt) p[j] = (uint16_t)h.get(j);
+    }
+}
+
+__device__ __forceinline__ void ld_f8(const float* base, int64_t idx, int cnt, float x[kVec])
+{
+    const float* p = base + idx;
+    if (cnt == kVec) {
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+        const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < kVec; j++)
+            x[j] = j < cnt ? p[j] : 0.0f;
+    }
+}
+
+__device__ __forceinline__ void st_f8(float* base, int64_t idx, int cnt, const float x[kVec])
+{
+    float* p = base + idx;
+    if (cnt == kVec) {
+        __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
+        __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(x[4], x[5], x[6], x[7]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < kVec; j++)
+            if (j < cnt) p[j] = x[j];
+    }
+}
+
+// Rank-order fp32 sum of the N ranks' 16-bit gradients for one group:
+// s[j] = (((0 + g_0[j]) + g_1[j]) + ...) + g_{N-1}[j].  Loads are issued in
+// batches of 8 ranks so that up to 8 x 16 bytes are in flight per thread.
+template <int DT>
+__device__ __forceinline__ void reduce_group(const StepArgs& a, int64_t gidx, int cnt, float s[kVec])
+{
+#pragma unroll
+    for (int j = 0; j < kVec; j++)
+        s[j] = 0.0f;
+    for (int r0 = 0; r0 < a.n_ranks; r0 += 8) {
+        H8 q[8];
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            if (r0 + k < a.n_ranks)
+                q[k] = ld_h8(a.grads[r0 + k], gidx, cnt);
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            if (r0 + k < a.n_ranks) {
+#pragma unroll
+                for (int j = 0; j < kVec; j++)
+                    s[j] = __fadd_rn(s[j], to_f32<DT>(q[k].get(j)));
+            }
+        }
+    }
+}
+
+// Adam (Kingma & Ba, Algorithm 1) on one element, one IEEE rounding per
+// operation in this order:
+//   m' = b1*m + (1-b1)*g;  v' = b2*v + (1-b2)*(g*g)
+//   w' = w - lr * ((m'/bc1) / (sqrt(v'/bc2) + eps))
+__device__ __forceinline__ void adam1(float g, float& w, float& m, float& v, const AdamHP& hp)
+{
+    const float t1 = __fmul_rn(hp.b1, m);
+    const float t2 = __fmul_rn(hp.omb1, g);
+    const float m1 = __fadd_rn(t1, t2);
+    const float t3 = __fmul_rn(g, g);
+    const float t4 = __fmul_rn(hp.omb2, t3);
+    const float t5 = __fmul_rn(hp.b2, v);
+    const float v1 = __fadd_rn(t5, t4);
+    const float mh = __fdiv_rn(m1, hp.bc1);
+    const float vh = __fdiv_rn(v1, hp.bc2);
+    const float d = __fadd_rn(__fsqrt_rn(vh), hp.eps);
+    const float u = __fdiv_rn(mh, d);
+    const float st = __fmul_rn(hp.lr, u);
+    w = __fsub_rn(w, st);
+    m = m1;
+    v = v1;
+}
+
+// ---- exact sum of squares --------------------------------------------------
+// A finite 16-bit value is h = M * 2^E with integer M (< 2^11 binary16,
+// < 2^8 bfloat16), so h^2 = M^2 * 2^(2E) exactly.  Terms with
+// 0 <= 2(E - win_lo) <= 64 are added, shifted, into a 128-bit fixed-point
+// accumulator with unit 2^(2 win_lo); the others (rare: a 33-binade window
+// covers every binary16 value and the usual bfloat16 gradient range) go to
+// per-exponent integer bins in the workspace.  Integer sums are exact and
+// independent of order.
+struct U128 {
+    unsigned long long lo, hi;
+};
+
+__device__ __forceinline__ void u128_add(U128& a, unsigned long long lo, unsigned long long hi)
+{
+    const unsigned long long l = a.lo + lo;
+    a.hi += hi + (l < lo ? 1ull : 0ull);
+    a.lo = l;
+}
+
+template <int DT>
+__device__ __forceinline__ void sumsq_add(uint32_t bits, int win_lo, U128& acc, unsigned long long* bins)
+{
+    uint32_t e, f, M;
+    int E;
+    if constexpr (DT == kBF16) {
+        e = (bits >> 7) & 0xffu;
+        f = bits & 0x7fu;
+        if (e == 0xffu) return;
+        M = e ? (f | 0x80u) : f;
+        E = (int)(e ? e : 1u) - 134;
+    } else {
+        e = (bits >> 10) & 0x1fu;
+        f = bits & 0x3ffu;
+        if (e == 0x1fu) return;
+        M = e ? (f | 0x400u) : f;
+        E = (int)(e ? e : 1u) - 25;
+    }
+    if (M == 0) return;
+    const unsigned long long m2 = (unsigned long long)M * M;
+    const int sh = 2 * (E - win_lo);
+    if (sh >= 0 && sh <= 64) {
+        const unsigned long long lo = sh < 64 ? (m2 << sh) : 0ull;
+        const unsigned long long hi = sh == 0 ? 0ull : (sh < 64 ? (m2 >> (64 - sh)) : m2);
+        u128_add(acc, lo, hi);
+    } else {
+        atomicAdd(bins + e, m2);
+    }
+}
+
+// Block-wide sum of the per-thread accumulators, added to the workspace as
+// four 32-bit limbs (each limb sum stays below 2^63 for < 2^31 blocks).
+__device__ __forceinline__ void sumsq_flush(U128 acc, unsigned long long* limbs)
+{
+    __shared__ unsigned long long sh_lo[kThreads / 32], sh_hi[kThreads / 32];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long lo = __shfl_down_sync(0xffffffffu, acc.lo, off);
+        const unsigned long long hi = __shfl_down_sync(0xffffffffu, acc.hi, off);
+        u128_add(acc, lo, hi);
+    }
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        sh_lo[warp] = acc.lo;
+        sh_hi[warp] = acc.hi;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        U128 t{0ull, 0ull};
+        for (int w = 0; w < kThreads / 32; w++)
+            u128_add(t, sh_lo[w], sh_hi[w]);
+        const unsigned long long l[4] = {t.lo & 0xffffffffull, t.lo >> 32, t.hi & 0xffffffffull, t.hi >> 32};
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+            if (l[k]) atomicAdd(limbs + k, l[k]);
+    }
+}
+
+__device__ __forceinline__ uint32_t* ws_flag(unsigned char* ws) { return reinterpret_cast<uint32_t*>(ws + ws::kFlag); }
+__device__ __forceinline__ unsigned long long* ws_acc(unsigned char* ws)
+{
+    return reinterpret_cast<unsigned long long*>(ws + ws::kAcc);
+}
+__device__ __forceinline__ unsigned long long* ws_bins(unsigned char* ws)
+{
+    return reinterpret_cast<unsigned long long*>(ws + ws::kBins);
+}
+
+// Stage 3: owner rank of a flat index and the index inside its shard.
+__device__ __forceinline__ int owner_of(int64_t i, int64_t shard)
+{
+    return (int)(i / shard);
+}
+
+}  // namespace zg

@@ -1,0 +1,171 @@
+// Fused per-bucket step: reduce-scatter + overflow check + unscale + Adam +
+// 16-bit cast + all-gather, one HBM pass.  New fp32 state goes to the shadow
+// copy; the host commits it once the global overflow flag is known.
+//
+// Stage 0 (plain data parallelism): the reduced gradient is written back to
+// every rank (all-reduce) and each of the N replicas updates its own full
+// state and parameter copy.
+// Stage 1 (P_os): all-reduce write-back; the owner updates its state shard and
+// the new parameters go to every rank (step-end all-gather).
+// Stage 2 (P_os+g): reduce-scatter to the owner, owner update, all-gather.
+// Stage 3 (P_os+g+p): reduce-scatter, owner update, the new parameters stay in
+// the owner's shard.
+// ("ZeRO：大模型训练的内存优化革命" 3.1.1-3.1.3; ZeRO visual reading, stage list
+// and communication accounting.)
+#include "dev_common.cuh"
+
+namespace zg {
+
+namespace {
+
+template <int DT>
+__device__ __forceinline__ void update_group(const StepArgs& a, int64_t si, int cnt, const float g[kVec], H8& p)
+{
+    float w[kVec], m[kVec], v[kVec];
+    ld_f8(a.w_in, si, cnt, w);
+    ld_f8(a.m_in, si, cnt, m);
+    ld_f8(a.v_in, si, cnt, v);
+#pragma unroll
+    for (int j = 0; j < kVec; j++) {
+        adam1(g[j], w[j], m[j], v[j], a.hp);
+        p.set(j, from_f32<DT>(w[j]));
+    }
+    st_f8(a.w_out, si, cnt, w);
+    st_f8(a.m_out, si, cnt, m);
+    st_f8(a.v_out, si, cnt, v);
+}
+
+template <int STAGE, int DT>
+__global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ StepArgs a)
+{
+    const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
+    bool bad = false;
+    for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
+         gi += (int64_t)gridDim.x * kThreads) {
+        const int64_t i = a.lo + gi * kVec;
+        const int cnt = (int)min((int64_t)kVec, a.hi - i);
+        const int64_t gidx = i - a.grad_base;
+
+        float s[kVec];
+        reduce_group<DT>(a, gidx, cnt, s);
+
+        H8 h;
+        float g[kVec];
+#pragma unroll
+        for (int j = 0; j < kVec; j++) {
+            const uint32_t b = from_f32<DT>(s[j]);
+            h.set(j, b);
+            bad |= (j < cnt) && nonfinite16<DT>(b);
+            g[j] = __fmul_rn(to_f32<DT>(b), a.inv);
+        }
+
+        if constexpr (STAGE <= 1) {
+            for (int r = 0; r < a.n_ranks; r++)
+                st_h8(const_cast<void*>(a.grads[r]), gidx, h, cnt);
+        }
+
+        if constexpr (STAGE == 0) {
+            for (int r = 0; r < a.n_ranks; r++) {
+                H8 p;
+                update_group<DT>(a, (int64_t)r * a.replica_stride + i, cnt, g, p);
+                st_h8(a.params16[r], i, p, cnt);
+            }
+        } else {
+            H8 p;
+            update_group<DT>(a, i, cnt, g, p);
+            if constexpr (STAGE == 3) {
+                const int o = owner_of(i, a.shard);
+                st_h8(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
+            } else {
+                for (int r = 0; r < a.n_ranks; r++)
+                    st_h8(a.params16[r], i, p, cnt);
+            }
+        }
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0)
+        atomicOr(ws_flag(a.ws), 1u);
+}
+
+// After an overflowed fused step: put back the 16-bit parameters the step
+// overwrote, as the cast of the unchanged master weights (w_in).
+template <int STAGE, int DT>
+__global__ void __launch_bounds__(kThreads) k_restore(const __grid_constant__ StepArgs a)
+{
+    const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
+    for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
+         gi += (int64_t)gridDim.x * kThreads) {
+        const int64_t i = a.lo + gi * kVec;
+        const int cnt = (int)min((int64_t)kVec, a.hi - i);
+        const int reps = STAGE == 0 ? a.n_ranks : 1;
+        for (int r = 0; r < reps; r++) {
+            float w[kVec];
+            ld_f8(a.w_in, (int64_t)r * a.replica_stride + i, cnt, w);
+            H8 p;
+#pragma unroll
+            for (int j = 0; j < kVec; j++)
+                p.set(j, from_f32<DT>(w[j]));
+            if constexpr (STAGE == 0) {
+                st_h8(a.params16[r], i, p, cnt);
+            } else if constexpr (STAGE == 3) {
+                const int o = owner_of(i, a.shard);
+                st_h8(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
+            } else {
+                for (int q = 0; q < a.n_ranks; q++)
+                    st_h8(a.params16[q], i, p, cnt);
+            }
+        }
+    }
+}
+
+template <int STAGE, int DT>
+cudaError_t run_fused(const StepArgs& a, cudaStream_t s)
+{
+    const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
+    if (groups <= 0) return cudaSuccess;
+    const int grid = grid_for((const void*)k_fused<STAGE, DT>, groups);
+    k_fused<STAGE, DT><<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int STAGE, int DT>
+cudaError_t run_restore(const StepArgs& a, cudaStream_t s)
+{
+    const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
+    if (groups <= 0) return cudaSuccess;
+    const int grid = grid_for((const void*)k_restore<STAGE, DT>, groups);
+    k_restore<STAGE, DT><<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+#define ZG_DISPATCH_STAGE_DT(fn, stage, dtype, ...)                                   \
+    do {                                                                              \
+        if ((dtype) == kBF16) {                                                       \
+            switch (stage) {                                                          \
+            case 0: return fn<0, kBF16>(__VA_ARGS__);                                 \
+            case 1: return fn<1, kBF16>(__VA_ARGS__);                                 \
+            case 2: return fn<2, kBF16>(__VA_ARGS__);                                 \
+            default: return fn<3, kBF16>(__VA_ARGS__);                                \
+            }                                                                         \
+        } else {                                                                      \
+            switch (stage) {                                                          \
+            case 0: return fn<0, kF16>(__VA_ARGS__);                                  \
+            case 1: return fn<1, kF16>(__VA_ARGS__);                                  \
+            case 2: return fn<2, kF16>(__VA_ARGS__);                                  \
+            default: return fn<3, kF16>(__VA_ARGS__);                                 \
+            }                                                                         \
+        }                                                                             \
+    } while (0)
+
+cudaError_t launch_fused(int stage, int dtype, const StepArgs& a, cudaStream_t s)
+{
+    ZG_DISPATCH_STAGE_DT(run_fused, stage, dtype, a, s);
+}
+
+cudaError_t launch_restore(int stage, int dtype, const StepArgs& a, cudaStream_t s)
+{
+    ZG_DISPATCH_STAGE_DT(run_restore, stage, dtype, a, s);
+}
+
+}  // namespace zg

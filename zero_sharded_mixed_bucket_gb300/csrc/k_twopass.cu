@@ -1,0 +1,261 @@
+// Two-pass step, used with gradient-norm clipping (the update needs the global
+// norm first) or when no shadow state is given.
+//   pass 1, per bucket  k_reduce:   rank-order reduce, overflow flag, reduced
+//                                   gradient materialised (all ranks' grad
+//                                   buffers in stages 0/1 -- the all-reduce --,
+//                                   the owner's reduced shard in stages 2/3),
+//                                   exact integer sum of squares.
+//   once                k_finalize: exact sum -> fp64 -> ||g||, clip coefficient.
+//   pass 2, per bucket  k_update:   Adam in place (skipped if the flag is set),
+//                                   16-bit cast, all-gather.
+#include "dev_common.cuh"
+
+namespace zg {
+
+namespace {
+
+// HDEST 0: write h to every rank's gradient buffer; 1: to the reduced buffer.
+template <int HDEST, int DT, bool CLIP>
+__global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ StepArgs a)
+{
+    const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
+    bool bad = false;
+    U128 acc{0ull, 0ull};
+    unsigned long long* bins = ws_bins(a.ws);
+    for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
+         gi += (int64_t)gridDim.x * kThreads) {
+        const int64_t i = a.lo + gi * kVec;
+        const int cnt = (int)min((int64_t)kVec, a.hi - i);
+        const int64_t gidx = i - a.grad_base;
+        float s[kVec];
+        reduce_group<DT>(a, gidx, cnt, s);
+        H8 h;
+#pragma unroll
+        for (int j = 0; j < kVec; j++) {
+            const uint32_t b = from_f32<DT>(s[j]);
+            h.set(j, b);
+            const bool valid = j < cnt;
+            bad |= valid && nonfinite16<DT>(b);
+            if constexpr (CLIP) {
+                if (valid) sumsq_add<DT>(b, a.win_lo, acc, bins);
+            }
+        }
+        if constexpr (HDEST == 0) {
+            for (int r = 0; r < a.n_ranks; r++)
+                st_h8(const_cast<void*>(a.grads[r]), gidx, h, cnt);
+        } else {
+            st_h8(a.reduced, i, h, cnt);
+        }
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0)
+        atomicOr(ws_flag(a.ws), 1u);
+    if constexpr (CLIP)
+        sumsq_flush(acc, ws_acc(a.ws));
+}
+
+template <int DT>
+__device__ __forceinline__ void update_inplace(const StepArgs& a, int64_t si, int cnt, const H8& h, float c, H8& p)
+{
+    float w[kVec], m[kVec], v[kVec];
+    ld_f8(a.w_in, si, cnt, w);
+    ld_f8(a.m_in, si, cnt, m);
+    ld_f8(a.v_in, si, cnt, v);
+#pragma unroll
+    for (int j = 0; j < kVec; j++) {
+        float g = __fmul_rn(to_f32<DT>(h.get(j)), a.inv);
+        if (c != 1.0f) g = __fmul_rn(g, c);
+        adam1(g, w[j], m[j], v[j], a.hp);
+        p.set(j, from_f32<DT>(w[j]));
+    }
+    st_f8(a.w_out, si, cnt, w);
+    st_f8(a.m_out, si, cnt, m);
+    st_f8(a.v_out, si, cnt, v);
+}
+
+template <int STAGE, int DT, bool CLIP>
+__global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ StepArgs a)
+{
+    if (*reinterpret_cast<volatile uint32_t*>(ws_flag(a.ws)))
+        return;   // overflow: the whole step is skipped
+    // With clipping on, multiply by c only when c < 1: g * 1 == g for every
+    // finite g, so both forms give the same bits.
+    const float c = CLIP ? *reinterpret_cast<const float*>(a.ws + ws::kClip) : 1.0f;
+    const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
+    for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
+         gi += (int64_t)gridDim.x * kThreads) {
+        const int64_t i = a.lo + gi * kVec;
+        const int cnt = (int)min((int64_t)kVec, a.hi - i);
+        if constexpr (STAGE == 0) {
+            for (int r = 0; r < a.n_ranks; r++) {
+                const H8 h = ld_h8(a.grads[r], i - a.grad_base, cnt);
+                H8 p;
+                update_inplace<DT>(a, (int64_t)r * a.replica_stride + i, cnt, h, c, p);
+                st_h8(a.params16[r], i, p, cnt);
+            }
+        } else {
+            H8 h;
+            if constexpr (STAGE == 1)
+                h = ld_h8(a.grads[owner_of(i, a.shard)], i - a.grad_base, cnt);
+            else
+                h = ld_h8(a.reduced, i, cnt);
+            H8 p;
+            update_inplace<DT>(a, i, cnt, h, c, p);
+            if constexpr (STAGE == 3) {
+                const int o = owner_of(i, a.shard);
+                st_h8(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
+            } else {
+                for (int r = 0; r < a.n_ranks; r++)
+                    st_h8(a.params16[r], i, p, cnt);
+            }
+        }
+    }
+}
+
+// ---- finalize: exact integer -> nearest fp64 -------------------------------
+constexpr int kBigWords = 10;   // 640 bits: covers 2^(2*(-133)) .. 2^(2*127 + 64)
+
+__device__ void big_add(unsigned long long big[kBigWords], unsigned long long val, int shift)
+{
+    if (!val || shift < 0 || (shift >> 6) >= kBigWords) return;   // callers stay below bit 600
+    int w = shift >> 6;
+    const int b = shift & 63;
+    unsigned long long lo = val << b;
+    unsigned long long hi = b ? (val >> (64 - b)) : 0ull;
+    unsigned long long s = big[w] + lo;
+    unsigned long long carry = s < lo;
+    big[w] = s;
+    w++;
+    while (w < kBigWords && (hi || carry)) {
+        const unsigned long long add = hi + carry;   // hi < 2^63, no wrap
+        s = big[w] + add;
+        carry = s < add;
+        big[w] = s;
+        hi = 0;
+        w++;
+    }
+}
+
+// The big integer (unit 2^scale_exp) rounded to the nearest double, ties to even.
+__device__ double big_to_double(const unsigned long long big[kBigWords], int scale_exp)
+{
+    int top = kBigWords - 1;
+    while (top >= 0 && big[top] == 0) top--;
+    if (top < 0) return 0.0;
+    const int lz = __clzll(big[top]);
+    const int msb = top * 64 + 63 - lz;   // bit index of the leading one
+    // 64 bits starting at the leading one
+    unsigned long long head = big[top] << lz;
+    if (lz && top > 0) head |= big[top - 1] >> (64 - lz);
+    bool sticky = false;
+    // bits below the 64-bit head
+    const int below = msb - 63;   // index of the lowest bit in head
+    if (below > 0) {
+        const int bw = below >> 6, bb = below & 63;
+        if (bb && (big[bw] & ((1ull << bb) - 1ull))) sticky = true;
+        for (int k = 0; k < bw && !sticky; k++)
+            if (big[k]) sticky = true;
+    }
+    unsigned long long mant = head >> 11;            // 53 bits
+    const unsigned long long rbit = (head >> 10) & 1ull;
+    const bool rest = (head & 0x3ffull) != 0 || sticky;
+    int exp = msb - 52;
+    if (rbit && (rest || (mant & 1ull))) {
+        mant++;
+        if (mant == (1ull << 53)) {
+            mant >>= 1;
+            exp++;
+        }
+    }
+    return scalbn((double)mant, exp + scale_exp);
+}
+
+__global__ void k_finalize(const FinalArgs a)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(a.ws + ws::kFlag);
+    double* norm_out = reinterpret_cast<double*>(a.ws + ws::kNorm);
+    float* clip_out = reinterpret_cast<float*>(a.ws + ws::kClip);
+    if (flag) {
+        *norm_out = __longlong_as_double(0x7ff0000000000000ll);   // +inf
+        *clip_out = 1.0f;
+        return;
+    }
+    const int emin = a.dtype == kBF16 ? -133 : -24;   // E of the smallest subnormal
+    unsigned long long big[kBigWords];
+    for (int k = 0; k < kBigWords; k++) big[k] = 0ull;
+    const unsigned long long* limbs = reinterpret_cast<const unsigned long long*>(a.ws + ws::kAcc);
+    for (int k = 0; k < 4; k++)
+        big_add(big, limbs[k], 2 * (a.win_lo - emin) + 32 * k);
+    const unsigned long long* bins = reinterpret_cast<const unsigned long long*>(a.ws + ws::kBins);
+    for (int e = 0; e < 256; e++) {
+        if (!bins[e]) continue;
+        const int E = a.dtype == kBF16 ? (e ? e : 1) - 134 : (e ? e : 1) - 25;
+        big_add(big, bins[e], 2 * (E - emin));
+    }
+    const double sumsq = big_to_double(big, 2 * emin);
+    const double norm = __dmul_rn(__dsqrt_rn(sumsq), a.inv);
+    const double q = __ddiv_rn(a.max_norm, __dadd_rn(norm, 1e-6));
+    *norm_out = norm;
+    *clip_out = __double2float_rn(q < 1.0 ? q : 1.0);
+}
+
+template <int HDEST, int DT, bool CLIP>
+cudaError_t run_reduce(const StepArgs& a, cudaStream_t s)
+{
+    const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
+    if (groups <= 0) return cudaSuccess;
+    const int grid = grid_for((const void*)k_reduce<HDEST, DT, CLIP>, groups);
+    k_reduce<HDEST, DT, CLIP><<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int STAGE, int DT, bool CLIP>
+cudaError_t run_update(const StepArgs& a, cudaStream_t s)
+{
+    const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
+    if (groups <= 0) return cudaSuccess;
+    const int grid = grid_for((const void*)k_update<STAGE, DT, CLIP>, groups);
+    k_update<STAGE, DT, CLIP><<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int DT, bool CLIP>
+cudaError_t reduce_dt(int stage, const StepArgs& a, cudaStream_t s)
+{
+    return stage <= 1 ? run_reduce<0, DT, CLIP>(a, s) : run_reduce<1, DT, CLIP>(a, s);
+}
+
+template <int DT, bool CLIP>
+cudaError_t update_dt(int stage, const StepArgs& a, cudaStream_t s)
+{
+    switch (stage) {
+    case 0: return run_update<0, DT, CLIP>(a, s);
+    case 1: return run_update<1, DT, CLIP>(a, s);
+    case 2: return run_update<2, DT, CLIP>(a, s);
+    default: return run_update<3, DT, CLIP>(a, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_reduce(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s)
+{
+    if (dtype == kBF16)
+        return clip ? reduce_dt<kBF16, true>(stage, a, s) : reduce_dt<kBF16, false>(stage, a, s);
+    return clip ? reduce_dt<kF16, true>(stage, a, s) : reduce_dt<kF16, false>(stage, a, s);
+}
+
+cudaError_t launch_update(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s)
+{
+    if (dtype == kBF16)
+        return clip ? update_dt<kBF16, true>(stage, a, s) : update_dt<kBF16, false>(stage, a, s);
+    return clip ? update_dt<kF16, true>(stage, a, s) : update_dt<kF16, false>(stage, a, s);
+}
+
+cudaError_t launch_finalize(const FinalArgs& a, cudaStream_t s)
+{
+    k_finalize<<<1, 32, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace zg

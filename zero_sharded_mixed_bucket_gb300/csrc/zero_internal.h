@@ -1,0 +1,84 @@
+// Internal interface between the host driver (zero_host.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zero_gb300.h"
+
+namespace zg {
+
+constexpr int kMaxRanks = ZERO_MAX_RANKS;
+constexpr int kThreads = 256;   // threads per block of every streaming kernel
+constexpr int kVec = 8;         // consecutive elements per thread and iteration (16 bytes of 16-bit data)
+
+// Workspace layout (caller-provided device memory, zeroed by zero_step_begin).
+namespace ws {
+constexpr size_t kFlag = 0;     // uint32: 1 once any reduced gradient element is inf/NaN
+constexpr size_t kNorm = 8;     // double: ||g||_2 (two-pass with clipping)
+constexpr size_t kClip = 16;    // float: clip coefficient
+constexpr size_t kAcc = 32;     // 4 x uint64: 32-bit limbs of the fixed-point sum of squares
+constexpr size_t kBins = 64;    // 256 x uint64: sum of M^2 per exponent field, outside the window
+constexpr size_t kEnd = kBins + 256 * 8;
+constexpr int64_t kBytes = 4096;
+}  // namespace ws
+
+struct AdamHP {
+    float lr, b1, omb1, b2, omb2, eps, bc1, bc2;
+};
+
+// Arguments of the per-bucket kernels.  Passed by value as a __grid_constant__
+// parameter; pointer arrays are indexed with warp-uniform indices.
+struct StepArgs {
+    const void* grads[kMaxRanks];   // grads[r] + (i - grad_base) addresses flat element i of rank r
+    void* params16[kMaxRanks];      // rank r's 16-bit parameters (full vector, or shard in stage 3)
+    const float* w_in;
+    const float* m_in;
+    const float* v_in;
+    float* w_out;
+    float* m_out;
+    float* v_out;
+    void* reduced;                  // 16-bit reduced gradient, flat index order
+    unsigned char* ws;              // workspace
+    int64_t lo, hi;                 // flat element window [lo, hi)
+    int64_t grad_base;
+    int64_t shard;                  // P
+    int64_t replica_stride;         // stage 0: elements between consecutive replicas' state
+    int32_t n_ranks;
+    float inv;                      // 1/(S*N)
+    AdamHP hp;
+    int32_t win_lo;                 // lowest exponent E of the sum-of-squares window
+};
+
+struct FinalArgs {
+    unsigned char* ws;
+    int32_t dtype;
+    int32_t win_lo;
+    double inv;
+    double max_norm;
+};
+
+struct GatherArgs {
+    const void* shards[kMaxRanks];
+    void* dst[kMaxRanks];
+    int64_t start;                  // flat index of the layer's first element
+    int64_t len;
+    int64_t shard;                  // P
+    int32_t n_dst;
+};
+
+// Launchers: return the CUDA error of the launch.  `stage` 0..3, `dtype`
+// ZERO_FP16 / ZERO_BF16.
+cudaError_t launch_fused(int stage, int dtype, const StepArgs& a, cudaStream_t s);
+cudaError_t launch_reduce(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s);
+cudaError_t launch_finalize(const FinalArgs& a, cudaStream_t s);
+cudaError_t launch_update(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s);
+cudaError_t launch_restore(int stage, int dtype, const StepArgs& a, cudaStream_t s);
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
+
+// Grid for a grid-stride kernel over `groups` work items of kThreads-thread
+// blocks: at most (SM count x resident blocks per SM), so every block stays
+// resident and each SM gets the same share.
+int grid_for(const void* kernel, int64_t groups);
+
+}  // namespace zg
