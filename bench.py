@@ -1,0 +1,497 @@
+"""Benchmark: ZeRO sharded mixed-precision Adam step on GB300.
+
+Workload (default): the parameter list of a 12-layer d=768 transformer
+(embedding 50257 x 768, per layer 4 d^2 attention + 8 d^2 MLP + 4 d
+LayerNorm vectors: 123,568,896 parameters), N_d = 8 simulated data-parallel
+ranks, ZeRO stage 2, gradient bucket 2^24 elements, fp16 gradients
+N(0, 1e-3), loss scale 1, Adam (lr 1e-4, betas 0.9/0.999, eps 1e-8).  A
+step is one pass of the whole hot path: every bucket's fused
+reduce-scatter + overflow check + unscale + Adam + cast + all-gather kernel,
+then the flag read and commit.  Stages 0 and 1 on the same workload are
+timed after the headline and reported under "stages".
+
+Output: one JSON line (rank 0).  `value` is parameters updated per second
+over all GPUs with inputs resident in HBM; `e2e` is the same through the C
+ABI with gradients arriving from pinned host memory every step; `roofline`
+is the fused kernel's algorithmic bytes per launch over its CUDA-event
+duration against the measured HBM copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With --gpus N > 1 (under torchrun) each rank runs an independent replica of
+the job on its own GPU: the simulated ranks live inside one GPU, so there is
+no data-path collective between GPUs; timing is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Gparams/s per sharded Adam step; achieved HBM GB/s vs GB300 peak"
+UNIT = "Gparams/s"
+VOCAB, D_MODEL, N_LAYERS = 50257, 768, 12
+N_RANKS = 8
+BUCKET = 1 << 24
+STAGE = 2
+SIGMA = 1e-3
+ADAM = dict(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8)
+GRAD_RING = 10          # distinct per-step gradient sets ("10 steps, fresh seeds per step")
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["zero_sharded_mixed_bucket_gb300/csrc/k_fused.cu",
+                  "zero_sharded_mixed_bucket_gb300/csrc/dev_common.cuh",
+                  "zero_sharded_mixed_bucket_gb300/csrc/zero_internal.h"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_fused_stage2_fp16_n8.md")
+
+
+def bytes_per_param(stage, n=N_RANKS):
+    """Algorithmic HBM bytes per parameter of the fused step (16-bit values 2
+    bytes, fp32 state 4): N gradient reads, the all-reduce write-back in
+    stages 0/1, w/m/v read and written, the 16-bit parameter writes."""
+    return {0: 30 * n, 1: 24 + 6 * n, 2: 24 + 4 * n, 3: 26 + 2 * n}[stage]
+
+
+def layer_sizes(vocab=VOCAB, d=D_MODEL, layers=N_LAYERS):
+    return [vocab * d] + [12 * d * d + 4 * d] * layers
+
+
+N_PARAMS = sum(layer_sizes())
+WORKLOAD = ("12-layer d=768 transformer parameter list (%d params), N_d=%d simulated ranks, ZeRO stage %d, "
+            "bucket 2^24 elements, fp16 gradients N(0,1e-3), Adam" % (N_PARAMS, N_RANKS, STAGE))
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """dram bytes per launch of the fused kernel from the committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    try:
+        text = open(PROFILE_SUMMARY, encoding="utf-8").read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples (with their own timestamps) while the GPU works."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-i", str(gpu), "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        rows = []
+        if self.proc is None:
+            return rows
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append(dict(t=ts, sm=float(parts[2]), max=float(parts[3]),
+                                 power=float(parts[4]) if parts[4] not in ("[N/A]", "N/A") else None,
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9]))
+            except (ValueError, IndexError):
+                continue
+        os.unlink(self.path)
+        return rows
+
+
+def clocks_summary(rows, t0, t1):
+    inside = [r for r in rows if t0 - 0.05 <= r["t"] <= t1 + 0.05]
+    window = "timed"
+    if not inside:
+        # the timed region is shorter than the sampling interval: nearest samples
+        inside = sorted(rows, key=lambda r: abs(r["t"] - (t0 + t1) / 2))[:3]
+        window = "nearest samples to the timed region"
+    if not inside:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    reasons = set()
+    for r in inside:
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                          ("pcap", "sw_power_cap")):
+            if r[key].lower().startswith("active"):
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(r["sm"] for r in inside), "sm_max_mhz": max(r["max"] for r in inside),
+            "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs
+# ---------------------------------------------------------------------------
+def oracle_sample_step(n_sample, seed_step):
+    import numpy as np
+
+    import oracle
+    import synth
+    grads = [synth.host_normal16(n_sample, synth.FP16, SIGMA, seed=0, stream=synth.STREAM_GRAD, step=seed_step,
+                                 rank=r) for r in range(N_RANKS)]
+    w = synth.host_normal32(n_sample, 0.02, seed=0, stream=synth.STREAM_WEIGHT)
+    m = np.zeros(n_sample, np.float32)
+    v = np.zeros(n_sample, np.float32)
+    return grads, w, m, v
+
+
+def run_oracle_steps(n_sample, steps, warmup):
+    import oracle
+    grads, w, m, v = oracle_sample_step(n_sample, 1)
+    t = 0
+    times = []
+    for k in range(warmup + steps):
+        t0 = time.perf_counter()
+        r = oracle.step(grads, w, m, v, dtype=oracle.FP16, t=t, loss_scale=1.0, **ADAM)
+        dt = time.perf_counter() - t0
+        t = r["t"]
+        if k >= warmup:
+            times.append(dt)
+    return times
+
+
+def cpu_baseline(n_sample=1 << 24, steps=2):
+    times = run_oracle_steps(n_sample, steps, 0)
+    sec = sum(times) / len(times)
+    return {"value": n_sample / sec / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d contiguous parameters of the workload, N_d=%d ranks, %d steps, single-threaded C oracle "
+                      "(unpartitioned step; stage 2 computes the same numbers)" % (n_sample, N_RANKS, steps),
+            "seconds": sum(times)}
+
+
+def reference_arm(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    n_sample = 1 << 22
+    times = run_oracle_steps(n_sample, args.steps, args.warmup)
+    sec = sum(times) / len(times)
+    value = n_sample / sec / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "n_params": N_PARAMS, "n_ranks": N_RANKS, "stage": STAGE,
+                       "bucket_elems": BUCKET, "sample_params": n_sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "%d parameters of the workload per step, N_d=%d, single-threaded C oracle"
+                                       % (n_sample, N_RANKS)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU legs
+# ---------------------------------------------------------------------------
+class GpuJob:
+    def __init__(self, stage, device, ring=GRAD_RING, n_params=None):
+        import torch
+
+        import synth
+        import zero_sharded_mixed_bucket_gb300 as zg
+        self.zg, self.torch = zg, torch
+        self.stage = stage
+        self.n = n_params or N_PARAMS
+        self.cfg = zg.Config(self.n, N_RANKS, stage, BUCKET, 0, layer_sizes() if self.n == N_PARAMS else None)
+        self.plan = zg.zero_plan(self.cfg)
+        self.bufs = zg.DeviceBuffers(self.cfg, self.plan, device=device, grads=True)
+        self.stream = torch.cuda.current_stream(device)
+        s = self.stream.cuda_stream
+        reps = N_RANKS if stage == 0 else 1
+        for r in range(reps):
+            synth.dev_normal32(self.bufs.w[0].data_ptr() + 4 * r * self.plan.padded_elems, self.n, 0.02, seed=0,
+                               stream=synth.STREAM_WEIGHT, cuda_stream=s)
+        # gradient ring: GRAD_RING steps' worth of fresh gradients, each set N_d buffers
+        self.ring = []
+        self.ring_ptrs = []
+        import ctypes
+        for k in range(ring):
+            bufs = [torch.empty(self.plan.grad16_elems, dtype=torch.int16, device=device) for _ in range(N_RANKS)]
+            for r in range(N_RANKS):
+                synth.dev_normal16(bufs[r].data_ptr(), self.n, synth.FP16, SIGMA, seed=0, stream=synth.STREAM_GRAD,
+                                   step=k + 1, rank=r, cuda_stream=s)
+            self.ring.append(bufs)
+            self.ring_ptrs.append((ctypes.c_void_p * N_RANKS)(*[b.data_ptr() for b in bufs]))
+        self.adam = zg.zero_adam_t(max_grad_norm=0.0, **ADAM)
+        self.state = zg.zero_state_t(t=0, loss_scale=1.0, min_loss_scale=1.0)
+        torch.cuda.synchronize(device)
+
+    def set_ring(self, k):
+        import ctypes
+        self.bufs.b.grads = ctypes.cast(self.ring_ptrs[k % len(self.ring_ptrs)], ctypes.POINTER(ctypes.c_void_p))
+
+    def step(self, k, events=None):
+        """One step with gradient set k; events: list of (start, end) CUDA
+        events per bucket, recorded around each bucket kernel."""
+        zg = self.zg
+        self.set_ring(k)
+        zg.zero_step_begin(self.cfg, self.plan, self.bufs, self.adam, self.state, self.stream)
+        for b in range(self.plan.n_buckets):
+            if events is not None:
+                events[b][0].record(self.stream)
+            zg.zero_step_bucket(self.cfg, self.plan, self.bufs, self.adam, self.state, b, None, self.stream)
+            if events is not None:
+                events[b][1].record(self.stream)
+        return zg.zero_step_end(self.cfg, self.plan, self.bufs, self.adam, self.state, self.stream)
+
+    def bucket_len(self, b):
+        lo = b * BUCKET
+        return min(lo + BUCKET, self.n) - lo
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed_steps(job, steps, warmup, world, with_events=True):
+    import torch
+    for k in range(warmup):
+        job.step(k)
+    nb = job.plan.n_buckets
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nb)]
+          for _ in range(steps)] if with_events else None
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(job.stream)
+    for k in range(steps):
+        res = job.step(warmup + k, ev[k] if with_events else None)
+        launches += res.kernel_launches
+        assert res.overflow == 0
+    end.record(job.stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    ms = start.elapsed_time(end)
+    kernel = None
+    if with_events:
+        durs = [[ev[k][b][0].elapsed_time(ev[k][b][1]) for b in range(nb)] for k in range(steps)]
+        total_ms = sum(sum(d) for d in durs)
+        total_bytes = steps * sum(job.bucket_len(b) for b in range(nb)) * bytes_per_param(job.stage)
+        full = [d for k in range(steps) for b, d in enumerate(durs[k]) if job.bucket_len(b) == BUCKET]
+        kernel = dict(total_ms=total_ms, bytes=total_bytes, launches=steps * nb,
+                      full_launch_ms=statistics.mean(full) if full else None)
+    return ms, launches, kernel, (t0, t1)
+
+
+def e2e_leg(job, steps, warmup, device):
+    """Same step through the C ABI with each step's gradients copied in from
+    pinned host memory (bucket by bucket on a copy stream, overlapped with the
+    previous bucket's kernel) and the step result read back by the library."""
+    import torch
+    zg = job.zg
+    n = N_PARAMS
+    host = []
+    for k in range(2):
+        hb = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(N_RANKS)]
+        for r in range(N_RANKS):
+            hb[r].copy_(job.ring[k][r][:n])
+        host.append(hb)
+    dev = job.ring[0]
+    job.set_ring(0)
+    copy_stream = torch.cuda.Stream(device)
+    nb = job.plan.n_buckets
+
+    def one(k):
+        hb = host[k % 2]
+        done = []
+        for b in range(nb):
+            lo, hi = b * BUCKET, min((b + 1) * BUCKET, n)
+            with torch.cuda.stream(copy_stream):
+                for r in range(N_RANKS):
+                    dev[r][lo:hi].copy_(hb[r][lo:hi], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(copy_stream)
+            done.append(e)
+        zg.zero_step_begin(job.cfg, job.plan, job.bufs, job.adam, job.state, job.stream)
+        for b in range(nb):
+            job.stream.wait_event(done[b])
+            zg.zero_step_bucket(job.cfg, job.plan, job.bufs, job.adam, job.state, b, None, job.stream)
+        res = zg.zero_step_end(job.cfg, job.plan, job.bufs, job.adam, job.state, job.stream)
+        # the next step's copies must not overwrite gradients still being read
+        copy_stream.wait_stream(job.stream)
+        return res
+
+    for k in range(warmup):
+        one(k)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(job.stream)
+    for k in range(steps):
+        one(warmup + k)
+    end.record(job.stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    h2d = N_RANKS * n * 2
+    return dict(value=n / (ms * 1e-3) / 1e9, unit=UNIT, h2d_bytes_per_step=h2d, d2h_bytes_per_step=32,
+                ms_per_step=ms, note="gradients copied per bucket from pinned host memory on a second stream, "
+                                     "overlapped with the previous bucket's kernel; 32-byte result read per step")
+
+
+def gpu_arm(args):
+    import torch
+    world, rank, local = dist_setup(args)
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    if rank == 0 or world > 1:
+        __graft_entry__.build()
+    job = GpuJob(STAGE, device, ring=args.ring, n_params=args.n_params)
+    n_params = job.n
+    sampler = ClockSampler(local)
+    ms, launches, kernel, (t0, t1) = timed_steps(job, args.steps, args.warmup, world)
+    rows = sampler.stop()
+    ms_max = max_over_ranks(ms, world)
+    ms_per_step = ms_max / args.steps
+    value = world * n_params / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peak_hbm()
+    achieved = kernel["bytes"] / (kernel["total_ms"] * 1e-3) / 1e9
+    per_launch = kernel["bytes"] / kernel["launches"]
+    traffic_full = profiled_traffic()
+    step_bytes = job.plan.hbm_bytes_fused
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "io_dtype": "fp16", "data": "synthetic",
+        "config": {"workload": WORKLOAD if n_params == N_PARAMS else
+                   "flat parameter vector of %d params, N_d=%d simulated ranks, ZeRO stage %d, bucket 2^24 "
+                   "elements, fp16 gradients N(0,1e-3), Adam" % (n_params, N_RANKS, STAGE),
+                   "n_params": n_params, "n_ranks": N_RANKS, "stage": STAGE,
+                   "bucket_elems": BUCKET, "parallelism": "replicas only (simulated ranks inside each GPU)",
+                   "l2": "inputs larger than L2: %.2f GB moved per step, %d-step gradient ring of %.1f GB"
+                         % (step_bytes / 1e9, args.ring, args.ring * N_RANKS * n_params * 2 / 1e9)},
+        "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "k_fused<stage 2, fp16>", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic_full, "algorithmic_bytes_per_launch": per_launch,
+                     "bytes_per_param": bytes_per_param(STAGE), "launches": kernel["launches"],
+                     "full_launch_ms": kernel["full_launch_ms"]},
+        "gpu_launches": launches,
+    }
+    out["clocks"] = clocks_summary(rows, t0, t1)
+    if rank == 0 and args.headline_only:
+        print(json.dumps(out))
+    elif rank == 0:
+        # stages 0 and 1 on the same workload (reported, not the headline)
+        stages = {}
+        del job
+        torch.cuda.empty_cache()
+        for st in (1, 0):
+            j = GpuJob(st, device, ring=2)
+            sms, _, sk, _ = timed_steps(j, max(3, args.steps // 4), 2, 1)
+            stages["stage%d" % st] = {"ms_per_step": sms / max(3, args.steps // 4),
+                                      "value": N_PARAMS / (sms / max(3, args.steps // 4) * 1e-3) / 1e9,
+                                      "kernel_gbs": sk["bytes"] / (sk["total_ms"] * 1e-3) / 1e9,
+                                      "bytes_per_param": bytes_per_param(st)}
+            del j
+            torch.cuda.empty_cache()
+        out["stages"] = stages
+        j2 = GpuJob(STAGE, device, ring=2)
+        out["e2e"] = e2e_leg(j2, max(3, args.steps // 2), 2, device)
+        del j2
+        if world == 1:
+            out["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--n-params", type=int, default=None,
+                    help="flat parameter vector of this size instead of the transformer list (smaller cases, "
+                         "e.g. for profiling captures)")
+    ap.add_argument("--ring", type=int, default=GRAD_RING, help="distinct per-step gradient sets kept in HBM")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time the stage-2 step only (no stage 0/1, end-to-end or CPU legs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    if args.impl == "reference":
+        return reference_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
