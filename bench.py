@@ -447,23 +447,33 @@ def gpu_arm(args):
     if rank == 0 and args.headline_only:
         print(json.dumps(out))
     elif rank == 0:
-        # stages 0 and 1 on the same workload (reported, not the headline)
-        stages = {}
+        # stages 0 and 1 on the same workload (reported, not the headline).
+        # Stages 0/1 overwrite each rank's gradient with the all-reduce result,
+        # so every step gets a gradient set of its own.
         del job
         torch.cuda.empty_cache()
+        stages = {}
+        st_steps, st_warm = 5, 3
         for st in (1, 0):
-            j = GpuJob(st, device, ring=2)
-            sms, _, sk, _ = timed_steps(j, max(3, args.steps // 4), 2, 1)
-            stages["stage%d" % st] = {"ms_per_step": sms / max(3, args.steps // 4),
-                                      "value": N_PARAMS / (sms / max(3, args.steps // 4) * 1e-3) / 1e9,
-                                      "kernel_gbs": sk["bytes"] / (sk["total_ms"] * 1e-3) / 1e9,
-                                      "bytes_per_param": bytes_per_param(st)}
-            del j
+            try:
+                j = GpuJob(st, device, ring=st_steps + st_warm)
+                sms, _, sk, _ = timed_steps(j, st_steps, st_warm, 1)
+                stages["stage%d" % st] = {"ms_per_step": sms / st_steps,
+                                          "value": N_PARAMS / (sms / st_steps * 1e-3) / 1e9,
+                                          "kernel_gbs": sk["bytes"] / (sk["total_ms"] * 1e-3) / 1e9,
+                                          "bytes_per_param": bytes_per_param(st), "steps": st_steps}
+                del j
+            except Exception as e:   # reported, never hides the headline
+                stages["stage%d" % st] = {"error": repr(e)}
             torch.cuda.empty_cache()
         out["stages"] = stages
-        j2 = GpuJob(STAGE, device, ring=2)
-        out["e2e"] = e2e_leg(j2, max(3, args.steps // 2), 2, device)
-        del j2
+        try:
+            j2 = GpuJob(STAGE, device, ring=2)
+            out["e2e"] = e2e_leg(j2, max(3, args.steps // 2), 3, device)
+            del j2
+        except Exception as e:
+            out["e2e"] = {"error": repr(e)}
+        torch.cuda.empty_cache()
         if world == 1:
             out["cpu_baseline"] = cpu_baseline()
         print(json.dumps(out))
