@@ -260,6 +260,28 @@ zero_status_t zero_step_end(const zero_config_t* cfg, const zero_plan_t* plan, z
 zero_status_t zero_gather_layer(const zero_config_t* cfg, const zero_plan_t* plan, int32_t layer,
                                 void* const* param_shards, void* const* dst, int32_t n_dst, void* stream);
 
+/* Stage-2 step that allocates nothing and needs no scratch from the caller.
+ * The paper has no counterpart: this exists for callers that cannot obtain
+ * device memory for the workspace and the reduced-gradient buffer -- code
+ * running inside another runtime that owns the device's memory pool, or code
+ * that must not allocate after start-up.  The scratch lives in one static
+ * device array inside the library (4 KB + 16 MiB, held by every GPU that
+ * loads the library until the process exits), so the plan's padded_elems
+ * must be at most 8,388,608 (ZERO_EUNSUPPORTED otherwise, with a message).
+ * Same arguments and results as zero_step_stage2, except: bufs->workspace,
+ * bufs->reduced and the shadow copies bufs->w/m/v[1-cur] are ignored; the
+ * step always takes the two-pass path and updates the [cur] state in place
+ * (clipping allowed).  The caller still passes the gradients, parameters and
+ * fp32 state.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.  Each call clears the array's workspace
+ * part before use; the rest keeps the last call's contents.  All calls share
+ * the array: calls whose kernels overlap on the GPU (other streams or host
+ * threads) race on it. */
+zero_status_t zero_step_stage2_noalloc(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                                       const zero_adam_t* adam, zero_state_t* state, void* stream,
+                                       zero_step_result_t* out);
+
 /* Thread-local message of the last failed call ("" if none). */
 const char* zero_last_error(void);
 int32_t zero_version(void);

@@ -24,6 +24,7 @@ __all__ = [
     "zero_buffers_t", "zero_step_result_t", "Config", "lib", "lib_path",
     "zero_plan", "zero_plan_bucket", "zero_plan_layer", "zero_model_state_bytes", "zero_comm_bytes",
     "zero_step", "zero_step_stage0", "zero_step_stage1", "zero_step_stage2", "zero_step_stage3",
+    "zero_step_stage2_noalloc",
     "zero_step_begin", "zero_step_bucket", "zero_step_end", "zero_gather_layer", "zero_last_error",
     "zero_version", "DeviceBuffers",
 ]
@@ -106,6 +107,7 @@ def lib():
             "zero_step_stage1": [cfg, plan, bufs, adam, state, c_vp, res],
             "zero_step_stage2": [cfg, plan, bufs, adam, state, c_vp, res],
             "zero_step_stage3": [cfg, plan, bufs, adam, state, c_vp, res],
+            "zero_step_stage2_noalloc": [cfg, plan, bufs, adam, state, c_vp, res],
             "zero_step_begin": [cfg, plan, bufs, adam, state, c_vp],
             "zero_step_bucket": [cfg, plan, bufs, adam, state, c_i64, P(c_vp), c_vp],
             "zero_step_end": [cfg, plan, bufs, adam, state, c_vp, res],
@@ -223,6 +225,12 @@ def zero_step_stage2(cfg, plan, bufs, adam, state, stream=None) -> zero_step_res
 
 def zero_step_stage3(cfg, plan, bufs, adam, state, stream=None) -> zero_step_result_t:
     return _step(lib().zero_step_stage3, cfg, plan, bufs, adam, state, stream)
+
+
+def zero_step_stage2_noalloc(cfg, plan, bufs, adam, state, stream=None) -> zero_step_result_t:
+    """Stage-2 step whose scratch comes from a static array in the library
+    (for callers that cannot allocate device memory); see the header."""
+    return _step(lib().zero_step_stage2_noalloc, cfg, plan, bufs, adam, state, stream)
 
 
 def zero_step_begin(cfg, plan, bufs, adam, state, stream=None):

@@ -398,6 +398,13 @@ zero_status_t step_impl(int want_stage, const zero_config_t* c, const zero_plan_
 }
 
 }  // namespace
+
+zero_status_t set_error(zero_status_t st, const char* msg)
+{
+    g_err = msg;
+    return st;
+}
+
 }  // namespace zg
 
 using namespace zg;

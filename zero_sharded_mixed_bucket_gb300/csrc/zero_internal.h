@@ -76,6 +76,10 @@ cudaError_t launch_update(int stage, int dtype, bool clip, const StepArgs& a, cu
 cudaError_t launch_restore(int stage, int dtype, const StepArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
 
+// Record the thread-local message that zero_last_error() returns; gives back
+// `st`.  For entry points defined outside zero_host.cu.
+zero_status_t set_error(zero_status_t st, const char* msg);
+
 // Grid for a grid-stride kernel over `groups` work items of kThreads-thread
 // blocks: at most (SM count x resident blocks per SM), so every block stays
 // resident and each SM gets the same share.
