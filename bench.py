@@ -270,19 +270,13 @@ class GpuJob:
         import ctypes
         self.bufs.b.grads = ctypes.cast(self.ring_ptrs[k % len(self.ring_ptrs)], ctypes.POINTER(ctypes.c_void_p))
 
-    def step(self, k, events=None):
-        """One step with gradient set k; events: list of (start, end) CUDA
-        events per bucket, recorded around each bucket kernel."""
+    def step(self, k):
+        """One optimizer step with gradient set k: one call into the library,
+        which launches every bucket's kernel and reads the overflow flag."""
         zg = self.zg
         self.set_ring(k)
-        zg.zero_step_begin(self.cfg, self.plan, self.bufs, self.adam, self.state, self.stream)
-        for b in range(self.plan.n_buckets):
-            if events is not None:
-                events[b][0].record(self.stream)
-            zg.zero_step_bucket(self.cfg, self.plan, self.bufs, self.adam, self.state, b, None, self.stream)
-            if events is not None:
-                events[b][1].record(self.stream)
-        return zg.zero_step_end(self.cfg, self.plan, self.bufs, self.adam, self.state, self.stream)
+        fn = [zg.zero_step_stage0, zg.zero_step_stage1, zg.zero_step_stage2, zg.zero_step_stage3][self.stage]
+        return fn(self.cfg, self.plan, self.bufs, self.adam, self.state, self.stream)
 
     def bucket_len(self, b):
         lo = b * BUCKET
@@ -317,36 +311,44 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def timed_steps(job, steps, warmup, world, with_events=True):
+def timed_steps(job, steps, warmup, world):
+    """Time `steps` steps after `warmup` untimed ones.  Returns the elapsed
+    milliseconds (CUDA events on the job's stream around all timed steps),
+    the kernels launched, the kernel span per step (events the library records
+    before the first and after the last kernel of each step) and the host
+    wall-clock window of the timed region."""
     import torch
+    zg = job.zg
     for k in range(warmup):
         job.step(k)
-    nb = job.plan.n_buckets
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nb)]
-          for _ in range(steps)] if with_events else None
+    span_start, span_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    span_start.record(job.stream)
+    span_end.record(job.stream)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.time()
-    start.record(job.stream)
-    for k in range(steps):
-        res = job.step(warmup + k, ev[k] if with_events else None)
-        launches += res.kernel_launches
-        assert res.overflow == 0
-    end.record(job.stream)
-    torch.cuda.synchronize()
-    t1 = time.time()
-    barrier(world)
+    spans = []
+    zg.zero_set_profile_events(span_start, span_end)
+    try:
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        start.record(job.stream)
+        for k in range(steps):
+            res = job.step(warmup + k)      # returns after the step's flag read (stream synchronised)
+            spans.append(span_start.elapsed_time(span_end))
+            launches += res.kernel_launches
+            assert res.overflow == 0
+        end.record(job.stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier(world)
+    finally:
+        zg.zero_set_profile_events(None, None)
     ms = start.elapsed_time(end)
-    kernel = None
-    if with_events:
-        durs = [[ev[k][b][0].elapsed_time(ev[k][b][1]) for b in range(nb)] for k in range(steps)]
-        total_ms = sum(sum(d) for d in durs)
-        total_bytes = steps * sum(job.bucket_len(b) for b in range(nb)) * bytes_per_param(job.stage)
-        full = [d for k in range(steps) for b, d in enumerate(durs[k]) if job.bucket_len(b) == BUCKET]
-        kernel = dict(total_ms=total_ms, bytes=total_bytes, launches=steps * nb,
-                      full_launch_ms=statistics.mean(full) if full else None)
+    nb = job.plan.n_buckets
+    step_bytes = sum(job.bucket_len(b) for b in range(nb)) * bytes_per_param(job.stage)
+    kernel = dict(total_ms=sum(spans), bytes=steps * step_bytes, launches=steps * nb,
+                  span_ms_per_step=sum(spans) / steps, launches_per_step=nb)
     return ms, launches, kernel, (t0, t1)
 
 
@@ -405,6 +407,8 @@ def e2e_leg(job, steps, warmup, device):
 
 
 def gpu_arm(args):
+    global BUCKET
+    BUCKET = args.bucket
     import torch
     world, rank, local = dist_setup(args)
     device = torch.device("cuda", local)
@@ -423,6 +427,8 @@ def gpu_arm(args):
     achieved = kernel["bytes"] / (kernel["total_ms"] * 1e-3) / 1e9
     per_launch = kernel["bytes"] / kernel["launches"]
     traffic_full = profiled_traffic()
+    # the capture is of a full 2^24-element bucket: scale to the average launch
+    traffic = None if traffic_full is None else traffic_full * (n_params / kernel["launches_per_step"]) / (1 << 24)
     step_bytes = job.plan.hbm_bytes_fused
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -438,9 +444,13 @@ def gpu_arm(args):
         "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": "k_fused<stage 2, fp16>", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic_full, "algorithmic_bytes_per_launch": per_launch,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": per_launch,
                      "bytes_per_param": bytes_per_param(STAGE), "launches": kernel["launches"],
-                     "full_launch_ms": kernel["full_launch_ms"]},
+                     "avg_launch_ms": kernel["total_ms"] / kernel["launches"],
+                     "kernel_span_ms_per_step": kernel["span_ms_per_step"],
+                     "timing": "library-recorded CUDA events around each step's bucket kernels on the step's "
+                               "stream; consecutive bucket kernels overlap their edges, so a launch's duration "
+                               "is the step's kernel span over its launches"},
         "gpu_launches": launches,
     }
     out["clocks"] = clocks_summary(rows, t0, t1)
@@ -493,6 +503,7 @@ def main():
                     help="flat parameter vector of this size instead of the transformer list (smaller cases, "
                          "e.g. for profiling captures)")
     ap.add_argument("--ring", type=int, default=GRAD_RING, help="distinct per-step gradient sets kept in HBM")
+    ap.add_argument("--bucket", type=int, default=BUCKET, help="gradient bucket size in elements")
     ap.add_argument("--headline-only", action="store_true",
                     help="time the stage-2 step only (no stage 0/1, end-to-end or CPU legs)")
     args = ap.parse_args()

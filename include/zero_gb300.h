@@ -66,6 +66,12 @@
  *             pass 2 per bucket updates the state in place, or does nothing
  *             when the flag is set.
  *
+ *   Inside zero_step / zero_step_stageK (and the update pass of
+ *   zero_step_end) consecutive bucket kernels use programmatic dependent
+ *   launch: a bucket kernel may start while its predecessor drains; kernels
+ *   still complete in stream order.  Kernels launched by zero_step_bucket
+ *   follow plain stream order.
+ *
  * Conventions
  * -----------
  *   The caller owns all memory; the library allocates nothing, keeps no
@@ -281,6 +287,15 @@ zero_status_t zero_gather_layer(const zero_config_t* cfg, const zero_plan_t* pla
 zero_status_t zero_step_stage2_noalloc(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
                                        const zero_adam_t* adam, zero_state_t* state, void* stream,
                                        zero_step_result_t* out);
+
+/* Profiling: for the step calls made afterwards on this thread, record
+ * start_event (a cudaEvent_t) on the step's stream right after the workspace
+ * clear, before the first kernel, and end_event after the step's last kernel,
+ * before the overflow flag is read.  The caller creates the events and keeps
+ * them valid; (NULL, NULL) turns recording off.  Bucket kernels launched
+ * back to back inside one call overlap their edges, so the events give the
+ * step's kernel span, not per-kernel durations. */
+zero_status_t zero_set_profile_events(void* start_event, void* end_event);
 
 /* Thread-local message of the last failed call ("" if none). */
 const char* zero_last_error(void);

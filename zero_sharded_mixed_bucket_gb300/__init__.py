@@ -26,7 +26,7 @@ __all__ = [
     "zero_step", "zero_step_stage0", "zero_step_stage1", "zero_step_stage2", "zero_step_stage3",
     "zero_step_stage2_noalloc",
     "zero_step_begin", "zero_step_bucket", "zero_step_end", "zero_gather_layer", "zero_last_error",
-    "zero_version", "DeviceBuffers",
+    "zero_version", "zero_set_profile_events", "DeviceBuffers",
 ]
 
 ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ENOMEM, ZERO_ECUDA, ZERO_ETIMEOUT, ZERO_EUNSUPPORTED = range(7)
@@ -117,6 +117,8 @@ def lib():
             fn = getattr(L, name)
             fn.argtypes = args
             fn.restype = ctypes.c_int
+        L.zero_set_profile_events.argtypes = [c_vp, c_vp]
+        L.zero_set_profile_events.restype = ctypes.c_int
         L.zero_last_error.restype = ctypes.c_char_p
         L.zero_last_error.argtypes = []
         L.zero_version.restype = c_i32
@@ -128,6 +130,17 @@ def lib():
 def _check(status: int):
     if status != ZERO_OK:
         raise ZeroError(status, zero_last_error())
+
+
+def zero_set_profile_events(start_event=None, end_event=None):
+    """Record two CUDA events around the kernels of every later step call on
+    this thread (torch.cuda.Event objects or raw cudaEvent_t ints; None, None
+    to stop)."""
+    def raw(e):
+        if e is None:
+            return None
+        return int(e) if isinstance(e, int) else int(e.cuda_event)
+    _check(lib().zero_set_profile_events(raw(start_event), raw(end_event)))
 
 
 def zero_last_error() -> str:

@@ -42,6 +42,18 @@ __device__ __forceinline__ bool nonfinite16(uint32_t bits)
         return (bits & 0x7c00u) == 0x7c00u;
 }
 
+// ---- consecutive bucket kernels ---------------------------------------------
+// Inside one step the library launches the bucket kernels back to back with
+// programmatic dependent launch.  Each bucket kernel lets the next one be
+// scheduled once all of its own blocks have started (so the next kernel's
+// blocks fill the SMs this one's finished blocks free, hiding its ramp-up
+// behind this one's tail), and waits for its predecessor to complete at its
+// very end, so kernels still complete in stream order.  Bucket kernels of one
+// step touch disjoint elements; the flag and the sums they share are
+// atomics.  Without the launch attribute both instructions have no effect.
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_prev_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- groups of 8 elements --------------------------------------------------
 // A group is 8 consecutive flat elements starting at a multiple of 8.  Full
 // groups use one 16-byte access per 16-bit array and two per fp32 array;

@@ -38,6 +38,7 @@ __device__ __forceinline__ void update_group(const StepArgs& a, int64_t si, int 
 template <int STAGE, int DT>
 __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ StepArgs a)
 {
+    allow_next_grid();
     const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
     bool bad = false;
     for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ Step
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0)
         atomicOr(ws_flag(a.ws), 1u);
+    wait_prev_grid();
 }
 
 // After an overflowed fused step: put back the 16-bit parameters the step
@@ -118,13 +120,12 @@ __global__ void __launch_bounds__(kThreads) k_restore(const __grid_constant__ St
 }
 
 template <int STAGE, int DT>
-cudaError_t run_fused(const StepArgs& a, cudaStream_t s)
+cudaError_t run_fused(const StepArgs& a, cudaStream_t s, bool overlap)
 {
     const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
     if (groups <= 0) return cudaSuccess;
     const int grid = grid_for((const void*)k_fused<STAGE, DT>, groups);
-    k_fused<STAGE, DT><<<grid, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_step_kernel(k_fused<STAGE, DT>, grid, s, overlap, a);
 }
 
 template <int STAGE, int DT>
@@ -158,9 +159,9 @@ cudaError_t run_restore(const StepArgs& a, cudaStream_t s)
         }                                                                             \
     } while (0)
 
-cudaError_t launch_fused(int stage, int dtype, const StepArgs& a, cudaStream_t s)
+cudaError_t launch_fused(int stage, int dtype, const StepArgs& a, cudaStream_t s, bool overlap)
 {
-    ZG_DISPATCH_STAGE_DT(run_fused, stage, dtype, a, s);
+    ZG_DISPATCH_STAGE_DT(run_fused, stage, dtype, a, s, overlap);
 }
 
 cudaError_t launch_restore(int stage, int dtype, const StepArgs& a, cudaStream_t s)

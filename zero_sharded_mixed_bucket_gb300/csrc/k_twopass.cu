@@ -18,6 +18,7 @@ namespace {
 template <int HDEST, int DT, bool CLIP>
 __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ StepArgs a)
 {
+    allow_next_grid();
     const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
     bool bad = false;
     U128 acc{0ull, 0ull};
@@ -51,6 +52,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Ste
         atomicOr(ws_flag(a.ws), 1u);
     if constexpr (CLIP)
         sumsq_flush(acc, ws_acc(a.ws));
+    wait_prev_grid();
 }
 
 template <int DT>
@@ -75,8 +77,14 @@ __device__ __forceinline__ void update_inplace(const StepArgs& a, int64_t si, in
 template <int STAGE, int DT, bool CLIP>
 __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ StepArgs a)
 {
-    if (*reinterpret_cast<volatile uint32_t*>(ws_flag(a.ws)))
+    // The first update kernel of a step is launched in plain stream order after
+    // the pass-1 kernels and the finalize, so the flag and the clip
+    // coefficient are final before any update kernel starts.
+    allow_next_grid();
+    if (*reinterpret_cast<volatile uint32_t*>(ws_flag(a.ws))) {
+        wait_prev_grid();
         return;   // overflow: the whole step is skipped
+    }
     // With clipping on, multiply by c only when c < 1: g * 1 == g for every
     // finite g, so both forms give the same bits.
     const float c = CLIP ? *reinterpret_cast<const float*>(a.ws + ws::kClip) : 1.0f;
@@ -109,6 +117,7 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
             }
         }
     }
+    wait_prev_grid();
 }
 
 // ---- finalize: exact integer -> nearest fp64 -------------------------------
@@ -200,56 +209,54 @@ __global__ void k_finalize(const FinalArgs a)
 }
 
 template <int HDEST, int DT, bool CLIP>
-cudaError_t run_reduce(const StepArgs& a, cudaStream_t s)
+cudaError_t run_reduce(const StepArgs& a, cudaStream_t s, bool overlap)
 {
     const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
     if (groups <= 0) return cudaSuccess;
     const int grid = grid_for((const void*)k_reduce<HDEST, DT, CLIP>, groups);
-    k_reduce<HDEST, DT, CLIP><<<grid, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_step_kernel(k_reduce<HDEST, DT, CLIP>, grid, s, overlap, a);
 }
 
 template <int STAGE, int DT, bool CLIP>
-cudaError_t run_update(const StepArgs& a, cudaStream_t s)
+cudaError_t run_update(const StepArgs& a, cudaStream_t s, bool overlap)
 {
     const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
     if (groups <= 0) return cudaSuccess;
     const int grid = grid_for((const void*)k_update<STAGE, DT, CLIP>, groups);
-    k_update<STAGE, DT, CLIP><<<grid, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_step_kernel(k_update<STAGE, DT, CLIP>, grid, s, overlap, a);
 }
 
 template <int DT, bool CLIP>
-cudaError_t reduce_dt(int stage, const StepArgs& a, cudaStream_t s)
+cudaError_t reduce_dt(int stage, const StepArgs& a, cudaStream_t s, bool overlap)
 {
-    return stage <= 1 ? run_reduce<0, DT, CLIP>(a, s) : run_reduce<1, DT, CLIP>(a, s);
+    return stage <= 1 ? run_reduce<0, DT, CLIP>(a, s, overlap) : run_reduce<1, DT, CLIP>(a, s, overlap);
 }
 
 template <int DT, bool CLIP>
-cudaError_t update_dt(int stage, const StepArgs& a, cudaStream_t s)
+cudaError_t update_dt(int stage, const StepArgs& a, cudaStream_t s, bool overlap)
 {
     switch (stage) {
-    case 0: return run_update<0, DT, CLIP>(a, s);
-    case 1: return run_update<1, DT, CLIP>(a, s);
-    case 2: return run_update<2, DT, CLIP>(a, s);
-    default: return run_update<3, DT, CLIP>(a, s);
+    case 0: return run_update<0, DT, CLIP>(a, s, overlap);
+    case 1: return run_update<1, DT, CLIP>(a, s, overlap);
+    case 2: return run_update<2, DT, CLIP>(a, s, overlap);
+    default: return run_update<3, DT, CLIP>(a, s, overlap);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_reduce(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s)
+cudaError_t launch_reduce(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s, bool overlap)
 {
     if (dtype == kBF16)
-        return clip ? reduce_dt<kBF16, true>(stage, a, s) : reduce_dt<kBF16, false>(stage, a, s);
-    return clip ? reduce_dt<kF16, true>(stage, a, s) : reduce_dt<kF16, false>(stage, a, s);
+        return clip ? reduce_dt<kBF16, true>(stage, a, s, overlap) : reduce_dt<kBF16, false>(stage, a, s, overlap);
+    return clip ? reduce_dt<kF16, true>(stage, a, s, overlap) : reduce_dt<kF16, false>(stage, a, s, overlap);
 }
 
-cudaError_t launch_update(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s)
+cudaError_t launch_update(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s, bool overlap)
 {
     if (dtype == kBF16)
-        return clip ? update_dt<kBF16, true>(stage, a, s) : update_dt<kBF16, false>(stage, a, s);
-    return clip ? update_dt<kF16, true>(stage, a, s) : update_dt<kF16, false>(stage, a, s);
+        return clip ? update_dt<kBF16, true>(stage, a, s, overlap) : update_dt<kBF16, false>(stage, a, s, overlap);
+    return clip ? update_dt<kF16, true>(stage, a, s, overlap) : update_dt<kF16, false>(stage, a, s, overlap);
 }
 
 cudaError_t launch_finalize(const FinalArgs& a, cudaStream_t s)

@@ -12,6 +12,9 @@ namespace zg {
 namespace {
 
 thread_local std::string g_err;
+// Caller-created CUDA events recorded around each step's kernels (profiling).
+thread_local cudaEvent_t g_prof_start = nullptr;
+thread_local cudaEvent_t g_prof_end = nullptr;
 
 zero_status_t fail(zero_status_t st, const char* fmt, ...)
 {
@@ -275,12 +278,16 @@ zero_status_t begin_impl(const zero_buffers_t* b, cudaStream_t st)
 {
     cudaError_t e = cudaMemsetAsync(b->workspace, 0, ws::kEnd, st);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace");
+    if (g_prof_start) {
+        e = cudaEventRecord(g_prof_start, st);
+        if (e != cudaSuccess) return cuda_fail(e, "recording the profiling start event");
+    }
     return ZERO_OK;
 }
 
 zero_status_t bucket_impl(const zero_config_t* c, const zero_plan_t* p, const zero_buffers_t* b,
                           const zero_adam_t* adam, const zero_state_t* s, int64_t bucket, void* const* bucket_grads,
-                          cudaStream_t st)
+                          cudaStream_t st, bool overlap)
 {
     const Path path = choose_path(b, adam);
     const int64_t lo = bucket * c->bucket_elems;
@@ -289,8 +296,8 @@ zero_status_t bucket_impl(const zero_config_t* c, const zero_plan_t* p, const ze
                               : make_args(c, p, b, adam, s, path.fused, b->grads, 0);
     a.lo = lo;
     a.hi = hi;
-    cudaError_t e = path.fused ? launch_fused(c->stage, c->dtype, a, st)
-                               : launch_reduce(c->stage, c->dtype, path.clip, a, st);
+    cudaError_t e = path.fused ? launch_fused(c->stage, c->dtype, a, st, overlap)
+                               : launch_reduce(c->stage, c->dtype, path.clip, a, st, overlap);
     if (e != cudaSuccess) return cuda_fail(e, "launching the bucket kernel");
     return ZERO_OK;
 }
@@ -317,10 +324,14 @@ zero_status_t end_impl(const zero_config_t* c, const zero_plan_t* p, zero_buffer
             StepArgs a = make_args(c, p, b, adam, s, false, c->stage <= 1 ? b->grads : nullptr, 0);
             a.lo = bk * c->bucket_elems;
             a.hi = a.lo + c->bucket_elems < c->n_params ? a.lo + c->bucket_elems : c->n_params;
-            e = launch_update(c->stage, c->dtype, path.clip, a, st);
+            e = launch_update(c->stage, c->dtype, path.clip, a, st, bk > 0);
             if (e != cudaSuccess) return cuda_fail(e, "launching the update kernel");
             launches++;
         }
+    }
+    if (g_prof_end) {
+        e = cudaEventRecord(g_prof_end, st);
+        if (e != cudaSuccess) return cuda_fail(e, "recording the profiling end event");
     }
     unsigned char head[ws::kAcc];
     e = cudaMemcpyAsync(head, b->workspace, sizeof head, cudaMemcpyDeviceToHost, st);
@@ -390,8 +401,9 @@ zero_status_t step_impl(int want_stage, const zero_config_t* c, const zero_plan_
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     st = begin_impl(b, cs);
     if (st != ZERO_OK) return st;
+    // consecutive bucket kernels launched here overlap their edges
     for (int64_t bk = 0; bk < p->n_buckets; bk++) {
-        st = bucket_impl(c, p, b, adam, s, bk, nullptr, cs);
+        st = bucket_impl(c, p, b, adam, s, bk, nullptr, cs, bk > 0);
         if (st != ZERO_OK) return st;
     }
     return end_impl(c, p, b, adam, s, cs, out);
@@ -528,7 +540,9 @@ zero_status_t zero_step_bucket(const zero_config_t* c, const zero_plan_t* p, zer
         st = check_grads(c, b->grads, "grads");
     }
     if (st != ZERO_OK) return st;
-    return bucket_impl(c, p, b, adam, s, bucket, bucket_grads, static_cast<cudaStream_t>(stream));
+    // The caller may have run work (a staging refill) since the previous bucket
+    // kernel: plain stream order.
+    return bucket_impl(c, p, b, adam, s, bucket, bucket_grads, static_cast<cudaStream_t>(stream), false);
 }
 
 zero_status_t zero_step_end(const zero_config_t* c, const zero_plan_t* p, zero_buffers_t* b, const zero_adam_t* adam,
@@ -570,6 +584,15 @@ zero_status_t zero_gather_layer(const zero_config_t* c, const zero_plan_t* p, in
     a.n_dst = n_dst;
     cudaError_t e = launch_gather(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "launching the layer gather kernel");
+    return ZERO_OK;
+}
+
+zero_status_t zero_set_profile_events(void* start_event, void* end_event)
+{
+    if ((start_event == nullptr) != (end_event == nullptr))
+        return fail(ZERO_EINVAL, "give both profiling events or neither");
+    g_prof_start = static_cast<cudaEvent_t>(start_event);
+    g_prof_end = static_cast<cudaEvent_t>(end_event);
     return ZERO_OK;
 }
 

@@ -69,16 +69,37 @@ struct GatherArgs {
 
 // Launchers: return the CUDA error of the launch.  `stage` 0..3, `dtype`
 // ZERO_FP16 / ZERO_BF16.
-cudaError_t launch_fused(int stage, int dtype, const StepArgs& a, cudaStream_t s);
-cudaError_t launch_reduce(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s);
+// `overlap`: launch with programmatic dependent launch on the previous kernel
+// of the stream -- only when that kernel is another bucket kernel of the same
+// step pass, launched by the library itself.
+cudaError_t launch_fused(int stage, int dtype, const StepArgs& a, cudaStream_t s, bool overlap);
+cudaError_t launch_reduce(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s, bool overlap);
 cudaError_t launch_finalize(const FinalArgs& a, cudaStream_t s);
-cudaError_t launch_update(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s);
+cudaError_t launch_update(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s, bool overlap);
 cudaError_t launch_restore(int stage, int dtype, const StepArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
 
 // Record the thread-local message that zero_last_error() returns; gives back
 // `st`.  For entry points defined outside zero_host.cu.
 zero_status_t set_error(zero_status_t st, const char* msg);
+
+// Launch a bucket kernel taking StepArgs, optionally as a programmatic
+// dependent of the previous kernel in the stream.
+template <typename K>
+inline cudaError_t launch_step_kernel(K kernel, int grid, cudaStream_t s, bool overlap, const StepArgs& a)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
 
 // Grid for a grid-stride kernel over `groups` work items of kThreads-thread
 // blocks: at most (SM count x resident blocks per SM), so every block stays
