@@ -504,6 +504,10 @@ def main():
                          "e.g. for profiling captures)")
     ap.add_argument("--ring", type=int, default=GRAD_RING, help="distinct per-step gradient sets kept in HBM")
     ap.add_argument("--bucket", type=int, default=BUCKET, help="gradient bucket size in elements")
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],
+                    help="workload: 2 (default) the headline; 1, 3, 4, 5 the others (bench_workloads.py)")
+    ap.add_argument("--ranks", type=int, default=None, help="--config 5: N_d of a single sweep point")
+    ap.add_argument("--dtype", default=None, choices=["fp16", "bf16"], help="--config 5: dtype of a single point")
     ap.add_argument("--headline-only", action="store_true",
                     help="time the stage-2 step only (no stage 0/1, end-to-end or CPU legs)")
     args = ap.parse_args()
@@ -511,6 +515,15 @@ def main():
         ap.error("at least 3 warm-up steps")
     if args.impl == "reference":
         return reference_arm(args)
+    if args.config != 2:
+        import torch
+
+        import __graft_entry__
+        import bench_workloads
+        __graft_entry__.build()
+        torch.cuda.set_device(0)
+        print(json.dumps(bench_workloads.LEGS[args.config](args)))
+        return 0
     return gpu_arm(args)
 
 

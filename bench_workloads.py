@@ -1,0 +1,341 @@
+"""The other workloads of the ZeRO step, run by ``bench.py --config K``.
+
+  1  stage 2, flat 2^20 parameters, N_d = 4, grads N(0,1e-3) x 1024 loss
+     scale (static), one bucket; L2-resident, so L2 is flushed between steps.
+  3  stage 2, 48-layer d=1600 parameter list (1,555,278,400 params), N_d = 8,
+     constant 5e8-element bucket, fp16 grads N(0,1e-3) x S with one +inf per
+     1e9 gradient elements, dynamic loss scale (halve and skip), S0 = 1024.
+     Two runs: the literal injection (every step overflows) and a companion
+     run with injection on odd steps only.
+  4  stage 3, 32-layer d=4096 parameter list (6,648,827,904 params), N_d = 64,
+     bucket 2^24: per step every layer is gathered into 64 constant-size
+     buffers for the forward and again for the backward, and each bucket's 64
+     gradient copies are generated into a staging area right before its
+     kernel (generation time is excluded).
+  5  stage 2 sweep, flat 2^20 .. 2^31 parameters, N_d in {2, 8, 32}, fp16 or
+     bf16 grads N(0,1e-3), bias correction, global-norm clipping at 1.0
+     (two-pass path), gradients generated per bucket (excluded).
+
+Each leg prints one JSON line with the same keys as the headline.  Times are
+CUDA events on the step's stream; input generation on the same stream is
+bracketed by its own events and subtracted.
+"""
+from __future__ import annotations
+
+import math
+import time
+
+import bench
+
+ADAM = bench.ADAM
+
+
+def transformer_layers(vocab, d, layers):
+    return [vocab * d] + [12 * d * d + 4 * d] * layers
+
+
+def _ev():
+    import torch
+    return torch.cuda.Event(enable_timing=True)
+
+
+def _base(metric_value, ms_per_step, steps, warmup, workload, extra_config, dtype="f32"):
+    return {"metric": bench.METRIC, "value": metric_value, "unit": bench.UNIT, "n_gpus": 1, "steps": steps,
+            "warmup": warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "config": dict({"workload": workload}, **extra_config)}
+
+
+def _roofline(bytes_per_step, kernel_ms_per_step, kernel_name):
+    peak, kind = bench.measured_peak_hbm()
+    achieved = bytes_per_step / (kernel_ms_per_step * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": kernel_name, "achieved": achieved, "peak": peak, "peak_kind": kind,
+            "unit": "GB/s", "frac": achieved / peak, "traffic": None, "algorithmic_bytes_per_step": bytes_per_step}
+
+
+class StagedGrads:
+    """Per-bucket gradient staging: N buffers of one bucket each, filled by
+    the device generator right before the bucket's kernel, on the step's
+    stream, between a pair of events (so the fill can be subtracted)."""
+
+    def __init__(self, n_ranks, bucket, dtype, device):
+        import torch
+        self.bufs = [torch.empty(bucket, dtype=torch.int16, device=device) for _ in range(n_ranks)]
+        self.ptrs = [b.data_ptr() for b in self.bufs]
+        self.dtype = dtype
+        self.events = []
+
+    def fill(self, lo, hi, sigma, seed, step, stream, inject=()):
+        import synth
+        e0, e1 = _ev(), _ev()
+        e0.record(stream)
+        for r, b in enumerate(self.bufs):
+            synth.dev_normal16(b.data_ptr(), hi - lo, self.dtype, sigma, seed=seed, stream=synth.STREAM_GRAD,
+                               step=step, rank=r, offset=lo, cuda_stream=stream.cuda_stream)
+        for r, e in inject:
+            if lo <= e < hi:
+                self.bufs[r][e - lo] = synth.inf_bits(self.dtype)      # 0x7C00 / 0x7F80 fit int16
+        e1.record(stream)
+        self.events.append((e0, e1))
+
+    def take_ms(self):
+        ms = sum(a.elapsed_time(b) for a, b in self.events)
+        self.events = []
+        return ms
+
+
+# ---------------------------------------------------------------------------
+def leg_cfg1(args):
+    import torch
+
+    import synth
+    import zero_sharded_mixed_bucket_gb300 as zg
+    n, N, S = 1 << 20, 4, 1024.0
+    dev = torch.device("cuda", 0)
+    cfg = zg.Config(n, N, 2, 1 << 24)
+    plan = zg.zero_plan(cfg)
+    bufs = zg.DeviceBuffers(cfg, plan, device=dev)
+    s = torch.cuda.current_stream(dev)
+    synth.dev_normal32(bufs.w[0].data_ptr(), n, 0.02, seed=0, stream=synth.STREAM_WEIGHT, cuda_stream=s.cuda_stream)
+    for r in range(N):
+        synth.dev_normal16(bufs.grads[r].data_ptr(), n, synth.FP16, 1e-3 * S, seed=0, stream=synth.STREAM_GRAD,
+                           step=1, rank=r, cuda_stream=s.cuda_stream)
+    adam = zg.zero_adam_t(max_grad_norm=0.0, **ADAM)
+    state = zg.zero_state_t(t=0, loss_scale=S, min_loss_scale=1.0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    e0, e1 = _ev(), _ev()
+    e0.record(s)        # materialise the events (the library records them by handle)
+    e1.record(s)
+    zg.zero_set_profile_events(e0, e1)
+    spans, walls = [], []
+    try:
+        for k in range(args.warmup + args.steps):
+            flush.fill_(k & 0xff)                      # evict the step's working set from L2
+            w0, w1 = _ev(), _ev()
+            w0.record(s)
+            res = zg.zero_step_stage2(cfg, plan, bufs, adam, state, s)
+            w1.record(s)
+            torch.cuda.synchronize()
+            if k >= args.warmup:
+                spans.append(e0.elapsed_time(e1))
+                walls.append(w0.elapsed_time(w1))
+            assert res.overflow == 0
+    finally:
+        zg.zero_set_profile_events(None, None)
+    ms = sum(walls) / len(walls)
+    out = _base(n / (ms * 1e-3) / 1e9, ms, args.steps, args.warmup,
+                "stage 2, flat 2^20 params, N_d=4, fp16 grads N(0,1e-3) x 1024 static loss scale, one bucket",
+                {"n_params": n, "n_ranks": N, "stage": 2, "l2": "flushed before every step (256 MB write)"})
+    out["roofline"] = _roofline(plan.hbm_bytes_fused, sum(spans) / len(spans), "k_fused<stage 2, fp16>")
+    out["note"] = "42 MB per step: launch latency and the flag read dominate; a parity case, not a bandwidth one"
+    return out
+
+
+# ---------------------------------------------------------------------------
+def leg_cfg3(args):
+    import torch
+
+    import synth
+    import zero_sharded_mixed_bucket_gb300 as zg
+    layers = transformer_layers(50257, 1600, 48)
+    n, N, B = sum(layers), 8, 500_000_000
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.current_stream(dev)
+    cfg = zg.Config(n, N, 2, B, 0, layers)
+    plan = zg.zero_plan(cfg)
+    bufs = zg.DeviceBuffers(cfg, plan, device=dev)
+    runs = {}
+    steps = max(args.steps, 4)
+    for run in ("literal", "odd_steps"):
+        # both runs start from the same master weights (m = v = 0)
+        synth.dev_normal32(bufs.w[bufs.cur].data_ptr(), n, 0.02, seed=0, stream=synth.STREAM_WEIGHT,
+                           cuda_stream=s.cuda_stream)
+        adam = zg.zero_adam_t(max_grad_norm=0.0, **ADAM)
+        state = zg.zero_state_t(t=0, loss_scale=1024.0, min_loss_scale=1.0, dynamic=1, growth_interval=0)
+        walls, skipped, scales = [], 0, []
+        for k in range(steps):
+            step_no = k + 1
+            S = state.loss_scale
+            for r in range(N):
+                synth.dev_normal16(bufs.grads[r].data_ptr(), n, synth.FP16, 1e-3 * S, seed=0,
+                                   stream=synth.STREAM_GRAD, step=step_no, rank=r, cuda_stream=s.cuda_stream)
+            if run == "literal" or step_no % 2 == 1:
+                for r, e in synth.inf_positions(n, N, seed=0, step=step_no):
+                    bufs.grads[r][e] = synth.inf_bits(synth.FP16)
+            w0, w1 = _ev(), _ev()
+            w0.record(s)
+            res = zg.zero_step_stage2(cfg, plan, bufs, adam, state, s)
+            w1.record(s)
+            torch.cuda.synchronize()
+            walls.append(w0.elapsed_time(w1))
+            skipped += res.skipped
+            scales.append(res.new_loss_scale)
+        ms = sum(walls) / len(walls)
+        runs[run] = {"ms_per_step": ms, "value": n / (ms * 1e-3) / 1e9, "steps": steps, "skipped": skipped,
+                     "loss_scales": scales, "t": state.t,
+                     "hbm_bytes_per_clean_step": plan.hbm_bytes_fused,
+                     "hbm_bytes_per_skipped_step": plan.hbm_bytes_fused + n * (4 + 2 * N)}
+    main = runs["odd_steps"]
+    out = _base(main["value"], main["ms_per_step"], steps, 0,
+                "stage 2, 48-layer d=1600 parameter list (%d params), N_d=8, bucket 5e8, fp16 grads N(0,1e-3) x S, "
+                "one +inf per 1e9 gradient elements, dynamic loss scale (halve and skip), S0=1024" % n,
+                {"n_params": n, "n_ranks": N, "stage": 2, "bucket_elems": B, "injection": "value: odd steps only; "
+                 "runs.literal: every step (12 infs over 1.24e10 gradient elements)"})
+    out["runs"] = runs
+    out["note"] = ("a skipped step also runs the parameter restore kernel (cast of the unchanged master weights "
+                   "to every rank); step times are CUDA events around the whole library call")
+    return out
+
+
+# ---------------------------------------------------------------------------
+def leg_cfg4(args):
+    import torch
+
+    import synth
+    import zero_sharded_mixed_bucket_gb300 as zg
+    layers = transformer_layers(50257, 4096, 32)
+    n, N, B = sum(layers), 64, 1 << 24
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.current_stream(dev)
+    cfg = zg.Config(n, N, 3, B, 0, layers)
+    plan = zg.zero_plan(cfg)
+    bufs = zg.DeviceBuffers(cfg, plan, device=dev, grads=False, reduced=False)
+    S = 1024.0
+    synth.dev_normal32(bufs.w[0].data_ptr(), n, 0.02, seed=0, stream=synth.STREAM_WEIGHT, cuda_stream=s.cuda_stream)
+    # the 16-bit shards start as the cast of the master weights: one clean step from lr = 0 would do it; the
+    # benchmark times steps, so initial shard contents only matter for the gathers' bandwidth, not results
+    staging = StagedGrads(N, B, synth.FP16, dev)
+    dst = [torch.empty(plan.max_layer_elems, dtype=torch.int16, device=dev) for _ in range(N)]
+    dst_ptrs = [d.data_ptr() for d in dst]
+    shard_ptrs = [t.data_ptr() for t in bufs.params16]
+    adam = zg.zero_adam_t(max_grad_norm=0.0, **ADAM)
+    state = zg.zero_state_t(t=0, loss_scale=S, min_loss_scale=1.0)
+    starts = [0]
+    for l in layers:
+        starts.append(starts[-1] + l)
+    nb = plan.n_buckets
+
+    def one_step(step_no):
+        zg.zero_step_begin(cfg, plan, bufs, adam, state, s)
+        for l in range(len(layers)):                       # forward: gather every layer
+            zg.zero_gather_layer(cfg, plan, l, shard_ptrs, dst_ptrs, s)
+        done = nb
+        for l in reversed(range(len(layers))):             # backward: gather again, then finished buckets
+            zg.zero_gather_layer(cfg, plan, l, shard_ptrs, dst_ptrs, s)
+            while done > 0 and (done - 1) * B >= starts[l]:
+                b = done - 1
+                lo, hi = b * B, min((b + 1) * B, n)
+                staging.fill(lo, hi, 1e-3 * S, 0, step_no, s)
+                zg.zero_step_bucket(cfg, plan, bufs, adam, state, b, staging.ptrs, s)
+                done -= 1
+        return zg.zero_step_end(cfg, plan, bufs, adam, state, s)
+
+    steps = max(1, min(args.steps, 3))
+    warm = 1
+    for k in range(warm):
+        one_step(k + 1)
+        staging.take_ms()
+    walls, gens = [], []
+    for k in range(steps):
+        w0, w1 = _ev(), _ev()
+        w0.record(s)
+        res = one_step(warm + k + 1)
+        w1.record(s)
+        torch.cuda.synchronize()
+        assert res.overflow == 0
+        walls.append(w0.elapsed_time(w1))
+        gens.append(staging.take_ms())
+    step_ms = [w - g for w, g in zip(walls, gens)]
+    ms = sum(step_ms) / len(step_ms)
+    bpp_gather = 2 + 2 * N
+    bytes_step = n * (2 * bpp_gather + bench.bytes_per_param(3, N))
+    out = _base(n / (ms * 1e-3) / 1e9, ms, steps, warm,
+                "stage 3, 32-layer d=4096 parameter list (%d params), N_d=64, bucket 2^24; two gathers per layer "
+                "into 64 constant-size buffers; 64 gradient copies generated per bucket (excluded)" % n,
+                {"n_params": n, "n_ranks": N, "stage": 3, "bucket_elems": B, "n_layers": len(layers),
+                 "gather_capacity_elems": plan.max_layer_elems})
+    out["roofline"] = _roofline(bytes_step, ms, "k_gather + k_fused<stage 3, fp16>")
+    out["bytes_per_param"] = 2 * bpp_gather + bench.bytes_per_param(3, N)
+    out["generation_ms_per_step"] = sum(gens) / len(gens)
+    out["device_memory_gb"] = torch.cuda.max_memory_allocated(dev) / 1e9
+    return out
+
+
+# ---------------------------------------------------------------------------
+SWEEP_DEFAULT = [(1 << 20, 8, "fp16"), (1 << 24, 8, "fp16"), (1 << 28, 2, "fp16"), (1 << 28, 8, "bf16"),
+                 (1 << 28, 32, "fp16"), (1 << 31, 2, "bf16"), (1 << 31, 8, "fp16"), (1 << 31, 32, "bf16")]
+
+
+def sweep_point(n, N, dtype_name, steps, warm):
+    import torch
+
+    import synth
+    import zero_sharded_mixed_bucket_gb300 as zg
+    dtype = zg.ZERO_BF16 if dtype_name == "bf16" else zg.ZERO_FP16
+    B = 1 << 24
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.current_stream(dev)
+    cfg = zg.Config(n, N, 2, B, 0, None, dtype)
+    plan = zg.zero_plan(cfg)
+    bufs = zg.DeviceBuffers(cfg, plan, device=dev, grads=False, shadow=False)
+    synth.dev_normal32(bufs.w[0].data_ptr(), n, 0.02, seed=0, stream=synth.STREAM_WEIGHT, cuda_stream=s.cuda_stream)
+    staging = StagedGrads(N, min(B, n), dtype, dev)
+    adam = zg.zero_adam_t(max_grad_norm=1.0, **ADAM)
+    state = zg.zero_state_t(t=0, loss_scale=1.0, min_loss_scale=1.0)
+    e0, e1 = _ev(), _ev()
+
+    def one_step(step_no):
+        zg.zero_step_begin(cfg, plan, bufs, adam, state, s)
+        for b in range(plan.n_buckets):
+            lo, hi = b * B, min((b + 1) * B, n)
+            staging.fill(lo, hi, 1e-3, 0, step_no, s)
+            zg.zero_step_bucket(cfg, plan, bufs, adam, state, b, staging.ptrs, s)
+        return zg.zero_step_end(cfg, plan, bufs, adam, state, s)
+
+    for k in range(warm):
+        one_step(k + 1)
+    staging.take_ms()
+    walls, gens, norms = [], [], []
+    for k in range(steps):
+        w0, w1 = _ev(), _ev()
+        w0.record(s)
+        res = one_step(warm + k + 1)
+        w1.record(s)
+        torch.cuda.synchronize()
+        walls.append(w0.elapsed_time(w1))
+        gens.append(staging.take_ms())
+        norms.append(res.grad_norm)
+        assert res.overflow == 0
+    ms = sum(w - g for w, g in zip(walls, gens)) / steps
+    bpp = 28 + 4 * N
+    out = {"n_params": n, "n_ranks": N, "dtype": dtype_name, "ms_per_step": ms, "value": n / (ms * 1e-3) / 1e9,
+           "hbm_gbs": n * bpp / (ms * 1e-3) / 1e9, "bytes_per_param": bpp, "grad_norm": norms[-1],
+           "clip_coef": res.clip_coef, "t": state.t}
+    del bufs, staging
+    torch.cuda.empty_cache()
+    return out
+
+
+def leg_cfg5(args):
+    points = SWEEP_DEFAULT
+    if args.n_params:
+        points = [(args.n_params, args.ranks or 8, args.dtype or "fp16")]
+    steps = max(1, min(args.steps, 3))
+    res = [sweep_point(n, N, d, steps, 1) for n, N, d in points]
+    peak, kind = bench.measured_peak_hbm()
+    for r in res:
+        r["frac"] = r["hbm_gbs"] / peak
+    best = max(res, key=lambda r: r["n_params"] * 1000 + r["n_ranks"])
+    out = _base(best["value"], best["ms_per_step"], steps, 1,
+                "stage 2 sweep, flat 2^20..2^31 params, N_d in {2,8,32}, fp16/bf16 grads N(0,1e-3), clipping at 1.0, "
+                "bias correction; gradients generated per bucket (excluded)",
+                {"stage": 2, "bucket_elems": 1 << 24, "value_point": {k: best[k] for k in ("n_params", "n_ranks",
+                                                                                            "dtype")}})
+    out["points"] = res
+    out["roofline"] = {"bound": "hbm", "kernel": "k_reduce + k_finalize + k_update (two-pass, clipping)",
+                       "achieved": best["hbm_gbs"], "peak": peak, "peak_kind": kind, "unit": "GB/s",
+                       "frac": best["hbm_gbs"] / peak, "traffic": None}
+    return out
+
+
+LEGS = {1: leg_cfg1, 3: leg_cfg3, 4: leg_cfg4, 5: leg_cfg5}
