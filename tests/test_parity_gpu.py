@@ -334,3 +334,20 @@ def test_full_size_sampled(stage):
         for r in range(1, N):
             assert torch.equal(bufs.state()[0][r * pad:r * pad + n], bufs.state()[0][:n])
     del w0_dev
+
+
+def test_gradients_in_pinned_host_memory():
+    """The fused kernel may read the ranks' gradients straight from pinned
+    host memory (NVLink-C2C on GB300): same results as the oracle."""
+    import ctypes
+    n, N = 3 * 4096 + 19, 4
+    job = Job(n, N, 2, 4096, 8, loss_scale=16.0)
+    grads = job.make_grads(1)
+    host = [torch.from_numpy(g.view(np.int16).copy()).pin_memory() for g in grads]
+    ptrs = (ctypes.c_void_p * N)(*[t.data_ptr() for t in host])
+    job.bufs.b.grads = ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p))
+    res = zg.zero_step_stage2(job.cfg, job.plan, job.bufs, job.adam, job.state, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    ref = oracle.step(grads, job.w, job.m, job.v, dtype=FP16, t=0, loss_scale=16.0, **job.hp)
+    job.p16, job.h, job.o["t"] = ref["p16"], ref["h"], ref["t"]
+    job.check(res, ref)
