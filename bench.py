@@ -528,7 +528,7 @@ def main():
                          "e.g. for profiling captures)")
     ap.add_argument("--ring", type=int, default=GRAD_RING, help="distinct per-step gradient sets kept in HBM")
     ap.add_argument("--bucket", type=int, default=BUCKET, help="gradient bucket size in elements")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6],
                     help="workload: 2 (default) the headline; 1, 3, 4, 5 the others (bench_workloads.py)")
     ap.add_argument("--ranks", type=int, default=None, help="--config 5: N_d of a single sweep point")
     ap.add_argument("--dtype", default=None, choices=["fp16", "bf16"], help="--config 5: dtype of a single point")

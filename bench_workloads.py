@@ -14,7 +14,10 @@
      kernel (generation time is excluded).
   5  stage 2 sweep, flat 2^20 .. 2^31 parameters, N_d in {2, 8, 32}, fp16 or
      bf16 grads N(0,1e-3), bias correction, global-norm clipping at 1.0
-     (two-pass path), gradients generated per bucket (excluded).
+     (two-pass path); gradients resident in HBM when all ranks' gradients
+     and parameters fit in 160 GB, else generated per bucket (excluded).
+  6  the headline workload with the fp32 optimizer state in pinned host
+     (Grace) memory, updated by the fused kernel over NVLink-C2C.
 
 Each leg prints one JSON line with the same keys as the headline.  Times are
 CUDA events on the step's stream; input generation on the same stream is
@@ -277,14 +280,20 @@ def sweep_point(n, N, dtype_name, steps, warm):
     s = torch.cuda.current_stream(dev)
     cfg = zg.Config(n, N, 2, B, 0, None, dtype)
     plan = zg.zero_plan(cfg)
-    bufs = zg.DeviceBuffers(cfg, plan, device=dev, grads=False, shadow=False)
+    resident = 2 * N * n * 2 <= 160e9          # all ranks' gradients and parameters in HBM
+    bufs = zg.DeviceBuffers(cfg, plan, device=dev, grads=resident, shadow=False)
     synth.dev_normal32(bufs.w[0].data_ptr(), n, 0.02, seed=0, stream=synth.STREAM_WEIGHT, cuda_stream=s.cuda_stream)
-    staging = StagedGrads(N, min(B, n), dtype, dev)
+    if resident:
+        for r in range(N):
+            synth.dev_normal16(bufs.grads[r].data_ptr(), n, dtype, 1e-3, seed=0, stream=synth.STREAM_GRAD, step=1,
+                               rank=r, cuda_stream=s.cuda_stream)
+    staging = None if resident else StagedGrads(N, min(B, n), dtype, dev)
     adam = zg.zero_adam_t(max_grad_norm=1.0, **ADAM)
     state = zg.zero_state_t(t=0, loss_scale=1.0, min_loss_scale=1.0)
-    e0, e1 = _ev(), _ev()
 
     def one_step(step_no):
+        if resident:            # stage 2 leaves the gradients unchanged: the same set serves every step
+            return zg.zero_step_stage2(cfg, plan, bufs, adam, state, s)
         zg.zero_step_begin(cfg, plan, bufs, adam, state, s)
         for b in range(plan.n_buckets):
             lo, hi = b * B, min((b + 1) * B, n)
@@ -294,7 +303,8 @@ def sweep_point(n, N, dtype_name, steps, warm):
 
     for k in range(warm):
         one_step(k + 1)
-    staging.take_ms()
+    if staging:
+        staging.take_ms()
     walls, gens, norms = [], [], []
     for k in range(steps):
         w0, w1 = _ev(), _ev()
@@ -303,14 +313,15 @@ def sweep_point(n, N, dtype_name, steps, warm):
         w1.record(s)
         torch.cuda.synchronize()
         walls.append(w0.elapsed_time(w1))
-        gens.append(staging.take_ms())
+        gens.append(staging.take_ms() if staging else 0.0)
         norms.append(res.grad_norm)
         assert res.overflow == 0
     ms = sum(w - g for w, g in zip(walls, gens)) / steps
     bpp = 28 + 4 * N
     out = {"n_params": n, "n_ranks": N, "dtype": dtype_name, "ms_per_step": ms, "value": n / (ms * 1e-3) / 1e9,
            "hbm_gbs": n * bpp / (ms * 1e-3) / 1e9, "bytes_per_param": bpp, "grad_norm": norms[-1],
-           "clip_coef": res.clip_coef, "t": state.t}
+           "clip_coef": res.clip_coef, "t": state.t,
+           "gradients": "resident in HBM" if resident else "generated per bucket into staging (excluded)"}
     del bufs, staging
     torch.cuda.empty_cache()
     return out
@@ -328,7 +339,7 @@ def leg_cfg5(args):
     best = max(res, key=lambda r: r["n_params"] * 1000 + r["n_ranks"])
     out = _base(best["value"], best["ms_per_step"], steps, 1,
                 "stage 2 sweep, flat 2^20..2^31 params, N_d in {2,8,32}, fp16/bf16 grads N(0,1e-3), clipping at 1.0, "
-                "bias correction; gradients generated per bucket (excluded)",
+                "bias correction; gradients resident when they fit, else generated per bucket (excluded)",
                 {"stage": 2, "bucket_elems": 1 << 24, "value_point": {k: best[k] for k in ("n_params", "n_ranks",
                                                                                             "dtype")}})
     out["points"] = res
@@ -338,4 +349,40 @@ def leg_cfg5(args):
     return out
 
 
-LEGS = {1: leg_cfg1, 3: leg_cfg3, 4: leg_cfg4, 5: leg_cfg5}
+# ---------------------------------------------------------------------------
+def leg_offload(args):
+    """The headline workload with the fp32 optimizer state (w, m, v and their
+    shadow copies: 2 x 12 B per parameter) in pinned host memory; the fused
+    kernel reads and writes it over NVLink-C2C, gradients and 16-bit
+    parameters stay in HBM."""
+    import ctypes
+
+    import torch
+    dev = torch.device("cuda", 0)
+    job = bench.GpuJob(2, dev, ring=2)
+    n = job.n
+    keep = []
+    for name in ("w", "m", "v"):
+        for k in range(2):
+            h = torch.zeros(job.plan.state_elems, dtype=torch.float32).pin_memory()
+            h.copy_(getattr(job.bufs, name)[k].cpu())
+            getattr(job.bufs.b, name)[k] = h.data_ptr()
+            keep.append(h)
+    for name in ("w", "m", "v"):
+        setattr(job.bufs, name, None)
+    torch.cuda.empty_cache()
+    ms, launches, kernel, _ = bench.timed_steps(job, max(3, min(args.steps, 20)), args.warmup, 1)
+    steps = max(3, min(args.steps, 20))
+    ms_step = ms / steps
+    out = _base(n / (ms_step * 1e-3) / 1e9, ms_step, steps, args.warmup,
+                "headline workload (12-layer d=768 list, N_d=8, stage 2, bucket 2^24) with the fp32 optimizer "
+                "state in pinned host memory", {"n_params": n, "n_ranks": 8, "stage": 2,
+                                                "state_location": "pinned host memory (Grace), via NVLink-C2C"})
+    out["host_link_bytes_per_step"] = n * 24
+    out["host_link_gbs"] = n * 24 / (kernel["span_ms_per_step"] * 1e-3) / 1e9
+    out["hbm_bytes_per_step"] = n * (4 * 8)
+    out["gpu_launches"] = launches
+    return out
+
+
+LEGS = {1: leg_cfg1, 3: leg_cfg3, 4: leg_cfg4, 5: leg_cfg5, 6: leg_offload}

@@ -351,3 +351,24 @@ def test_gradients_in_pinned_host_memory():
     ref = oracle.step(grads, job.w, job.m, job.v, dtype=FP16, t=0, loss_scale=16.0, **job.hp)
     job.p16, job.h, job.o["t"] = ref["p16"], ref["h"], ref["t"]
     job.check(res, ref)
+
+
+@pytest.mark.parametrize("shadow", [True, False])
+def test_optimizer_state_in_pinned_host_memory(shadow):
+    """fp32 master weights, momentum and variance (and the shadow copy) kept
+    in pinned host memory and updated by the kernels over NVLink-C2C -- the
+    optimizer-state offload axis: three steps against the oracle."""
+    n, N = 5 * 2048 + 3, 4
+    job = Job(n, N, 2, 2048, 8, shadow=shadow, loss_scale=4.0, max_norm=0.0 if shadow else 1.0, sigma=0.05)
+    ncopy = 2 if shadow else 1
+    host = {}
+    for name in ("w", "m", "v"):
+        dev_t = getattr(job.bufs, name)
+        host[name] = [torch.empty(dev_t[0].numel(), dtype=torch.float32).pin_memory() for _ in range(ncopy)]
+        for k in range(ncopy):
+            host[name][k].copy_(dev_t[k].cpu())
+            getattr(job.bufs.b, name)[k] = host[name][k].data_ptr()
+    job.bufs.w, job.bufs.m, job.bufs.v = host["w"], host["m"], host["v"]     # state() now reads host tensors
+    for t in (1, 2, 3):
+        res, ref = job.step(job.make_grads(t))
+        job.check(res, ref)
