@@ -302,13 +302,23 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest of every rank's x (the slowest rank's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(ms_local: float, n_params: int, steps: int, world: int):
+    """Whole-job figures: every rank runs its own replica of the job, so the
+    job processes world * n_params parameters per step in the slowest rank's
+    time.  Returns (ms_per_step, Gparams/s)."""
+    ms_per_step = max_over_ranks(ms_local, world) / steps
+    return ms_per_step, world * n_params / (ms_per_step * 1e-3) / 1e9
 
 
 def timed_steps(job, steps, warmup, world):
@@ -437,16 +447,15 @@ def gpu_arm(args):
     world, rank, local = dist_setup(args)
     device = torch.device("cuda", local)
     import __graft_entry__
-    if rank == 0 or world > 1:
-        __graft_entry__.build()
+    if rank == 0:
+        __graft_entry__.build()      # one builder: concurrent builds would write the same object files
+    barrier(world)
     job = GpuJob(STAGE, device, ring=args.ring, n_params=args.n_params)
     n_params = job.n
     sampler = ClockSampler(local)
     ms, launches, kernel, (t0, t1) = timed_steps(job, args.steps, args.warmup, world)
     rows = sampler.stop()
-    ms_max = max_over_ranks(ms, world)
-    ms_per_step = ms_max / args.steps
-    value = world * n_params / (ms_per_step * 1e-3) / 1e9
+    ms_per_step, value = aggregate(ms, n_params, args.steps, world)
     peak, peak_kind = measured_peak_hbm()
     achieved = kernel["bytes"] / (kernel["total_ms"] * 1e-3) / 1e9
     per_launch = kernel["bytes"] / kernel["launches"]
