@@ -89,6 +89,7 @@ def lib():
         L.oracle_sumsq_bins.argtypes = [i64, vp, i32, vp]
         L.oracle_adam.argtypes = [i64, vp, i32, ctypes.POINTER(Hyper), vp, vp, vp, vp]
         L.oracle_cast.argtypes = [i64, vp, i32, vp]
+        L.oracle_sgd.argtypes = [i64, vp, i32, ctypes.POINTER(Hyper), vp, vp, vp]
         _lib = L
     return _lib
 
@@ -262,6 +263,23 @@ def adam(h, dtype: int, hyper: Hyper, w: np.ndarray, m: np.ndarray, v: np.ndarra
     return p16
 
 
+def sgd(h, dtype: int, hyper: Hyper, w: np.ndarray, m=None) -> np.ndarray:
+    """SGD (with momentum when m is given, mu = hyper.beta1) on the fp32
+    master weights (in place) and the 16-bit cast."""
+    h = _u16(h)
+    for a in (w,) + ((m,) if m is not None else ()):
+        if a.dtype != np.float32 or not a.flags.c_contiguous or a.size != h.size:
+            raise ValueError("state arrays are contiguous float32 of the gradient's length")
+    p16 = np.empty(h.size, np.uint16)
+    lib().oracle_sgd(h.size, _ptr(h), dtype, ctypes.byref(hyper), _ptr(w), _ptr(m) if m is not None else None,
+                     _ptr(p16))
+    return p16
+
+
+OPTIMIZERS = ("adam", "sgdm", "sgd")
+OPTIM_K = {"adam": 12, "sgdm": 8, "sgd": 4}   # fp32 bytes per parameter incl. the fp32 master copy
+
+
 def cast16(w: np.ndarray, dtype: int) -> np.ndarray:
     w = _f32arr(w)
     p = np.empty(w.size, np.uint16)
@@ -271,8 +289,11 @@ def cast16(w: np.ndarray, dtype: int) -> np.ndarray:
 
 def step(grads, w, m, v, *, dtype: int, lr: float, beta1: float, beta2: float, eps: float,
          t: int, loss_scale: float, max_grad_norm: float = 0.0, dynamic: bool = False,
-         min_scale: float = 1.0, growth_interval: int = 0, good_steps: int = 0) -> dict:
-    """One unpartitioned mixed-precision Adam step.
+         min_scale: float = 1.0, growth_interval: int = 0, good_steps: int = 0, optimizer: str = "adam",
+         momentum: float = 0.0) -> dict:
+    """One unpartitioned mixed-precision optimizer step (Adam by default;
+    optimizer="sgdm" -- SGD with momentum `momentum`, state w, m -- or "sgd",
+    state w only).
 
     grads: list of N_d uint16 arrays (each rank's 16-bit gradient, loss-scaled)
     w, m, v: fp32 master weights, momentum, variance (updated in place unless
@@ -295,8 +316,14 @@ def step(grads, w, m, v, *, dtype: int, lr: float, beta1: float, beta2: float, e
         if max_grad_norm > 0:
             norm = grad_norm(exact_sumsq(h, dtype), inv)
             clip = clip_coef(norm, max_grad_norm)
-        hyper = make_hyper(inv=inv, clip=clip, lr=lr, beta1=beta1, beta2=beta2, eps=eps, t=t + 1)
-        p16 = adam(h, dtype, hyper, w, m, v)
+        if optimizer == "adam":
+            hyper = make_hyper(inv=inv, clip=clip, lr=lr, beta1=beta1, beta2=beta2, eps=eps, t=t + 1)
+            p16 = adam(h, dtype, hyper, w, m, v)
+        elif optimizer in ("sgdm", "sgd"):
+            hyper = make_hyper(inv=inv, clip=clip, lr=lr, beta1=momentum, beta2=0.0, eps=0.0, t=1)
+            p16 = sgd(h, dtype, hyper, w, m if optimizer == "sgdm" else None)
+        else:
+            raise ValueError(optimizer)
         t_new = t + 1
     new_scale, good = scaler_update(loss_scale, good_steps, bool(overflow), dynamic,
                                     min_scale, growth_interval)
@@ -404,16 +431,17 @@ def comm_bytes(psi: int, n_ranks: int, stage: int, b: int = 2) -> dict:
                 counted_passes=COLLECTIVE_PASSES[stage])
 
 
-def hbm_bytes_per_param(n_ranks: int, stage: int, mode: str) -> int:
+def hbm_bytes_per_param(n_ranks: int, stage: int, mode: str, state_bytes: int = 12) -> int:
     """Algorithmic HBM bytes per parameter of one step with N_d simulated
     ranks in one memory.  mode 'fused': one pass, new state written beside the
     old; 'two_pass': reduced gradient materialised, then read back.
-    16-bit values are 2 bytes, fp32 state 4 bytes each of w, m, v."""
-    N = n_ranks
+    16-bit values are 2 bytes; state_bytes = fp32 state per parameter (12 for
+    Adam's w, m, v; 8 for SGD with momentum; 4 for SGD), read and written."""
+    N, sb = n_ranks, state_bytes
     if mode == "fused":
-        return {0: 30 * N, 1: 24 + 6 * N, 2: 24 + 4 * N, 3: 26 + 2 * N}[stage]
+        return {0: N * (6 + 2 * sb), 1: 6 * N + 2 * sb, 2: 4 * N + 2 * sb, 3: 2 * N + 2 * sb + 2}[stage]
     if mode == "two_pass":
-        return {0: 32 * N, 1: 26 + 6 * N, 2: 28 + 4 * N, 3: 30 + 2 * N}[stage]
+        return {0: N * (8 + 2 * sb), 1: 6 * N + 2 + 2 * sb, 2: 4 * N + 4 + 2 * sb, 3: 2 * N + 6 + 2 * sb}[stage]
     raise ValueError(mode)
 
 

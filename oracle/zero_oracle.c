@@ -256,6 +256,34 @@ void oracle_adam(int64_t n, const uint16_t* h, int32_t dtype, const oracle_hyper
     }
 }
 
+/* SGD on the fp32 master weights (the other optimizers of the (2b+K)
+ * accounting; PyTorch's SGD without dampening, Nesterov or weight decay):
+ *   g  = h * (1/(S N))            [* c when clipping]
+ *   with momentum mu (m != NULL):  m' = mu*m + g;  w' = w - lr*m'
+ *   plain (m == NULL):             w' = w - lr*g
+ *   p  = round16(w')
+ * hp->beta1 carries mu; beta2, eps and the bias corrections are unused. */
+void oracle_sgd(int64_t n, const uint16_t* h, int32_t dtype, const oracle_hyper_t* hp,
+                float* w, float* m, uint16_t* p16)
+{
+    for (int64_t i = 0; i < n; i++) {
+        float g = to_f32(h[i], dtype) * hp->inv_scale;
+        if (hp->use_clip)
+            g = g * hp->clip;
+        float d = g;
+        if (m) {
+            float t1 = hp->beta1 * m[i];
+            float m1 = t1 + g;
+            m[i] = m1;
+            d = m1;
+        }
+        float step = hp->lr * d;
+        float w1 = w[i] - step;
+        w[i] = w1;
+        p16[i] = to_16(w1, dtype);
+    }
+}
+
 /* The 16-bit model copy of the master weights (used to initialise the
  * parameters and, after a skipped step, as their unchanged value). */
 void oracle_cast(int64_t n, const float* w, int32_t dtype, uint16_t* p16)

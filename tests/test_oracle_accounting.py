@@ -208,3 +208,19 @@ def test_hbm_bytes_per_param_count():
     assert oracle.hbm_bytes_per_param(N, 2, "two_pass") == oracle.hbm_bytes_per_param(N, 2, "fused") + 4
     # stage 0: all-reduce write-back to N grad buffers, N replicas updated
     assert oracle.hbm_bytes_per_param(N, 0, "fused") == 2 * N + 2 * N + N * (24 + 2)
+
+
+def test_mixed_precision_optimizer_multipliers():
+    # the page's calculator: K = optimizer multiplier + 4 B fp32 master in mixed
+    # precision (Adam 8 + 4 = 12, SGD+m 4 + 4 = 8, SGD 0 + 4 = 4); stage 0 = (2b+K) Psi
+    import oracle as o
+    assert o.OPTIM_K == {"adam": 12, "sgdm": 8, "sgd": 4}
+    for name, K in o.OPTIM_K.items():
+        assert o.model_state_bytes(10 ** 9, 1, 0, b=2, K=K)["total"] == (4 + K) * 10 ** 9
+    # byte counts per parameter reduce to the Adam table for 12-byte state
+    for stage in range(4):
+        for N in (1, 8, 64):
+            assert oracle.hbm_bytes_per_param(N, stage, "fused", 12) == {0: 30 * N, 1: 24 + 6 * N, 2: 24 + 4 * N,
+                                                                        3: 26 + 2 * N}[stage]
+            assert oracle.hbm_bytes_per_param(N, stage, "two_pass", 12) == {0: 32 * N, 1: 26 + 6 * N,
+                                                                           2: 28 + 4 * N, 3: 30 + 2 * N}[stage]

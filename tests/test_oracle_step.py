@@ -415,3 +415,58 @@ def test_planted_reduce_mistakes_are_caught():
     duplicated = oracle.reduce(grads + grads[:1], FP16)[0]
     assert not np.array_equal(dropped, ref)
     assert not np.array_equal(duplicated, ref)
+
+
+# --- SGD variants (the other optimizers of the (2b+K) accounting) -----------
+@pytest.mark.parametrize("momentum", [0.0, 0.9])
+@pytest.mark.parametrize("n_ranks,loss_scale", [(1, 1.0), (4, 1024.0)])
+def test_sgd_matches_torch(momentum, n_ranks, loss_scale):
+    rng = np.random.default_rng(40 + n_ranks)
+    n = 3000
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    steps = [_grads(rng, n_ranks, n, 1e-3, loss_scale) for _ in range(5)]
+    w, m = w0.copy(), np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    opt_name = "sgdm" if momentum else "sgd"
+    t = 0
+    for grads in steps:
+        r = oracle.step(grads, w, m, v, dtype=FP16, t=t, loss_scale=loss_scale, optimizer=opt_name,
+                        momentum=momentum, **ADAM)
+        t = r["t"]
+    assert not v.any()                                   # SGD keeps no variance
+    if not momentum:
+        assert not m.any()
+    p = torch.nn.Parameter(torch.from_numpy(w0.copy()))
+    opt = torch.optim.SGD([p], lr=ADAM["lr"], momentum=float(np.float32(momentum)), foreach=False)
+    for grads in steps:
+        s = np.zeros(n, np.float32)
+        for g in grads:
+            s = s + g.view(np.float16).astype(np.float32)
+        h = s.astype(np.float16).astype(np.float64)
+        p.grad = torch.from_numpy((h / (loss_scale * n_ranks)).astype(np.float32))
+        opt.step()
+    assert _close_w(w, p.detach().numpy(), w0, len(steps))
+    if momentum:
+        buf = opt.state[p]["momentum_buffer"].numpy()
+        assert np.allclose(m, buf, rtol=1e-6, atol=1e-12)
+
+
+def test_sgd_closed_form_and_planted_mistakes():
+    """Plain SGD: w' = w - lr*g in one step; a wrong sign or a dropped
+    unscale is caught."""
+    rng = np.random.default_rng(44)
+    n = 2000
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    grads = _grads(rng, 2, n, 1e-3, 8.0)
+    w, m, v = w0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    r = oracle.step(grads, w, m, v, dtype=FP16, t=0, loss_scale=8.0, optimizer="sgd", **ADAM)
+    g = oracle.to_f32(r["h"], FP16).astype(np.float64) / 16.0
+    assert _close_w(w, w0 - ADAM["lr"] * g, w0, 1)
+    h, _ = oracle.reduce(grads, FP16)
+    for mutate in (lambda hp: setattr(hp, "lr", -hp.lr), lambda hp: setattr(hp, "inv_scale", 1.0)):
+        hp = oracle.make_hyper(inv=oracle.inv_scale(8.0, 2), clip=None, lr=ADAM["lr"], beta1=0.0, beta2=0.0,
+                               eps=0.0, t=1)
+        mutate(hp)
+        wm = w0.copy()
+        oracle.sgd(h, FP16, hp, wm)
+        assert not _close_w(wm, w0 - ADAM["lr"] * g, w0, 1)
