@@ -56,11 +56,12 @@ KERNEL_SOURCES = ["zero_sharded_mixed_bucket_gb300/csrc/k_fused.cu",
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_fused_stage2_fp16_n8.md")
 
 
-def bytes_per_param(stage, n=N_RANKS):
+def bytes_per_param(stage, n=N_RANKS, sb=12):
     """Algorithmic HBM bytes per parameter of the fused step (16-bit values 2
-    bytes, fp32 state 4): N gradient reads, the all-reduce write-back in
-    stages 0/1, w/m/v read and written, the 16-bit parameter writes."""
-    return {0: 30 * n, 1: 24 + 6 * n, 2: 24 + 4 * n, 3: 26 + 2 * n}[stage]
+    bytes, sb bytes of fp32 state -- 12 for Adam's w, m, v): N gradient
+    reads, the all-reduce write-back in stages 0/1, the state read and
+    written, the 16-bit parameter writes."""
+    return {0: n * (6 + 2 * sb), 1: 6 * n + 2 * sb, 2: 4 * n + 2 * sb, 3: 2 * n + 2 * sb + 2}[stage]
 
 
 def layer_sizes(vocab=VOCAB, d=D_MODEL, layers=N_LAYERS):
@@ -233,8 +234,12 @@ def reference_arm(args):
 # ---------------------------------------------------------------------------
 # GPU legs
 # ---------------------------------------------------------------------------
+OPTIMIZERS = {"adam": 0, "sgdm": 1, "sgd": 2}
+STATE_BYTES = {0: 12, 1: 8, 2: 4}
+
+
 class GpuJob:
-    def __init__(self, stage, device, ring=GRAD_RING, n_params=None):
+    def __init__(self, stage, device, ring=GRAD_RING, n_params=None, optimizer=0):
         import torch
 
         import synth
@@ -242,7 +247,9 @@ class GpuJob:
         self.zg, self.torch = zg, torch
         self.stage = stage
         self.n = n_params or N_PARAMS
-        self.cfg = zg.Config(self.n, N_RANKS, stage, BUCKET, 0, layer_sizes() if self.n == N_PARAMS else None)
+        self.optimizer = optimizer
+        self.cfg = zg.Config(self.n, N_RANKS, stage, BUCKET, 0, layer_sizes() if self.n == N_PARAMS else None,
+                             zg.ZERO_FP16, optimizer)
         self.plan = zg.zero_plan(self.cfg)
         self.bufs = zg.DeviceBuffers(self.cfg, self.plan, device=device, grads=True)
         self.stream = torch.cuda.current_stream(device)
@@ -262,7 +269,7 @@ class GpuJob:
                                    step=k + 1, rank=r, cuda_stream=s)
             self.ring.append(bufs)
             self.ring_ptrs.append((ctypes.c_void_p * N_RANKS)(*[b.data_ptr() for b in bufs]))
-        self.adam = zg.zero_adam_t(max_grad_norm=0.0, **ADAM)
+        self.adam = zg.zero_adam_t(max_grad_norm=0.0, momentum=0.9, **ADAM)
         self.state = zg.zero_state_t(t=0, loss_scale=1.0, min_loss_scale=1.0)
         torch.cuda.synchronize(device)
 
@@ -356,7 +363,8 @@ def timed_steps(job, steps, warmup, world):
         zg.zero_set_profile_events(None, None)
     ms = start.elapsed_time(end)
     nb = job.plan.n_buckets
-    step_bytes = sum(job.bucket_len(b) for b in range(nb)) * bytes_per_param(job.stage)
+    step_bytes = sum(job.bucket_len(b) for b in range(nb)) * bytes_per_param(job.stage, N_RANKS,
+                                                                              STATE_BYTES[job.optimizer])
     kernel = dict(total_ms=sum(spans), bytes=steps * step_bytes, launches=steps * nb,
                   span_ms_per_step=sum(spans) / steps, launches_per_step=nb)
     return ms, launches, kernel, (t0, t1)
@@ -450,7 +458,7 @@ def gpu_arm(args):
     if rank == 0:
         __graft_entry__.build()      # one builder: concurrent builds would write the same object files
     barrier(world)
-    job = GpuJob(STAGE, device, ring=args.ring, n_params=args.n_params)
+    job = GpuJob(STAGE, device, ring=args.ring, n_params=args.n_params, optimizer=OPTIMIZERS[args.optimizer])
     n_params = job.n
     sampler = ClockSampler(local)
     ms, launches, kernel, (t0, t1) = timed_steps(job, args.steps, args.warmup, world)
@@ -475,10 +483,11 @@ def gpu_arm(args):
                    "l2": "inputs larger than L2: %.2f GB moved per step, %d-step gradient ring of %.1f GB"
                          % (step_bytes / 1e9, args.ring, args.ring * N_RANKS * n_params * 2 / 1e9)},
         "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "k_fused<stage 2, fp16>", "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": "k_fused<stage 2, fp16, %s>" % args.optimizer, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes_per_launch": per_launch,
-                     "bytes_per_param": bytes_per_param(STAGE), "launches": kernel["launches"],
+                     "bytes_per_param": bytes_per_param(STAGE, N_RANKS, STATE_BYTES[job.optimizer]),
+                     "launches": kernel["launches"],
                      "avg_launch_ms": kernel["total_ms"] / kernel["launches"],
                      "kernel_span_ms_per_step": kernel["span_ms_per_step"],
                      "timing": "library-recorded CUDA events around each step's bucket kernels on the step's "
@@ -486,9 +495,12 @@ def gpu_arm(args):
                                "is the step's kernel span over its launches"},
         "gpu_launches": launches,
     }
+    out["optimizer"] = args.optimizer
     out["clocks"] = clocks_summary(rows, t0, t1)
     if rank == 0 and args.headline_only:
         print(json.dumps(out))
+    elif rank == 0 and args.optimizer != "adam":
+        raise SystemExit("--optimizer other than adam needs --headline-only")
     elif rank == 0:
         # stages 0 and 1 on the same workload (reported, not the headline).
         # Stages 0/1 overwrite each rank's gradient with the all-reduce result,
@@ -540,6 +552,8 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6],
                     help="workload: 2 (default) the headline; 1, 3, 4, 5 the others (bench_workloads.py)")
     ap.add_argument("--ranks", type=int, default=None, help="--config 5: N_d of a single sweep point")
+    ap.add_argument("--optimizer", default="adam", choices=sorted(OPTIMIZERS),
+                    help="optimizer of the headline step (with --headline-only)")
     ap.add_argument("--dtype", default=None, choices=["fp16", "bf16"], help="--config 5: dtype of a single point")
     ap.add_argument("--headline-only", action="store_true",
                     help="time the stage-2 step only (no stage 0/1, end-to-end or CPU legs)")

@@ -42,7 +42,8 @@
  *                 reduced gradient (the all-reduce result).
  *     params16[r] 16-bit parameters: the full vector (padded elements) in
  *                 stages 0-2; only rank r's shard (P elements) in stage 3.
- *   fp32 state w, m, v: state_elems floats each.  Stages 1-3: the N shards
+ *   fp32 state w, m, v: state_elems floats each (the arrays the optimizer
+ *   uses; see zero_optimizer_t).  Stages 1-3: the N shards
  *   concatenated, i.e. flat index order (padded elements).  Stage 0: N full
  *   replicas, replica r at offset r*padded.  Two copies of each may be given:
  *   [cur] holds the current state; [1-cur] is the shadow that a fused step
@@ -109,7 +110,13 @@ typedef enum {
 
 typedef enum { ZERO_FP16 = 0, ZERO_BF16 = 1 } zero_dtype_t;
 
-/* Job description.  48 bytes. */
+/* Optimizer on the fp32 master weights ("ZeRO visual reading", accounting
+ * with b and K: mixed-precision Adam K = 12, SGD with momentum K = 8, SGD
+ * K = 4, each counting the 4-byte fp32 master copy).  State arrays used:
+ * Adam w, m, v; SGD with momentum w, m; SGD w (the others may be NULL). */
+typedef enum { ZERO_ADAM = 0, ZERO_SGD_MOMENTUM = 1, ZERO_SGD = 2 } zero_optimizer_t;
+
+/* Job description.  56 bytes. */
 typedef struct zero_config {
     int64_t n_params;            /* Psi >= 0 */
     int64_t bucket_elems;        /* B > 0, multiple of 8 (gradient bucket, C_B) */
@@ -119,6 +126,8 @@ typedef struct zero_config {
     int32_t stage;               /* ZeRO-DP stage 0..3 */
     int32_t n_ranks;             /* N_d, 1..64 */
     int32_t dtype;               /* zero_dtype_t of parameters and gradients */
+    int32_t optimizer;           /* zero_optimizer_t (0: Adam) */
+    int32_t reserved;            /* 0 */
 } zero_config_t;
 
 /* Partition and sizes derived from a config by zero_plan.  128 bytes. */
@@ -137,15 +146,18 @@ typedef struct zero_plan {
     int64_t hbm_bytes_two_pass;  /* algorithmic HBM bytes of one two-pass step */
     int64_t comm_counted_bytes;  /* bytes crossing simulated rank boundaries per step, all ranks */
     double comm_paper_bytes;     /* per rank per step: 2*Psi*2 (stages 0-2), 3*Psi*2 (stage 3) */
-    double mem_total_bytes;      /* per rank, paper formula (b = 2, K = 12), see zero_model_state_bytes */
+    double mem_total_bytes;      /* per rank, paper formula (b = 2, K of the optimizer), see zero_model_state_bytes */
     double reserved;
 } zero_plan_t;
 
-/* Adam hyper-parameters (Kingma & Ba): 24 bytes. */
+/* Optimizer hyper-parameters.  Adam (Kingma & Ba, Algorithm 1) uses lr,
+ * beta1, beta2, eps; SGD with momentum (PyTorch's rule without dampening:
+ * m' = momentum*m + g, w' = w - lr*m') uses lr and momentum; SGD
+ * (w' = w - lr*g) uses lr.  24 bytes. */
 typedef struct zero_adam {
     float lr, beta1, beta2, eps;
     float max_grad_norm;         /* > 0: clip the global L2 norm of the unscaled gradient; <= 0: off */
-    int32_t reserved;
+    float momentum;              /* SGD with momentum only */
 } zero_adam_t;
 
 /* Host-side step state, read and updated by a step.  32 bytes. */

@@ -44,15 +44,24 @@ def max_rel(a: np.ndarray, b: np.ndarray) -> float:
 class Job:
     """One simulated ZeRO job on the GPU plus the oracle's unpartitioned copy."""
 
+    OPT_NAMES = {zg.ZERO_ADAM: "adam", zg.ZERO_SGD_MOMENTUM: "sgdm", zg.ZERO_SGD: "sgd"}
+
     def __init__(self, n, N, stage, B, A=0, layers=None, dtype=oracle.FP16, shadow=True, seed=0,
-                 loss_scale=1.0, dynamic=False, min_scale=1.0, growth=0, max_norm=0.0, sigma=1e-3, adam=None):
+                 loss_scale=1.0, dynamic=False, min_scale=1.0, growth=0, max_norm=0.0, sigma=1e-3, adam=None,
+                 optimizer=zg.ZERO_ADAM, momentum=0.9):
         self.n, self.N, self.stage, self.dtype = n, N, stage, dtype
         self.seed, self.sigma = seed, sigma
-        self.cfg = zg.Config(n, N, stage, B, A, layers, dtype)
+        self.optimizer, self.momentum = optimizer, momentum
+        self.cfg = zg.Config(n, N, stage, B, A, layers, dtype, optimizer)
         self.plan = zg.zero_plan(self.cfg)
         self.bufs = zg.DeviceBuffers(self.cfg, self.plan, device="cuda", shadow=shadow)
+        if optimizer != zg.ZERO_ADAM:          # arrays the optimizer does not use are not handed over
+            for k in range(2):
+                self.bufs.b.v[k] = None
+                if optimizer == zg.ZERO_SGD:
+                    self.bufs.b.m[k] = None
         self.hp = dict(ADAM if adam is None else adam)
-        self.adam = zg.zero_adam_t(max_grad_norm=max_norm, **self.hp)
+        self.adam = zg.zero_adam_t(max_grad_norm=max_norm, momentum=momentum, **self.hp)
         self.max_norm = max_norm
         self.state = zg.zero_state_t(t=0, loss_scale=loss_scale, min_loss_scale=min_scale, dynamic=int(dynamic),
                                      growth_interval=growth)
@@ -109,7 +118,7 @@ class Job:
         ref = oracle.step(grads, self.w, self.m, self.v, dtype=self.dtype, t=self.o["t"],
                           loss_scale=self.o["loss_scale"], max_grad_norm=self.max_norm, dynamic=self.dynamic,
                           min_scale=self.min_scale, growth_interval=self.growth, good_steps=self.o["good_steps"],
-                          **self.hp)
+                          optimizer=self.OPT_NAMES[self.optimizer], momentum=self.momentum, **self.hp)
         self.o.update(t=ref["t"], loss_scale=ref["loss_scale"], good_steps=ref["good_steps"])
         self.p16 = ref["p16"]
         self.h = ref["h"]

@@ -65,6 +65,13 @@ def test_plan_matches_oracle(n, N, stage, B, A, layers):
     assert p.param16_elems == (o["shard"] if stage == 3 else o["padded"])
     assert p.hbm_bytes_fused == oracle.hbm_bytes_per_param(N, stage, "fused") * n
     assert p.hbm_bytes_two_pass == oracle.hbm_bytes_per_param(N, stage, "two_pass") * n
+    for opt, name in ((zg.ZERO_SGD_MOMENTUM, "sgdm"), (zg.ZERO_SGD, "sgd")):
+        q = zg.zero_plan(zg.Config(n, N, stage, B, A, layers, zg.ZERO_FP16, opt))
+        K = oracle.OPTIM_K[name]
+        assert q.hbm_bytes_fused == oracle.hbm_bytes_per_param(N, stage, "fused", K) * n
+        assert q.hbm_bytes_two_pass == oracle.hbm_bytes_per_param(N, stage, "two_pass", K) * n
+        exact = oracle.model_state_bytes(n, N, stage, K=K)["total"]
+        assert abs(Fraction(q.mem_total_bytes) - exact) <= exact * Fraction(1, 10 ** 15)
     c = oracle.comm_bytes(n, N, stage)
     assert p.comm_counted_bytes == c["counted"] and Fraction(p.comm_paper_bytes) == c["paper"]
     # a double: exact when N is a power of two, else within a few ulps
@@ -121,9 +128,10 @@ def test_examples_and_comm_through_the_library():
     (dict(align_elems=6), zg.ZERO_EINVAL),
     (dict(n_params=-1), zg.ZERO_EINVAL),
     (dict(dtype=2), zg.ZERO_EINVAL),
+    (dict(optimizer=3), zg.ZERO_EINVAL),
 ])
 def test_config_rejected(kw, status):
-    base = dict(n_params=1000, n_ranks=4, stage=2, bucket_elems=64, align_elems=0, dtype=0)
+    base = dict(n_params=1000, n_ranks=4, stage=2, bucket_elems=64, align_elems=0, dtype=0, optimizer=0)
     base.update(kw)
     cfg = zg.zero_config_t(**base)
     with pytest.raises(zg.ZeroError) as e:

@@ -372,3 +372,29 @@ def test_optimizer_state_in_pinned_host_memory(shadow):
     for t in (1, 2, 3):
         res, ref = job.step(job.make_grads(t))
         job.check(res, ref)
+
+
+@pytest.mark.parametrize("optimizer", [zg.ZERO_SGD_MOMENTUM, zg.ZERO_SGD])
+@pytest.mark.parametrize("stage", [0, 1, 2, 3])
+@pytest.mark.parametrize("shadow,max_norm", [(True, 0.0), (False, 0.0), (False, 1.0)])
+def test_sgd_variants(optimizer, stage, shadow, max_norm):
+    """SGD with momentum and plain SGD in the same kernels: fused and
+    two-pass paths, with and without clipping, three steps (the unused state
+    arrays are not handed to the library)."""
+    n = 3 * 4096 + 29
+    job = Job(n, 3, stage, 4096, 16, shadow=shadow, max_norm=max_norm, sigma=0.05, loss_scale=8.0,
+              optimizer=optimizer, momentum=0.9, adam=dict(lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-8))
+    for t in (1, 2, 3):
+        res, ref = job.step(job.make_grads(t))
+        job.check(res, ref)
+
+
+def test_sgd_overflow_skips():
+    n = 2 * 2048 + 5
+    job = Job(n, 2, 2, 2048, 8, optimizer=zg.ZERO_SGD_MOMENTUM, loss_scale=64.0, dynamic=True,
+              adam=dict(lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-8))
+    res, ref = job.step(job.make_grads(1))
+    job.check(res, ref)
+    res, ref = job.step(job.make_grads(2, inject=[(1, 100, 0x7C00)]))
+    assert res.skipped == 1
+    job.check(res, ref)

@@ -20,7 +20,7 @@ from . import build as _build
 
 __all__ = [
     "ZERO_OK", "ZERO_EINVAL", "ZERO_EALIGN", "ZERO_ENOMEM", "ZERO_ECUDA", "ZERO_ETIMEOUT", "ZERO_EUNSUPPORTED",
-    "ZERO_FP16", "ZERO_BF16", "ZeroError", "zero_config_t", "zero_plan_t", "zero_adam_t", "zero_state_t",
+    "ZERO_FP16", "ZERO_BF16", "ZERO_ADAM", "ZERO_SGD_MOMENTUM", "ZERO_SGD", "ZeroError", "zero_config_t", "zero_plan_t", "zero_adam_t", "zero_state_t",
     "zero_buffers_t", "zero_step_result_t", "Config", "lib", "lib_path",
     "zero_plan", "zero_plan_bucket", "zero_plan_layer", "zero_model_state_bytes", "zero_comm_bytes",
     "zero_step", "zero_step_stage0", "zero_step_stage1", "zero_step_stage2", "zero_step_stage3",
@@ -31,6 +31,7 @@ __all__ = [
 
 ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ENOMEM, ZERO_ECUDA, ZERO_ETIMEOUT, ZERO_EUNSUPPORTED = range(7)
 ZERO_FP16, ZERO_BF16 = 0, 1
+ZERO_ADAM, ZERO_SGD_MOMENTUM, ZERO_SGD = 0, 1, 2
 
 c_i64, c_i32, c_u32, c_f, c_d, c_vp = (ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_float,
                                        ctypes.c_double, ctypes.c_void_p)
@@ -39,7 +40,7 @@ c_i64, c_i32, c_u32, c_f, c_d, c_vp = (ctypes.c_int64, ctypes.c_int32, ctypes.c_
 class zero_config_t(ctypes.Structure):
     _fields_ = [("n_params", c_i64), ("bucket_elems", c_i64), ("align_elems", c_i64),
                 ("layer_sizes", ctypes.POINTER(c_i64)), ("n_layers", c_i32), ("stage", c_i32),
-                ("n_ranks", c_i32), ("dtype", c_i32)]
+                ("n_ranks", c_i32), ("dtype", c_i32), ("optimizer", c_i32), ("reserved", c_i32)]
 
 
 class zero_plan_t(ctypes.Structure):
@@ -52,7 +53,7 @@ class zero_plan_t(ctypes.Structure):
 
 class zero_adam_t(ctypes.Structure):
     _fields_ = [("lr", c_f), ("beta1", c_f), ("beta2", c_f), ("eps", c_f), ("max_grad_norm", c_f),
-                ("reserved", c_i32)]
+                ("momentum", c_f)]
 
 
 class zero_state_t(ctypes.Structure):
@@ -155,10 +156,10 @@ class Config:
     """A zero_config_t that keeps its layer-size array alive."""
 
     def __init__(self, n_params: int, n_ranks: int, stage: int, bucket_elems: int, align_elems: int = 0,
-                 layer_sizes=None, dtype: int = ZERO_FP16):
+                 layer_sizes=None, dtype: int = ZERO_FP16, optimizer: int = ZERO_ADAM):
         self._layers = None
         self.c = zero_config_t(n_params=n_params, bucket_elems=bucket_elems, align_elems=align_elems,
-                               n_layers=0, stage=stage, n_ranks=n_ranks, dtype=dtype)
+                               n_layers=0, stage=stage, n_ranks=n_ranks, dtype=dtype, optimizer=optimizer)
         if layer_sizes is not None:
             self._layers = (c_i64 * len(layer_sizes))(*[int(x) for x in layer_sizes])
             self.c.layer_sizes = ctypes.cast(self._layers, ctypes.POINTER(c_i64))

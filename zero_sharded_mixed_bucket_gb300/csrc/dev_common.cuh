@@ -175,6 +175,57 @@ __device__ __forceinline__ void adam1(float g, float& w, float& m, float& v, con
     v = v1;
 }
 
+// SGD with momentum (PyTorch's rule, no dampening): m' = mu*m + g; w' = w - lr*m'.
+__device__ __forceinline__ void sgdm1(float g, float& w, float& m, const AdamHP& hp)
+{
+    const float t1 = __fmul_rn(hp.mu, m);
+    const float m1 = __fadd_rn(t1, g);
+    const float st = __fmul_rn(hp.lr, m1);
+    w = __fsub_rn(w, st);
+    m = m1;
+}
+
+// Plain SGD: w' = w - lr*g.
+__device__ __forceinline__ void sgd1(float g, float& w, const AdamHP& hp)
+{
+    w = __fsub_rn(w, __fmul_rn(hp.lr, g));
+}
+
+// The optimizer update of one group: load the fp32 state the optimizer keeps
+// at state index si (w; m; v), update it with the 8 unscaled gradients g,
+// store it to the output state and give back the 16-bit cast in p.
+template <int DT, int OPT>
+__device__ __forceinline__ void update_state(const StepArgs& a, int64_t si, int cnt, const float g[kVec], H8& p)
+{
+    float w[kVec];
+    ld_f8(a.w_in, si, cnt, w);
+    if constexpr (OPT == kAdam) {
+        float m[kVec], v[kVec];
+        ld_f8(a.m_in, si, cnt, m);
+        ld_f8(a.v_in, si, cnt, v);
+#pragma unroll
+        for (int j = 0; j < kVec; j++)
+            adam1(g[j], w[j], m[j], v[j], a.hp);
+        st_f8(a.m_out, si, cnt, m);
+        st_f8(a.v_out, si, cnt, v);
+    } else if constexpr (OPT == kSgdm) {
+        float m[kVec];
+        ld_f8(a.m_in, si, cnt, m);
+#pragma unroll
+        for (int j = 0; j < kVec; j++)
+            sgdm1(g[j], w[j], m[j], a.hp);
+        st_f8(a.m_out, si, cnt, m);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kVec; j++)
+            sgd1(g[j], w[j], a.hp);
+    }
+#pragma unroll
+    for (int j = 0; j < kVec; j++)
+        p.set(j, from_f32<DT>(w[j]));
+    st_f8(a.w_out, si, cnt, w);
+}
+
 // ---- exact sum of squares --------------------------------------------------
 // A finite 16-bit value is h = M * 2^E with integer M (< 2^11 binary16,
 // < 2^8 bfloat16), so h^2 = M^2 * 2^(2E) exactly.  Terms with

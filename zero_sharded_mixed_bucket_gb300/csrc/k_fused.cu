@@ -18,24 +18,7 @@ namespace zg {
 
 namespace {
 
-template <int DT>
-__device__ __forceinline__ void update_group(const StepArgs& a, int64_t si, int cnt, const float g[kVec], H8& p)
-{
-    float w[kVec], m[kVec], v[kVec];
-    ld_f8(a.w_in, si, cnt, w);
-    ld_f8(a.m_in, si, cnt, m);
-    ld_f8(a.v_in, si, cnt, v);
-#pragma unroll
-    for (int j = 0; j < kVec; j++) {
-        adam1(g[j], w[j], m[j], v[j], a.hp);
-        p.set(j, from_f32<DT>(w[j]));
-    }
-    st_f8(a.w_out, si, cnt, w);
-    st_f8(a.m_out, si, cnt, m);
-    st_f8(a.v_out, si, cnt, v);
-}
-
-template <int STAGE, int DT>
+template <int STAGE, int DT, int OPT>
 __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ StepArgs a)
 {
     allow_next_grid();
@@ -68,12 +51,12 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ Step
         if constexpr (STAGE == 0) {
             for (int r = 0; r < a.n_ranks; r++) {
                 H8 p;
-                update_group<DT>(a, (int64_t)r * a.replica_stride + i, cnt, g, p);
+                update_state<DT, OPT>(a, (int64_t)r * a.replica_stride + i, cnt, g, p);
                 st_h8(a.params16[r], i, p, cnt);
             }
         } else {
             H8 p;
-            update_group<DT>(a, i, cnt, g, p);
+            update_state<DT, OPT>(a, i, cnt, g, p);
             if constexpr (STAGE == 3) {
                 const int o = owner_of(i, a.shard);
                 st_h8(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
@@ -119,13 +102,23 @@ __global__ void __launch_bounds__(kThreads) k_restore(const __grid_constant__ St
     }
 }
 
-template <int STAGE, int DT>
-cudaError_t run_fused(const StepArgs& a, cudaStream_t s, bool overlap)
+template <int STAGE, int DT, int OPT>
+cudaError_t run_fused3(const StepArgs& a, cudaStream_t s, bool overlap)
 {
     const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
     if (groups <= 0) return cudaSuccess;
-    const int grid = grid_for((const void*)k_fused<STAGE, DT>, groups);
-    return launch_step_kernel(k_fused<STAGE, DT>, grid, s, overlap, a);
+    const int grid = grid_for((const void*)k_fused<STAGE, DT, OPT>, groups);
+    return launch_step_kernel(k_fused<STAGE, DT, OPT>, grid, s, overlap, a);
+}
+
+template <int STAGE, int DT>
+cudaError_t run_fused(int opt, const StepArgs& a, cudaStream_t s, bool overlap)
+{
+    switch (opt) {
+    case kSgdm: return run_fused3<STAGE, DT, kSgdm>(a, s, overlap);
+    case kSgd: return run_fused3<STAGE, DT, kSgd>(a, s, overlap);
+    default: return run_fused3<STAGE, DT, kAdam>(a, s, overlap);
+    }
 }
 
 template <int STAGE, int DT>
@@ -159,9 +152,9 @@ cudaError_t run_restore(const StepArgs& a, cudaStream_t s)
         }                                                                             \
     } while (0)
 
-cudaError_t launch_fused(int stage, int dtype, const StepArgs& a, cudaStream_t s, bool overlap)
+cudaError_t launch_fused(int stage, int dtype, int opt, const StepArgs& a, cudaStream_t s, bool overlap)
 {
-    ZG_DISPATCH_STAGE_DT(run_fused, stage, dtype, a, s, overlap);
+    ZG_DISPATCH_STAGE_DT(run_fused, stage, dtype, opt, a, s, overlap);
 }
 
 cudaError_t launch_restore(int stage, int dtype, const StepArgs& a, cudaStream_t s)

@@ -6,8 +6,7 @@
 //                                   the owner's reduced shard in stages 2/3),
 //                                   exact integer sum of squares.
 //   once                k_finalize: exact sum -> fp64 -> ||g||, clip coefficient.
-//   pass 2, per bucket  k_update:   Adam in place (skipped if the flag is set),
-//                                   16-bit cast, all-gather.
+//   pass 2, per bucket  k_update:   optimizer update in place (k_update.cu).
 #include "dev_common.cuh"
 
 namespace zg {
@@ -52,71 +51,6 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Ste
         atomicOr(ws_flag(a.ws), 1u);
     if constexpr (CLIP)
         sumsq_flush(acc, ws_acc(a.ws));
-    wait_prev_grid();
-}
-
-template <int DT>
-__device__ __forceinline__ void update_inplace(const StepArgs& a, int64_t si, int cnt, const H8& h, float c, H8& p)
-{
-    float w[kVec], m[kVec], v[kVec];
-    ld_f8(a.w_in, si, cnt, w);
-    ld_f8(a.m_in, si, cnt, m);
-    ld_f8(a.v_in, si, cnt, v);
-#pragma unroll
-    for (int j = 0; j < kVec; j++) {
-        float g = __fmul_rn(to_f32<DT>(h.get(j)), a.inv);
-        if (c != 1.0f) g = __fmul_rn(g, c);
-        adam1(g, w[j], m[j], v[j], a.hp);
-        p.set(j, from_f32<DT>(w[j]));
-    }
-    st_f8(a.w_out, si, cnt, w);
-    st_f8(a.m_out, si, cnt, m);
-    st_f8(a.v_out, si, cnt, v);
-}
-
-template <int STAGE, int DT, bool CLIP>
-__global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ StepArgs a)
-{
-    // The first update kernel of a step is launched in plain stream order after
-    // the pass-1 kernels and the finalize, so the flag and the clip
-    // coefficient are final before any update kernel starts.
-    allow_next_grid();
-    if (*reinterpret_cast<volatile uint32_t*>(ws_flag(a.ws))) {
-        wait_prev_grid();
-        return;   // overflow: the whole step is skipped
-    }
-    // With clipping on, multiply by c only when c < 1: g * 1 == g for every
-    // finite g, so both forms give the same bits.
-    const float c = CLIP ? *reinterpret_cast<const float*>(a.ws + ws::kClip) : 1.0f;
-    const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
-    for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
-         gi += (int64_t)gridDim.x * kThreads) {
-        const int64_t i = a.lo + gi * kVec;
-        const int cnt = (int)min((int64_t)kVec, a.hi - i);
-        if constexpr (STAGE == 0) {
-            for (int r = 0; r < a.n_ranks; r++) {
-                const H8 h = ld_h8(a.grads[r], i - a.grad_base, cnt);
-                H8 p;
-                update_inplace<DT>(a, (int64_t)r * a.replica_stride + i, cnt, h, c, p);
-                st_h8(a.params16[r], i, p, cnt);
-            }
-        } else {
-            H8 h;
-            if constexpr (STAGE == 1)
-                h = ld_h8(a.grads[owner_of(i, a.shard)], i - a.grad_base, cnt);
-            else
-                h = ld_h8(a.reduced, i, cnt);
-            H8 p;
-            update_inplace<DT>(a, i, cnt, h, c, p);
-            if constexpr (STAGE == 3) {
-                const int o = owner_of(i, a.shard);
-                st_h8(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
-            } else {
-                for (int r = 0; r < a.n_ranks; r++)
-                    st_h8(a.params16[r], i, p, cnt);
-            }
-        }
-    }
     wait_prev_grid();
 }
 
@@ -217,30 +151,10 @@ cudaError_t run_reduce(const StepArgs& a, cudaStream_t s, bool overlap)
     return launch_step_kernel(k_reduce<HDEST, DT, CLIP>, grid, s, overlap, a);
 }
 
-template <int STAGE, int DT, bool CLIP>
-cudaError_t run_update(const StepArgs& a, cudaStream_t s, bool overlap)
-{
-    const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
-    if (groups <= 0) return cudaSuccess;
-    const int grid = grid_for((const void*)k_update<STAGE, DT, CLIP>, groups);
-    return launch_step_kernel(k_update<STAGE, DT, CLIP>, grid, s, overlap, a);
-}
-
 template <int DT, bool CLIP>
 cudaError_t reduce_dt(int stage, const StepArgs& a, cudaStream_t s, bool overlap)
 {
     return stage <= 1 ? run_reduce<0, DT, CLIP>(a, s, overlap) : run_reduce<1, DT, CLIP>(a, s, overlap);
-}
-
-template <int DT, bool CLIP>
-cudaError_t update_dt(int stage, const StepArgs& a, cudaStream_t s, bool overlap)
-{
-    switch (stage) {
-    case 0: return run_update<0, DT, CLIP>(a, s, overlap);
-    case 1: return run_update<1, DT, CLIP>(a, s, overlap);
-    case 2: return run_update<2, DT, CLIP>(a, s, overlap);
-    default: return run_update<3, DT, CLIP>(a, s, overlap);
-    }
 }
 
 }  // namespace
@@ -250,13 +164,6 @@ cudaError_t launch_reduce(int stage, int dtype, bool clip, const StepArgs& a, cu
     if (dtype == kBF16)
         return clip ? reduce_dt<kBF16, true>(stage, a, s, overlap) : reduce_dt<kBF16, false>(stage, a, s, overlap);
     return clip ? reduce_dt<kF16, true>(stage, a, s, overlap) : reduce_dt<kF16, false>(stage, a, s, overlap);
-}
-
-cudaError_t launch_update(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s, bool overlap)
-{
-    if (dtype == kBF16)
-        return clip ? update_dt<kBF16, true>(stage, a, s, overlap) : update_dt<kBF16, false>(stage, a, s, overlap);
-    return clip ? update_dt<kF16, true>(stage, a, s, overlap) : update_dt<kF16, false>(stage, a, s, overlap);
 }
 
 cudaError_t launch_finalize(const FinalArgs& a, cudaStream_t s)

@@ -36,22 +36,26 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Algorithmic HBM bytes per parameter (16-bit values 2 bytes, fp32 4 bytes).
-int64_t bytes_per_param(int stage, int64_t N, bool fused)
+// fp32 state bytes per parameter the optimizer keeps (w, m, v / w, m / w).
+int64_t state_bytes(int optimizer) { return optimizer == ZERO_SGD ? 4 : (optimizer == ZERO_SGD_MOMENTUM ? 8 : 12); }
+
+// Algorithmic HBM bytes per parameter (16-bit values 2 bytes, fp32 state sb
+// bytes, read once and written once).
+int64_t bytes_per_param(int stage, int64_t N, bool fused, int64_t sb)
 {
     if (fused) {
         switch (stage) {
-        case 0: return 30 * N;           // N grads + N write-backs + N x (w,m,v r/w + param)
-        case 1: return 24 + 6 * N;       // N grads + N write-backs + state + N params
-        case 2: return 24 + 4 * N;       // N grads + state + N params
-        default: return 26 + 2 * N;      // N grads + state + owner's param
+        case 0: return N * (6 + 2 * sb);    // N grads + N write-backs + N x (state r/w + param)
+        case 1: return 6 * N + 2 * sb;      // N grads + N write-backs + state + N params
+        case 2: return 4 * N + 2 * sb;      // N grads + state + N params
+        default: return 2 * N + 2 * sb + 2; // N grads + state + owner's param
         }
     }
     switch (stage) {
-    case 0: return 32 * N;               // pass 1: 4N; pass 2: N x (h + state + param)
-    case 1: return 26 + 6 * N;           // pass 1: 4N; pass 2: h + state + N params
-    case 2: return 28 + 4 * N;           // pass 1: 2N + h; pass 2: h + state + N params
-    default: return 30 + 2 * N;          // pass 1: 2N + h; pass 2: h + state + param
+    case 0: return N * (8 + 2 * sb);        // pass 1: 4N; pass 2: N x (h + state + param)
+    case 1: return 6 * N + 2 + 2 * sb;      // pass 1: 4N; pass 2: h + state + N params
+    case 2: return 4 * N + 4 + 2 * sb;      // pass 1: 2N + h; pass 2: h + state + N params
+    default: return 2 * N + 6 + 2 * sb;     // pass 1: 2N + h; pass 2: h + state + param
     }
 }
 
@@ -71,6 +75,8 @@ zero_status_t check_config(const zero_config_t* c)
     if (c->align_elems < 0 || c->align_elems % kVec)
         return fail(ZERO_EINVAL, "align_elems %lld must be 0 or a positive multiple of 8", (long long)c->align_elems);
     if (c->dtype != ZERO_FP16 && c->dtype != ZERO_BF16) return fail(ZERO_EINVAL, "dtype %d unknown", c->dtype);
+    if (c->optimizer < ZERO_ADAM || c->optimizer > ZERO_SGD)
+        return fail(ZERO_EINVAL, "optimizer %d unknown", c->optimizer);
     if (c->layer_sizes) {
         if (c->n_layers <= 0) return fail(ZERO_EINVAL, "layer_sizes given with n_layers %d", c->n_layers);
         int64_t sum = 0;
@@ -123,12 +129,13 @@ void make_plan(const zero_config_t* c, zero_plan_t* p)
     p->grad16_elems = p->padded_elems;
     p->reduced_elems = c->stage >= 2 ? p->padded_elems : 0;
     p->workspace_bytes = ws::kBytes;
-    p->hbm_bytes_fused = bytes_per_param(c->stage, N, true) * psi;
-    p->hbm_bytes_two_pass = bytes_per_param(c->stage, N, false) * psi;
+    const int64_t sb = state_bytes(c->optimizer);
+    p->hbm_bytes_fused = bytes_per_param(c->stage, N, true, sb) * psi;
+    p->hbm_bytes_two_pass = bytes_per_param(c->stage, N, false, sb) * psi;
     p->comm_counted_bytes = (int64_t)kCollectivePasses[c->stage] * (N - 1) * psi * 2;
     p->comm_paper_bytes = (c->stage == 3 ? 3.0 : 2.0) * (double)psi * 2.0;
     double m[4];
-    model_state(psi, c->n_ranks, c->stage, 2, 12, m);
+    model_state(psi, c->n_ranks, c->stage, 2, (int32_t)sb, m);
     p->mem_total_bytes = m[3];
 }
 
@@ -138,12 +145,18 @@ struct Path {
     bool fused;
 };
 
-Path choose_path(const zero_buffers_t* b, const zero_adam_t* adam)
+// Number of fp32 state arrays the optimizer uses: w; w, m; w, m, v.
+int state_arrays(int optimizer) { return optimizer == ZERO_SGD ? 1 : (optimizer == ZERO_SGD_MOMENTUM ? 2 : 3); }
+
+Path choose_path(const zero_config_t* c, const zero_buffers_t* b, const zero_adam_t* adam)
 {
     const int sh = 1 - b->cur;
+    const float* shadow[3] = {b->w[sh], b->m[sh], b->v[sh]};
     Path p;
     p.clip = adam->max_grad_norm > 0.0f;
-    p.fused = !p.clip && b->w[sh] && b->m[sh] && b->v[sh];
+    p.fused = !p.clip;
+    for (int k = 0; k < state_arrays(c->optimizer); k++)
+        p.fused = p.fused && shadow[k] != nullptr;
     return p;
 }
 
@@ -166,9 +179,14 @@ zero_status_t check_step(const zero_config_t* c, const zero_plan_t* plan, const 
     if (st != ZERO_OK) return st;
     if (!b || !adam || !s) return fail(ZERO_EINVAL, "buffers, adam and state must not be NULL");
     if (b->cur != 0 && b->cur != 1) return fail(ZERO_EINVAL, "cur is %d, not 0 or 1", b->cur);
-    if (!(std::isfinite(adam->lr) && adam->beta1 >= 0.0f && adam->beta1 < 1.0f && adam->beta2 >= 0.0f &&
-          adam->beta2 < 1.0f && std::isfinite(adam->eps) && adam->eps >= 0.0f && std::isfinite(adam->max_grad_norm)))
+    if (!(std::isfinite(adam->lr) && std::isfinite(adam->max_grad_norm)))
+        return fail(ZERO_EINVAL, "learning rate and max_grad_norm must be finite");
+    if (c->optimizer == ZERO_ADAM &&
+        !(adam->beta1 >= 0.0f && adam->beta1 < 1.0f && adam->beta2 >= 0.0f && adam->beta2 < 1.0f &&
+          std::isfinite(adam->eps) && adam->eps >= 0.0f))
         return fail(ZERO_EINVAL, "Adam hyper-parameters out of range");
+    if (c->optimizer == ZERO_SGD_MOMENTUM && !(std::isfinite(adam->momentum) && adam->momentum >= 0.0f))
+        return fail(ZERO_EINVAL, "momentum must be finite and non-negative");
     if (!(std::isfinite(s->loss_scale) && s->loss_scale > 0.0f))
         return fail(ZERO_EINVAL, "loss_scale must be positive and finite");
     if (s->dynamic && !(std::isfinite(s->min_loss_scale) && s->min_loss_scale > 0.0f))
@@ -182,7 +200,7 @@ zero_status_t check_step(const zero_config_t* c, const zero_plan_t* plan, const 
     }
     const int cur = b->cur, sh = 1 - b->cur;
     const float* need[3] = {b->w[cur], b->m[cur], b->v[cur]};
-    for (int k = 0; k < 3; k++) {
+    for (int k = 0; k < state_arrays(c->optimizer); k++) {
         if (!need[k]) return fail(ZERO_ENOMEM, "current fp32 state buffer %d is NULL", k);
         if (!aligned16(need[k])) return fail(ZERO_EALIGN, "current fp32 state buffer %d is not 16-byte aligned", k);
     }
@@ -192,7 +210,7 @@ zero_status_t check_step(const zero_config_t* c, const zero_plan_t* plan, const 
             return fail(ZERO_EALIGN, "shadow fp32 state buffer %d is not 16-byte aligned", k);
     if (!b->workspace) return fail(ZERO_ENOMEM, "workspace is NULL");
     if (!aligned16(b->workspace)) return fail(ZERO_EALIGN, "workspace is not 16-byte aligned");
-    const Path path = choose_path(b, adam);
+    const Path path = choose_path(c, b, adam);
     if (!path.fused && c->stage >= 2) {
         if (!b->reduced) return fail(ZERO_ENOMEM, "the two-pass path needs the reduced-gradient buffer");
         if (!aligned16(b->reduced)) return fail(ZERO_EALIGN, "reduced is not 16-byte aligned");
@@ -268,8 +286,11 @@ StepArgs make_args(const zero_config_t* c, const zero_plan_t* p, const zero_buff
     a.hp.b2 = adam->beta2;
     a.hp.omb2 = 1.0f - adam->beta2;
     a.hp.eps = adam->eps;
-    a.hp.bc1 = bias_correction(adam->beta1, s->t + 1);
-    a.hp.bc2 = bias_correction(adam->beta2, s->t + 1);
+    if (c->optimizer == ZERO_ADAM) {
+        a.hp.bc1 = bias_correction(adam->beta1, s->t + 1);
+        a.hp.bc2 = bias_correction(adam->beta2, s->t + 1);
+    }
+    a.hp.mu = adam->momentum;
     a.win_lo = window_lo(c->dtype, s->loss_scale, N);
     return a;
 }
@@ -289,14 +310,14 @@ zero_status_t bucket_impl(const zero_config_t* c, const zero_plan_t* p, const ze
                           const zero_adam_t* adam, const zero_state_t* s, int64_t bucket, void* const* bucket_grads,
                           cudaStream_t st, bool overlap)
 {
-    const Path path = choose_path(b, adam);
+    const Path path = choose_path(c, b, adam);
     const int64_t lo = bucket * c->bucket_elems;
     const int64_t hi = lo + c->bucket_elems < c->n_params ? lo + c->bucket_elems : c->n_params;
     StepArgs a = bucket_grads ? make_args(c, p, b, adam, s, path.fused, bucket_grads, lo)
                               : make_args(c, p, b, adam, s, path.fused, b->grads, 0);
     a.lo = lo;
     a.hi = hi;
-    cudaError_t e = path.fused ? launch_fused(c->stage, c->dtype, a, st, overlap)
+    cudaError_t e = path.fused ? launch_fused(c->stage, c->dtype, c->optimizer, a, st, overlap)
                                : launch_reduce(c->stage, c->dtype, path.clip, a, st, overlap);
     if (e != cudaSuccess) return cuda_fail(e, "launching the bucket kernel");
     return ZERO_OK;
@@ -305,7 +326,7 @@ zero_status_t bucket_impl(const zero_config_t* c, const zero_plan_t* p, const ze
 zero_status_t end_impl(const zero_config_t* c, const zero_plan_t* p, zero_buffers_t* b, const zero_adam_t* adam,
                        zero_state_t* s, cudaStream_t st, zero_step_result_t* out)
 {
-    const Path path = choose_path(b, adam);
+    const Path path = choose_path(c, b, adam);
     int launches = (int)p->n_buckets;
     cudaError_t e;
     if (!path.fused) {
@@ -324,7 +345,7 @@ zero_status_t end_impl(const zero_config_t* c, const zero_plan_t* p, zero_buffer
             StepArgs a = make_args(c, p, b, adam, s, false, c->stage <= 1 ? b->grads : nullptr, 0);
             a.lo = bk * c->bucket_elems;
             a.hi = a.lo + c->bucket_elems < c->n_params ? a.lo + c->bucket_elems : c->n_params;
-            e = launch_update(c->stage, c->dtype, path.clip, a, st, bk > 0);
+            e = launch_update(c->stage, c->dtype, c->optimizer, path.clip, a, st, bk > 0);
             if (e != cudaSuccess) return cuda_fail(e, "launching the update kernel");
             launches++;
         }

@@ -23,8 +23,11 @@ constexpr size_t kEnd = kBins + 256 * 8;
 constexpr int64_t kBytes = 4096;
 }  // namespace ws
 
+enum { kAdam = ZERO_ADAM, kSgdm = ZERO_SGD_MOMENTUM, kSgd = ZERO_SGD };
+
 struct AdamHP {
     float lr, b1, omb1, b2, omb2, eps, bc1, bc2;
+    float mu;   // SGD momentum
 };
 
 // Arguments of the per-bucket kernels.  Passed by value as a __grid_constant__
@@ -72,10 +75,11 @@ struct GatherArgs {
 // `overlap`: launch with programmatic dependent launch on the previous kernel
 // of the stream -- only when that kernel is another bucket kernel of the same
 // step pass, launched by the library itself.
-cudaError_t launch_fused(int stage, int dtype, const StepArgs& a, cudaStream_t s, bool overlap);
+cudaError_t launch_fused(int stage, int dtype, int opt, const StepArgs& a, cudaStream_t s, bool overlap);
 cudaError_t launch_reduce(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s, bool overlap);
 cudaError_t launch_finalize(const FinalArgs& a, cudaStream_t s);
-cudaError_t launch_update(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s, bool overlap);
+cudaError_t launch_update(int stage, int dtype, int opt, bool clip, const StepArgs& a, cudaStream_t s,
+                          bool overlap);
 cudaError_t launch_restore(int stage, int dtype, const StepArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
 
