@@ -278,6 +278,45 @@ zero_status_t zero_step_end(const zero_config_t* cfg, const zero_plan_t* plan, z
 zero_status_t zero_gather_layer(const zero_config_t* cfg, const zero_plan_t* plan, int32_t layer,
                                 void* const* param_shards, void* const* dst, int32_t n_dst, void* stream);
 
+/* ---- stage 3: gathers ahead of use under a live-parameter budget ---------
+ * A fetcher gathers the layers of one pass (an order of layers: forward
+ * 0..L-1, backward L-1..0, any sequence) into a caller-owned pool of
+ * `capacity` 16-bit elements per destination, placing them as a ring in
+ * fetch order, so the layers resident at once never exceed the capacity
+ * (DeepSpeed's stage3_max_live_parameters; ZeRO visual reading, stage-3
+ * section: gather the next layers ahead of time, release after use).  Up to
+ * `depth` layers ahead are gathered on `side_stream`; a fetch makes the
+ * caller's stream wait for that layer only; a release makes the side stream
+ * wait before reusing the space.  Protocol, per position pos = 0, 1, ...:
+ * zero_fetch_layer(pos) -> use the layer at *offset in every pool buffer on
+ * `stream` -> zero_release_layer(pos).  The caller keeps `order`, the pool,
+ * the shards and the 2*(depth+1) events (cudaEvent_t, created by the caller)
+ * alive while the fetcher is used; zero_fetcher_t is caller memory holding
+ * the fetcher's state (no allocation).  Layer sizes are rounded up to 8
+ * elements in the pool; capacity must hold the largest layer. */
+#define ZERO_FETCH_MAX_DEPTH 32
+#define ZERO_FETCH_MAX_RESIDENT 128
+typedef struct zero_fetcher { int64_t opaque[1024]; } zero_fetcher_t;   /* 8 KB */
+
+zero_status_t zero_fetcher_init(zero_fetcher_t* f, const zero_config_t* cfg, const zero_plan_t* plan,
+                                void* const* param_shards, void* const* pool, int32_t n_dst, int64_t capacity,
+                                const int32_t* order, int32_t n_order, int32_t depth, void* side_stream,
+                                void* const* events, int32_t n_events);
+/* Make layer order[pos] resident and ordered before later work on `stream`;
+ * *offset receives its element offset in each pool buffer. */
+zero_status_t zero_fetch_layer(zero_fetcher_t* f, int32_t pos, void* stream, int64_t* offset);
+/* Done with order[pos] (after the work already enqueued on `stream`). */
+zero_status_t zero_release_layer(zero_fetcher_t* f, int32_t pos, void* stream);
+/* Largest resident element count reached, gathers issued. */
+zero_status_t zero_fetcher_stats(const zero_fetcher_t* f, int64_t* max_live, int32_t* gathers);
+/* The fetcher's decisions without a GPU: for each position q, issue_at[q] is
+ * the position at whose fetch its gather is issued and offsets[q] its pool
+ * offset; *max_live the largest resident element count.  ZERO_ENOMEM if a
+ * layer cannot fit; ZERO_EINVAL if capacity is below the largest layer. */
+zero_status_t zero_fetch_schedule(const int64_t* layer_sizes, int32_t n_layers, const int32_t* order, int32_t n_order,
+                                  int64_t capacity, int32_t depth, int32_t* issue_at, int64_t* offsets,
+                                  int64_t* max_live);
+
 /* Stage-2 step that allocates nothing and needs no scratch from the caller.
  * The paper has no counterpart: this exists for callers that cannot obtain
  * device memory for the workspace and the reduced-gradient buffer -- code

@@ -398,3 +398,58 @@ def test_sgd_overflow_skips():
     res, ref = job.step(job.make_grads(2, inject=[(1, 100, 0x7C00)]))
     assert res.skipped == 1
     job.check(res, ref)
+
+
+@pytest.mark.parametrize("depth", [0, 2])
+def test_fetcher_prefetch_under_budget_with_step(depth):
+    """Forward and backward passes of layer fetches (side-stream prefetch,
+    live budget below the sum of the layers) around a stage-3 step whose
+    bucket kernels update shards while later layers are being prefetched.
+    Every layer, copied on the main stream when used, must hold the
+    parameters from before the step; the step must match the oracle."""
+    layers = [1001, 4096, 7, 20_000, 3333, 900, 12_000]
+    n, N, B = sum(layers), 4, 2048
+    job = Job(n, N, 3, B, 8, layers=layers, loss_scale=4.0)
+    starts = np.cumsum([0] + layers)
+    p_before = job.p16.copy()
+    cap = 20_008 + 1008                     # the largest layer plus a little: prefetch is budget-limited
+    n_dst = 3
+    pool = [torch.full((cap,), -1, dtype=torch.int16, device="cuda") for _ in range(n_dst)]
+    shards = [t.data_ptr() for t in job.bufs.params16]
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    grads = job.make_grads(1)
+    job.load_grads(grads)
+
+    def run_pass(order, between=None):
+        f = zg.Fetcher(job.cfg, job.plan, shards, pool, cap, order, depth, side)
+        snaps = []
+        for pos, layer in enumerate(order):
+            off = f.fetch(pos, main)
+            snaps.append((layer, [d[off:off + layers[layer]].clone() for d in pool]))
+            if between:
+                between(layer)
+            f.release(pos, main)
+        ml, g = f.stats()
+        assert ml <= cap and g == len(order)
+        return snaps
+
+    fwd = run_pass(list(range(len(layers))))
+    zg.zero_step_begin(job.cfg, job.plan, job.bufs, job.adam, job.state, main)
+    done = [job.plan.n_buckets]
+
+    def buckets_of(layer):                   # buckets whose first element lies in this layer or above
+        while done[0] > 0 and (done[0] - 1) * B >= starts[layer]:
+            zg.zero_step_bucket(job.cfg, job.plan, job.bufs, job.adam, job.state, done[0] - 1, None, main)
+            done[0] -= 1
+
+    bwd = run_pass(list(reversed(range(len(layers)))), between=buckets_of)
+    assert done[0] == 0
+    res = zg.zero_step_end(job.cfg, job.plan, job.bufs, job.adam, job.state, main)
+    torch.cuda.synchronize()
+    for layer, copies in fwd + bwd:
+        for c in copies:
+            assert np.array_equal(as_u16(c), p_before[starts[layer]:starts[layer + 1]]), layer
+    ref = oracle.step(grads, job.w, job.m, job.v, dtype=FP16, t=0, loss_scale=4.0, **job.hp)
+    job.p16, job.h, job.o["t"] = ref["p16"], ref["h"], ref["t"]
+    job.check(res, ref)

@@ -26,7 +26,7 @@ __all__ = [
     "zero_step", "zero_step_stage0", "zero_step_stage1", "zero_step_stage2", "zero_step_stage3",
     "zero_step_stage2_noalloc",
     "zero_step_begin", "zero_step_bucket", "zero_step_end", "zero_gather_layer", "zero_last_error",
-    "zero_version", "zero_set_profile_events", "DeviceBuffers",
+    "zero_version", "zero_set_profile_events", "zero_fetch_schedule", "Fetcher", "DeviceBuffers",
 ]
 
 ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ENOMEM, ZERO_ECUDA, ZERO_ETIMEOUT, ZERO_EUNSUPPORTED = range(7)
@@ -113,6 +113,12 @@ def lib():
             "zero_step_bucket": [cfg, plan, bufs, adam, state, c_i64, P(c_vp), c_vp],
             "zero_step_end": [cfg, plan, bufs, adam, state, c_vp, res],
             "zero_gather_layer": [cfg, plan, c_i32, P(c_vp), P(c_vp), c_i32, c_vp],
+            "zero_fetcher_init": [c_vp, cfg, plan, P(c_vp), P(c_vp), c_i32, c_i64, P(c_i32), c_i32, c_i32, c_vp,
+                                  P(c_vp), c_i32],
+            "zero_fetch_layer": [c_vp, c_i32, c_vp, P(c_i64)],
+            "zero_release_layer": [c_vp, c_i32, c_vp],
+            "zero_fetcher_stats": [c_vp, P(c_i64), P(c_i32)],
+            "zero_fetch_schedule": [P(c_i64), c_i32, P(c_i32), c_i32, c_i64, c_i32, P(c_i32), P(c_i64), P(c_i64)],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -274,6 +280,57 @@ def zero_gather_layer(cfg, plan, layer: int, param_shards, dst, stream=None):
     """param_shards: N device pointers; dst: n_dst device pointers."""
     _check(lib().zero_gather_layer(_cfg(cfg), ctypes.byref(plan), layer, _ptr_array(param_shards),
                                    _ptr_array(dst), len(dst), _stream(stream)))
+
+
+def zero_fetch_schedule(layer_sizes, order, capacity: int, depth: int):
+    """The fetcher's decisions without a GPU: (issue_at, offsets, max_live)."""
+    n, L = len(order), len(layer_sizes)
+    sizes = (c_i64 * L)(*[int(x) for x in layer_sizes])
+    ordr = (c_i32 * n)(*[int(x) for x in order])
+    issue = (c_i32 * n)()
+    offs = (c_i64 * n)()
+    ml = c_i64()
+    _check(lib().zero_fetch_schedule(sizes, L, ordr, n, capacity, depth, issue, offs, ctypes.byref(ml)))
+    return list(issue), list(offs), ml.value
+
+
+class Fetcher:
+    """Stage-3 layer fetches ahead of use under a live-parameter budget (see
+    the header).  pool: n_dst device buffers (int16 tensors) of `capacity`
+    elements; order: layer sequence of one pass; events are created here
+    with torch (the library allocates nothing)."""
+
+    FETCHER_BYTES = 8192
+
+    def __init__(self, cfg, plan, param_shards, pool, capacity: int, order, depth: int, side_stream):
+        import torch
+        self._state = (ctypes.c_byte * self.FETCHER_BYTES)()
+        self._order = (c_i32 * len(order))(*[int(x) for x in order])
+        self._shards = _ptr_array([int(p) for p in param_shards])
+        self._pool = _ptr_array([t.data_ptr() for t in pool])
+        self.pool = pool
+        self.events = [torch.cuda.Event() for _ in range(2 * (depth + 1))]
+        side = torch.cuda.current_stream() if side_stream is None else side_stream
+        for e in self.events:          # materialise the events (the library records them by handle)
+            e.record(side)
+        self._events = _ptr_array([int(e.cuda_event) for e in self.events])
+        self.side = side
+        _check(lib().zero_fetcher_init(ctypes.addressof(self._state), _cfg(cfg), ctypes.byref(plan), self._shards,
+                                       self._pool, len(pool), capacity, self._order, len(order), depth,
+                                       _stream(side), self._events, len(self.events)))
+
+    def fetch(self, pos: int, stream=None) -> int:
+        off = c_i64()
+        _check(lib().zero_fetch_layer(ctypes.addressof(self._state), pos, _stream(stream), ctypes.byref(off)))
+        return off.value
+
+    def release(self, pos: int, stream=None):
+        _check(lib().zero_release_layer(ctypes.addressof(self._state), pos, _stream(stream)))
+
+    def stats(self):
+        ml, g = c_i64(), c_i32()
+        _check(lib().zero_fetcher_stats(ctypes.addressof(self._state), ctypes.byref(ml), ctypes.byref(g)))
+        return ml.value, g.value
 
 
 class DeviceBuffers:
