@@ -192,6 +192,10 @@ def leg_cfg3(args):
 
 # ---------------------------------------------------------------------------
 def leg_cfg4(args):
+    """Stage 3 at 6.65B parameters, N_d = 64.  Two runs: (a) every gather on
+    the step's stream into 64 constant-size buffers of the largest layer;
+    (b) a fetcher prefetching one layer ahead on a side stream into a pool of
+    two largest layers (the live-parameter budget)."""
     import torch
 
     import synth
@@ -205,11 +209,7 @@ def leg_cfg4(args):
     bufs = zg.DeviceBuffers(cfg, plan, device=dev, grads=False, reduced=False)
     S = 1024.0
     synth.dev_normal32(bufs.w[0].data_ptr(), n, 0.02, seed=0, stream=synth.STREAM_WEIGHT, cuda_stream=s.cuda_stream)
-    # the 16-bit shards start as the cast of the master weights: one clean step from lr = 0 would do it; the
-    # benchmark times steps, so initial shard contents only matter for the gathers' bandwidth, not results
     staging = StagedGrads(N, B, synth.FP16, dev)
-    dst = [torch.empty(plan.max_layer_elems, dtype=torch.int16, device=dev) for _ in range(N)]
-    dst_ptrs = [d.data_ptr() for d in dst]
     shard_ptrs = [t.data_ptr() for t in bufs.params16]
     adam = zg.zero_adam_t(max_grad_norm=0.0, **ADAM)
     state = zg.zero_state_t(t=0, loss_scale=S, min_loss_scale=1.0)
@@ -217,49 +217,84 @@ def leg_cfg4(args):
     for l in layers:
         starts.append(starts[-1] + l)
     nb = plan.n_buckets
+    L = len(layers)
 
-    def one_step(step_no):
+    def run_buckets(layer, step_no, done):
+        while done[0] > 0 and (done[0] - 1) * B >= starts[layer]:
+            b = done[0] - 1
+            lo, hi = b * B, min((b + 1) * B, n)
+            staging.fill(lo, hi, 1e-3 * S, 0, step_no, s)
+            zg.zero_step_bucket(cfg, plan, bufs, adam, state, b, staging.ptrs, s)
+            done[0] -= 1
+
+    def step_plain(step_no, dst_ptrs):
         zg.zero_step_begin(cfg, plan, bufs, adam, state, s)
-        for l in range(len(layers)):                       # forward: gather every layer
+        for l in range(L):
             zg.zero_gather_layer(cfg, plan, l, shard_ptrs, dst_ptrs, s)
-        done = nb
-        for l in reversed(range(len(layers))):             # backward: gather again, then finished buckets
+        done = [nb]
+        for l in reversed(range(L)):
             zg.zero_gather_layer(cfg, plan, l, shard_ptrs, dst_ptrs, s)
-            while done > 0 and (done - 1) * B >= starts[l]:
-                b = done - 1
-                lo, hi = b * B, min((b + 1) * B, n)
-                staging.fill(lo, hi, 1e-3 * S, 0, step_no, s)
-                zg.zero_step_bucket(cfg, plan, bufs, adam, state, b, staging.ptrs, s)
-                done -= 1
+            run_buckets(l, step_no, done)
         return zg.zero_step_end(cfg, plan, bufs, adam, state, s)
 
-    steps = max(1, min(args.steps, 3))
-    warm = 1
-    for k in range(warm):
-        one_step(k + 1)
-        staging.take_ms()
-    walls, gens = [], []
-    for k in range(steps):
-        w0, w1 = _ev(), _ev()
-        w0.record(s)
-        res = one_step(warm + k + 1)
-        w1.record(s)
+    def step_prefetch(step_no, pool, cap, side):
+        zg.zero_step_begin(cfg, plan, bufs, adam, state, s)
+        f = zg.Fetcher(cfg, plan, shard_ptrs, pool, cap, list(range(L)), 1, side)
+        for pos in range(L):
+            f.fetch(pos, s)
+            f.release(pos, s)
+        f = zg.Fetcher(cfg, plan, shard_ptrs, pool, cap, list(reversed(range(L))), 1, side)
+        done = [nb]
+        for pos, l in enumerate(reversed(range(L))):
+            f.fetch(pos, s)
+            run_buckets(l, step_no, done)
+            f.release(pos, s)
+        return zg.zero_step_end(cfg, plan, bufs, adam, state, s)
+
+    def timed(fn, steps, warm):
+        for k in range(warm):
+            fn(k + 1)
         torch.cuda.synchronize()
-        assert res.overflow == 0
-        walls.append(w0.elapsed_time(w1))
-        gens.append(staging.take_ms())
-    step_ms = [w - g for w, g in zip(walls, gens)]
-    ms = sum(step_ms) / len(step_ms)
+        staging.take_ms()
+        walls, gens = [], []
+        for k in range(steps):
+            w0, w1 = _ev(), _ev()
+            w0.record(s)
+            res = fn(warm + k + 1)
+            w1.record(s)
+            torch.cuda.synchronize()
+            assert res.overflow == 0
+            walls.append(w0.elapsed_time(w1))
+            gens.append(staging.take_ms())
+        return sum(w - g for w, g in zip(walls, gens)) / steps, sum(gens) / steps
+
+    steps = max(1, min(args.steps, 3))
+    dst = [torch.empty(plan.max_layer_elems, dtype=torch.int16, device=dev) for _ in range(N)]
+    ms_plain, gen_ms = timed(lambda k: step_plain(k, [d.data_ptr() for d in dst]), steps, 1)
+    del dst
+    torch.cuda.empty_cache()
+    cap = 2 * ((plan.max_layer_elems + 7) // 8 * 8)
+    pool = [torch.empty(cap, dtype=torch.int16, device=dev) for _ in range(N)]
+    side = torch.cuda.Stream(dev)
+    ms_pf, _ = timed(lambda k: step_prefetch(k, pool, cap, side), steps, 1)
+    ms = ms_plain       # the prefetch run overlaps the excluded generation: reported, not the value
     bpp_gather = 2 + 2 * N
     bytes_step = n * (2 * bpp_gather + bench.bytes_per_param(3, N))
-    out = _base(n / (ms * 1e-3) / 1e9, ms, steps, warm,
+    out = _base(n / (ms * 1e-3) / 1e9, ms, steps, 1,
                 "stage 3, 32-layer d=4096 parameter list (%d params), N_d=64, bucket 2^24; two gathers per layer "
-                "into 64 constant-size buffers; 64 gradient copies generated per bucket (excluded)" % n,
-                {"n_params": n, "n_ranks": N, "stage": 3, "bucket_elems": B, "n_layers": len(layers),
+                "for 64 destinations; 64 gradient copies generated per bucket (excluded)" % n,
+                {"n_params": n, "n_ranks": N, "stage": 3, "bucket_elems": B, "n_layers": L,
                  "gather_capacity_elems": plan.max_layer_elems})
-    out["roofline"] = _roofline(bytes_step, ms, "k_gather + k_fused<stage 3, fp16>")
+    out["runs"] = {"gathers_in_stream": {"ms_per_step": ms_plain, "value": n / (ms_plain * 1e-3) / 1e9,
+                                         "buffers": "64 x the largest layer"},
+                   "prefetch_depth_1": {"ms_per_step": ms_pf, "value": n / (ms_pf * 1e-3) / 1e9,
+                                        "buffers": "pool of 64 x 2 largest layers (live budget)",
+                                        "note": "gathers overlap the bucket kernels and the excluded gradient "
+                                                "generation, so subtracting the generation time overstates "
+                                                "this run's speed by up to the overlap"}}
+    out["roofline"] = _roofline(bytes_step, ms_plain, "k_gather + k_fused<stage 3, fp16> (gathers in stream)")
     out["bytes_per_param"] = 2 * bpp_gather + bench.bytes_per_param(3, N)
-    out["generation_ms_per_step"] = sum(gens) / len(gens)
+    out["generation_ms_per_step"] = gen_ms
     out["device_memory_gb"] = torch.cuda.max_memory_allocated(dev) / 1e9
     return out
 
