@@ -453,3 +453,29 @@ def test_fetcher_prefetch_under_budget_with_step(depth):
     ref = oracle.step(grads, job.w, job.m, job.v, dtype=FP16, t=0, loss_scale=4.0, **job.hp)
     job.p16, job.h, job.o["t"] = ref["p16"], ref["h"], ref["t"]
     job.check(res, ref)
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+def test_clip_norm_over_full_exponent_range(dtype):
+    """Gradients with random exponents over the whole 16-bit range
+    (subnormals to near overflow): for bfloat16 many squares fall outside the
+    fixed-point window and go through the exponent bins; the norm and the
+    clip coefficient must still equal the oracle's bit for bit."""
+    n, N = 3 * 4096 + 77, 2
+    job = Job(n, N, 2, 4096, 8, dtype=dtype, shadow=False, max_norm=1.0)
+    rng = np.random.default_rng(123)
+    grads = []
+    for r in range(N):
+        if dtype == BF16:
+            e = rng.integers(-130, 60, n).astype(np.float64)     # stays finite after the 2-rank sum
+        else:
+            e = rng.integers(-24, 14, n).astype(np.float64)
+        x = (rng.choice([-1.0, 1.0], n) * rng.uniform(1.0, 2.0, n) * 2.0 ** e).astype(np.float32)
+        grads.append(oracle.from_f32(x, dtype))
+    res, ref = job.step(grads)
+    assert res.overflow == 0 and ref["overflow"] == 0
+    job.check(res, ref)
+    # the bins were exercised: some squares lie outside the window
+    if dtype == BF16:
+        h = oracle.to_f32(ref["h"], dtype)
+        assert (np.abs(h[h != 0]) < 2.0 ** -40).any() and (np.abs(h) > 2.0 ** 10).any()
