@@ -248,30 +248,31 @@ __device__ __forceinline__ void u128_add(U128& a, unsigned long long lo, unsigne
 template <int DT>
 __device__ __forceinline__ void sumsq_add(uint32_t bits, int win_lo, U128& acc, unsigned long long* bins)
 {
-    uint32_t e, f, M;
-    int E;
+    // Non-finite values are not skipped: they set the step's overflow flag,
+    // and an overflowed step discards the norm.
     if constexpr (DT == kBF16) {
-        e = (bits >> 7) & 0xffu;
-        f = bits & 0x7fu;
-        if (e == 0xffu) return;
-        M = e ? (f | 0x80u) : f;
-        E = (int)(e ? e : 1u) - 134;
+        const uint32_t e = (bits >> 7) & 0xffu;
+        const uint32_t M = (bits & 0x7fu) | (e ? 0x80u : 0u);
+        const int E = (int)(e ? e : 1u) - 134;
+        const unsigned long long m2 = (unsigned long long)(M * M);
+        const int sh = 2 * (E - win_lo);
+        if (sh >= 0 && sh <= 64) {
+            const unsigned long long lo = sh < 64 ? (m2 << sh) : 0ull;
+            const unsigned long long hi = sh == 0 ? 0ull : (sh < 64 ? (m2 >> (64 - sh)) : m2);
+            u128_add(acc, lo, hi);
+        } else if (m2) {
+            atomicAdd(bins + e, m2);
+        }
     } else {
-        e = (bits >> 10) & 0x1fu;
-        f = bits & 0x3ffu;
-        if (e == 0x1fu) return;
-        M = e ? (f | 0x400u) : f;
-        E = (int)(e ? e : 1u) - 25;
-    }
-    if (M == 0) return;
-    const unsigned long long m2 = (unsigned long long)M * M;
-    const int sh = 2 * (E - win_lo);
-    if (sh >= 0 && sh <= 64) {
-        const unsigned long long lo = sh < 64 ? (m2 << sh) : 0ull;
-        const unsigned long long hi = sh == 0 ? 0ull : (sh < 64 ? (m2 >> (64 - sh)) : m2);
+        // binary16: the window starts at the smallest subnormal (win_lo = -24),
+        // so every square lands in it at shift sh = 2*(max(e,1) - 1) <= 60.
+        const uint32_t e = (bits >> 10) & 0x1fu;
+        const uint32_t M = (bits & 0x3ffu) | (e ? 0x400u : 0u);
+        const int sh = 2 * (int)((e ? e : 1u) - 1u);
+        const unsigned long long m2 = (unsigned long long)(M * M);
+        const unsigned long long lo = m2 << sh;
+        const unsigned long long hi = (m2 >> 1) >> (63 - sh);   // 0 when sh == 0
         u128_add(acc, lo, hi);
-    } else {
-        atomicAdd(bins + e, m2);
     }
 }
 
