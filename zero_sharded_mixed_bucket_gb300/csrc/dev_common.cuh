@@ -42,6 +42,41 @@ __device__ __forceinline__ bool nonfinite16(uint32_t bits)
         return (bits & 0x7c00u) == 0x7c00u;
 }
 
+// Two 16-bit values packed in a word (element 2p in the low half).
+template <int DT>
+__device__ __forceinline__ float2 to_f32x2(uint32_t w)
+{
+    if constexpr (DT == kBF16)
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    else
+        return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+// Round two floats to nearest even and pack them (lo in the low half).
+template <int DT>
+__device__ __forceinline__ uint32_t from_f32x2(float lo, float hi)
+{
+    if constexpr (DT == kBF16) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&b);
+    } else {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+
+// Nonzero if either packed value has an all-ones exponent (inf or NaN):
+// adding one exponent LSB to the masked exponent carries into the sign bit
+// only then, and never across the two halves.
+template <int DT>
+__device__ __forceinline__ uint32_t nonfinite_x2(uint32_t w)
+{
+    if constexpr (DT == kBF16)
+        return ((w & 0x7f807f80u) + 0x00800080u) & 0x80008000u;
+    else
+        return ((w & 0x7c007c00u) + 0x04000400u) & 0x80008000u;
+}
+
 // ---- consecutive bucket kernels ---------------------------------------------
 // Inside one step the library launches the bucket kernels back to back with
 // programmatic dependent launch.  Each bucket kernel lets the next one be
@@ -145,8 +180,11 @@ __device__ __forceinline__ void reduce_group(const StepArgs& a, int64_t gidx, in
         for (int k = 0; k < 8; k++) {
             if (r0 + k < a.n_ranks) {
 #pragma unroll
-                for (int j = 0; j < kVec; j++)
-                    s[j] = __fadd_rn(s[j], to_f32<DT>(q[k].get(j)));
+                for (int p = 0; p < kVec / 2; p++) {
+                    const float2 f = to_f32x2<DT>(q[k].w[p]);
+                    s[2 * p] = __fadd_rn(s[2 * p], f.x);
+                    s[2 * p + 1] = __fadd_rn(s[2 * p + 1], f.y);
+                }
             }
         }
     }

@@ -33,15 +33,19 @@ __global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ Step
         float s[kVec];
         reduce_group<DT>(a, gidx, cnt, s);
 
+        // round to 16 bits (elements past cnt are 0: finite, no effect)
         H8 h;
         float g[kVec];
+        uint32_t nf = 0;
 #pragma unroll
-        for (int j = 0; j < kVec; j++) {
-            const uint32_t b = from_f32<DT>(s[j]);
-            h.set(j, b);
-            bad |= (j < cnt) && nonfinite16<DT>(b);
-            g[j] = __fmul_rn(to_f32<DT>(b), a.inv);
+        for (int p = 0; p < kVec / 2; p++) {
+            h.w[p] = from_f32x2<DT>(s[2 * p], s[2 * p + 1]);
+            nf |= nonfinite_x2<DT>(h.w[p]);
+            const float2 f = to_f32x2<DT>(h.w[p]);
+            g[2 * p] = __fmul_rn(f.x, a.inv);
+            g[2 * p + 1] = __fmul_rn(f.y, a.inv);
         }
+        bad |= nf != 0;
 
         if constexpr (STAGE <= 1) {
             for (int r = 0; r < a.n_ranks; r++)

@@ -29,17 +29,19 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Ste
         const int64_t gidx = i - a.grad_base;
         float s[kVec];
         reduce_group<DT>(a, gidx, cnt, s);
+        // round to 16 bits; elements past cnt are 0 (finite, square 0)
         H8 h;
+        uint32_t nf = 0;
 #pragma unroll
-        for (int j = 0; j < kVec; j++) {
-            const uint32_t b = from_f32<DT>(s[j]);
-            h.set(j, b);
-            const bool valid = j < cnt;
-            bad |= valid && nonfinite16<DT>(b);
+        for (int p = 0; p < kVec / 2; p++) {
+            h.w[p] = from_f32x2<DT>(s[2 * p], s[2 * p + 1]);
+            nf |= nonfinite_x2<DT>(h.w[p]);
             if constexpr (CLIP) {
-                if (valid) sumsq_add<DT>(b, a.win_lo, acc, bins);
+                sumsq_add<DT>(h.w[p] & 0xffffu, a.win_lo, acc, bins);
+                sumsq_add<DT>(h.w[p] >> 16, a.win_lo, acc, bins);
             }
         }
+        bad |= nf != 0;
         if constexpr (HDEST == 0) {
             for (int r = 0; r < a.n_ranks; r++)
                 st_h8(const_cast<void*>(a.grads[r]), gidx, h, cnt);

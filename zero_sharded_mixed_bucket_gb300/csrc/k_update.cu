@@ -37,9 +37,15 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
                 h = ld_h8(a.reduced, i, cnt);
             float g[kVec];
 #pragma unroll
-            for (int j = 0; j < kVec; j++) {
-                g[j] = __fmul_rn(to_f32<DT>(h.get(j)), a.inv);
-                if (c != 1.0f) g[j] = __fmul_rn(g[j], c);
+            for (int p = 0; p < kVec / 2; p++) {
+                const float2 f = to_f32x2<DT>(h.w[p]);
+                g[2 * p] = __fmul_rn(f.x, a.inv);
+                g[2 * p + 1] = __fmul_rn(f.y, a.inv);
+            }
+            if (c != 1.0f) {
+#pragma unroll
+                for (int j = 0; j < kVec; j++)
+                    g[j] = __fmul_rn(g[j], c);
             }
             H8 p;
             update_state<DT, OPT>(a, (int64_t)r * a.replica_stride + i, cnt, g, p);
