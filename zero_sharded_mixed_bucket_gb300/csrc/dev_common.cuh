@@ -278,9 +278,7 @@ struct U128 {
 
 __device__ __forceinline__ void u128_add(U128& a, unsigned long long lo, unsigned long long hi)
 {
-    const unsigned long long l = a.lo + lo;
-    a.hi += hi + (l < lo ? 1ull : 0ull);
-    a.lo = l;
+    asm("add.cc.u64 %0, %0, %2;\n\taddc.u64 %1, %1, %3;" : "+l"(a.lo), "+l"(a.hi) : "l"(lo), "l"(hi));
 }
 
 template <int DT>
