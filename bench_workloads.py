@@ -25,9 +25,6 @@ bracketed by its own events and subtracted.
 """
 from __future__ import annotations
 
-import math
-import time
-
 import bench
 
 ADAM = bench.ADAM

@@ -1,6 +1,6 @@
 /*
- * zero_gb300.h -- C ABI of the ZeRO sharded mixed-precision Adam step on one
- * GB300 (sm_103a).
+ * zero_gb300.h -- C ABI of the ZeRO sharded mixed-precision optimizer step
+ * (Adam; also SGD with momentum and SGD) on one GB300 (sm_103a).
  *
  * What the library computes
  * -------------------------
@@ -21,10 +21,11 @@
  * of one GPU's memory, and each collective is the memory traffic of the fused
  * kernels.  Per bucket, one kernel reads the N_d ranks' 16-bit gradients,
  * sums them in rank order in fp32, rounds once to 16 bits, checks for inf/NaN
- * (loss-scale overflow), unscales by 1/(S*N_d), applies Adam (Kingma & Ba,
- * Algorithm 1: bias correction, eps outside the square root, no weight decay)
- * to the owned fp32 state and writes the 16-bit cast to every rank (stages
- * 0-2) or to the owner's shard (stage 3).  The partition does not change the
+ * (loss-scale overflow), unscales by 1/(S*N_d), applies the optimizer --
+ * Adam (Kingma & Ba, Algorithm 1: bias correction, eps outside the square
+ * root, no weight decay), or SGD with momentum, or SGD -- to the owned fp32
+ * state and writes the 16-bit cast to every rank (stages 0-2) or to the
+ * owner's shard (stage 3).  The partition does not change the
  * step's result: every stage gives the same numbers as one unpartitioned step.
  *
  * Layout
@@ -75,13 +76,17 @@
  *
  * Conventions
  * -----------
- *   The caller owns all memory; the library allocates nothing, keeps no
- *   state between calls and never throws.  Every function returns a
- *   zero_status_t; on failure zero_last_error() gives a message
- *   (thread-local).  Kernels run asynchronously on the caller's stream
+ *   The caller owns all memory; the library allocates nothing and never
+ *   throws.  Between calls it keeps only the thread-local error text and
+ *   profiling events; a fetcher's state lives in caller memory.  Every
+ *   function returns a zero_status_t; on failure zero_last_error() gives a
+ *   message (thread-local).  Kernels run asynchronously on the caller's stream
  *   (a cudaStream_t passed as void*; NULL = legacy default stream).  The
  *   end of a step synchronises that stream once to read the overflow flag.
- *   Device pointers must be 16-byte aligned (ZERO_EALIGN otherwise).
+ *   Device pointers must be 16-byte aligned (ZERO_EALIGN otherwise).  Any
+ *   pointer the GPU can load from and store to is accepted: on GB300 the
+ *   gradients or the fp32 optimizer state may live in pinned host memory,
+ *   which the kernels then reach over NVLink-C2C.
  *   Pointer arrays (grads, params16, dst) are host arrays of device
  *   pointers, read during the call only.
  */
@@ -104,7 +109,7 @@ typedef enum {
     ZERO_EALIGN = 2,         /* a device pointer is not 16-byte aligned */
     ZERO_ENOMEM = 3,         /* a caller-provided buffer is missing or too small */
     ZERO_ECUDA = 4,          /* a CUDA runtime call failed (message has the CUDA error) */
-    ZERO_ETIMEOUT = 5,       /* reserved: no kernel here waits on another */
+    ZERO_ETIMEOUT = 5,       /* reserved: no kernel here spins on a flag another kernel sets */
     ZERO_EUNSUPPORTED = 6    /* n_ranks outside 1..64, or another unsupported size */
 } zero_status_t;
 
