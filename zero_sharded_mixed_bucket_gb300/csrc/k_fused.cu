@@ -18,8 +18,11 @@ namespace zg {
 
 namespace {
 
+// Stage 0 walks the N replicas' state per group; unconstrained it takes ~107
+// registers (4 blocks per SM).  Asking for 5 resident blocks brings it to 96
+// without spills and measured 6130 -> 6636 GB/s on GB300.
 template <int STAGE, int DT, int OPT>
-__global__ void __launch_bounds__(kThreads) k_fused(const __grid_constant__ StepArgs a)
+__global__ void __launch_bounds__(kThreads, STAGE == 0 ? 5 : 1) k_fused(const __grid_constant__ StepArgs a)
 {
     allow_next_grid();
     const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
