@@ -27,7 +27,6 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import re
 import statistics
@@ -116,10 +115,10 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu: int):
-        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.f = tempfile.NamedTemporaryFile("w", prefix="clocks_", suffix=".csv", delete=False)
+        self.path = self.f.name
         self.proc = None
         try:
-            self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
                                           "-i", str(gpu), "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:

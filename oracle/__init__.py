@@ -442,6 +442,8 @@ def hbm_bytes_per_param(n_ranks: int, stage: int, mode: str, state_bytes: int = 
         return {0: N * (6 + 2 * sb), 1: 6 * N + 2 * sb, 2: 4 * N + 2 * sb, 3: 2 * N + 2 * sb + 2}[stage]
     if mode == "two_pass":
         return {0: N * (8 + 2 * sb), 1: 6 * N + 2 + 2 * sb, 2: 4 * N + 4 + 2 * sb, 3: 2 * N + 6 + 2 * sb}[stage]
+    if mode == "restore":   # after an overflowed fused step: read w, write each 16-bit copy
+        return {0: 6 * N, 1: 4 + 2 * N, 2: 4 + 2 * N, 3: 6}[stage]
     raise ValueError(mode)
 
 

@@ -83,6 +83,10 @@ def test_overflow_skips_and_halves(shadow, dtype):
     res, ref = job.step(job.make_grads(2, inject=[(3, n - 2, inf)]))
     assert res.overflow == 1 and res.skipped == 1 and res.new_loss_scale == 512.0 and res.t == 1
     job.check(res, ref)
+    if shadow:     # the skipped fused step also ran the parameter restore
+        assert res.hbm_bytes == job.plan.hbm_bytes_fused + n * oracle.hbm_bytes_per_param(4, 2, "restore")
+    else:
+        assert res.hbm_bytes == job.plan.hbm_bytes_two_pass
     assert np.array_equal(as_u32(job.bufs.state()[0][:n]), w_before)
     assert np.array_equal(as_u16(job.bufs.params16[2][:n]), p_before)
     res, ref = job.step(job.make_grads(3))
@@ -97,6 +101,7 @@ def test_overflow_other_stages(stage):
     res, ref = job.step(job.make_grads(1, inject=[(0, 17, 0x7E00)]))   # NaN
     assert res.overflow == 1
     job.check(res, ref)
+    assert res.hbm_bytes == job.plan.hbm_bytes_fused + n * oracle.hbm_bytes_per_param(2, stage, "restore")
     res, ref = job.step(job.make_grads(2))
     job.check(res, ref)
 

@@ -59,6 +59,16 @@ int64_t bytes_per_param(int stage, int64_t N, bool fused, int64_t sb)
     }
 }
 
+// Bytes per parameter of the restore after an overflowed fused step: read
+// the unchanged master weight, write its 16-bit cast to each copy (every
+// replica in stage 0, every rank in stages 1-2, the owner in stage 3).
+int64_t restore_bytes_per_param(int stage, int64_t N)
+{
+    if (stage == 0) return N * (4 + 2);
+    if (stage == 3) return 4 + 2;
+    return 4 + 2 * N;
+}
+
 const int kCollectivePasses[4] = {2, 3, 2, 3};   // RS+AG, AR+AG, RS+AG, RS+2AG
 
 zero_status_t check_config(const zero_config_t* c)
@@ -387,8 +397,7 @@ zero_status_t end_impl(const zero_config_t* c, const zero_plan_t* p, zero_buffer
     r.hbm_bytes = path.fused ? p->hbm_bytes_fused : p->hbm_bytes_two_pass;
     r.comm_counted_bytes = p->comm_counted_bytes;
     if (overflow) {
-        if (path.fused) r.hbm_bytes += c->n_params * (4 + 2 * (c->stage == 3 ? 1 : (int64_t)c->n_ranks)) *
-                                       (c->stage == 0 ? 1 : 1);
+        if (path.fused) r.hbm_bytes += c->n_params * restore_bytes_per_param(c->stage, c->n_ranks);
         if (s->dynamic) {
             float h = s->loss_scale * 0.5f;
             s->loss_scale = h > s->min_loss_scale ? h : s->min_loss_scale;
