@@ -484,3 +484,20 @@ def test_clip_norm_over_full_exponent_range(dtype):
     if dtype == BF16:
         h = oracle.to_f32(ref["h"], dtype)
         assert (np.abs(h[h != 0]) < 2.0 ** -40).any() and (np.abs(h) > 2.0 ** 10).any()
+
+
+def test_tiny_partitions_brute_force():
+    """Every combination of tiny sizes, rank counts, bucket sizes, alignments
+    and stages (448 jobs, one step each) against the oracle: partition
+    offsets, owner shards and ragged tails all exercised."""
+    count = 0
+    for n in (1, 7, 8, 9, 17, 63, 64):
+        for N in (1, 2, 3, 4):
+            for B in (8, 24):
+                for A in (8, 32):
+                    for stage in (0, 1, 2, 3):
+                        job = Job(n, N, stage, B, A, seed=n * 131 + N, loss_scale=2.0)
+                        res, ref = job.step(job.make_grads(1))
+                        job.check(res, ref)
+                        count += 1
+    assert count == 448
