@@ -82,7 +82,8 @@
  *   function returns a zero_status_t; on failure zero_last_error() gives a
  *   message (thread-local).  Kernels run asynchronously on the caller's stream
  *   (a cudaStream_t passed as void*; NULL = legacy default stream).  The
- *   end of a step synchronises that stream once to read the overflow flag.
+ *   end of a step synchronises that stream once to read the overflow flag
+ *   (zero_step_async, below, keeps the step state on the device instead).
  *   Device pointers must be 16-byte aligned (ZERO_EALIGN otherwise).  Any
  *   pointer the GPU can load from and store to is accepted: on GB300 the
  *   gradients or the fp32 optimizer state may live in pinned host memory,
@@ -282,6 +283,37 @@ zero_status_t zero_step_end(const zero_config_t* cfg, const zero_plan_t* plan, z
  * accounting; "ZeRO：大模型训练的内存优化革命" 3.1.3).  n_dst 1..64. */
 zero_status_t zero_gather_layer(const zero_config_t* cfg, const zero_plan_t* plan, int32_t layer,
                                 void* const* param_shards, void* const* dst, int32_t n_dst, void* stream);
+
+/* ---- steps without host synchronisation ------------------------------------
+ * The step state (t, the beta powers of the bias correction, the loss scale
+ * and its scaler) can live in device memory instead: zero_step_async then
+ * enqueues the whole step and returns without waiting, so steps pipeline
+ * back to back and a step can be captured in a CUDA graph.  A one-thread
+ * prepare kernel derives the step's scalars from the state block; a
+ * one-thread commit kernel writes the outcome back (t and the beta powers
+ * advance on a clean step; the scaler halves on overflow and grows after
+ * growth_interval clean steps) together with the last step's flag, norm and
+ * clip coefficient, which zero_dev_state_read brings to the host.  Results
+ * equal the synchronised step's bit for bit.
+ * Fused path: the host does not learn the flag, so bufs->cur flips on every
+ * call; after an overflow a restore kernel copies the unchanged state into
+ * the copy the next step reads and restores the 16-bit parameters.  A graph
+ * captured from one call therefore serves every other step: capture one
+ * call per value of bufs->cur and replay them alternately.
+ * The device state block is 64 bytes, 16-byte aligned, caller-owned. */
+typedef struct zero_dev_state { int64_t opaque[8]; } zero_dev_state_t;   /* 64 bytes */
+
+/* Initialise the block from a host state (synchronises `stream`); `adam`
+ * must carry the betas the steps will use (both in [0, 1)). */
+zero_status_t zero_dev_state_init(void* dev_state, const zero_adam_t* adam, const zero_state_t* state, void* stream);
+/* Enqueue one step (all buckets); never synchronises.  *kernel_launches
+ * (may be NULL) receives the kernels it launched. */
+zero_status_t zero_step_async(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                              const zero_adam_t* adam, void* dev_state, void* stream, int32_t* kernel_launches);
+/* Copy the block to the host (synchronises `stream`): the current step state
+ * and the last step's outcome (t, overflow, skipped, grad_norm, clip_coef,
+ * new_loss_scale; path -1). */
+zero_status_t zero_dev_state_read(const void* dev_state, zero_state_t* state, zero_step_result_t* last, void* stream);
 
 /* ---- stage 3: gathers ahead of use under a live-parameter budget ---------
  * A fetcher gathers the layers of one pass (an order of layers: forward

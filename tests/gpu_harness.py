@@ -115,6 +115,10 @@ class Job:
             fn = [zg.zero_step_stage0, zg.zero_step_stage1, zg.zero_step_stage2, zg.zero_step_stage3][self.stage]
             res = fn(self.cfg, self.plan, self.bufs, self.adam, self.state, s)
         torch.cuda.synchronize()
+        return res, self.oracle_step(grads)
+
+    def oracle_step(self, grads):
+        """The same step on the oracle's copy; updates the expected state."""
         ref = oracle.step(grads, self.w, self.m, self.v, dtype=self.dtype, t=self.o["t"],
                           loss_scale=self.o["loss_scale"], max_grad_norm=self.max_norm, dynamic=self.dynamic,
                           min_scale=self.min_scale, growth_interval=self.growth, good_steps=self.o["good_steps"],
@@ -123,7 +127,7 @@ class Job:
         self.p16 = ref["p16"]
         self.h = ref["h"]
         self.last_ref = ref
-        return res, ref
+        return ref
 
     # -- comparisons ---------------------------------------------------------
     def check(self, res, ref):

@@ -252,3 +252,38 @@ def test_bias_correction_early_exit_is_exact():
     for beta in (0.9, 0.99, 0.999):
         bc = oracle.bias_corrections(beta, beta, 5000)[0]
         assert bc == (1.0 if beta < 0.999 else bc)
+
+
+def test_device_state_checks_reject_before_any_copy():
+    cfg = zg.Config(1000, 4, 2, 64)
+    plan = zg.zero_plan(cfg)
+    adam = zg.zero_adam_t(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8)
+    L = zg.lib()
+    state = zg.zero_state_t(t=0, loss_scale=1.0, min_loss_scale=1.0)
+    assert L.zero_dev_state_init(None, ctypes.byref(adam), ctypes.byref(state), None) == zg.ZERO_EINVAL
+    assert L.zero_dev_state_init(0x10000008, ctypes.byref(adam), ctypes.byref(state), None) == zg.ZERO_EALIGN
+    bad = zg.zero_state_t(t=0, loss_scale=0.0)
+    assert L.zero_dev_state_init(0x10000000, ctypes.byref(adam), ctypes.byref(bad), None) == zg.ZERO_EINVAL
+    bad = zg.zero_state_t(t=-1, loss_scale=1.0)
+    assert L.zero_dev_state_init(0x10000000, ctypes.byref(adam), ctypes.byref(bad), None) == zg.ZERO_EINVAL
+    bad = zg.zero_state_t(t=0, loss_scale=1.0, min_loss_scale=0.0, dynamic=1)
+    assert L.zero_dev_state_init(0x10000000, ctypes.byref(adam), ctypes.byref(bad), None) == zg.ZERO_EINVAL
+    one = zg.zero_adam_t(lr=1e-4, beta1=1.0, beta2=0.999)
+    assert L.zero_dev_state_init(0x10000000, ctypes.byref(one), ctypes.byref(state), None) == zg.ZERO_EINVAL
+    assert L.zero_dev_state_read(None, None, None, None) == zg.ZERO_EINVAL
+    n = ctypes.c_int32(-1)
+
+    def step(fb, dev=0x10000000, a=adam):
+        return L.zero_step_async(ctypes.byref(cfg.c), ctypes.byref(plan), ctypes.byref(fb.b), ctypes.byref(a),
+                                 dev, None, ctypes.byref(n))
+
+    assert step(_FakeBuffers(4), dev=None) == zg.ZERO_EALIGN
+    assert step(_FakeBuffers(4), dev=0x10000004) == zg.ZERO_EALIGN
+    fb = _FakeBuffers(4)
+    fb.pp[1] = 0x10000002
+    assert step(fb) == zg.ZERO_EALIGN
+    fb = _FakeBuffers(4)
+    fb.gp[0] = None
+    assert step(fb) == zg.ZERO_ENOMEM
+    assert step(_FakeBuffers(4), a=one) == zg.ZERO_EINVAL
+    assert n.value == -1                       # nothing was launched

@@ -1,0 +1,128 @@
+"""Steps whose step state lives in device memory (zero_step_async): equal to
+the oracle bit for bit across stages, paths, optimizers and 16-bit types,
+through an overflowed step, loss-scale growth and a resumed step count; and
+two CUDA graphs captured from it (one per value of the state-copy index)
+replayed alternately with new gradients between replays."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import zero_sharded_mixed_bucket_gb300 as zg
+from tests.gpu_harness import Job
+
+pytestmark = pytest.mark.gpu
+
+
+class AsyncJob(Job):
+    def __init__(self, *args, shadow=True, t0=0, **kw):
+        super().__init__(*args, shadow=shadow, **kw)
+        if t0:
+            self.state.t = t0
+            self.o["t"] = t0
+        self.dev = torch.zeros(zg.DEV_STATE_BYTES // 8, dtype=torch.int64, device="cuda")
+        zg.zero_dev_state_init(self.dev, self.adam, self.state, torch.cuda.current_stream())
+        self.two_pass = self.max_norm > 0 or not shadow
+
+    def launch(self, stream=None):
+        return zg.zero_step_async(self.cfg, self.plan, self.bufs, self.adam, self.dev,
+                                  stream or torch.cuda.current_stream())
+
+    def read(self):
+        st, res = zg.zero_dev_state_read(self.dev, torch.cuda.current_stream())
+        assert res.path == -1
+        res.path = 1 if self.two_pass else 0
+        self.state = st
+        return res
+
+    def step(self, grads):
+        self.load_grads(grads)
+        n = self.launch()
+        fused = not self.two_pass
+        per_bucket = 2 if self.two_pass else 1
+        assert n == 2 + per_bucket * self.plan.n_buckets + (1 if self.max_norm > 0 else 0) + \
+            (1 if fused and self.n > 0 else 0)
+        return self.read(), self.oracle_step(grads)
+
+
+def inf_at(job, r, i):
+    return (r, i, synth.inf_bits(job.dtype))
+
+
+CASES = [
+    # stage, N, n, B, dtype, shadow, max_norm, optimizer
+    (2, 8, 5 * 1024 + 3, 1024, oracle.FP16, True, 0.0, zg.ZERO_ADAM),
+    (2, 4, 5 * 1024 + 3, 1024, oracle.FP16, True, 1e-3, zg.ZERO_ADAM),
+    (2, 4, 5 * 1024 + 3, 1024, oracle.BF16, False, 0.0, zg.ZERO_ADAM),
+    (0, 3, 3 * 1024 + 5, 1024, oracle.FP16, True, 0.0, zg.ZERO_ADAM),
+    (0, 3, 3 * 1024 + 5, 1024, oracle.BF16, False, 5e-3, zg.ZERO_ADAM),
+    (1, 4, 4 * 512 + 9, 512, oracle.FP16, True, 0.0, zg.ZERO_SGD_MOMENTUM),
+    (1, 4, 4 * 512 + 9, 512, oracle.FP16, False, 0.0, zg.ZERO_SGD),
+    (3, 5, 7 * 256 + 1, 256, oracle.FP16, True, 0.0, zg.ZERO_SGD),
+    (3, 5, 7 * 256 + 1, 256, oracle.BF16, True, 0.0, zg.ZERO_ADAM),
+    (3, 5, 7 * 256 + 1, 256, oracle.FP16, True, 2e-3, zg.ZERO_SGD_MOMENTUM),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_async_steps_match_oracle(case):
+    stage, N, n, B, dtype, shadow, max_norm, opt = case
+    job = AsyncJob(n, N, stage, B, 8, None, dtype, shadow=shadow, loss_scale=256.0, dynamic=True, growth=2,
+                   max_norm=max_norm, optimizer=opt)
+    plan = [(), (), (inf_at(job, N - 1, n - 1),), (), (), (), (inf_at(job, 0, B + 1),), ()]
+    for step, inject in enumerate(plan, start=1):
+        res, ref = job.step(job.make_grads(step, inject))
+        job.check(res, ref)
+        assert res.overflow == (1 if inject else 0)
+    # two overflows, two growth doublings (growth interval 2) from 256
+    assert job.state.t == 6 and job.state.loss_scale == ref["loss_scale"]
+
+
+def test_async_resumes_at_a_later_step_count():
+    job = AsyncJob(3000, 4, 2, 1024, 8, None, oracle.FP16, t0=37, loss_scale=64.0)
+    for step in (1, 2):
+        res, ref = job.step(job.make_grads(step))
+        job.check(res, ref)
+    assert job.state.t == 39
+
+
+def test_async_state_round_trip():
+    dev = torch.zeros(8, dtype=torch.int64, device="cuda")
+    adam = zg.zero_adam_t(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8)
+    st = zg.zero_state_t(t=12, loss_scale=512.0, min_loss_scale=2.0, dynamic=1, growth_interval=7, good_steps=3)
+    zg.zero_dev_state_init(dev, adam, st)
+    got, last = zg.zero_dev_state_read(dev)
+    assert (got.t, got.loss_scale, got.min_loss_scale, got.dynamic, got.growth_interval, got.good_steps) == \
+        (12, 512.0, 2.0, 1, 7, 3)
+    assert last.overflow == 0 and last.grad_norm == -1.0 and last.clip_coef == 1.0
+
+
+@pytest.mark.parametrize("max_norm", [0.0, 1e-3])
+def test_two_captured_graphs_replayed_alternately(max_norm):
+    n, N, B = 6 * 2048 + 17, 8, 2048
+    job = AsyncJob(n, N, 2, B, 8, None, oracle.FP16, loss_scale=1024.0, dynamic=True, growth=3, max_norm=max_norm)
+    s = torch.cuda.Stream()
+    # one eager step first: it warms the library's launch-shape cache
+    res, ref = job.step(job.make_grads(1))
+    job.check(res, ref)
+    graphs = []
+    torch.cuda.synchronize()
+    cur0 = job.bufs.cur
+    for _ in range(2):                       # one graph per value of the copy index
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            job.launch(torch.cuda.current_stream())
+        graphs.append(g)
+    assert job.bufs.cur == cur0              # two captures flipped it twice (fused) or never (two-pass)
+    inject = {4: (inf_at(job, 3, 5),), 7: (inf_at(job, 7, n - 1),)}
+    for step in range(2, 12):
+        grads = job.make_grads(step, inject.get(step, ()))
+        job.load_grads(grads)
+        graphs[(step - 2) % 2].replay()
+        torch.cuda.synchronize()
+        res, ref = job.read(), job.oracle_step(grads)
+        if not job.two_pass:
+            job.bufs.b.cur = 1 - job.bufs.b.cur   # what the call does on the host, replayed by hand
+        job.check(res, ref)
+        assert res.overflow == (1 if step in inject else 0)

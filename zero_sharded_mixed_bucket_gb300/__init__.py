@@ -24,7 +24,8 @@ __all__ = [
     "zero_buffers_t", "zero_step_result_t", "Config", "lib", "lib_path",
     "zero_plan", "zero_plan_bucket", "zero_plan_layer", "zero_model_state_bytes", "zero_comm_bytes",
     "zero_step", "zero_step_stage0", "zero_step_stage1", "zero_step_stage2", "zero_step_stage3",
-    "zero_step_stage2_noalloc",
+    "zero_step_stage2_noalloc", "zero_dev_state_init", "zero_step_async", "zero_dev_state_read",
+    "DEV_STATE_BYTES",
     "zero_step_begin", "zero_step_bucket", "zero_step_end", "zero_gather_layer", "zero_last_error",
     "zero_version", "zero_set_profile_events", "zero_fetch_schedule", "Fetcher", "DeviceBuffers",
 ]
@@ -109,6 +110,9 @@ def lib():
             "zero_step_stage2": [cfg, plan, bufs, adam, state, c_vp, res],
             "zero_step_stage3": [cfg, plan, bufs, adam, state, c_vp, res],
             "zero_step_stage2_noalloc": [cfg, plan, bufs, adam, state, c_vp, res],
+            "zero_dev_state_init": [c_vp, adam, state, c_vp],
+            "zero_step_async": [cfg, plan, bufs, adam, c_vp, c_vp, P(c_i32)],
+            "zero_dev_state_read": [c_vp, state, res, c_vp],
             "zero_step_begin": [cfg, plan, bufs, adam, state, c_vp],
             "zero_step_bucket": [cfg, plan, bufs, adam, state, c_i64, P(c_vp), c_vp],
             "zero_step_end": [cfg, plan, bufs, adam, state, c_vp, res],
@@ -251,6 +255,35 @@ def zero_step_stage2_noalloc(cfg, plan, bufs, adam, state, stream=None) -> zero_
     """Stage-2 step whose scratch comes from a static array in the library
     (for callers that cannot allocate device memory); see the header."""
     return _step(lib().zero_step_stage2_noalloc, cfg, plan, bufs, adam, state, stream)
+
+
+DEV_STATE_BYTES = 64
+
+
+def _dptr(x) -> int:
+    return x if isinstance(x, int) else int(x.data_ptr())
+
+
+def zero_dev_state_init(dev_state, adam, state, stream=None):
+    """Upload `state` into a 64-byte device block (a pointer or a tensor)."""
+    _check(lib().zero_dev_state_init(_dptr(dev_state), ctypes.byref(adam), ctypes.byref(state), _stream(stream)))
+
+
+def zero_step_async(cfg, plan, bufs, adam, dev_state, stream=None) -> int:
+    """Enqueue one step whose step state lives in `dev_state`; no host
+    synchronisation.  Returns the number of kernels launched."""
+    b = bufs.b if isinstance(bufs, DeviceBuffers) else bufs
+    n = c_i32(0)
+    _check(lib().zero_step_async(_cfg(cfg), ctypes.byref(plan), ctypes.byref(b), ctypes.byref(adam),
+                                 _dptr(dev_state), _stream(stream), ctypes.byref(n)))
+    return n.value
+
+
+def zero_dev_state_read(dev_state, stream=None):
+    """(zero_state_t, zero_step_result_t of the last step) from the device block."""
+    st, res = zero_state_t(), zero_step_result_t()
+    _check(lib().zero_dev_state_read(_dptr(dev_state), ctypes.byref(st), ctypes.byref(res), _stream(stream)))
+    return st, res
 
 
 def zero_step_begin(cfg, plan, bufs, adam, state, stream=None):

@@ -233,7 +233,8 @@ __device__ __forceinline__ void sgd1(float g, float& w, const AdamHP& hp)
 // at state index si (w; m; v), update it with the 8 unscaled gradients g,
 // store it to the output state and give back the 16-bit cast in p.
 template <int DT, int OPT>
-__device__ __forceinline__ void update_state(const StepArgs& a, int64_t si, int cnt, const float g[kVec], H8& p)
+__device__ __forceinline__ void update_state(const StepArgs& a, const AdamHP& hp, int64_t si, int cnt,
+                                             const float g[kVec], H8& p)
 {
     float w[kVec];
     ld_f8(a.w_in, si, cnt, w);
@@ -243,7 +244,7 @@ __device__ __forceinline__ void update_state(const StepArgs& a, int64_t si, int 
         ld_f8(a.v_in, si, cnt, v);
 #pragma unroll
         for (int j = 0; j < kVec; j++)
-            adam1(g[j], w[j], m[j], v[j], a.hp);
+            adam1(g[j], w[j], m[j], v[j], hp);
         st_f8(a.m_out, si, cnt, m);
         st_f8(a.v_out, si, cnt, v);
     } else if constexpr (OPT == kSgdm) {
@@ -251,12 +252,12 @@ __device__ __forceinline__ void update_state(const StepArgs& a, int64_t si, int 
         ld_f8(a.m_in, si, cnt, m);
 #pragma unroll
         for (int j = 0; j < kVec; j++)
-            sgdm1(g[j], w[j], m[j], a.hp);
+            sgdm1(g[j], w[j], m[j], hp);
         st_f8(a.m_out, si, cnt, m);
     } else {
 #pragma unroll
         for (int j = 0; j < kVec; j++)
-            sgd1(g[j], w[j], a.hp);
+            sgd1(g[j], w[j], hp);
     }
 #pragma unroll
     for (int j = 0; j < kVec; j++)

@@ -25,6 +25,15 @@ template <int STAGE, int DT, int OPT>
 __global__ void __launch_bounds__(kThreads, STAGE == 0 ? 5 : 1) k_fused(const __grid_constant__ StepArgs a)
 {
     allow_next_grid();
+    // Step scalars: from the launch, or from the prepare kernel in a
+    // device-state step.
+    float inv = a.inv;
+    AdamHP hp = a.hp;
+    if (a.dyn) {
+        inv = a.dyn->inv;
+        hp.bc1 = a.dyn->bc1;
+        hp.bc2 = a.dyn->bc2;
+    }
     const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
     bool bad = false;
     for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
@@ -45,8 +54,8 @@ __global__ void __launch_bounds__(kThreads, STAGE == 0 ? 5 : 1) k_fused(const __
             h.w[p] = from_f32x2<DT>(s[2 * p], s[2 * p + 1]);
             nf |= nonfinite_x2<DT>(h.w[p]);
             const float2 f = to_f32x2<DT>(h.w[p]);
-            g[2 * p] = __fmul_rn(f.x, a.inv);
-            g[2 * p + 1] = __fmul_rn(f.y, a.inv);
+            g[2 * p] = __fmul_rn(f.x, inv);
+            g[2 * p + 1] = __fmul_rn(f.y, inv);
         }
         bad |= nf != 0;
 
@@ -58,12 +67,12 @@ __global__ void __launch_bounds__(kThreads, STAGE == 0 ? 5 : 1) k_fused(const __
         if constexpr (STAGE == 0) {
             for (int r = 0; r < a.n_ranks; r++) {
                 H8 p;
-                update_state<DT, OPT>(a, (int64_t)r * a.replica_stride + i, cnt, g, p);
+                update_state<DT, OPT>(a, hp, (int64_t)r * a.replica_stride + i, cnt, g, p);
                 st_h8(a.params16[r], i, p, cnt);
             }
         } else {
             H8 p;
-            update_state<DT, OPT>(a, i, cnt, g, p);
+            update_state<DT, OPT>(a, hp, i, cnt, g, p);
             if constexpr (STAGE == 3) {
                 const int o = owner_of(i, a.shard);
                 st_h8(a.params16[o], i - (int64_t)o * a.shard, p, cnt);

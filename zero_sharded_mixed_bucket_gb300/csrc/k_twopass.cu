@@ -18,6 +18,7 @@ template <int HDEST, int DT, bool CLIP>
 __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ StepArgs a)
 {
     allow_next_grid();
+    const int win_lo = a.dyn ? a.dyn->win_lo : a.win_lo;
     const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
     bool bad = false;
     U128 acc{0ull, 0ull};
@@ -37,8 +38,8 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Ste
             h.w[p] = from_f32x2<DT>(s[2 * p], s[2 * p + 1]);
             nf |= nonfinite_x2<DT>(h.w[p]);
             if constexpr (CLIP) {
-                sumsq_add<DT>(h.w[p] & 0xffffu, a.win_lo, acc, bins);
-                sumsq_add<DT>(h.w[p] >> 16, a.win_lo, acc, bins);
+                sumsq_add<DT>(h.w[p] & 0xffffu, win_lo, acc, bins);
+                sumsq_add<DT>(h.w[p] >> 16, win_lo, acc, bins);
             }
         }
         bad |= nf != 0;
@@ -126,11 +127,13 @@ __global__ void k_finalize(const FinalArgs a)
         return;
     }
     const int emin = a.dtype == kBF16 ? -133 : -24;   // E of the smallest subnormal
+    const int win_lo = a.dyn ? a.dyn->win_lo : a.win_lo;
+    const double inv = a.dyn ? a.dyn->inv_d : a.inv;
     unsigned long long big[kBigWords];
     for (int k = 0; k < kBigWords; k++) big[k] = 0ull;
     const unsigned long long* limbs = reinterpret_cast<const unsigned long long*>(a.ws + ws::kAcc);
     for (int k = 0; k < 4; k++)
-        big_add(big, limbs[k], 2 * (a.win_lo - emin) + 32 * k);
+        big_add(big, limbs[k], 2 * (win_lo - emin) + 32 * k);
     const unsigned long long* bins = reinterpret_cast<const unsigned long long*>(a.ws + ws::kBins);
     for (int e = 0; e < 256; e++) {
         if (!bins[e]) continue;
@@ -138,7 +141,7 @@ __global__ void k_finalize(const FinalArgs a)
         big_add(big, bins[e], 2 * (E - emin));
     }
     const double sumsq = big_to_double(big, 2 * emin);
-    const double norm = __dmul_rn(__dsqrt_rn(sumsq), a.inv);
+    const double norm = __dmul_rn(__dsqrt_rn(sumsq), inv);
     const double q = __ddiv_rn(a.max_norm, __dadd_rn(norm, 1e-6));
     *norm_out = norm;
     *clip_out = __double2float_rn(q < 1.0 ? q : 1.0);

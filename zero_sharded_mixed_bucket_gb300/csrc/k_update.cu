@@ -21,6 +21,13 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
     // With clipping on, multiply by c only when c < 1: g * 1 == g for every
     // finite g, so both forms give the same bits.
     const float c = CLIP ? *reinterpret_cast<const float*>(a.ws + ws::kClip) : 1.0f;
+    float inv = a.inv;
+    AdamHP hp = a.hp;
+    if (a.dyn) {
+        inv = a.dyn->inv;
+        hp.bc1 = a.dyn->bc1;
+        hp.bc2 = a.dyn->bc2;
+    }
     const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
     for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
          gi += (int64_t)gridDim.x * kThreads) {
@@ -39,8 +46,8 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
 #pragma unroll
             for (int p = 0; p < kVec / 2; p++) {
                 const float2 f = to_f32x2<DT>(h.w[p]);
-                g[2 * p] = __fmul_rn(f.x, a.inv);
-                g[2 * p + 1] = __fmul_rn(f.y, a.inv);
+                g[2 * p] = __fmul_rn(f.x, inv);
+                g[2 * p + 1] = __fmul_rn(f.y, inv);
             }
             if (c != 1.0f) {
 #pragma unroll
@@ -48,7 +55,7 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
                     g[j] = __fmul_rn(g[j], c);
             }
             H8 p;
-            update_state<DT, OPT>(a, (int64_t)r * a.replica_stride + i, cnt, g, p);
+            update_state<DT, OPT>(a, hp, (int64_t)r * a.replica_stride + i, cnt, g, p);
             if constexpr (STAGE == 0) {
                 st_h8(a.params16[r], i, p, cnt);
             } else if constexpr (STAGE == 3) {

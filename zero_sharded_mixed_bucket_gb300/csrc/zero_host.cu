@@ -347,6 +347,7 @@ zero_status_t end_impl(const zero_config_t* c, const zero_plan_t* p, zero_buffer
             f.win_lo = window_lo(c->dtype, s->loss_scale, c->n_ranks);
             f.inv = (double)(float)(1.0 / ((double)s->loss_scale * (double)c->n_ranks));
             f.max_norm = (double)adam->max_grad_norm;
+            f.dyn = nullptr;
             e = launch_finalize(f, st);
             if (e != cudaSuccess) return cuda_fail(e, "launching the norm finalize kernel");
             launches++;
@@ -614,6 +615,153 @@ zero_status_t zero_gather_layer(const zero_config_t* c, const zero_plan_t* p, in
     a.n_dst = n_dst;
     cudaError_t e = launch_gather(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "launching the layer gather kernel");
+    return ZERO_OK;
+}
+
+// ---- device-state steps -------------------------------------------------------
+
+static_assert(sizeof(DevState) == sizeof(zero_dev_state_t), "device state block size");
+static_assert(ws::kDyn + sizeof(Dyn) <= ws::kBytes, "workspace too small for the step scalars");
+
+zero_status_t zero_dev_state_init(void* dev_state, const zero_adam_t* adam, const zero_state_t* s, void* stream)
+{
+    if (!dev_state || !adam || !s) return fail(ZERO_EINVAL, "dev_state, adam and state must not be NULL");
+    if (!aligned16(dev_state)) return fail(ZERO_EALIGN, "dev_state is not 16-byte aligned");
+    if (!(std::isfinite(s->loss_scale) && s->loss_scale > 0.0f) || s->t < 0)
+        return fail(ZERO_EINVAL, "loss_scale must be positive and finite, t >= 0");
+    if (s->dynamic && !(std::isfinite(s->min_loss_scale) && s->min_loss_scale > 0.0f))
+        return fail(ZERO_EINVAL, "min_loss_scale must be positive and finite");
+    if (s->growth_interval < 0 || s->good_steps < 0) return fail(ZERO_EINVAL, "negative step counters");
+    if (!(adam->beta1 >= 0.0f && adam->beta1 < 1.0f && adam->beta2 >= 0.0f && adam->beta2 < 1.0f))
+        return fail(ZERO_EINVAL, "beta1 and beta2 must lie in [0, 1)");
+    DevState d;
+    std::memset(&d, 0, sizeof d);
+    d.t = s->t;
+    d.beta1_pow = d.beta2_pow = 1.0;
+    // beta^t as the same sequence of multiplications; below 2^-60 the bias
+    // correction is 1 whatever follows, so the loop may stop there
+    for (int64_t k = 0; k < s->t && (d.beta1_pow >= 0x1p-60 || d.beta2_pow >= 0x1p-60); k++) {
+        d.beta1_pow *= (double)adam->beta1;
+        d.beta2_pow *= (double)adam->beta2;
+    }
+    d.loss_scale = s->loss_scale;
+    d.min_loss_scale = s->min_loss_scale;
+    d.dynamic = s->dynamic;
+    d.growth_interval = s->growth_interval;
+    d.good_steps = s->good_steps;
+    d.last_grad_norm = -1.0;
+    d.last_clip_coef = 1.0f;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(dev_state, &d, sizeof d, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "uploading the device step state");
+    return ZERO_OK;
+}
+
+zero_status_t zero_step_async(const zero_config_t* c, const zero_plan_t* p, zero_buffers_t* b, const zero_adam_t* adam,
+                              void* dev_state, void* stream, int32_t* kernel_launches)
+{
+    zero_state_t host_view;   // the real step state is on the device; this only passes the host checks
+    std::memset(&host_view, 0, sizeof host_view);
+    host_view.loss_scale = 1.0f;
+    host_view.min_loss_scale = 1.0f;
+    zero_status_t st = check_step(c, p, b, adam, &host_view);
+    if (st != ZERO_OK) return st;
+    st = check_grads(c, b->grads, "grads");
+    if (st != ZERO_OK) return st;
+    if (!dev_state || !aligned16(dev_state)) return fail(ZERO_EALIGN, "dev_state is NULL or not 16-byte aligned");
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const Path path = choose_path(c, b, adam);
+    unsigned char* ws_ptr = static_cast<unsigned char*>(b->workspace);
+    Dyn* dyn = reinterpret_cast<Dyn*>(ws_ptr + ws::kDyn);
+    DevState* dst = static_cast<DevState*>(dev_state);
+    int launches = 0;
+    cudaError_t e = cudaMemsetAsync(b->workspace, 0, ws::kEnd, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace");
+    PrepArgs pa{dst, dyn, adam->beta1, adam->beta2, c->n_ranks, c->dtype};
+    e = launch_prepare(pa, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the prepare kernel");
+    launches++;
+    if (g_prof_start && (e = cudaEventRecord(g_prof_start, cs)) != cudaSuccess)
+        return cuda_fail(e, "recording the profiling start event");
+    for (int64_t bk = 0; bk < p->n_buckets; bk++) {
+        StepArgs a = make_args(c, p, b, adam, &host_view, path.fused, b->grads, 0);
+        a.dyn = dyn;
+        a.lo = bk * c->bucket_elems;
+        a.hi = a.lo + c->bucket_elems < c->n_params ? a.lo + c->bucket_elems : c->n_params;
+        e = path.fused ? launch_fused(c->stage, c->dtype, c->optimizer, a, cs, bk > 0)
+                       : launch_reduce(c->stage, c->dtype, path.clip, a, cs, bk > 0);
+        if (e != cudaSuccess) return cuda_fail(e, "launching a bucket kernel");
+        launches++;
+    }
+    if (!path.fused) {
+        if (path.clip) {
+            FinalArgs f;
+            f.ws = ws_ptr;
+            f.dtype = c->dtype;
+            f.win_lo = 0;
+            f.inv = 0.0;
+            f.max_norm = (double)adam->max_grad_norm;
+            f.dyn = dyn;
+            e = launch_finalize(f, cs);
+            if (e != cudaSuccess) return cuda_fail(e, "launching the norm finalize kernel");
+            launches++;
+        }
+        for (int64_t bk = 0; bk < p->n_buckets; bk++) {
+            StepArgs a = make_args(c, p, b, adam, &host_view, false, c->stage <= 1 ? b->grads : nullptr, 0);
+            a.dyn = dyn;
+            a.lo = bk * c->bucket_elems;
+            a.hi = a.lo + c->bucket_elems < c->n_params ? a.lo + c->bucket_elems : c->n_params;
+            e = launch_update(c->stage, c->dtype, c->optimizer, path.clip, a, cs, bk > 0);
+            if (e != cudaSuccess) return cuda_fail(e, "launching an update kernel");
+            launches++;
+        }
+    } else if (c->n_params > 0) {
+        StepArgs a = make_args(c, p, b, adam, &host_view, true, nullptr, 0);
+        a.dyn = dyn;
+        a.lo = 0;
+        a.hi = c->n_params;
+        e = launch_restore_async(c->stage, c->dtype, c->optimizer, a, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "launching the restore kernel");
+        launches++;
+    }
+    CommitArgs ca{dst, dyn, ws_ptr, path.clip ? 1 : 0};
+    e = launch_commit(ca, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the commit kernel");
+    launches++;
+    if (g_prof_end && (e = cudaEventRecord(g_prof_end, cs)) != cudaSuccess)
+        return cuda_fail(e, "recording the profiling end event");
+    if (path.fused) b->cur = 1 - b->cur;   // alternate on every call: an overflow copies the state across
+    if (kernel_launches) *kernel_launches = launches;
+    return ZERO_OK;
+}
+
+zero_status_t zero_dev_state_read(const void* dev_state, zero_state_t* s, zero_step_result_t* last, void* stream)
+{
+    if (!dev_state) return fail(ZERO_EINVAL, "dev_state is NULL");
+    DevState d;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&d, dev_state, sizeof d, cudaMemcpyDeviceToHost, cs);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device step state");
+    if (s) {
+        s->t = d.t;
+        s->loss_scale = d.loss_scale;
+        s->min_loss_scale = d.min_loss_scale;
+        s->dynamic = d.dynamic;
+        s->growth_interval = d.growth_interval;
+        s->good_steps = d.good_steps;
+    }
+    if (last) {
+        std::memset(last, 0, sizeof *last);
+        last->t = d.t;
+        last->overflow = d.last_overflow;
+        last->skipped = d.last_skipped;
+        last->grad_norm = d.last_grad_norm;
+        last->clip_coef = d.last_clip_coef;
+        last->new_loss_scale = d.loss_scale;
+        last->path = -1;
+    }
     return ZERO_OK;
 }
 

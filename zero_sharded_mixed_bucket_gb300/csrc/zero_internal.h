@@ -20,8 +20,19 @@ constexpr size_t kClip = 16;    // float: clip coefficient
 constexpr size_t kAcc = 32;     // 4 x uint64: 32-bit limbs of the fixed-point sum of squares
 constexpr size_t kBins = 64;    // 256 x uint64: sum of M^2 per exponent field, outside the window
 constexpr size_t kEnd = kBins + 256 * 8;
+constexpr size_t kDyn = 2176;   // Dyn: per-step scalars of a device-state step (written by the prepare kernel)
 constexpr int64_t kBytes = 4096;
 }  // namespace ws
+
+// Per-step scalars of a step whose loss scale and step count live on the
+// device: written by the prepare kernel, read by the step kernels.
+struct Dyn {
+    float inv;                      // 1/(S*N)
+    float bc1, bc2;                 // 1 - beta^(t+1)
+    int32_t win_lo;                 // sum-of-squares window
+    double inv_d;                   // the same 1/(S*N) as a double (finalize)
+    double beta1_pow_next, beta2_pow_next;
+};
 
 enum { kAdam = ZERO_ADAM, kSgdm = ZERO_SGD_MOMENTUM, kSgd = ZERO_SGD };
 
@@ -51,6 +62,7 @@ struct StepArgs {
     float inv;                      // 1/(S*N)
     AdamHP hp;
     int32_t win_lo;                 // lowest exponent E of the sum-of-squares window
+    const Dyn* dyn;                 // device-state step: scalars above come from here (else NULL)
 };
 
 struct FinalArgs {
@@ -59,6 +71,19 @@ struct FinalArgs {
     int32_t win_lo;
     double inv;
     double max_norm;
+    const Dyn* dyn;                 // device-state step: inv and win_lo from here
+};
+
+// Device-resident step state (the C ABI's zero_dev_state_t, same layout).
+struct DevState {
+    int64_t t;
+    double beta1_pow, beta2_pow;    // beta^t, by repeated multiplication
+    float loss_scale, min_loss_scale;
+    int32_t dynamic, growth_interval, good_steps;
+    uint32_t last_overflow;
+    double last_grad_norm;
+    float last_clip_coef;
+    int32_t last_skipped;
 };
 
 struct GatherArgs {
@@ -82,6 +107,26 @@ cudaError_t launch_update(int stage, int dtype, int opt, bool clip, const StepAr
                           bool overlap);
 cudaError_t launch_restore(int stage, int dtype, const StepArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
+
+// Device-state steps: per-step scalars from the state block, commit of the
+// outcome into it, and (fused path) the restore that also copies the
+// unchanged state into the copy the next step reads.
+struct PrepArgs {
+    DevState* st;
+    Dyn* dyn;
+    float beta1, beta2;
+    int32_t n_ranks;
+    int32_t dtype;
+};
+struct CommitArgs {
+    DevState* st;
+    const Dyn* dyn;
+    const unsigned char* ws;
+    int32_t clip;                   // the step clips (norm and coefficient valid)
+};
+cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s);
+cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);
+cudaError_t launch_restore_async(int stage, int dtype, int opt, const StepArgs& a, cudaStream_t s);
 
 // Record the thread-local message that zero_last_error() returns; gives back
 // `st`.  For entry points defined outside zero_host.cu.
