@@ -716,7 +716,11 @@ zero_status_t zero_step_async(const zero_config_t* c, const zero_plan_t* p, zero
             if (e != cudaSuccess) return cuda_fail(e, "launching an update kernel");
             launches++;
         }
-    } else if (c->n_params > 0) {
+    }
+    // the profiling span covers the bucket (and update) kernels, as in zero_step
+    if (g_prof_end && (e = cudaEventRecord(g_prof_end, cs)) != cudaSuccess)
+        return cuda_fail(e, "recording the profiling end event");
+    if (path.fused && c->n_params > 0) {
         StepArgs a = make_args(c, p, b, adam, &host_view, true, nullptr, 0);
         a.dyn = dyn;
         a.lo = 0;
@@ -729,8 +733,6 @@ zero_status_t zero_step_async(const zero_config_t* c, const zero_plan_t* p, zero
     e = launch_commit(ca, cs);
     if (e != cudaSuccess) return cuda_fail(e, "launching the commit kernel");
     launches++;
-    if (g_prof_end && (e = cudaEventRecord(g_prof_end, cs)) != cudaSuccess)
-        return cuda_fail(e, "recording the profiling end event");
     if (path.fused) b->cur = 1 - b->cur;   // alternate on every call: an overflow copies the state across
     if (kernel_launches) *kernel_launches = launches;
     return ZERO_OK;
