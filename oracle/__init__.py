@@ -28,7 +28,8 @@ What is here
     examples, display rule, Table 1, Table 2) and [P1] section 04.
 ``step``
     The unpartitioned mixed-precision Adam step (see zero_oracle.c for the
-    elementwise part).  The exact gradient norm for clipping uses
+    elementwise part); with dtype FP32 the fp32-training variant of the
+    pages' fp32 SGD examples (binary32 parameters and gradients).  The exact gradient norm for clipping uses
     ``math.fsum`` (a correctly rounded sum) of the squares, which are exact
     in fp64 for 16-bit inputs.
 
@@ -48,6 +49,7 @@ from . import build as _build
 
 FP16 = 0
 BF16 = 1
+FP32 = 2        # fp32 training: parameters and gradients in binary32 (b = 4)
 
 _lib = None
 
@@ -105,6 +107,18 @@ def _u16(a) -> np.ndarray:
     return a
 
 
+def bits_dtype(dtype: int):
+    """numpy type of the bit patterns of model-precision values."""
+    return np.uint32 if dtype == FP32 else np.uint16
+
+
+def _bits(a, dtype: int) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != bits_dtype(dtype):
+        raise TypeError("values are passed as %s bit patterns" % np.dtype(bits_dtype(dtype)).name)
+    return a
+
+
 def _f32arr(a) -> np.ndarray:
     a = np.ascontiguousarray(a)
     if a.dtype != np.float32:
@@ -121,7 +135,7 @@ def f32(x: float) -> float:
 # 16-bit formats
 # ---------------------------------------------------------------------------
 def to_f32(bits, dtype: int) -> np.ndarray:
-    bits = _u16(bits)
+    bits = _bits(bits, dtype)
     out = np.empty(bits.shape, np.float32)
     lib().oracle_to_f32_array(bits.size, _ptr(bits), dtype, _ptr(out))
     return out
@@ -129,7 +143,7 @@ def to_f32(bits, dtype: int) -> np.ndarray:
 
 def from_f32(x, dtype: int) -> np.ndarray:
     x = _f32arr(x)
-    out = np.empty(x.shape, np.uint16)
+    out = np.empty(x.shape, bits_dtype(dtype))
     lib().oracle_from_f32_array(x.size, _ptr(x), dtype, _ptr(out))
     return out
 
@@ -166,8 +180,9 @@ def bias_corrections(beta1: float, beta2: float, t: int) -> tuple[float, float]:
 def exact_sumsq(h, dtype: int) -> float:
     """sum_i h_i^2 over the finite elements, correctly rounded to fp64.
 
-    Each square of a 16-bit value is exact in fp64; math.fsum returns the
-    correctly rounded value of their exact sum."""
+    Each square of a 16-bit or binary32 value is exact in fp64 (at most 48
+    significant bits, exponents well inside fp64's range); math.fsum returns
+    the correctly rounded value of their exact sum."""
     x = to_f32(h, dtype).astype(np.float64)
     x = x[np.isfinite(x)]
     return math.fsum((x * x).tolist())
@@ -175,7 +190,11 @@ def exact_sumsq(h, dtype: int) -> float:
 
 def sumsq_fraction(h, dtype: int) -> Fraction:
     """The exact sum of squares as a rational, from the C oracle's exponent
-    bins (used to pin exact_sumsq and the GPU's integer accumulator)."""
+    bins (used to pin exact_sumsq and the GPU's integer accumulator); for
+    binary32 values, the sum of the exact rational squares."""
+    if dtype == FP32:
+        x = to_f32(h, dtype)
+        return sum((Fraction(float(v)) ** 2 for v in x[np.isfinite(x)]), Fraction(0))
     h = _u16(h)
     bins = np.zeros(256, np.uint64)
     lib().oracle_sumsq_bins(h.size, _ptr(h), dtype, _ptr(bins))
@@ -227,13 +246,14 @@ def scaler_update(scale: float, good_steps: int, overflow: bool, dynamic: bool,
 # ---------------------------------------------------------------------------
 def reduce(grads, dtype: int) -> tuple[np.ndarray, int]:
     """Rank-order fp32 sum of the N_d ranks' 16-bit gradients, rounded once to
-    the 16-bit type, and the overflow flag (any inf/NaN)."""
-    grads = [_u16(g) for g in grads]
+    the 16-bit type (FP32: the fp32 sum itself), and the overflow flag (any
+    inf/NaN)."""
+    grads = [_bits(g, dtype) for g in grads]
     n = grads[0].size
     if any(g.size != n for g in grads):
         raise ValueError("all ranks hold the same number of gradient elements")
     ptrs = (ctypes.c_void_p * len(grads))(*[_ptr(g) for g in grads])
-    h = np.empty(n, np.uint16)
+    h = np.empty(n, bits_dtype(dtype))
     flag = lib().oracle_reduce(len(grads), n, ptrs, dtype, _ptr(h))
     return h, int(flag)
 
@@ -254,11 +274,11 @@ def make_hyper(*, inv: float, clip: float | None, lr: float, beta1: float, beta2
 
 def adam(h, dtype: int, hyper: Hyper, w: np.ndarray, m: np.ndarray, v: np.ndarray) -> np.ndarray:
     """Adam on the fp32 master state (in place) and the 16-bit cast."""
-    h = _u16(h)
+    h = _bits(h, dtype)
     for a in (w, m, v):
         if a.dtype != np.float32 or not a.flags.c_contiguous or a.size != h.size:
             raise ValueError("state arrays are contiguous float32 of the gradient's length")
-    p16 = np.empty(h.size, np.uint16)
+    p16 = np.empty(h.size, bits_dtype(dtype))
     lib().oracle_adam(h.size, _ptr(h), dtype, ctypes.byref(hyper), _ptr(w), _ptr(m), _ptr(v), _ptr(p16))
     return p16
 
@@ -266,11 +286,11 @@ def adam(h, dtype: int, hyper: Hyper, w: np.ndarray, m: np.ndarray, v: np.ndarra
 def sgd(h, dtype: int, hyper: Hyper, w: np.ndarray, m=None) -> np.ndarray:
     """SGD (with momentum when m is given, mu = hyper.beta1) on the fp32
     master weights (in place) and the 16-bit cast."""
-    h = _u16(h)
+    h = _bits(h, dtype)
     for a in (w,) + ((m,) if m is not None else ()):
         if a.dtype != np.float32 or not a.flags.c_contiguous or a.size != h.size:
             raise ValueError("state arrays are contiguous float32 of the gradient's length")
-    p16 = np.empty(h.size, np.uint16)
+    p16 = np.empty(h.size, bits_dtype(dtype))
     lib().oracle_sgd(h.size, _ptr(h), dtype, ctypes.byref(hyper), _ptr(w), _ptr(m) if m is not None else None,
                      _ptr(p16))
     return p16
@@ -281,8 +301,9 @@ OPTIM_K = {"adam": 12, "sgdm": 8, "sgd": 4}   # fp32 bytes per parameter incl. t
 
 
 def cast16(w: np.ndarray, dtype: int) -> np.ndarray:
+    """The model-precision copy of w (16-bit patterns; FP32: w's own bits)."""
     w = _f32arr(w)
-    p = np.empty(w.size, np.uint16)
+    p = np.empty(w.size, bits_dtype(dtype))
     lib().oracle_cast(w.size, _ptr(w), dtype, _ptr(p))
     return p
 
@@ -295,7 +316,9 @@ def step(grads, w, m, v, *, dtype: int, lr: float, beta1: float, beta2: float, e
     optimizer="sgdm" -- SGD with momentum `momentum`, state w, m -- or "sgd",
     state w only).
 
-    grads: list of N_d uint16 arrays (each rank's 16-bit gradient, loss-scaled)
+    grads: list of N_d uint16 arrays (each rank's 16-bit gradient, loss-scaled;
+    uint32 binary32 patterns for dtype FP32, whose outputs h and p16 are
+    binary32 patterns too)
     w, m, v: fp32 master weights, momentum, variance (updated in place unless
     the step is skipped).  t: number of steps applied so far; this step
     applies Adam step t+1.
@@ -431,19 +454,21 @@ def comm_bytes(psi: int, n_ranks: int, stage: int, b: int = 2) -> dict:
                 counted_passes=COLLECTIVE_PASSES[stage])
 
 
-def hbm_bytes_per_param(n_ranks: int, stage: int, mode: str, state_bytes: int = 12) -> int:
+def hbm_bytes_per_param(n_ranks: int, stage: int, mode: str, state_bytes: int = 12, value_bytes: int = 2) -> int:
     """Algorithmic HBM bytes per parameter of one step with N_d simulated
     ranks in one memory.  mode 'fused': one pass, new state written beside the
     old; 'two_pass': reduced gradient materialised, then read back.
-    16-bit values are 2 bytes; state_bytes = fp32 state per parameter (12 for
-    Adam's w, m, v; 8 for SGD with momentum; 4 for SGD), read and written."""
-    N, sb = n_ranks, state_bytes
+    Gradient and parameter values are value_bytes each (2 for 16-bit, 4 for
+    fp32 training); state_bytes = fp32 state per parameter (12 for Adam's w,
+    m, v; 8 for SGD with momentum; 4 for SGD), read and written."""
+    N, sb, e = n_ranks, state_bytes, value_bytes
     if mode == "fused":
-        return {0: N * (6 + 2 * sb), 1: 6 * N + 2 * sb, 2: 4 * N + 2 * sb, 3: 2 * N + 2 * sb + 2}[stage]
+        return {0: N * (3 * e + 2 * sb), 1: 3 * e * N + 2 * sb, 2: 2 * e * N + 2 * sb, 3: e * N + 2 * sb + e}[stage]
     if mode == "two_pass":
-        return {0: N * (8 + 2 * sb), 1: 6 * N + 2 + 2 * sb, 2: 4 * N + 4 + 2 * sb, 3: 2 * N + 6 + 2 * sb}[stage]
-    if mode == "restore":   # after an overflowed fused step: read w, write each 16-bit copy
-        return {0: 6 * N, 1: 4 + 2 * N, 2: 4 + 2 * N, 3: 6}[stage]
+        return {0: N * (4 * e + 2 * sb), 1: 3 * e * N + e + 2 * sb, 2: 2 * e * N + 2 * e + 2 * sb,
+                3: e * N + 3 * e + 2 * sb}[stage]
+    if mode == "restore":   # after an overflowed fused step: read w, write each model-precision copy
+        return {0: (4 + e) * N, 1: 4 + e * N, 2: 4 + e * N, 3: 4 + e}[stage]
     raise ValueError(mode)
 
 

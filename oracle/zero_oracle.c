@@ -29,6 +29,11 @@
  * clipping and all scalar bookkeeping (bias-correction terms, loss scale)
  * live in oracle/__init__.py.
  *
+ * fp32 training (the pages' fp32 SGD / SGD-with-momentum examples, b = 4 bytes
+ * per parameter and gradient: ZeRO visual reading, worked examples C) is the
+ * same step with the model-precision type binary32: the rank-order sum is
+ * not rounded again and the "cast" of the master weights is the identity.
+ *
  * Build: gcc -O2 -ffp-contract=off -fno-fast-math -shared -fPIC (no FMA
  * contraction, so every fp32 operation below is one IEEE-754 rounding).
  */
@@ -38,6 +43,7 @@
 
 #define ORACLE_FP16 0
 #define ORACLE_BF16 1
+#define ORACLE_FP32 2
 
 /* ---------------------------------------------------------------------------
  * 16-bit formats, written from their definitions.
@@ -143,36 +149,58 @@ static uint16_t to_16(float x, int dtype)
     return dtype == ORACLE_BF16 ? oracle_f32_to_bf16(x) : oracle_f32_to_f16(x);
 }
 
-/* Bulk conversions, for the tests that pin the format code against library
- * routines. */
-void oracle_to_f32_array(int64_t n, const uint16_t* src, int32_t dtype, float* dst)
+/* Element i of an array of model-precision values (16-bit patterns, or
+ * binary32 for ORACLE_FP32), widened to fp32; and the store that rounds an
+ * fp32 value to the model precision (exact for ORACLE_FP32). */
+static float get_val(const void* a, int64_t i, int dtype)
 {
-    for (int64_t i = 0; i < n; i++)
-        dst[i] = to_f32(src[i], dtype);
+    if (dtype == ORACLE_FP32) {
+        float x;
+        memcpy(&x, (const char*)a + 4 * i, 4);
+        return x;
+    }
+    return to_f32(((const uint16_t*)a)[i], dtype);
 }
 
-void oracle_from_f32_array(int64_t n, const float* src, int32_t dtype, uint16_t* dst)
+static void put_val(void* a, int64_t i, float x, int dtype)
+{
+    if (dtype == ORACLE_FP32)
+        memcpy((char*)a + 4 * i, &x, 4);
+    else
+        ((uint16_t*)a)[i] = to_16(x, dtype);
+}
+
+/* Bulk conversions, for the tests that pin the format code against library
+ * routines. */
+void oracle_to_f32_array(int64_t n, const void* src, int32_t dtype, float* dst)
 {
     for (int64_t i = 0; i < n; i++)
-        dst[i] = to_16(src[i], dtype);
+        dst[i] = get_val(src, i, dtype);
+}
+
+void oracle_from_f32_array(int64_t n, const float* src, int32_t dtype, void* dst)
+{
+    for (int64_t i = 0; i < n; i++)
+        put_val(dst, i, src[i], dtype);
 }
 
 /* ---------------------------------------------------------------------------
  * Steps 1-2: gradient all-reduce in rank order, and the overflow check.
  *
  * h[i] = round16( (((0 + g_0[i]) + g_1[i]) + ...) + g_{N-1}[i] ), the sum in
- * fp32.  Returns 1 if any h[i] is inf or NaN, else 0.
+ * fp32 (for ORACLE_FP32 the fp32 sum itself).  Returns 1 if any h[i] is inf
+ * or NaN, else 0.
  * ------------------------------------------------------------------------- */
-uint32_t oracle_reduce(int32_t n_ranks, int64_t n, const uint16_t* const* grads,
-                       int32_t dtype, uint16_t* h)
+uint32_t oracle_reduce(int32_t n_ranks, int64_t n, const void* const* grads,
+                       int32_t dtype, void* h)
 {
     uint32_t overflow = 0;
     for (int64_t i = 0; i < n; i++) {
         float s = 0.0f;
         for (int32_t r = 0; r < n_ranks; r++)
-            s = s + to_f32(grads[r][i], dtype);
-        h[i] = to_16(s, dtype);
-        if (!isfinite(to_f32(h[i], dtype)))
+            s = s + get_val(grads[r], i, dtype);
+        put_val(h, i, s, dtype);
+        if (!isfinite(get_val(h, i, dtype)))
             overflow = 1;
     }
     return overflow;
@@ -229,11 +257,11 @@ typedef struct {
  *   w' = w - lr * ( (m'/bc1) / (sqrt(v'/bc2) + eps) )
  *   p  = round16(w')
  * w, m, v are updated in place; p16 receives the cast. */
-void oracle_adam(int64_t n, const uint16_t* h, int32_t dtype, const oracle_hyper_t* hp,
-                 float* w, float* m, float* v, uint16_t* p16)
+void oracle_adam(int64_t n, const void* h, int32_t dtype, const oracle_hyper_t* hp,
+                 float* w, float* m, float* v, void* p16)
 {
     for (int64_t i = 0; i < n; i++) {
-        float g = to_f32(h[i], dtype) * hp->inv_scale;
+        float g = get_val(h, i, dtype) * hp->inv_scale;
         if (hp->use_clip)
             g = g * hp->clip;
         float t1 = hp->beta1 * m[i];
@@ -252,7 +280,7 @@ void oracle_adam(int64_t n, const uint16_t* h, int32_t dtype, const oracle_hyper
         w[i] = w1;
         m[i] = m1;
         v[i] = v1;
-        p16[i] = to_16(w1, dtype);
+        put_val(p16, i, w1, dtype);
     }
 }
 
@@ -263,11 +291,11 @@ void oracle_adam(int64_t n, const uint16_t* h, int32_t dtype, const oracle_hyper
  *   plain (m == NULL):             w' = w - lr*g
  *   p  = round16(w')
  * hp->beta1 carries mu; beta2, eps and the bias corrections are unused. */
-void oracle_sgd(int64_t n, const uint16_t* h, int32_t dtype, const oracle_hyper_t* hp,
-                float* w, float* m, uint16_t* p16)
+void oracle_sgd(int64_t n, const void* h, int32_t dtype, const oracle_hyper_t* hp,
+                float* w, float* m, void* p16)
 {
     for (int64_t i = 0; i < n; i++) {
-        float g = to_f32(h[i], dtype) * hp->inv_scale;
+        float g = get_val(h, i, dtype) * hp->inv_scale;
         if (hp->use_clip)
             g = g * hp->clip;
         float d = g;
@@ -280,14 +308,14 @@ void oracle_sgd(int64_t n, const uint16_t* h, int32_t dtype, const oracle_hyper_
         float step = hp->lr * d;
         float w1 = w[i] - step;
         w[i] = w1;
-        p16[i] = to_16(w1, dtype);
+        put_val(p16, i, w1, dtype);
     }
 }
 
-/* The 16-bit model copy of the master weights (used to initialise the
+/* The model-precision copy of the master weights (used to initialise the
  * parameters and, after a skipped step, as their unchanged value). */
-void oracle_cast(int64_t n, const float* w, int32_t dtype, uint16_t* p16)
+void oracle_cast(int64_t n, const float* w, int32_t dtype, void* p16)
 {
     for (int64_t i = 0; i < n; i++)
-        p16[i] = to_16(w[i], dtype);
+        put_val(p16, i, w[i], dtype);
 }

@@ -15,7 +15,7 @@ import numpy as np
 
 from . import build as _build
 
-FP16, BF16 = 0, 1
+FP16, BF16, FP32 = 0, 1, 2
 STREAM_GRAD = 1
 STREAM_WEIGHT = 2
 STREAM_INJECT = 3
@@ -117,4 +117,27 @@ def inf_positions(n_params, n_ranks, *, seed, step, period=10 ** 9):
 
 
 def inf_bits(dtype):
-    return 0x7C00 if dtype == FP16 else 0x7F80
+    return {FP16: 0x7C00, BF16: 0x7F80, FP32: 0x7F800000}[dtype]
+
+
+# Gradients of any model precision, as bit patterns (uint16, or uint32 for
+# FP32, whose values are the fp32 draws themselves).
+def host_grad(n, dtype, sigma, *, seed, stream, step=0, rank=0, offset=0):
+    if dtype == FP32:
+        return host_normal32(n, sigma, seed=seed, stream=stream, step=step, rank=rank, offset=offset).view(np.uint32)
+    return host_normal16(n, dtype, sigma, seed=seed, stream=stream, step=step, rank=rank, offset=offset)
+
+
+def host_grad_at(idx, dtype, sigma, *, seed, stream, step=0, rank=0):
+    if dtype == FP32:
+        return host_normal32_at(idx, sigma, seed=seed, stream=stream, step=step, rank=rank).view(np.uint32)
+    return host_normal16_at(idx, dtype, sigma, seed=seed, stream=stream, step=step, rank=rank)
+
+
+def dev_grad(ptr, n, dtype, sigma, *, seed, stream, step=0, rank=0, offset=0, cuda_stream=0):
+    if dtype == FP32:
+        dev_normal32(ptr, n, sigma, seed=seed, stream=stream, step=step, rank=rank, offset=offset,
+                     cuda_stream=cuda_stream)
+    else:
+        dev_normal16(ptr, n, dtype, sigma, seed=seed, stream=stream, step=step, rank=rank, offset=offset,
+                     cuda_stream=cuda_stream)
