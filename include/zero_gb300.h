@@ -37,6 +37,9 @@
  *   in parameter order; the last one may be shorter.  Padding elements
  *   [Psi, padded) are never read or written by a step (keep them zero).
  *   16-bit buffers hold IEEE binary16 or bfloat16 bit patterns (dtype).
+ *   With dtype ZERO_FP32 (fp32 training) the gradient, parameter and
+ *   reduced buffers hold binary32 values instead -- 4 bytes per element,
+ *   the same element counts -- and the "16-bit" cast is the identity.
  *   Per rank r (device memory, caller-owned):
  *     grads[r]    16-bit gradient, grad16_elems = padded elements, flat index
  *                 order (loss-scaled).  Stages 0 and 1 overwrite it with the
@@ -114,7 +117,17 @@ typedef enum {
     ZERO_EUNSUPPORTED = 6    /* n_ranks outside 1..64, or another unsupported size */
 } zero_status_t;
 
-typedef enum { ZERO_FP16 = 0, ZERO_BF16 = 1 } zero_dtype_t;
+/* Model precision of gradients and parameters.  ZERO_FP16 / ZERO_BF16:
+ * mixed precision (b = 2 bytes, fp32 master state).  ZERO_FP32: fp32
+ * training as in the pages' fp32 SGD and SGD-with-momentum examples (b = 4;
+ * ZeRO visual reading, worked examples C): the reduced gradient is the fp32
+ * rank-order sum itself and the parameters equal the fp32 master weights
+ * bit for bit.  The library still keeps the master shard w apart from the
+ * parameter copies (a step can then be discarded), so its state holds 4
+ * bytes per parameter more than the pages' K; gradient clipping is not
+ * available with ZERO_FP32 (ZERO_EUNSUPPORTED).  The no-allocation stage-2
+ * entry point takes 16-bit types only. */
+typedef enum { ZERO_FP16 = 0, ZERO_BF16 = 1, ZERO_FP32 = 2 } zero_dtype_t;
 
 /* Optimizer on the fp32 master weights ("ZeRO visual reading", accounting
  * with b and K: mixed-precision Adam K = 12, SGD with momentum K = 8, SGD
@@ -148,11 +161,12 @@ typedef struct zero_plan {
     int64_t grad16_elems;        /* per rank: N*P */
     int64_t reduced_elems;       /* N*P in stages 2-3 (two-pass path), else 0 */
     int64_t workspace_bytes;
-    int64_t hbm_bytes_fused;     /* algorithmic HBM bytes of one fused step (below) */
+    int64_t hbm_bytes_fused;     /* algorithmic HBM bytes of one fused step (each array access once) */
     int64_t hbm_bytes_two_pass;  /* algorithmic HBM bytes of one two-pass step */
     int64_t comm_counted_bytes;  /* bytes crossing simulated rank boundaries per step, all ranks */
-    double comm_paper_bytes;     /* per rank per step: 2*Psi*2 (stages 0-2), 3*Psi*2 (stage 3) */
-    double mem_total_bytes;      /* per rank, paper formula (b = 2, K of the optimizer), see zero_model_state_bytes */
+    double comm_paper_bytes;     /* per rank per step: 2*Psi*b (stages 0-2), 3*Psi*b (stage 3) */
+    double mem_total_bytes;      /* per rank, paper formula (b = 2, or 4 for ZERO_FP32; K = the fp32
+                                    state bytes kept), see zero_model_state_bytes */
     double reserved;
 } zero_plan_t;
 

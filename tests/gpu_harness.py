@@ -18,6 +18,17 @@ def as_u16(t: torch.Tensor) -> np.ndarray:
     return t.cpu().numpy().view(np.uint16)
 
 
+def as_bits(t: torch.Tensor) -> np.ndarray:
+    """Bit patterns of a value buffer: uint16 (16-bit types) or uint32
+    (binary32 values, held in int32 tensors)."""
+    return t.cpu().numpy().view(np.uint32 if t.dtype == torch.int32 else np.uint16)
+
+
+def as_signed(a: np.ndarray) -> np.ndarray:
+    """Host bit patterns in the signed type of the device tensors."""
+    return a.view(np.int32 if a.dtype == np.uint32 else np.int16)
+
+
 def as_u32(a) -> np.ndarray:
     if isinstance(a, torch.Tensor):
         a = a.cpu().numpy()
@@ -81,9 +92,9 @@ class Job:
             if stage == 3:
                 lo, hi = r * P, min((r + 1) * P, n)
                 if hi > lo:
-                    self.bufs.params16[r][:hi - lo].copy_(torch.from_numpy(p0[lo:hi].view(np.int16)))
+                    self.bufs.params16[r][:hi - lo].copy_(torch.from_numpy(as_signed(p0[lo:hi])))
             else:
-                self.bufs.params16[r][:n].copy_(torch.from_numpy(p0.view(np.int16)))
+                self.bufs.params16[r][:n].copy_(torch.from_numpy(as_signed(p0)))
         self.p16 = p0
         self.h = None
         self.last_ref = None
@@ -92,7 +103,7 @@ class Job:
     # -- inputs -------------------------------------------------------------
     def make_grads(self, step, inject=()):
         S = self.o["loss_scale"]
-        grads = [synth.host_normal16(self.n, self.dtype, self.sigma * S, seed=self.seed, stream=synth.STREAM_GRAD,
+        grads = [synth.host_grad(self.n, self.dtype, self.sigma * S, seed=self.seed, stream=synth.STREAM_GRAD,
                                      step=step, rank=r) for r in range(self.N)]
         for r, i, bits in inject:
             grads[r][i] = bits
@@ -100,7 +111,7 @@ class Job:
 
     def load_grads(self, grads):
         for r in range(self.N):
-            self.bufs.grads[r][:self.n].copy_(torch.from_numpy(grads[r].view(np.int16)))
+            self.bufs.grads[r][:self.n].copy_(torch.from_numpy(as_signed(grads[r])))
 
     # -- one step on both sides ------------------------------------------------
     def step(self, grads, per_bucket=False):
@@ -158,16 +169,16 @@ class Job:
         for r in range(N):
             if self.stage == 3:
                 lo, hi = r * P, min((r + 1) * P, n)
-                got = as_u16(self.bufs.params16[r][:max(hi - lo, 0)])
+                got = as_bits(self.bufs.params16[r][:max(hi - lo, 0)])
                 assert np.array_equal(got, self.p16[lo:hi]), "param shard of rank %d differs" % r
                 assert not self.bufs.params16[r][max(hi - lo, 0):].any().item()
             else:
-                got = as_u16(self.bufs.params16[r][:n])
+                got = as_bits(self.bufs.params16[r][:n])
                 bad = int((got != self.p16).sum())
                 assert bad == 0, "params16 of rank %d: %d elements differ" % (r, bad)
                 assert not self.bufs.params16[r][n:].any().item()
         if self.stage <= 1:
             for r in range(N):
-                assert same16(as_u16(self.bufs.grads[r][:n]), self.h, self.dtype), "all-reduce result, rank %d" % r
+                assert same16(as_bits(self.bufs.grads[r][:n]), self.h, self.dtype), "all-reduce result, rank %d" % r
         elif res.path == 1:
-            assert same16(as_u16(self.bufs.reduced[:n]), self.h, self.dtype), "reduced gradient"
+            assert same16(as_bits(self.bufs.reduced[:n]), self.h, self.dtype), "reduced gradient"

@@ -72,6 +72,17 @@ def test_plan_matches_oracle(n, N, stage, B, A, layers):
         assert q.hbm_bytes_two_pass == oracle.hbm_bytes_per_param(N, stage, "two_pass", K) * n
         exact = oracle.model_state_bytes(n, N, stage, K=K)["total"]
         assert abs(Fraction(q.mem_total_bytes) - exact) <= exact * Fraction(1, 10 ** 15)
+    for opt, name in ((zg.ZERO_ADAM, "adam"), (zg.ZERO_SGD_MOMENTUM, "sgdm"), (zg.ZERO_SGD, "sgd")):
+        # fp32 training: 4-byte gradients and parameters, the same fp32 state
+        q = zg.zero_plan(zg.Config(n, N, stage, B, A, layers, zg.ZERO_FP32, opt))
+        K = oracle.OPTIM_K[name]
+        assert (q.shard_elems, q.padded_elems, q.grad16_elems) == (p.shard_elems, p.padded_elems, p.grad16_elems)
+        assert q.hbm_bytes_fused == oracle.hbm_bytes_per_param(N, stage, "fused", K, 4) * n
+        assert q.hbm_bytes_two_pass == oracle.hbm_bytes_per_param(N, stage, "two_pass", K, 4) * n
+        c4 = oracle.comm_bytes(n, N, stage, b=4)
+        assert q.comm_counted_bytes == c4["counted"] and Fraction(q.comm_paper_bytes) == c4["paper"]
+        exact = oracle.model_state_bytes(n, N, stage, b=4, K=K)["total"]
+        assert abs(Fraction(q.mem_total_bytes) - exact) <= exact * Fraction(1, 10 ** 15)
     c = oracle.comm_bytes(n, N, stage)
     assert p.comm_counted_bytes == c["counted"] and Fraction(p.comm_paper_bytes) == c["paper"]
     # a double: exact when N is a power of two, else within a few ulps
@@ -127,7 +138,7 @@ def test_examples_and_comm_through_the_library():
     (dict(bucket_elems=0), zg.ZERO_EINVAL),
     (dict(align_elems=6), zg.ZERO_EINVAL),
     (dict(n_params=-1), zg.ZERO_EINVAL),
-    (dict(dtype=2), zg.ZERO_EINVAL),
+    (dict(dtype=3), zg.ZERO_EINVAL),
     (dict(optimizer=3), zg.ZERO_EINVAL),
 ])
 def test_config_rejected(kw, status):
@@ -208,6 +219,20 @@ def test_step_argument_checks_reject_before_any_launch():
     fb.b.reduced = None
     assert _step_status(cfg, plan, fb, adam=zg.zero_adam_t(lr=1e-4, beta1=0.9, beta2=0.999,
                                                            max_grad_norm=1.0)) == zg.ZERO_ENOMEM
+    # fp32 training has no clipping path
+    cfg32 = zg.Config(1000, 4, 2, 64, 0, None, zg.ZERO_FP32)
+    plan32 = zg.zero_plan(cfg32)
+    assert _step_status(cfg32, plan32, _FakeBuffers(4), adam=zg.zero_adam_t(lr=1e-4, beta1=0.9, beta2=0.999,
+                                                                           max_grad_norm=1.0)) == zg.ZERO_EUNSUPPORTED
+    assert "ZERO_FP32" in zg.zero_last_error()
+    res32 = zg.zero_step_result_t()
+    st = zg.lib().zero_step_stage2_noalloc(ctypes.byref(cfg32.c), ctypes.byref(plan32),
+                                           ctypes.byref(_FakeBuffers(4).b),
+                                           ctypes.byref(zg.zero_adam_t(lr=1e-4, beta1=0.9, beta2=0.999)),
+                                           ctypes.byref(zg.zero_state_t(loss_scale=1.0)), None, ctypes.byref(res32))
+    assert st == zg.ZERO_EUNSUPPORTED
+    assert zg.lib().zero_plan(ctypes.byref(zg.Config(1000, 4, 2, 64, 0, None, 3).c),
+                              ctypes.byref(zg.zero_plan_t())) == zg.ZERO_EINVAL
     # wrong stage entry point
     res = zg.zero_step_result_t()
     st = zg.lib().zero_step_stage3(ctypes.byref(cfg.c), ctypes.byref(plan), ctypes.byref(_FakeBuffers(4).b),

@@ -1,7 +1,8 @@
 """Out-of-bounds writes, checked without a sanitizer: every buffer the
 library is given sits between two guard regions filled with a pattern, and
-after steps across stages, paths, optimizers and ragged sizes (plus stage-3
-gathers and fetches) every guard must still hold its pattern."""
+after steps across stages, paths, optimizers, value types (16-bit and
+binary32) and ragged sizes (plus stage-3 gathers and fetches) every guard
+must still hold its pattern."""
 import ctypes
 
 import pytest
@@ -22,7 +23,7 @@ class Guarded:
 
     def __init__(self, n, dtype):
         self.full = torch.empty(n + 2 * GUARD, dtype=dtype, device="cuda")
-        if dtype == torch.float32:
+        if dtype in (torch.float32, torch.int32):
             self.full.view(torch.int32).fill_(PAT32)
         else:
             self.full.fill_(PAT16 if dtype == torch.int16 else 0xA5)
@@ -42,10 +43,11 @@ class Guarded:
 
 def _buffers(cfg, plan, shadow, reduced):
     N = cfg.c.n_ranks
-    g = [Guarded(plan.grad16_elems, torch.int16) for _ in range(N)]
-    p = [Guarded(plan.param16_elems, torch.int16) for _ in range(N)]
+    vt = torch.int32 if cfg.c.dtype == zg.ZERO_FP32 else torch.int16    # binary32 values, or 16-bit
+    g = [Guarded(plan.grad16_elems, vt) for _ in range(N)]
+    p = [Guarded(plan.param16_elems, vt) for _ in range(N)]
     st = {k: [Guarded(plan.state_elems, torch.float32) for _ in range(2 if shadow else 1)] for k in "wmv"}
-    red = Guarded(max(plan.reduced_elems, 1), torch.int16) if reduced else None
+    red = Guarded(max(plan.reduced_elems, 1), vt) if reduced else None
     ws = Guarded(plan.workspace_bytes, torch.uint8)
     for k in "wmv":
         for x in st[k]:
@@ -75,6 +77,10 @@ CASES = [
     (3, 5, 7 * 256 + 1, 256, 8, 0, True, 0.0, zg.ZERO_SGD),
     (3, 5, 7 * 256 + 1, 256, 64, 0, False, 1.0, zg.ZERO_ADAM),
     (0, 1, 7, 8, 8, 0, True, 0.0, zg.ZERO_ADAM),
+    (0, 3, 3 * 1024 + 5, 1024, 8, 2, True, 0.0, zg.ZERO_ADAM),
+    (1, 3, 2 * 1024 + 7, 1024, 16, 2, False, 0.0, zg.ZERO_SGD_MOMENTUM),
+    (2, 4, 5 * 512 + 3, 512, 8, 2, True, 0.0, zg.ZERO_SGD_MOMENTUM),
+    (3, 5, 7 * 256 + 1, 256, 8, 2, False, 0.0, zg.ZERO_SGD),
 ]
 
 
@@ -93,7 +99,7 @@ def test_steps_write_only_inside_their_buffers(case):
     s = torch.cuda.current_stream()
     for step in (1, 2, 3):
         for r in range(N):
-            synth.dev_normal16(grads[r].ptr(), n, dtype, 8e-3, seed=0, stream=synth.STREAM_GRAD, step=step, rank=r)
+            synth.dev_grad(grads[r].ptr(), n, dtype, 8e-3, seed=0, stream=synth.STREAM_GRAD, step=step, rank=r)
         if step == 2:
             grads[N - 1].t[n - 1] = synth.inf_bits(dtype)       # an overflowed step (restore path)
         res = zg.zero_step(cfg, plan, b, adam, state, s)

@@ -20,7 +20,7 @@ from . import build as _build
 
 __all__ = [
     "ZERO_OK", "ZERO_EINVAL", "ZERO_EALIGN", "ZERO_ENOMEM", "ZERO_ECUDA", "ZERO_ETIMEOUT", "ZERO_EUNSUPPORTED",
-    "ZERO_FP16", "ZERO_BF16", "ZERO_ADAM", "ZERO_SGD_MOMENTUM", "ZERO_SGD", "ZeroError", "zero_config_t", "zero_plan_t", "zero_adam_t", "zero_state_t",
+    "ZERO_FP16", "ZERO_BF16", "ZERO_FP32", "ZERO_ADAM", "ZERO_SGD_MOMENTUM", "ZERO_SGD", "ZeroError", "zero_config_t", "zero_plan_t", "zero_adam_t", "zero_state_t",
     "zero_buffers_t", "zero_step_result_t", "Config", "lib", "lib_path",
     "zero_plan", "zero_plan_bucket", "zero_plan_layer", "zero_model_state_bytes", "zero_comm_bytes",
     "zero_step", "zero_step_stage0", "zero_step_stage1", "zero_step_stage2", "zero_step_stage3",
@@ -31,7 +31,7 @@ __all__ = [
 ]
 
 ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ENOMEM, ZERO_ECUDA, ZERO_ETIMEOUT, ZERO_EUNSUPPORTED = range(7)
-ZERO_FP16, ZERO_BF16 = 0, 1
+ZERO_FP16, ZERO_BF16, ZERO_FP32 = 0, 1, 2
 ZERO_ADAM, ZERO_SGD_MOMENTUM, ZERO_SGD = 0, 1, 2
 
 c_i64, c_i32, c_u32, c_f, c_d, c_vp = (ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_float,
@@ -369,9 +369,11 @@ class Fetcher:
 class DeviceBuffers:
     """Device memory for one job, allocated with PyTorch to the plan's sizes.
 
-    grads[r], params16[r]: int16 tensors (16-bit bit patterns); w/m/v[k]:
-    float32 tensors (k = 0 current, 1 shadow when shadow=True); reduced
-    (stages 2-3); workspace.  ``b`` is the zero_buffers_t that points at them.
+    grads[r], params16[r]: int16 tensors (16-bit bit patterns; int32 tensors
+    of binary32 patterns for ZERO_FP32); w/m/v[k]: float32 tensors (k = 0
+    current, 1 shadow when shadow=True); reduced (stages 2-3, same element
+    type as the gradients); workspace.  ``b`` is the zero_buffers_t that
+    points at them.
     """
 
     def __init__(self, cfg, plan: zero_plan_t, device="cuda", shadow: bool = True, reduced: bool = True,
@@ -380,13 +382,15 @@ class DeviceBuffers:
         c = cfg.c if isinstance(cfg, Config) else cfg
         N = c.n_ranks
         z = lambda n, dt: torch.zeros(max(int(n), 1), dtype=dt, device=device)
-        self.grads = [z(plan.grad16_elems, torch.int16) for _ in range(N)] if grads else []
-        self.params16 = [z(plan.param16_elems, torch.int16) for _ in range(N)]
+        vt = torch.int32 if c.dtype == ZERO_FP32 else torch.int16
+        self.value_dtype = vt
+        self.grads = [z(plan.grad16_elems, vt) for _ in range(N)] if grads else []
+        self.params16 = [z(plan.param16_elems, vt) for _ in range(N)]
         ncopy = 2 if shadow else 1
         self.w = [z(plan.state_elems, torch.float32) for _ in range(ncopy)]
         self.m = [z(plan.state_elems, torch.float32) for _ in range(ncopy)]
         self.v = [z(plan.state_elems, torch.float32) for _ in range(ncopy)]
-        self.reduced = z(plan.reduced_elems, torch.int16) if (reduced and plan.reduced_elems) else None
+        self.reduced = z(plan.reduced_elems, vt) if (reduced and plan.reduced_elems) else None
         self.workspace = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device=device)
         self._gp = (c_vp * N)(*[t.data_ptr() for t in self.grads]) if grads else None
         self._pp = (c_vp * N)(*[t.data_ptr() for t in self.params16])

@@ -1,5 +1,6 @@
-// Device helpers shared by the step kernels: 16-bit formats, vector memory
-// access with streaming cache hints, the Adam element update and the exact
+// Device helpers shared by the step kernels: the model-precision formats
+// (binary16, bfloat16, and binary32 for fp32 training), vector memory access
+// with streaming cache hints, the optimizer element updates and the exact
 // sum-of-squares accumulator.
 #pragma once
 
@@ -7,17 +8,24 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "zero_internal.h"
 
 namespace zg {
 
-enum { kF16 = ZERO_FP16, kBF16 = ZERO_BF16 };
+enum { kF16 = ZERO_FP16, kBF16 = ZERO_BF16, kF32 = ZERO_FP32 };
 
-// ---- 16-bit formats --------------------------------------------------------
+// ---- model-precision formats -------------------------------------------------
+// Gradients and parameters are binary16 or bfloat16 bit patterns in mixed
+// precision, binary32 in fp32 training (where widening and narrowing are the
+// identity).
 template <int DT>
 __device__ __forceinline__ float to_f32(uint32_t bits)
 {
-    if constexpr (DT == kBF16)
+    if constexpr (DT == kF32)
+        return __uint_as_float(bits);
+    else if constexpr (DT == kBF16)
         return __uint_as_float(bits << 16);
     else
         return __half2float(__ushort_as_half((unsigned short)bits));
@@ -27,19 +35,12 @@ __device__ __forceinline__ float to_f32(uint32_t bits)
 template <int DT>
 __device__ __forceinline__ uint32_t from_f32(float x)
 {
-    if constexpr (DT == kBF16)
+    if constexpr (DT == kF32)
+        return __float_as_uint(x);
+    else if constexpr (DT == kBF16)
         return __bfloat16_as_ushort(__float2bfloat16_rn(x));
     else
         return __half_as_ushort(__float2half_rn(x));
-}
-
-template <int DT>
-__device__ __forceinline__ bool nonfinite16(uint32_t bits)
-{
-    if constexpr (DT == kBF16)
-        return (bits & 0x7f80u) == 0x7f80u;
-    else
-        return (bits & 0x7c00u) == 0x7c00u;
 }
 
 // Two 16-bit values packed in a word (element 2p in the low half).
@@ -133,6 +134,109 @@ __device__ __forceinline__ void st_h8(void* base, int64_t idx, const H8& h, int 
     }
 }
 
+// 8 binary32 values (fp32 training), as bit patterns.
+struct W8 {
+    uint32_t w[8];
+    __device__ __forceinline__ uint32_t get(int j) const { return w[j]; }
+    __device__ __forceinline__ void set(int j, uint32_t b) { w[j] = b; }
+};
+
+// A group of 8 model-precision values.
+template <int DT>
+using V8 = typename std::conditional<DT == kF32, W8, H8>::type;
+
+__device__ __forceinline__ W8 ld_w8(const void* base, int64_t idx, int cnt)
+{
+    const uint32_t* p = static_cast<const uint32_t*>(base) + idx;
+    W8 r;
+    if (cnt == kVec) {
+        const uint4 a = __ldcs(reinterpret_cast<const uint4*>(p));
+        const uint4 b = __ldcs(reinterpret_cast<const uint4*>(p) + 1);
+        r.w[0] = a.x; r.w[1] = a.y; r.w[2] = a.z; r.w[3] = a.w;
+        r.w[4] = b.x; r.w[5] = b.y; r.w[6] = b.z; r.w[7] = b.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < kVec; j++)
+            r.w[j] = j < cnt ? p[j] : 0u;
+    }
+    return r;
+}
+
+__device__ __forceinline__ void st_w8(void* base, int64_t idx, const W8& v, int cnt)
+{
+    uint32_t* p = static_cast<uint32_t*>(base) + idx;
+    if (cnt == kVec) {
+        __stcs(reinterpret_cast<uint4*>(p), make_uint4(v.w[0], v.w[1], v.w[2], v.w[3]));
+        __stcs(reinterpret_cast<uint4*>(p) + 1, make_uint4(v.w[4], v.w[5], v.w[6], v.w[7]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < kVec; j++)
+            if (j < cnt) p[j] = v.w[j];
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ V8<DT> ld8(const void* base, int64_t idx, int cnt)
+{
+    if constexpr (DT == kF32)
+        return ld_w8(base, idx, cnt);
+    else
+        return ld_h8(base, idx, cnt);
+}
+
+template <int DT>
+__device__ __forceinline__ void st8(void* base, int64_t idx, const V8<DT>& v, int cnt)
+{
+    if constexpr (DT == kF32)
+        st_w8(base, idx, v, cnt);
+    else
+        st_h8(base, idx, v, cnt);
+}
+
+// Nonzero if the binary32 pattern is inf or NaN.
+__device__ __forceinline__ uint32_t nonfinite32(uint32_t b) { return (~b & 0x7f800000u) == 0u; }
+
+// h = the fp32 sums s in the model precision (one rounding to nearest even
+// for 16-bit types, none for binary32); returns nonzero if any element of h
+// is inf or NaN.  Elements past cnt are 0: finite.
+template <int DT>
+__device__ __forceinline__ uint32_t round_group(const float s[kVec], V8<DT>& h)
+{
+    uint32_t nf = 0;
+    if constexpr (DT == kF32) {
+#pragma unroll
+        for (int j = 0; j < kVec; j++) {
+            h.w[j] = __float_as_uint(s[j]);
+            nf |= nonfinite32(h.w[j]);
+        }
+    } else {
+#pragma unroll
+        for (int p = 0; p < kVec / 2; p++) {
+            h.w[p] = from_f32x2<DT>(s[2 * p], s[2 * p + 1]);
+            nf |= nonfinite_x2<DT>(h.w[p]);
+        }
+    }
+    return nf;
+}
+
+// g = float(h) * inv, elementwise.
+template <int DT>
+__device__ __forceinline__ void unscale_group(const V8<DT>& h, float inv, float g[kVec])
+{
+    if constexpr (DT == kF32) {
+#pragma unroll
+        for (int j = 0; j < kVec; j++)
+            g[j] = __fmul_rn(__uint_as_float(h.w[j]), inv);
+    } else {
+#pragma unroll
+        for (int p = 0; p < kVec / 2; p++) {
+            const float2 f = to_f32x2<DT>(h.w[p]);
+            g[2 * p] = __fmul_rn(f.x, inv);
+            g[2 * p + 1] = __fmul_rn(f.y, inv);
+        }
+    }
+}
+
 __device__ __forceinline__ void ld_f8(const float* base, int64_t idx, int cnt, float x[kVec])
 {
     const float* p = base + idx;
@@ -161,15 +265,34 @@ __device__ __forceinline__ void st_f8(float* base, int64_t idx, int cnt, const f
     }
 }
 
-// Rank-order fp32 sum of the N ranks' 16-bit gradients for one group:
+// Rank-order fp32 sum of the N ranks' gradients for one group:
 // s[j] = (((0 + g_0[j]) + g_1[j]) + ...) + g_{N-1}[j].  Loads are issued in
-// batches of 8 ranks so that up to 8 x 16 bytes are in flight per thread.
+// batches of 8 ranks (16-bit) or 4 ranks (binary32), so that up to 128
+// bytes are in flight per thread.
 template <int DT>
 __device__ __forceinline__ void reduce_group(const StepArgs& a, int64_t gidx, int cnt, float s[kVec])
 {
 #pragma unroll
     for (int j = 0; j < kVec; j++)
         s[j] = 0.0f;
+    if constexpr (DT == kF32) {
+        for (int r0 = 0; r0 < a.n_ranks; r0 += 4) {
+            W8 q[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++)
+                if (r0 + k < a.n_ranks)
+                    q[k] = ld_w8(a.grads[r0 + k], gidx, cnt);
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                if (r0 + k < a.n_ranks) {
+#pragma unroll
+                    for (int j = 0; j < kVec; j++)
+                        s[j] = __fadd_rn(s[j], __uint_as_float(q[k].w[j]));
+                }
+            }
+        }
+        return;
+    }
     for (int r0 = 0; r0 < a.n_ranks; r0 += 8) {
         H8 q[8];
 #pragma unroll
@@ -231,10 +354,10 @@ __device__ __forceinline__ void sgd1(float g, float& w, const AdamHP& hp)
 
 // The optimizer update of one group: load the fp32 state the optimizer keeps
 // at state index si (w; m; v), update it with the 8 unscaled gradients g,
-// store it to the output state and give back the 16-bit cast in p.
+// store it to the output state and give back the model-precision cast in p.
 template <int DT, int OPT>
 __device__ __forceinline__ void update_state(const StepArgs& a, const AdamHP& hp, int64_t si, int cnt,
-                                             const float g[kVec], H8& p)
+                                             const float g[kVec], V8<DT>& p)
 {
     float w[kVec];
     ld_f8(a.w_in, si, cnt, w);

@@ -100,18 +100,18 @@ __global__ void __launch_bounds__(kThreads) k_restore_async(const __grid_constan
                 ld_f8(a.v_in, si, cnt, v);
                 st_f8(a.v_out, si, cnt, v);
             }
-            H8 p;
+            V8<DT> p;
 #pragma unroll
-            for (int q = 0; q < kVec / 2; q++)
-                p.w[q] = from_f32x2<DT>(w[2 * q], w[2 * q + 1]);
+            for (int j = 0; j < kVec; j++)
+                p.set(j, from_f32<DT>(w[j]));
             if constexpr (STAGE == 0) {
-                st_h8(a.params16[r], i, p, cnt);
+                st8<DT>(a.params16[r], i, p, cnt);
             } else if constexpr (STAGE == 3) {
                 const int o = owner_of(i, a.shard);
-                st_h8(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
+                st8<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
             } else {
                 for (int q = 0; q < a.n_ranks; q++)
-                    st_h8(a.params16[q], i, p, cnt);
+                    st8<DT>(a.params16[q], i, p, cnt);
             }
         }
     }
@@ -164,6 +164,7 @@ cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s)
 
 cudaError_t launch_restore_async(int stage, int dtype, int opt, const StepArgs& a, cudaStream_t s)
 {
+    if (dtype == kF32) return restore_stage<kF32>(stage, opt, a, s);
     return dtype == kBF16 ? restore_stage<kBF16>(stage, opt, a, s) : restore_stage<kF16>(stage, opt, a, s);
 }
 

@@ -1,5 +1,5 @@
 // Fused per-bucket step: reduce-scatter + overflow check + unscale + Adam +
-// 16-bit cast + all-gather, one HBM pass.  New fp32 state goes to the shadow
+// model-precision cast + all-gather, one HBM pass.  New fp32 state goes to the shadow
 // copy; the host commits it once the global overflow flag is known.
 //
 // Stage 0 (plain data parallelism): the reduced gradient is written back to
@@ -45,40 +45,32 @@ __global__ void __launch_bounds__(kThreads, STAGE == 0 ? 5 : 1) k_fused(const __
         float s[kVec];
         reduce_group<DT>(a, gidx, cnt, s);
 
-        // round to 16 bits (elements past cnt are 0: finite, no effect)
-        H8 h;
+        // round to the model precision (elements past cnt are 0: finite, no effect)
+        V8<DT> h;
+        bad |= round_group<DT>(s, h) != 0;
         float g[kVec];
-        uint32_t nf = 0;
-#pragma unroll
-        for (int p = 0; p < kVec / 2; p++) {
-            h.w[p] = from_f32x2<DT>(s[2 * p], s[2 * p + 1]);
-            nf |= nonfinite_x2<DT>(h.w[p]);
-            const float2 f = to_f32x2<DT>(h.w[p]);
-            g[2 * p] = __fmul_rn(f.x, inv);
-            g[2 * p + 1] = __fmul_rn(f.y, inv);
-        }
-        bad |= nf != 0;
+        unscale_group<DT>(h, inv, g);
 
         if constexpr (STAGE <= 1) {
             for (int r = 0; r < a.n_ranks; r++)
-                st_h8(const_cast<void*>(a.grads[r]), gidx, h, cnt);
+                st8<DT>(const_cast<void*>(a.grads[r]), gidx, h, cnt);
         }
 
         if constexpr (STAGE == 0) {
             for (int r = 0; r < a.n_ranks; r++) {
-                H8 p;
+                V8<DT> p;
                 update_state<DT, OPT>(a, hp, (int64_t)r * a.replica_stride + i, cnt, g, p);
-                st_h8(a.params16[r], i, p, cnt);
+                st8<DT>(a.params16[r], i, p, cnt);
             }
         } else {
-            H8 p;
+            V8<DT> p;
             update_state<DT, OPT>(a, hp, i, cnt, g, p);
             if constexpr (STAGE == 3) {
                 const int o = owner_of(i, a.shard);
-                st_h8(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
+                st8<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
             } else {
                 for (int r = 0; r < a.n_ranks; r++)
-                    st_h8(a.params16[r], i, p, cnt);
+                    st8<DT>(a.params16[r], i, p, cnt);
             }
         }
     }
@@ -101,18 +93,18 @@ __global__ void __launch_bounds__(kThreads) k_restore(const __grid_constant__ St
         for (int r = 0; r < reps; r++) {
             float w[kVec];
             ld_f8(a.w_in, (int64_t)r * a.replica_stride + i, cnt, w);
-            H8 p;
+            V8<DT> p;
 #pragma unroll
             for (int j = 0; j < kVec; j++)
                 p.set(j, from_f32<DT>(w[j]));
             if constexpr (STAGE == 0) {
-                st_h8(a.params16[r], i, p, cnt);
+                st8<DT>(a.params16[r], i, p, cnt);
             } else if constexpr (STAGE == 3) {
                 const int o = owner_of(i, a.shard);
-                st_h8(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
+                st8<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
             } else {
                 for (int q = 0; q < a.n_ranks; q++)
-                    st_h8(a.params16[q], i, p, cnt);
+                    st8<DT>(a.params16[q], i, p, cnt);
             }
         }
     }
@@ -157,6 +149,13 @@ cudaError_t run_restore(const StepArgs& a, cudaStream_t s)
             case 1: return fn<1, kBF16>(__VA_ARGS__);                                 \
             case 2: return fn<2, kBF16>(__VA_ARGS__);                                 \
             default: return fn<3, kBF16>(__VA_ARGS__);                                \
+            }                                                                         \
+        } else if ((dtype) == kF32) {                                                 \
+            switch (stage) {                                                          \
+            case 0: return fn<0, kF32>(__VA_ARGS__);                                  \
+            case 1: return fn<1, kF32>(__VA_ARGS__);                                  \
+            case 2: return fn<2, kF32>(__VA_ARGS__);                                  \
+            default: return fn<3, kF32>(__VA_ARGS__);                                 \
             }                                                                         \
         } else {                                                                      \
             switch (stage) {                                                          \

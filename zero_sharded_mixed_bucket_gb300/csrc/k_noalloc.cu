@@ -68,6 +68,8 @@ extern "C" zero_status_t zero_step_stage2_noalloc(const zero_config_t* cfg, cons
         std::snprintf(msg, sizeof msg, "zero_step_stage2_noalloc needs a stage-2 config (got stage %d)", cfg->stage);
         return zg::set_error(ZERO_EINVAL, msg);
     }
+    if (cfg->dtype == ZERO_FP32)
+        return zg::set_error(ZERO_EUNSUPPORTED, "zero_step_stage2_noalloc takes 16-bit gradients only");
     if (fresh.padded_elems > kNoAllocMaxReduced) {
         std::snprintf(msg, sizeof msg,
                       "zero_step_stage2_noalloc: the plan's padded_elems %lld exceed the %lld that fit the static "

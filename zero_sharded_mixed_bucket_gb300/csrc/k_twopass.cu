@@ -30,24 +30,22 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Ste
         const int64_t gidx = i - a.grad_base;
         float s[kVec];
         reduce_group<DT>(a, gidx, cnt, s);
-        // round to 16 bits; elements past cnt are 0 (finite, square 0)
-        H8 h;
-        uint32_t nf = 0;
+        // round to the model precision; elements past cnt are 0 (finite, square 0)
+        V8<DT> h;
+        bad |= round_group<DT>(s, h) != 0;
+        if constexpr (CLIP) {
+            static_assert(DT != kF32, "no exact sum of squares for binary32 values");
 #pragma unroll
-        for (int p = 0; p < kVec / 2; p++) {
-            h.w[p] = from_f32x2<DT>(s[2 * p], s[2 * p + 1]);
-            nf |= nonfinite_x2<DT>(h.w[p]);
-            if constexpr (CLIP) {
+            for (int p = 0; p < kVec / 2; p++) {
                 sumsq_add<DT>(h.w[p] & 0xffffu, win_lo, acc, bins);
                 sumsq_add<DT>(h.w[p] >> 16, win_lo, acc, bins);
             }
         }
-        bad |= nf != 0;
         if constexpr (HDEST == 0) {
             for (int r = 0; r < a.n_ranks; r++)
-                st_h8(const_cast<void*>(a.grads[r]), gidx, h, cnt);
+                st8<DT>(const_cast<void*>(a.grads[r]), gidx, h, cnt);
         } else {
-            st_h8(a.reduced, i, h, cnt);
+            st8<DT>(a.reduced, i, h, cnt);
         }
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0)
@@ -168,6 +166,8 @@ cudaError_t launch_reduce(int stage, int dtype, bool clip, const StepArgs& a, cu
 {
     if (dtype == kBF16)
         return clip ? reduce_dt<kBF16, true>(stage, a, s, overlap) : reduce_dt<kBF16, false>(stage, a, s, overlap);
+    if (dtype == kF32)   // binary32 steps do not clip (the host refuses the combination)
+        return clip ? cudaErrorNotSupported : reduce_dt<kF32, false>(stage, a, s, overlap);
     return clip ? reduce_dt<kF16, true>(stage, a, s, overlap) : reduce_dt<kF16, false>(stage, a, s, overlap);
 }
 

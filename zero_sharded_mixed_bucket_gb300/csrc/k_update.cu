@@ -1,6 +1,6 @@
 // Two-pass step, pass 2 (see k_twopass.cu for pass 1 and the finalize): per
 // bucket, the optimizer update in place on the current state, unless the
-// step's overflow flag is set, then the 16-bit cast and the all-gather.
+// step's overflow flag is set, then the model-precision cast and the all-gather.
 #include "dev_common.cuh"
 
 namespace zg {
@@ -35,35 +35,30 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
         const int cnt = (int)min((int64_t)kVec, a.hi - i);
         const int reps = STAGE == 0 ? a.n_ranks : 1;
         for (int r = 0; r < reps; r++) {
-            H8 h;
+            V8<DT> h;
             if constexpr (STAGE == 0)
-                h = ld_h8(a.grads[r], i - a.grad_base, cnt);        // each replica its own all-reduced copy
+                h = ld8<DT>(a.grads[r], i - a.grad_base, cnt);        // each replica its own all-reduced copy
             else if constexpr (STAGE == 1)
-                h = ld_h8(a.grads[owner_of(i, a.shard)], i - a.grad_base, cnt);
+                h = ld8<DT>(a.grads[owner_of(i, a.shard)], i - a.grad_base, cnt);
             else
-                h = ld_h8(a.reduced, i, cnt);
+                h = ld8<DT>(a.reduced, i, cnt);
             float g[kVec];
-#pragma unroll
-            for (int p = 0; p < kVec / 2; p++) {
-                const float2 f = to_f32x2<DT>(h.w[p]);
-                g[2 * p] = __fmul_rn(f.x, inv);
-                g[2 * p + 1] = __fmul_rn(f.y, inv);
-            }
+            unscale_group<DT>(h, inv, g);
             if (c != 1.0f) {
 #pragma unroll
                 for (int j = 0; j < kVec; j++)
                     g[j] = __fmul_rn(g[j], c);
             }
-            H8 p;
+            V8<DT> p;
             update_state<DT, OPT>(a, hp, (int64_t)r * a.replica_stride + i, cnt, g, p);
             if constexpr (STAGE == 0) {
-                st_h8(a.params16[r], i, p, cnt);
+                st8<DT>(a.params16[r], i, p, cnt);
             } else if constexpr (STAGE == 3) {
                 const int o = owner_of(i, a.shard);
-                st_h8(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
+                st8<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
             } else {
                 for (int q = 0; q < a.n_ranks; q++)
-                    st_h8(a.params16[q], i, p, cnt);
+                    st8<DT>(a.params16[q], i, p, cnt);
             }
         }
     }
@@ -93,7 +88,11 @@ cudaError_t update_stage(int stage, const StepArgs& a, cudaStream_t s, bool over
 template <int DT, int OPT>
 cudaError_t update_clip(int stage, bool clip, const StepArgs& a, cudaStream_t s, bool overlap)
 {
-    return clip ? update_stage<DT, true, OPT>(stage, a, s, overlap) : update_stage<DT, false, OPT>(stage, a, s, overlap);
+    if constexpr (DT == kF32)   // binary32 steps do not clip (the host refuses the combination)
+        return clip ? cudaErrorNotSupported : update_stage<DT, false, OPT>(stage, a, s, overlap);
+    else
+        return clip ? update_stage<DT, true, OPT>(stage, a, s, overlap)
+                    : update_stage<DT, false, OPT>(stage, a, s, overlap);
 }
 
 template <int DT>
@@ -110,6 +109,7 @@ cudaError_t update_opt(int stage, int opt, bool clip, const StepArgs& a, cudaStr
 
 cudaError_t launch_update(int stage, int dtype, int opt, bool clip, const StepArgs& a, cudaStream_t s, bool overlap)
 {
+    if (dtype == kF32) return update_opt<kF32>(stage, opt, clip, a, s, overlap);
     return dtype == kBF16 ? update_opt<kBF16>(stage, opt, clip, a, s, overlap)
                           : update_opt<kF16>(stage, opt, clip, a, s, overlap);
 }

@@ -74,6 +74,7 @@ struct Ring {
 struct Fetcher {
     uint32_t magic;
     int32_t n_ranks, n_dst, depth, n_order, n_layers;
+    int32_t units;                 // 16-bit units per value: 1, or 2 for binary32
     int64_t shard;
     const int64_t* layer_sizes;    // caller's (config)
     int64_t total;                 // n_params (for a config without layer sizes)
@@ -222,6 +223,7 @@ zero_status_t zero_fetcher_init(zero_fetcher_t* f, const zero_config_t* cfg, con
     F->depth = depth;
     F->n_order = n_order;
     F->n_layers = (int32_t)plan->n_layers;
+    F->units = cfg->dtype == ZERO_FP32 ? 2 : 1;
     F->shard = plan->shard_elems;
     F->layer_sizes = cfg->layer_sizes;
     F->total = cfg->n_params;
@@ -245,10 +247,11 @@ zero_status_t zero_fetch_layer(zero_fetcher_t* f, int32_t pos, void* stream, int
         GatherArgs a;
         std::memset(&a, 0, sizeof a);
         for (int r = 0; r < F->n_ranks; r++) a.shards[r] = F->shards[r];
-        for (int d = 0; d < F->n_dst; d++) a.dst[d] = static_cast<uint16_t*>(F->pool[d]) + off;
-        a.start = F->layer_sizes ? layer_start(F->layer_sizes, layer) : 0;
-        a.len = layer_len(F->layer_sizes, F->total, layer);
-        a.shard = F->shard;
+        // the gather copies 16-bit units (two per binary32 value); offsets stay in values
+        for (int d = 0; d < F->n_dst; d++) a.dst[d] = static_cast<uint16_t*>(F->pool[d]) + off * F->units;
+        a.start = (F->layer_sizes ? layer_start(F->layer_sizes, layer) : 0) * F->units;
+        a.len = layer_len(F->layer_sizes, F->total, layer) * F->units;
+        a.shard = F->shard * F->units;
         a.n_dst = F->n_dst;
         err = launch_gather(a, F->side);
         if (err == cudaSuccess) err = cudaEventRecord(F->ev[q % (F->depth + 1)], F->side);

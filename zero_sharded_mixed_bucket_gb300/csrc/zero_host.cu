@@ -39,34 +39,37 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // fp32 state bytes per parameter the optimizer keeps (w, m, v / w, m / w).
 int64_t state_bytes(int optimizer) { return optimizer == ZERO_SGD ? 4 : (optimizer == ZERO_SGD_MOMENTUM ? 8 : 12); }
 
-// Algorithmic HBM bytes per parameter (16-bit values 2 bytes, fp32 state sb
-// bytes, read once and written once).
-int64_t bytes_per_param(int stage, int64_t N, bool fused, int64_t sb)
+// Bytes of one gradient or parameter value: 2 (16-bit types) or 4 (binary32).
+int64_t value_bytes(int dtype) { return dtype == ZERO_FP32 ? 4 : 2; }
+
+// Algorithmic HBM bytes per parameter (gradient and parameter values e
+// bytes, fp32 state sb bytes, read once and written once).
+int64_t bytes_per_param(int stage, int64_t N, bool fused, int64_t sb, int64_t e)
 {
     if (fused) {
         switch (stage) {
-        case 0: return N * (6 + 2 * sb);    // N grads + N write-backs + N x (state r/w + param)
-        case 1: return 6 * N + 2 * sb;      // N grads + N write-backs + state + N params
-        case 2: return 4 * N + 2 * sb;      // N grads + state + N params
-        default: return 2 * N + 2 * sb + 2; // N grads + state + owner's param
+        case 0: return N * (3 * e + 2 * sb);    // N grads + N write-backs + N x (state r/w + param)
+        case 1: return 3 * e * N + 2 * sb;      // N grads + N write-backs + state + N params
+        case 2: return 2 * e * N + 2 * sb;      // N grads + state + N params
+        default: return e * N + 2 * sb + e;     // N grads + state + owner's param
         }
     }
     switch (stage) {
-    case 0: return N * (8 + 2 * sb);        // pass 1: 4N; pass 2: N x (h + state + param)
-    case 1: return 6 * N + 2 + 2 * sb;      // pass 1: 4N; pass 2: h + state + N params
-    case 2: return 4 * N + 4 + 2 * sb;      // pass 1: 2N + h; pass 2: h + state + N params
-    default: return 2 * N + 6 + 2 * sb;     // pass 1: 2N + h; pass 2: h + state + param
+    case 0: return N * (4 * e + 2 * sb);        // pass 1: 2eN; pass 2: N x (h + state + param)
+    case 1: return 3 * e * N + e + 2 * sb;      // pass 1: 2eN; pass 2: h + state + N params
+    case 2: return 2 * e * N + 2 * e + 2 * sb;  // pass 1: eN + h; pass 2: h + state + N params
+    default: return e * N + 3 * e + 2 * sb;     // pass 1: eN + h; pass 2: h + state + param
     }
 }
 
 // Bytes per parameter of the restore after an overflowed fused step: read
-// the unchanged master weight, write its 16-bit cast to each copy (every
-// replica in stage 0, every rank in stages 1-2, the owner in stage 3).
-int64_t restore_bytes_per_param(int stage, int64_t N)
+// the unchanged master weight, write its cast to each copy (every replica in
+// stage 0, every rank in stages 1-2, the owner in stage 3).
+int64_t restore_bytes_per_param(int stage, int64_t N, int64_t e)
 {
-    if (stage == 0) return N * (4 + 2);
-    if (stage == 3) return 4 + 2;
-    return 4 + 2 * N;
+    if (stage == 0) return N * (4 + e);
+    if (stage == 3) return 4 + e;
+    return 4 + e * N;
 }
 
 const int kCollectivePasses[4] = {2, 3, 2, 3};   // RS+AG, AR+AG, RS+AG, RS+2AG
@@ -84,7 +87,8 @@ zero_status_t check_config(const zero_config_t* c)
         return fail(ZERO_EINVAL, "bucket_elems %lld must be a positive multiple of 8", (long long)c->bucket_elems);
     if (c->align_elems < 0 || c->align_elems % kVec)
         return fail(ZERO_EINVAL, "align_elems %lld must be 0 or a positive multiple of 8", (long long)c->align_elems);
-    if (c->dtype != ZERO_FP16 && c->dtype != ZERO_BF16) return fail(ZERO_EINVAL, "dtype %d unknown", c->dtype);
+    if (c->dtype != ZERO_FP16 && c->dtype != ZERO_BF16 && c->dtype != ZERO_FP32)
+        return fail(ZERO_EINVAL, "dtype %d unknown", c->dtype);
     if (c->optimizer < ZERO_ADAM || c->optimizer > ZERO_SGD)
         return fail(ZERO_EINVAL, "optimizer %d unknown", c->optimizer);
     if (c->layer_sizes) {
@@ -140,12 +144,13 @@ void make_plan(const zero_config_t* c, zero_plan_t* p)
     p->reduced_elems = c->stage >= 2 ? p->padded_elems : 0;
     p->workspace_bytes = ws::kBytes;
     const int64_t sb = state_bytes(c->optimizer);
-    p->hbm_bytes_fused = bytes_per_param(c->stage, N, true, sb) * psi;
-    p->hbm_bytes_two_pass = bytes_per_param(c->stage, N, false, sb) * psi;
-    p->comm_counted_bytes = (int64_t)kCollectivePasses[c->stage] * (N - 1) * psi * 2;
-    p->comm_paper_bytes = (c->stage == 3 ? 3.0 : 2.0) * (double)psi * 2.0;
+    const int64_t e = value_bytes(c->dtype);
+    p->hbm_bytes_fused = bytes_per_param(c->stage, N, true, sb, e) * psi;
+    p->hbm_bytes_two_pass = bytes_per_param(c->stage, N, false, sb, e) * psi;
+    p->comm_counted_bytes = (int64_t)kCollectivePasses[c->stage] * (N - 1) * psi * e;
+    p->comm_paper_bytes = (c->stage == 3 ? 3.0 : 2.0) * (double)psi * (double)e;
     double m[4];
-    model_state(psi, c->n_ranks, c->stage, 2, (int32_t)sb, m);
+    model_state(psi, c->n_ranks, c->stage, (int32_t)e, (int32_t)sb, m);
     p->mem_total_bytes = m[3];
 }
 
@@ -197,6 +202,8 @@ zero_status_t check_step(const zero_config_t* c, const zero_plan_t* plan, const 
         return fail(ZERO_EINVAL, "Adam hyper-parameters out of range");
     if (c->optimizer == ZERO_SGD_MOMENTUM && !(std::isfinite(adam->momentum) && adam->momentum >= 0.0f))
         return fail(ZERO_EINVAL, "momentum must be finite and non-negative");
+    if (c->dtype == ZERO_FP32 && adam->max_grad_norm > 0.0f)
+        return fail(ZERO_EUNSUPPORTED, "gradient clipping is not available with ZERO_FP32");
     if (!(std::isfinite(s->loss_scale) && s->loss_scale > 0.0f))
         return fail(ZERO_EINVAL, "loss_scale must be positive and finite");
     if (s->dynamic && !(std::isfinite(s->min_loss_scale) && s->min_loss_scale > 0.0f))
@@ -398,7 +405,7 @@ zero_status_t end_impl(const zero_config_t* c, const zero_plan_t* p, zero_buffer
     r.hbm_bytes = path.fused ? p->hbm_bytes_fused : p->hbm_bytes_two_pass;
     r.comm_counted_bytes = p->comm_counted_bytes;
     if (overflow) {
-        if (path.fused) r.hbm_bytes += c->n_params * restore_bytes_per_param(c->stage, c->n_ranks);
+        if (path.fused) r.hbm_bytes += c->n_params * restore_bytes_per_param(c->stage, c->n_ranks, value_bytes(c->dtype));
         if (s->dynamic) {
             float h = s->loss_scale * 0.5f;
             s->loss_scale = h > s->min_loss_scale ? h : s->min_loss_scale;
@@ -609,9 +616,11 @@ zero_status_t zero_gather_layer(const zero_config_t* c, const zero_plan_t* p, in
         if (!aligned16(dst[d])) return fail(ZERO_EALIGN, "dst[%d] is not 16-byte aligned", d);
         a.dst[d] = dst[d];
     }
-    a.start = start;
-    a.len = len;
-    a.shard = p->shard_elems;
+    // the gather copies 16-bit units; a binary32 value is two of them
+    const int64_t u = value_bytes(c->dtype) / 2;
+    a.start = start * u;
+    a.len = len * u;
+    a.shard = p->shard_elems * u;
     a.n_dst = n_dst;
     cudaError_t e = launch_gather(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "launching the layer gather kernel");
