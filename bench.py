@@ -55,12 +55,16 @@ KERNEL_SOURCES = ["zero_sharded_mixed_bucket_gb300/csrc/k_fused.cu",
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_fused_stage2_fp16_n8.md")
 
 
-def bytes_per_param(stage, n=N_RANKS, sb=12):
-    """Algorithmic HBM bytes per parameter of the fused step (16-bit values 2
-    bytes, sb bytes of fp32 state -- 12 for Adam's w, m, v): N gradient
-    reads, the all-reduce write-back in stages 0/1, the state read and
-    written, the 16-bit parameter writes."""
-    return {0: n * (6 + 2 * sb), 1: 6 * n + 2 * sb, 2: 4 * n + 2 * sb, 3: 2 * n + 2 * sb + 2}[stage]
+def bytes_per_param(stage, n=N_RANKS, sb=12, e=2):
+    """Algorithmic HBM bytes per parameter of the fused step (gradient and
+    parameter values e bytes -- 2 for 16-bit, 4 for fp32 training -- and sb
+    bytes of fp32 state -- 12 for Adam's w, m, v): N gradient reads, the
+    all-reduce write-back in stages 0/1, the state read and written, the
+    parameter writes."""
+    return {0: n * (3 * e + 2 * sb), 1: 3 * e * n + 2 * sb, 2: 2 * e * n + 2 * sb, 3: e * n + 2 * sb + e}[stage]
+
+
+DTYPES = {"fp16": 0, "bf16": 1, "fp32": 2}
 
 
 def layer_sizes(vocab=VOCAB, d=D_MODEL, layers=N_LAYERS):
@@ -238,7 +242,7 @@ STATE_BYTES = {0: 12, 1: 8, 2: 4}
 
 
 class GpuJob:
-    def __init__(self, stage, device, ring=GRAD_RING, n_params=None, optimizer=0):
+    def __init__(self, stage, device, ring=GRAD_RING, n_params=None, optimizer=0, dtype=0):
         import torch
 
         import synth
@@ -247,8 +251,10 @@ class GpuJob:
         self.stage = stage
         self.n = n_params or N_PARAMS
         self.optimizer = optimizer
+        self.dtype = dtype
+        self.e = 4 if dtype == zg.ZERO_FP32 else 2          # bytes per gradient / parameter value
         self.cfg = zg.Config(self.n, N_RANKS, stage, BUCKET, 0, layer_sizes() if self.n == N_PARAMS else None,
-                             zg.ZERO_FP16, optimizer)
+                             dtype, optimizer)
         self.plan = zg.zero_plan(self.cfg)
         self.bufs = zg.DeviceBuffers(self.cfg, self.plan, device=device, grads=True)
         self.stream = torch.cuda.current_stream(device)
@@ -262,10 +268,11 @@ class GpuJob:
         self.ring_ptrs = []
         import ctypes
         for k in range(ring):
-            bufs = [torch.empty(self.plan.grad16_elems, dtype=torch.int16, device=device) for _ in range(N_RANKS)]
+            vt = torch.int32 if self.e == 4 else torch.int16
+            bufs = [torch.empty(self.plan.grad16_elems, dtype=vt, device=device) for _ in range(N_RANKS)]
             for r in range(N_RANKS):
-                synth.dev_normal16(bufs[r].data_ptr(), self.n, synth.FP16, SIGMA, seed=0, stream=synth.STREAM_GRAD,
-                                   step=k + 1, rank=r, cuda_stream=s)
+                synth.dev_grad(bufs[r].data_ptr(), self.n, dtype, SIGMA, seed=0, stream=synth.STREAM_GRAD,
+                               step=k + 1, rank=r, cuda_stream=s)
             self.ring.append(bufs)
             self.ring_ptrs.append((ctypes.c_void_p * N_RANKS)(*[b.data_ptr() for b in bufs]))
         self.adam = zg.zero_adam_t(max_grad_norm=0.0, momentum=0.9, **ADAM)
@@ -381,7 +388,7 @@ def timed_steps(job, steps, warmup, world, api="sync"):
     ms = start.elapsed_time(end)
     nb = job.plan.n_buckets
     step_bytes = sum(job.bucket_len(b) for b in range(nb)) * bytes_per_param(job.stage, N_RANKS,
-                                                                              STATE_BYTES[job.optimizer])
+                                                                              STATE_BYTES[job.optimizer], job.e)
     kernel = dict(total_ms=sum(spans), bytes=steps * step_bytes, launches=steps * nb,
                   span_ms_per_step=sum(spans) / steps, launches_per_step=nb)
     return ms, launches, kernel, (t0, t1)
@@ -419,7 +426,7 @@ def _timed_steps_async(job, steps, warmup, world):
     spans = [a.elapsed_time(b) for a, b in evs]
     nb = job.plan.n_buckets
     step_bytes = sum(job.bucket_len(b) for b in range(nb)) * bytes_per_param(job.stage, N_RANKS,
-                                                                              STATE_BYTES[job.optimizer])
+                                                                              STATE_BYTES[job.optimizer], job.e)
     kernel = dict(total_ms=sum(spans), bytes=steps * step_bytes, launches=steps * nb,
                   span_ms_per_step=sum(spans) / steps, launches_per_step=nb)
     return ms, launches, kernel, (t0, t1)
@@ -513,7 +520,9 @@ def gpu_arm(args):
     if rank == 0:
         __graft_entry__.build()      # one builder: concurrent builds would write the same object files
     barrier(world)
-    job = GpuJob(STAGE, device, ring=args.ring, n_params=args.n_params, optimizer=OPTIMIZERS[args.optimizer])
+    dt_name = args.dtype or "fp16"
+    job = GpuJob(STAGE, device, ring=args.ring, n_params=args.n_params, optimizer=OPTIMIZERS[args.optimizer],
+                 dtype=DTYPES[dt_name])
     n_params = job.n
     sampler = ClockSampler(local)
     ms, launches, kernel, (t0, t1) = timed_steps(job, args.steps, args.warmup, world, api=args.step_api)
@@ -522,26 +531,30 @@ def gpu_arm(args):
     peak, peak_kind = measured_peak_hbm()
     achieved = kernel["bytes"] / (kernel["total_ms"] * 1e-3) / 1e9
     per_launch = kernel["bytes"] / kernel["launches"]
-    traffic_full = profiled_traffic()
+    # the committed capture is of the fp16 Adam kernel: no counters for the other variants
+    traffic_full = profiled_traffic() if (dt_name, args.optimizer) == ("fp16", "adam") else None
     # the capture is of a full 2^24-element bucket: scale to the average launch
     traffic = None if traffic_full is None else traffic_full * (n_params / kernel["launches_per_step"]) / (1 << 24)
     step_bytes = job.plan.hbm_bytes_fused
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "io_dtype": "fp16", "data": "synthetic",
-        "config": {"workload": WORKLOAD if n_params == N_PARAMS else
-                   "flat parameter vector of %d params, N_d=%d simulated ranks, ZeRO stage %d, bucket 2^24 "
-                   "elements, fp16 gradients N(0,1e-3), Adam" % (n_params, N_RANKS, STAGE),
+        "dtype": "f32", "io_dtype": dt_name, "data": "synthetic",
+        "config": {"workload": (WORKLOAD if n_params == N_PARAMS else
+                                "flat parameter vector of %d params, N_d=%d simulated ranks, ZeRO stage %d, bucket "
+                                "2^24 elements, fp16 gradients N(0,1e-3), Adam" % (n_params, N_RANKS, STAGE))
+                   .replace("fp16 gradients", "%s gradients" % dt_name)
+                   .replace("Adam", {"adam": "Adam", "sgdm": "SGD with momentum 0.9", "sgd": "SGD"}[args.optimizer]),
                    "n_params": n_params, "n_ranks": N_RANKS, "stage": STAGE,
                    "bucket_elems": BUCKET, "parallelism": "replicas only (simulated ranks inside each GPU)",
                    "l2": "inputs larger than L2: %.2f GB moved per step, %d-step gradient ring of %.1f GB"
                          % (step_bytes / 1e9, args.ring, args.ring * N_RANKS * n_params * 2 / 1e9)},
         "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "k_fused<stage 2, fp16, %s>" % args.optimizer, "achieved": achieved, "peak": peak,
+        "roofline": {"bound": "hbm", "kernel": "k_fused<stage 2, %s, %s>" % (dt_name, args.optimizer),
+                     "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes_per_launch": per_launch,
-                     "bytes_per_param": bytes_per_param(STAGE, N_RANKS, STATE_BYTES[job.optimizer]),
+                     "bytes_per_param": bytes_per_param(STAGE, N_RANKS, STATE_BYTES[job.optimizer], job.e),
                      "launches": kernel["launches"],
                      "avg_launch_ms": kernel["total_ms"] / kernel["launches"],
                      "kernel_span_ms_per_step": kernel["span_ms_per_step"],
@@ -557,8 +570,8 @@ def gpu_arm(args):
     out["clocks"] = clocks_summary(rows, t0, t1)
     if rank == 0 and args.headline_only:
         print(json.dumps(out))
-    elif rank == 0 and args.optimizer != "adam":
-        raise SystemExit("--optimizer other than adam needs --headline-only")
+    elif rank == 0 and (args.optimizer != "adam" or dt_name != "fp16"):
+        raise SystemExit("--optimizer other than adam or --dtype other than fp16 needs --headline-only")
     elif rank == 0:
         # stages 0 and 1 on the same workload (reported, not the headline).
         # Stages 0/1 overwrite each rank's gradient with the all-reduce result,
@@ -621,7 +634,9 @@ def main():
     ap.add_argument("--ranks", type=int, default=None, help="--config 5: N_d of a single sweep point")
     ap.add_argument("--optimizer", default="adam", choices=sorted(OPTIMIZERS),
                     help="optimizer of the headline step (with --headline-only)")
-    ap.add_argument("--dtype", default=None, choices=["fp16", "bf16"], help="--config 5: dtype of a single point")
+    ap.add_argument("--dtype", default=None, choices=["fp16", "bf16", "fp32"],
+                    help="--config 5: dtype of a single point (fp16/bf16); --config 2 with --headline-only: the "
+                         "value type of the headline step (fp32: fp32 training)")
     ap.add_argument("--step-api", default="async", choices=["async", "sync"],
                     help="entry point of the timed steps: zero_step_async (default) or the synchronising "
                          "zero_step_stage2")

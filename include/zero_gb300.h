@@ -302,16 +302,17 @@ zero_status_t zero_gather_layer(const zero_config_t* cfg, const zero_plan_t* pla
  * The step state (t, the beta powers of the bias correction, the loss scale
  * and its scaler) can live in device memory instead: zero_step_async then
  * enqueues the whole step and returns without waiting, so steps pipeline
- * back to back and a step can be captured in a CUDA graph.  A one-thread
- * prepare kernel derives the step's scalars from the state block; a
- * one-thread commit kernel writes the outcome back (t and the beta powers
- * advance on a clean step; the scaler halves on overflow and grows after
- * growth_interval clean steps) together with the last step's flag, norm and
- * clip coefficient, which zero_dev_state_read brings to the host.  Results
- * equal the synchronised step's bit for bit.
+ * back to back and a step can be captured in a CUDA graph.  A prepare
+ * kernel clears the workspace head and derives the step's scalars from the
+ * state block; after the bucket kernels a commit writes the outcome back (t
+ * and the beta powers advance on a clean step; the scaler halves on
+ * overflow and grows after growth_interval clean steps) together with the
+ * last step's flag, norm and clip coefficient, which zero_dev_state_read
+ * brings to the host.  Results equal the synchronised step's bit for bit.
  * Fused path: the host does not learn the flag, so bufs->cur flips on every
- * call; after an overflow a restore kernel copies the unchanged state into
- * the copy the next step reads and restores the 16-bit parameters.  A graph
+ * call; after an overflow the restore (which also runs the commit) copies
+ * the unchanged state into the copy the next step reads and restores the
+ * parameters.  A graph
  * captured from one call therefore serves every other step: capture one
  * call per value of bufs->cur and replay them alternately.
  * The device state block is 64 bytes, 16-byte aligned, caller-owned. */

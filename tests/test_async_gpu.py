@@ -39,10 +39,10 @@ class AsyncJob(Job):
     def step(self, grads):
         self.load_grads(grads)
         n = self.launch()
-        fused = not self.two_pass
         per_bucket = 2 if self.two_pass else 1
-        assert n == 2 + per_bucket * self.plan.n_buckets + (1 if self.max_norm > 0 else 0) + \
-            (1 if fused and self.n > 0 else 0)
+        # prepare, the bucket kernels (and the finalize and updates), then the
+        # commit (joined with the restore on the fused path)
+        assert n == 2 + per_bucket * self.plan.n_buckets + (1 if self.max_norm > 0 else 0)
         return self.read(), self.oracle_step(grads)
 
 

@@ -1,19 +1,22 @@
 // Steps whose loss scale and step count live in device memory, so a step
 // needs no host synchronisation and can be captured in a CUDA graph.
 //
-//   k_prepare        one thread: the step's scalars (bias corrections for step
-//                    t+1, 1/(S*N), the sum-of-squares window) from the state
-//                    block into the workspace, where the bucket kernels read
-//                    them;
-//   k_restore_async  fused path: does nothing unless the step overflowed;
-//                    then it puts the unchanged state into the copy the next
-//                    step reads (the host alternates the copies on every
-//                    call, since it no longer learns the flag) and restores
-//                    the 16-bit parameters to the cast of the master weights;
-//   k_commit         one thread: the step's outcome into the state block --
+//   k_prepare        one block: clears the workspace head (flag, sums) and,
+//                    in one thread, derives the step's scalars (bias
+//                    corrections for step t+1, 1/(S*N), the sum-of-squares
+//                    window) from the state block into the workspace, where
+//                    the bucket kernels read them;
+//   commit           one thread: the step's outcome into the state block --
 //                    t and the beta powers advance on a clean step, the loss
 //                    scaler halves on overflow or grows after a run of clean
-//                    steps -- and the last step's flag, norm and coefficient.
+//                    steps -- and the last step's flag, norm and coefficient;
+//                    run by k_restore_async on the fused path, by k_commit
+//                    after the two-pass path's updates;
+//   k_restore_async  fused path: does nothing else unless the step
+//                    overflowed; then it puts the unchanged state into the
+//                    copy the next step reads (the host alternates the copies
+//                    on every call, since it no longer learns the flag) and
+//                    restores the parameters to the cast of the master weights.
 // The arithmetic matches the host-synchronised step exactly: beta^t is kept
 // as the same sequence of fp64 multiplications, 1/(S*N) and the scaler use
 // the same fp64 and fp32 operations.
@@ -25,7 +28,13 @@ namespace {
 
 __global__ void k_prepare(const PrepArgs a)
 {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    // clear the step's flag and sums (the workspace head) ...
+    static_assert(ws::kEnd % 16 == 0, "workspace head is cleared in 16-byte words");
+    uint4* head = reinterpret_cast<uint4*>(a.ws);
+    for (int k = threadIdx.x; k < (int)(ws::kEnd / 16); k += blockDim.x)
+        head[k] = make_uint4(0u, 0u, 0u, 0u);
+    // ... and derive the step's scalars from the state block
+    if (threadIdx.x != 0) return;
     const DevState* st = a.st;
     Dyn d;
     d.beta1_pow_next = __dmul_rn(st->beta1_pow, (double)a.beta1);
@@ -46,9 +55,8 @@ __global__ void k_prepare(const PrepArgs a)
     *a.dyn = d;
 }
 
-__global__ void k_commit(const CommitArgs a)
+__device__ void commit(const CommitArgs& a)
 {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
     DevState* st = a.st;
     const uint32_t flag = *reinterpret_cast<const volatile uint32_t*>(a.ws + ws::kFlag);
     if (flag) {
@@ -75,9 +83,18 @@ __global__ void k_commit(const CommitArgs a)
     st->last_clip_coef = a.clip && !flag ? clip : 1.0f;
 }
 
-template <int STAGE, int DT, int OPT>
-__global__ void __launch_bounds__(kThreads) k_restore_async(const __grid_constant__ StepArgs a)
+__global__ void k_commit(const CommitArgs a)
 {
+    if (threadIdx.x == 0) commit(a);
+}
+
+// Also commits the step (block 0, thread 0): the commit writes only the
+// state block, which the restore does not touch.
+template <int STAGE, int DT, int OPT>
+__global__ void __launch_bounds__(kThreads) k_restore_async(const __grid_constant__ StepArgs a,
+                                                             const CommitArgs c)
+{
+    if (blockIdx.x == 0 && threadIdx.x == 0) commit(c);
     if (!*reinterpret_cast<const volatile uint32_t*>(ws_flag(a.ws))) return;   // clean step: nothing to do
     const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
     const int reps = STAGE == 0 ? a.n_ranks : 1;
@@ -118,33 +135,32 @@ __global__ void __launch_bounds__(kThreads) k_restore_async(const __grid_constan
 }
 
 template <int STAGE, int DT, int OPT>
-cudaError_t run_restore_async(const StepArgs& a, cudaStream_t s)
+cudaError_t run_restore_async(const StepArgs& a, const CommitArgs& c, cudaStream_t s)
 {
     const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
-    if (groups <= 0) return cudaSuccess;
-    const int grid = grid_for((const void*)k_restore_async<STAGE, DT, OPT>, groups);
-    k_restore_async<STAGE, DT, OPT><<<grid, kThreads, 0, s>>>(a);
+    const int grid = groups > 0 ? grid_for((const void*)k_restore_async<STAGE, DT, OPT>, groups) : 1;
+    k_restore_async<STAGE, DT, OPT><<<grid, kThreads, 0, s>>>(a, c);
     return cudaGetLastError();
 }
 
 template <int STAGE, int DT>
-cudaError_t restore_opt(int opt, const StepArgs& a, cudaStream_t s)
+cudaError_t restore_opt(int opt, const StepArgs& a, const CommitArgs& c, cudaStream_t s)
 {
     switch (opt) {
-    case kSgdm: return run_restore_async<STAGE, DT, kSgdm>(a, s);
-    case kSgd: return run_restore_async<STAGE, DT, kSgd>(a, s);
-    default: return run_restore_async<STAGE, DT, kAdam>(a, s);
+    case kSgdm: return run_restore_async<STAGE, DT, kSgdm>(a, c, s);
+    case kSgd: return run_restore_async<STAGE, DT, kSgd>(a, c, s);
+    default: return run_restore_async<STAGE, DT, kAdam>(a, c, s);
     }
 }
 
 template <int DT>
-cudaError_t restore_stage(int stage, int opt, const StepArgs& a, cudaStream_t s)
+cudaError_t restore_stage(int stage, int opt, const StepArgs& a, const CommitArgs& c, cudaStream_t s)
 {
     switch (stage) {
-    case 0: return restore_opt<0, DT>(opt, a, s);
-    case 1: return restore_opt<1, DT>(opt, a, s);
-    case 2: return restore_opt<2, DT>(opt, a, s);
-    default: return restore_opt<3, DT>(opt, a, s);
+    case 0: return restore_opt<0, DT>(opt, a, c, s);
+    case 1: return restore_opt<1, DT>(opt, a, c, s);
+    case 2: return restore_opt<2, DT>(opt, a, c, s);
+    default: return restore_opt<3, DT>(opt, a, c, s);
     }
 }
 
@@ -152,7 +168,7 @@ cudaError_t restore_stage(int stage, int opt, const StepArgs& a, cudaStream_t s)
 
 cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s)
 {
-    k_prepare<<<1, 32, 0, s>>>(a);
+    k_prepare<<<1, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -162,10 +178,11 @@ cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s)
     return cudaGetLastError();
 }
 
-cudaError_t launch_restore_async(int stage, int dtype, int opt, const StepArgs& a, cudaStream_t s)
+cudaError_t launch_restore_async(int stage, int dtype, int opt, const StepArgs& a, const CommitArgs& c,
+                                 cudaStream_t s)
 {
-    if (dtype == kF32) return restore_stage<kF32>(stage, opt, a, s);
-    return dtype == kBF16 ? restore_stage<kBF16>(stage, opt, a, s) : restore_stage<kF16>(stage, opt, a, s);
+    if (dtype == kF32) return restore_stage<kF32>(stage, opt, a, c, s);
+    return dtype == kBF16 ? restore_stage<kBF16>(stage, opt, a, c, s) : restore_stage<kF16>(stage, opt, a, c, s);
 }
 
 }  // namespace zg

@@ -685,10 +685,8 @@ zero_status_t zero_step_async(const zero_config_t* c, const zero_plan_t* p, zero
     Dyn* dyn = reinterpret_cast<Dyn*>(ws_ptr + ws::kDyn);
     DevState* dst = static_cast<DevState*>(dev_state);
     int launches = 0;
-    cudaError_t e = cudaMemsetAsync(b->workspace, 0, ws::kEnd, cs);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace");
-    PrepArgs pa{dst, dyn, adam->beta1, adam->beta2, c->n_ranks, c->dtype};
-    e = launch_prepare(pa, cs);
+    PrepArgs pa{dst, dyn, ws_ptr, adam->beta1, adam->beta2, c->n_ranks, c->dtype};
+    cudaError_t e = launch_prepare(pa, cs);   // also clears the workspace head
     if (e != cudaSuccess) return cuda_fail(e, "launching the prepare kernel");
     launches++;
     if (g_prof_start && (e = cudaEventRecord(g_prof_start, cs)) != cudaSuccess)
@@ -729,18 +727,18 @@ zero_status_t zero_step_async(const zero_config_t* c, const zero_plan_t* p, zero
     // the profiling span covers the bucket (and update) kernels, as in zero_step
     if (g_prof_end && (e = cudaEventRecord(g_prof_end, cs)) != cudaSuccess)
         return cuda_fail(e, "recording the profiling end event");
-    if (path.fused && c->n_params > 0) {
+    CommitArgs ca{dst, dyn, ws_ptr, path.clip ? 1 : 0};
+    if (path.fused) {   // restore on overflow, and the commit, in one kernel
         StepArgs a = make_args(c, p, b, adam, &host_view, true, nullptr, 0);
         a.dyn = dyn;
         a.lo = 0;
         a.hi = c->n_params;
-        e = launch_restore_async(c->stage, c->dtype, c->optimizer, a, cs);
-        if (e != cudaSuccess) return cuda_fail(e, "launching the restore kernel");
-        launches++;
+        e = launch_restore_async(c->stage, c->dtype, c->optimizer, a, ca, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "launching the restore and commit kernel");
+    } else {
+        e = launch_commit(ca, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "launching the commit kernel");
     }
-    CommitArgs ca{dst, dyn, ws_ptr, path.clip ? 1 : 0};
-    e = launch_commit(ca, cs);
-    if (e != cudaSuccess) return cuda_fail(e, "launching the commit kernel");
     launches++;
     if (path.fused) b->cur = 1 - b->cur;   // alternate on every call: an overflow copies the state across
     if (kernel_launches) *kernel_launches = launches;

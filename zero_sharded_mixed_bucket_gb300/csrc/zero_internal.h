@@ -114,6 +114,7 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
 struct PrepArgs {
     DevState* st;
     Dyn* dyn;
+    unsigned char* ws;              // its head [0, ws::kEnd) is cleared
     float beta1, beta2;
     int32_t n_ranks;
     int32_t dtype;
@@ -126,7 +127,8 @@ struct CommitArgs {
 };
 cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s);
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);
-cudaError_t launch_restore_async(int stage, int dtype, int opt, const StepArgs& a, cudaStream_t s);
+cudaError_t launch_restore_async(int stage, int dtype, int opt, const StepArgs& a, const CommitArgs& c,
+                                 cudaStream_t s);
 
 // Record the thread-local message that zero_last_error() returns; gives back
 // `st`.  For entry points defined outside zero_host.cu.
