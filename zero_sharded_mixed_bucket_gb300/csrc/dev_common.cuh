@@ -90,14 +90,22 @@ __device__ __forceinline__ uint32_t nonfinite_x2(uint32_t w)
 __device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void wait_prev_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// ---- groups of 8 elements --------------------------------------------------
-// A group is 8 consecutive flat elements starting at a multiple of 8.  Full
-// groups use one 16-byte access per 16-bit array and two per fp32 array;
-// the ragged last group of a bucket uses scalar accesses for its `cnt` < 8
+// ---- groups of elements ------------------------------------------------------
+// A group is VEC consecutive flat elements starting at a multiple of VEC:
+// 8 for 16-bit value types (one 16-byte access per gradient or parameter
+// array, two per fp32 state array), 4 for binary32 values (one 16-byte
+// access per array).  Measured on GB300, 4-element groups lift the binary32
+// steps from 0.91-0.94 to 0.99 of the copy bandwidth (every warp access a
+// contiguous 512 bytes) but drop the 16-bit Adam step from 1.01 to 0.90.
+// The ragged last group of a bucket uses scalar accesses for its cnt < VEC
 // elements.
+template <int DT>
+constexpr int kVecOf = DT == kF32 ? 4 : 8;
 
-struct H8 {
-    uint32_t w[4];   // 8 x 16-bit, little-endian pairs
+// V 16-bit values, little-endian pairs.
+template <int V>
+struct H16 {
+    uint32_t w[V / 2];
     __device__ __forceinline__ uint32_t get(int j) const { return (w[j >> 1] >> ((j & 1) * 16)) & 0xffffu; }
     __device__ __forceinline__ void set(int j, uint32_t b)
     {
@@ -106,91 +114,121 @@ struct H8 {
     }
 };
 
-__device__ __forceinline__ H8 ld_h8(const void* base, int64_t idx, int cnt)
+// V binary32 values, as bit patterns.
+template <int V>
+struct W32 {
+    uint32_t w[V];
+    __device__ __forceinline__ uint32_t get(int j) const { return w[j]; }
+    __device__ __forceinline__ void set(int j, uint32_t b) { w[j] = b; }
+};
+
+// A group of model-precision values.
+template <int DT>
+using Vals = typename std::conditional<DT == kF32, W32<kVecOf<DT>>, H16<kVecOf<DT>>>::type;
+
+template <int V>
+__device__ __forceinline__ H16<V> ld_h16(const void* base, int64_t idx, int cnt)
 {
+    static_assert(V == 8, "16-bit groups are 8 values, one 16-byte access");
     const uint16_t* p = static_cast<const uint16_t*>(base) + idx;
-    H8 r;
-    if (cnt == kVec) {
+    H16<V> r;
+    if (cnt == V) {
         const uint4 v = __ldcs(reinterpret_cast<const uint4*>(p));
         r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
     } else {
         r.w[0] = r.w[1] = r.w[2] = r.w[3] = 0;
 #pragma unroll
-        for (int j = 0; j < kVec; j++)
+        for (int j = 0; j < V; j++)
             if (j < cnt) r.set(j, p[j]);
     }
     return r;
 }
 
-__device__ __forceinline__ void st_h8(void* base, int64_t idx, const H8& h, int cnt)
+template <int V>
+__device__ __forceinline__ void st_h16(void* base, int64_t idx, const H16<V>& h, int cnt)
 {
     uint16_t* p = static_cast<uint16_t*>(base) + idx;
-    if (cnt == kVec) {
+    if (cnt == V) {
         __stcs(reinterpret_cast<uint4*>(p), make_uint4(h.w[0], h.w[1], h.w[2], h.w[3]));
     } else {
 #pragma unroll
-        for (int j = 0; j < kVec; j++)
+        for (int j = 0; j < V; j++)
             if (j < cnt) p[j] = (uint16_t)h.get(j);
     }
 }
 
-// 8 binary32 values (fp32 training), as bit patterns.
-struct W8 {
-    uint32_t w[8];
-    __device__ __forceinline__ uint32_t get(int j) const { return w[j]; }
-    __device__ __forceinline__ void set(int j, uint32_t b) { w[j] = b; }
-};
-
-// A group of 8 model-precision values.
-template <int DT>
-using V8 = typename std::conditional<DT == kF32, W8, H8>::type;
-
-__device__ __forceinline__ W8 ld_w8(const void* base, int64_t idx, int cnt)
+// V 32-bit words (binary32 values or fp32 state), one 16-byte access per 4.
+template <int V>
+__device__ __forceinline__ void ld_u32(const void* base, int64_t idx, int cnt, uint32_t x[V])
 {
     const uint32_t* p = static_cast<const uint32_t*>(base) + idx;
-    W8 r;
-    if (cnt == kVec) {
-        const uint4 a = __ldcs(reinterpret_cast<const uint4*>(p));
-        const uint4 b = __ldcs(reinterpret_cast<const uint4*>(p) + 1);
-        r.w[0] = a.x; r.w[1] = a.y; r.w[2] = a.z; r.w[3] = a.w;
-        r.w[4] = b.x; r.w[5] = b.y; r.w[6] = b.z; r.w[7] = b.w;
+    if (cnt == V) {
+#pragma unroll
+        for (int k = 0; k < V / 4; k++) {
+            const uint4 a = __ldcs(reinterpret_cast<const uint4*>(p) + k);
+            x[4 * k] = a.x; x[4 * k + 1] = a.y; x[4 * k + 2] = a.z; x[4 * k + 3] = a.w;
+        }
     } else {
 #pragma unroll
-        for (int j = 0; j < kVec; j++)
-            r.w[j] = j < cnt ? p[j] : 0u;
+        for (int j = 0; j < V; j++)
+            x[j] = j < cnt ? p[j] : 0u;
     }
-    return r;
 }
 
-__device__ __forceinline__ void st_w8(void* base, int64_t idx, const W8& v, int cnt)
+template <int V>
+__device__ __forceinline__ void st_u32(void* base, int64_t idx, int cnt, const uint32_t x[V])
 {
     uint32_t* p = static_cast<uint32_t*>(base) + idx;
-    if (cnt == kVec) {
-        __stcs(reinterpret_cast<uint4*>(p), make_uint4(v.w[0], v.w[1], v.w[2], v.w[3]));
-        __stcs(reinterpret_cast<uint4*>(p) + 1, make_uint4(v.w[4], v.w[5], v.w[6], v.w[7]));
+    if (cnt == V) {
+#pragma unroll
+        for (int k = 0; k < V / 4; k++)
+            __stcs(reinterpret_cast<uint4*>(p) + k, make_uint4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]));
     } else {
 #pragma unroll
-        for (int j = 0; j < kVec; j++)
-            if (j < cnt) p[j] = v.w[j];
+        for (int j = 0; j < V; j++)
+            if (j < cnt) p[j] = x[j];
     }
 }
 
 template <int DT>
-__device__ __forceinline__ V8<DT> ld8(const void* base, int64_t idx, int cnt)
+__device__ __forceinline__ Vals<DT> ld_vals(const void* base, int64_t idx, int cnt)
 {
-    if constexpr (DT == kF32)
-        return ld_w8(base, idx, cnt);
-    else
-        return ld_h8(base, idx, cnt);
+    if constexpr (DT == kF32) {
+        Vals<DT> r;
+        ld_u32<kVecOf<DT>>(base, idx, cnt, r.w);
+        return r;
+    } else {
+        return ld_h16<kVecOf<DT>>(base, idx, cnt);
+    }
 }
 
 template <int DT>
-__device__ __forceinline__ void st8(void* base, int64_t idx, const V8<DT>& v, int cnt)
+__device__ __forceinline__ void st_vals(void* base, int64_t idx, const Vals<DT>& v, int cnt)
 {
     if constexpr (DT == kF32)
-        st_w8(base, idx, v, cnt);
+        st_u32<kVecOf<DT>>(base, idx, cnt, v.w);
     else
-        st_h8(base, idx, v, cnt);
+        st_h16<kVecOf<DT>>(base, idx, v, cnt);
+}
+
+template <int V>
+__device__ __forceinline__ void ld_f(const float* base, int64_t idx, int cnt, float x[V])
+{
+    uint32_t u[V];
+    ld_u32<V>(base, idx, cnt, u);
+#pragma unroll
+    for (int j = 0; j < V; j++)
+        x[j] = __uint_as_float(u[j]);
+}
+
+template <int V>
+__device__ __forceinline__ void st_f(float* base, int64_t idx, int cnt, const float x[V])
+{
+    uint32_t u[V];
+#pragma unroll
+    for (int j = 0; j < V; j++)
+        u[j] = __float_as_uint(x[j]);
+    st_u32<V>(base, idx, cnt, u);
 }
 
 // Nonzero if the binary32 pattern is inf or NaN.
@@ -200,18 +238,19 @@ __device__ __forceinline__ uint32_t nonfinite32(uint32_t b) { return (~b & 0x7f8
 // for 16-bit types, none for binary32); returns nonzero if any element of h
 // is inf or NaN.  Elements past cnt are 0: finite.
 template <int DT>
-__device__ __forceinline__ uint32_t round_group(const float s[kVec], V8<DT>& h)
+__device__ __forceinline__ uint32_t round_group(const float s[kVecOf<DT>], Vals<DT>& h)
 {
+    constexpr int V = kVecOf<DT>;
     uint32_t nf = 0;
     if constexpr (DT == kF32) {
 #pragma unroll
-        for (int j = 0; j < kVec; j++) {
+        for (int j = 0; j < V; j++) {
             h.w[j] = __float_as_uint(s[j]);
             nf |= nonfinite32(h.w[j]);
         }
     } else {
 #pragma unroll
-        for (int p = 0; p < kVec / 2; p++) {
+        for (int p = 0; p < V / 2; p++) {
             h.w[p] = from_f32x2<DT>(s[2 * p], s[2 * p + 1]);
             nf |= nonfinite_x2<DT>(h.w[p]);
         }
@@ -221,15 +260,16 @@ __device__ __forceinline__ uint32_t round_group(const float s[kVec], V8<DT>& h)
 
 // g = float(h) * inv, elementwise.
 template <int DT>
-__device__ __forceinline__ void unscale_group(const V8<DT>& h, float inv, float g[kVec])
+__device__ __forceinline__ void unscale_group(const Vals<DT>& h, float inv, float g[kVecOf<DT>])
 {
+    constexpr int V = kVecOf<DT>;
     if constexpr (DT == kF32) {
 #pragma unroll
-        for (int j = 0; j < kVec; j++)
+        for (int j = 0; j < V; j++)
             g[j] = __fmul_rn(__uint_as_float(h.w[j]), inv);
     } else {
 #pragma unroll
-        for (int p = 0; p < kVec / 2; p++) {
+        for (int p = 0; p < V / 2; p++) {
             const float2 f = to_f32x2<DT>(h.w[p]);
             g[2 * p] = __fmul_rn(f.x, inv);
             g[2 * p + 1] = __fmul_rn(f.y, inv);
@@ -237,76 +277,38 @@ __device__ __forceinline__ void unscale_group(const V8<DT>& h, float inv, float 
     }
 }
 
-__device__ __forceinline__ void ld_f8(const float* base, int64_t idx, int cnt, float x[kVec])
-{
-    const float* p = base + idx;
-    if (cnt == kVec) {
-        const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
-        const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-    } else {
-#pragma unroll
-        for (int j = 0; j < kVec; j++)
-            x[j] = j < cnt ? p[j] : 0.0f;
-    }
-}
-
-__device__ __forceinline__ void st_f8(float* base, int64_t idx, int cnt, const float x[kVec])
-{
-    float* p = base + idx;
-    if (cnt == kVec) {
-        __stcs(reinterpret_cast<float4*>(p), make_float4(x[0], x[1], x[2], x[3]));
-        __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(x[4], x[5], x[6], x[7]));
-    } else {
-#pragma unroll
-        for (int j = 0; j < kVec; j++)
-            if (j < cnt) p[j] = x[j];
-    }
-}
-
 // Rank-order fp32 sum of the N ranks' gradients for one group:
 // s[j] = (((0 + g_0[j]) + g_1[j]) + ...) + g_{N-1}[j].  Loads are issued in
-// batches of 8 ranks (16-bit) or 4 ranks (binary32), so that up to 128
-// bytes are in flight per thread.
+// batches of 8 ranks, i.e. 128 bytes in flight per thread (8 x 16 bytes of
+// 16-bit values, or 8 x 16 bytes of binary32 values).
 template <int DT>
-__device__ __forceinline__ void reduce_group(const StepArgs& a, int64_t gidx, int cnt, float s[kVec])
+__device__ __forceinline__ void reduce_group(const StepArgs& a, int64_t gidx, int cnt, float s[kVecOf<DT>])
 {
+    constexpr int V = kVecOf<DT>;
+    constexpr int kB = 8;
 #pragma unroll
-    for (int j = 0; j < kVec; j++)
+    for (int j = 0; j < V; j++)
         s[j] = 0.0f;
-    if constexpr (DT == kF32) {
-        for (int r0 = 0; r0 < a.n_ranks; r0 += 4) {
-            W8 q[4];
+    for (int r0 = 0; r0 < a.n_ranks; r0 += kB) {
+        Vals<DT> q[kB];
 #pragma unroll
-            for (int k = 0; k < 4; k++)
-                if (r0 + k < a.n_ranks)
-                    q[k] = ld_w8(a.grads[r0 + k], gidx, cnt);
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                if (r0 + k < a.n_ranks) {
-#pragma unroll
-                    for (int j = 0; j < kVec; j++)
-                        s[j] = __fadd_rn(s[j], __uint_as_float(q[k].w[j]));
-                }
-            }
-        }
-        return;
-    }
-    for (int r0 = 0; r0 < a.n_ranks; r0 += 8) {
-        H8 q[8];
-#pragma unroll
-        for (int k = 0; k < 8; k++)
+        for (int k = 0; k < kB; k++)
             if (r0 + k < a.n_ranks)
-                q[k] = ld_h8(a.grads[r0 + k], gidx, cnt);
+                q[k] = ld_vals<DT>(a.grads[r0 + k], gidx, cnt);
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
+        for (int k = 0; k < kB; k++) {
             if (r0 + k < a.n_ranks) {
+                if constexpr (DT == kF32) {
 #pragma unroll
-                for (int p = 0; p < kVec / 2; p++) {
-                    const float2 f = to_f32x2<DT>(q[k].w[p]);
-                    s[2 * p] = __fadd_rn(s[2 * p], f.x);
-                    s[2 * p + 1] = __fadd_rn(s[2 * p + 1], f.y);
+                    for (int j = 0; j < V; j++)
+                        s[j] = __fadd_rn(s[j], __uint_as_float(q[k].w[j]));
+                } else {
+#pragma unroll
+                    for (int p = 0; p < V / 2; p++) {
+                        const float2 f = to_f32x2<DT>(q[k].w[p]);
+                        s[2 * p] = __fadd_rn(s[2 * p], f.x);
+                        s[2 * p + 1] = __fadd_rn(s[2 * p + 1], f.y);
+                    }
                 }
             }
         }
@@ -353,39 +355,40 @@ __device__ __forceinline__ void sgd1(float g, float& w, const AdamHP& hp)
 }
 
 // The optimizer update of one group: load the fp32 state the optimizer keeps
-// at state index si (w; m; v), update it with the 8 unscaled gradients g,
+// at state index si (w; m; v), update it with the unscaled gradients g,
 // store it to the output state and give back the model-precision cast in p.
 template <int DT, int OPT>
 __device__ __forceinline__ void update_state(const StepArgs& a, const AdamHP& hp, int64_t si, int cnt,
-                                             const float g[kVec], V8<DT>& p)
+                                             const float g[kVecOf<DT>], Vals<DT>& p)
 {
-    float w[kVec];
-    ld_f8(a.w_in, si, cnt, w);
+    constexpr int V = kVecOf<DT>;
+    float w[V];
+    ld_f<V>(a.w_in, si, cnt, w);
     if constexpr (OPT == kAdam) {
-        float m[kVec], v[kVec];
-        ld_f8(a.m_in, si, cnt, m);
-        ld_f8(a.v_in, si, cnt, v);
+        float m[V], v[V];
+        ld_f<V>(a.m_in, si, cnt, m);
+        ld_f<V>(a.v_in, si, cnt, v);
 #pragma unroll
-        for (int j = 0; j < kVec; j++)
+        for (int j = 0; j < V; j++)
             adam1(g[j], w[j], m[j], v[j], hp);
-        st_f8(a.m_out, si, cnt, m);
-        st_f8(a.v_out, si, cnt, v);
+        st_f<V>(a.m_out, si, cnt, m);
+        st_f<V>(a.v_out, si, cnt, v);
     } else if constexpr (OPT == kSgdm) {
-        float m[kVec];
-        ld_f8(a.m_in, si, cnt, m);
+        float m[V];
+        ld_f<V>(a.m_in, si, cnt, m);
 #pragma unroll
-        for (int j = 0; j < kVec; j++)
+        for (int j = 0; j < V; j++)
             sgdm1(g[j], w[j], m[j], hp);
-        st_f8(a.m_out, si, cnt, m);
+        st_f<V>(a.m_out, si, cnt, m);
     } else {
 #pragma unroll
-        for (int j = 0; j < kVec; j++)
+        for (int j = 0; j < V; j++)
             sgd1(g[j], w[j], hp);
     }
 #pragma unroll
-    for (int j = 0; j < kVec; j++)
+    for (int j = 0; j < V; j++)
         p.set(j, from_f32<DT>(w[j]));
-    st_f8(a.w_out, si, cnt, w);
+    st_f<V>(a.w_out, si, cnt, w);
 }
 
 // ---- exact sum of squares --------------------------------------------------

@@ -96,39 +96,39 @@ __global__ void __launch_bounds__(kThreads) k_restore_async(const __grid_constan
 {
     if (blockIdx.x == 0 && threadIdx.x == 0) commit(c);
     if (!*reinterpret_cast<const volatile uint32_t*>(ws_flag(a.ws))) return;   // clean step: nothing to do
-    const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
+    const int64_t ngroups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     const int reps = STAGE == 0 ? a.n_ranks : 1;
     for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
          gi += (int64_t)gridDim.x * kThreads) {
-        const int64_t i = a.lo + gi * kVec;
-        const int cnt = (int)min((int64_t)kVec, a.hi - i);
+        const int64_t i = a.lo + gi * kVecOf<DT>;
+        const int cnt = (int)min((int64_t)kVecOf<DT>, a.hi - i);
         for (int r = 0; r < reps; r++) {
             const int64_t si = (int64_t)r * a.replica_stride + i;
-            float w[kVec];
-            ld_f8(a.w_in, si, cnt, w);
-            st_f8(a.w_out, si, cnt, w);
+            float w[kVecOf<DT>];
+            ld_f<kVecOf<DT>>(a.w_in, si, cnt, w);
+            st_f<kVecOf<DT>>(a.w_out, si, cnt, w);
             if constexpr (OPT != kSgd) {
-                float m[kVec];
-                ld_f8(a.m_in, si, cnt, m);
-                st_f8(a.m_out, si, cnt, m);
+                float m[kVecOf<DT>];
+                ld_f<kVecOf<DT>>(a.m_in, si, cnt, m);
+                st_f<kVecOf<DT>>(a.m_out, si, cnt, m);
             }
             if constexpr (OPT == kAdam) {
-                float v[kVec];
-                ld_f8(a.v_in, si, cnt, v);
-                st_f8(a.v_out, si, cnt, v);
+                float v[kVecOf<DT>];
+                ld_f<kVecOf<DT>>(a.v_in, si, cnt, v);
+                st_f<kVecOf<DT>>(a.v_out, si, cnt, v);
             }
-            V8<DT> p;
+            Vals<DT> p;
 #pragma unroll
-            for (int j = 0; j < kVec; j++)
+            for (int j = 0; j < kVecOf<DT>; j++)
                 p.set(j, from_f32<DT>(w[j]));
             if constexpr (STAGE == 0) {
-                st8<DT>(a.params16[r], i, p, cnt);
+                st_vals<DT>(a.params16[r], i, p, cnt);
             } else if constexpr (STAGE == 3) {
                 const int o = owner_of(i, a.shard);
-                st8<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
+                st_vals<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
             } else {
                 for (int q = 0; q < a.n_ranks; q++)
-                    st8<DT>(a.params16[q], i, p, cnt);
+                    st_vals<DT>(a.params16[q], i, p, cnt);
             }
         }
     }
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kThreads) k_restore_async(const __grid_constan
 template <int STAGE, int DT, int OPT>
 cudaError_t run_restore_async(const StepArgs& a, const CommitArgs& c, cudaStream_t s)
 {
-    const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
+    const int64_t groups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     const int grid = groups > 0 ? grid_for((const void*)k_restore_async<STAGE, DT, OPT>, groups) : 1;
     k_restore_async<STAGE, DT, OPT><<<grid, kThreads, 0, s>>>(a, c);
     return cudaGetLastError();

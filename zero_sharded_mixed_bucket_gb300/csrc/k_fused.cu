@@ -34,43 +34,43 @@ __global__ void __launch_bounds__(kThreads, STAGE == 0 ? 5 : 1) k_fused(const __
         hp.bc1 = a.dyn->bc1;
         hp.bc2 = a.dyn->bc2;
     }
-    const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
+    const int64_t ngroups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     bool bad = false;
     for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
          gi += (int64_t)gridDim.x * kThreads) {
-        const int64_t i = a.lo + gi * kVec;
-        const int cnt = (int)min((int64_t)kVec, a.hi - i);
+        const int64_t i = a.lo + gi * kVecOf<DT>;
+        const int cnt = (int)min((int64_t)kVecOf<DT>, a.hi - i);
         const int64_t gidx = i - a.grad_base;
 
-        float s[kVec];
+        float s[kVecOf<DT>];
         reduce_group<DT>(a, gidx, cnt, s);
 
         // round to the model precision (elements past cnt are 0: finite, no effect)
-        V8<DT> h;
+        Vals<DT> h;
         bad |= round_group<DT>(s, h) != 0;
-        float g[kVec];
+        float g[kVecOf<DT>];
         unscale_group<DT>(h, inv, g);
 
         if constexpr (STAGE <= 1) {
             for (int r = 0; r < a.n_ranks; r++)
-                st8<DT>(const_cast<void*>(a.grads[r]), gidx, h, cnt);
+                st_vals<DT>(const_cast<void*>(a.grads[r]), gidx, h, cnt);
         }
 
         if constexpr (STAGE == 0) {
             for (int r = 0; r < a.n_ranks; r++) {
-                V8<DT> p;
+                Vals<DT> p;
                 update_state<DT, OPT>(a, hp, (int64_t)r * a.replica_stride + i, cnt, g, p);
-                st8<DT>(a.params16[r], i, p, cnt);
+                st_vals<DT>(a.params16[r], i, p, cnt);
             }
         } else {
-            V8<DT> p;
+            Vals<DT> p;
             update_state<DT, OPT>(a, hp, i, cnt, g, p);
             if constexpr (STAGE == 3) {
                 const int o = owner_of(i, a.shard);
-                st8<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
+                st_vals<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
             } else {
                 for (int r = 0; r < a.n_ranks; r++)
-                    st8<DT>(a.params16[r], i, p, cnt);
+                    st_vals<DT>(a.params16[r], i, p, cnt);
             }
         }
     }
@@ -84,27 +84,27 @@ __global__ void __launch_bounds__(kThreads, STAGE == 0 ? 5 : 1) k_fused(const __
 template <int STAGE, int DT>
 __global__ void __launch_bounds__(kThreads) k_restore(const __grid_constant__ StepArgs a)
 {
-    const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
+    const int64_t ngroups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
          gi += (int64_t)gridDim.x * kThreads) {
-        const int64_t i = a.lo + gi * kVec;
-        const int cnt = (int)min((int64_t)kVec, a.hi - i);
+        const int64_t i = a.lo + gi * kVecOf<DT>;
+        const int cnt = (int)min((int64_t)kVecOf<DT>, a.hi - i);
         const int reps = STAGE == 0 ? a.n_ranks : 1;
         for (int r = 0; r < reps; r++) {
-            float w[kVec];
-            ld_f8(a.w_in, (int64_t)r * a.replica_stride + i, cnt, w);
-            V8<DT> p;
+            float w[kVecOf<DT>];
+            ld_f<kVecOf<DT>>(a.w_in, (int64_t)r * a.replica_stride + i, cnt, w);
+            Vals<DT> p;
 #pragma unroll
-            for (int j = 0; j < kVec; j++)
+            for (int j = 0; j < kVecOf<DT>; j++)
                 p.set(j, from_f32<DT>(w[j]));
             if constexpr (STAGE == 0) {
-                st8<DT>(a.params16[r], i, p, cnt);
+                st_vals<DT>(a.params16[r], i, p, cnt);
             } else if constexpr (STAGE == 3) {
                 const int o = owner_of(i, a.shard);
-                st8<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
+                st_vals<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
             } else {
                 for (int q = 0; q < a.n_ranks; q++)
-                    st8<DT>(a.params16[q], i, p, cnt);
+                    st_vals<DT>(a.params16[q], i, p, cnt);
             }
         }
     }
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kThreads) k_restore(const __grid_constant__ St
 template <int STAGE, int DT, int OPT>
 cudaError_t run_fused3(const StepArgs& a, cudaStream_t s, bool overlap)
 {
-    const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
+    const int64_t groups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     if (groups <= 0) return cudaSuccess;
     const int grid = grid_for((const void*)k_fused<STAGE, DT, OPT>, groups);
     return launch_step_kernel(k_fused<STAGE, DT, OPT>, grid, s, overlap, a);
@@ -132,7 +132,7 @@ cudaError_t run_fused(int opt, const StepArgs& a, cudaStream_t s, bool overlap)
 template <int STAGE, int DT>
 cudaError_t run_restore(const StepArgs& a, cudaStream_t s)
 {
-    const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
+    const int64_t groups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     if (groups <= 0) return cudaSuccess;
     const int grid = grid_for((const void*)k_restore<STAGE, DT>, groups);
     k_restore<STAGE, DT><<<grid, kThreads, 0, s>>>(a);

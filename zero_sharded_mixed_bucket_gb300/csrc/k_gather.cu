@@ -16,31 +16,41 @@ namespace zg {
 
 namespace {
 
+// Groups of 8 16-bit units (16 bytes) per thread.
+constexpr int kG = 8;
+
 __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ GatherArgs a)
 {
-    const int64_t ngroups = (a.len + kVec - 1) / kVec;
+    const int64_t ngroups = (a.len + kG - 1) / kG;
     for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
          gi += (int64_t)gridDim.x * kThreads) {
-        const int64_t j0 = gi * kVec;
-        const int cnt = (int)min((int64_t)kVec, a.len - j0);
+        const int64_t j0 = gi * kG;
+        const int cnt = (int)min((int64_t)kG, a.len - j0);
         const int64_t i = a.start + j0;
-        H8 h;
-        if (cnt == kVec && (i & (kVec - 1)) == 0) {
-            // shards are multiples of 8 elements: an aligned group has one owner
+        if (cnt == kG && (i & (kG - 1)) == 0) {
+            // shards are multiples of 8 units: an aligned group has one owner
             const int o = owner_of(i, a.shard);
-            h = ld_h8(a.shards[o], i - (int64_t)o * a.shard, kVec);
+            const uint4 v = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.shards[o]) +
+                                                                  (i - (int64_t)o * a.shard)));
+            for (int d = 0; d < a.n_dst; d++)
+                __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dst[d]) + j0), v);
         } else {
-            h.w[0] = h.w[1] = h.w[2] = h.w[3] = 0;
+            uint16_t u[kG];
 #pragma unroll
-            for (int j = 0; j < kVec; j++) {
+            for (int j = 0; j < kG; j++) {
+                u[j] = 0;
                 if (j < cnt) {
                     const int o = owner_of(i + j, a.shard);
-                    h.set(j, static_cast<const uint16_t*>(a.shards[o])[i + j - (int64_t)o * a.shard]);
+                    u[j] = static_cast<const uint16_t*>(a.shards[o])[i + j - (int64_t)o * a.shard];
                 }
             }
+            for (int d = 0; d < a.n_dst; d++) {
+                uint16_t* p = static_cast<uint16_t*>(a.dst[d]) + j0;
+#pragma unroll
+                for (int j = 0; j < kG; j++)
+                    if (j < cnt) p[j] = u[j];
+            }
         }
-        for (int d = 0; d < a.n_dst; d++)
-            st_h8(a.dst[d], j0, h, cnt);
     }
 }
 
@@ -48,7 +58,7 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Gat
 
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s)
 {
-    const int64_t groups = (a.len + kVec - 1) / kVec;
+    const int64_t groups = (a.len + kG - 1) / kG;
     if (groups <= 0) return cudaSuccess;
     const int grid = grid_for((const void*)k_gather, groups);
     k_gather<<<grid, kThreads, 0, s>>>(a);

@@ -19,33 +19,33 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ Ste
 {
     allow_next_grid();
     const int win_lo = a.dyn ? a.dyn->win_lo : a.win_lo;
-    const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
+    const int64_t ngroups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     bool bad = false;
     U128 acc{0ull, 0ull};
     unsigned long long* bins = ws_bins(a.ws);
     for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
          gi += (int64_t)gridDim.x * kThreads) {
-        const int64_t i = a.lo + gi * kVec;
-        const int cnt = (int)min((int64_t)kVec, a.hi - i);
+        const int64_t i = a.lo + gi * kVecOf<DT>;
+        const int cnt = (int)min((int64_t)kVecOf<DT>, a.hi - i);
         const int64_t gidx = i - a.grad_base;
-        float s[kVec];
+        float s[kVecOf<DT>];
         reduce_group<DT>(a, gidx, cnt, s);
         // round to the model precision; elements past cnt are 0 (finite, square 0)
-        V8<DT> h;
+        Vals<DT> h;
         bad |= round_group<DT>(s, h) != 0;
         if constexpr (CLIP) {
             static_assert(DT != kF32, "no exact sum of squares for binary32 values");
 #pragma unroll
-            for (int p = 0; p < kVec / 2; p++) {
+            for (int p = 0; p < kVecOf<DT> / 2; p++) {
                 sumsq_add<DT>(h.w[p] & 0xffffu, win_lo, acc, bins);
                 sumsq_add<DT>(h.w[p] >> 16, win_lo, acc, bins);
             }
         }
         if constexpr (HDEST == 0) {
             for (int r = 0; r < a.n_ranks; r++)
-                st8<DT>(const_cast<void*>(a.grads[r]), gidx, h, cnt);
+                st_vals<DT>(const_cast<void*>(a.grads[r]), gidx, h, cnt);
         } else {
-            st8<DT>(a.reduced, i, h, cnt);
+            st_vals<DT>(a.reduced, i, h, cnt);
         }
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0)
@@ -148,7 +148,7 @@ __global__ void k_finalize(const FinalArgs a)
 template <int HDEST, int DT, bool CLIP>
 cudaError_t run_reduce(const StepArgs& a, cudaStream_t s, bool overlap)
 {
-    const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
+    const int64_t groups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     if (groups <= 0) return cudaSuccess;
     const int grid = grid_for((const void*)k_reduce<HDEST, DT, CLIP>, groups);
     return launch_step_kernel(k_reduce<HDEST, DT, CLIP>, grid, s, overlap, a);

@@ -28,37 +28,37 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
         hp.bc1 = a.dyn->bc1;
         hp.bc2 = a.dyn->bc2;
     }
-    const int64_t ngroups = (a.hi - a.lo + kVec - 1) / kVec;
+    const int64_t ngroups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
          gi += (int64_t)gridDim.x * kThreads) {
-        const int64_t i = a.lo + gi * kVec;
-        const int cnt = (int)min((int64_t)kVec, a.hi - i);
+        const int64_t i = a.lo + gi * kVecOf<DT>;
+        const int cnt = (int)min((int64_t)kVecOf<DT>, a.hi - i);
         const int reps = STAGE == 0 ? a.n_ranks : 1;
         for (int r = 0; r < reps; r++) {
-            V8<DT> h;
+            Vals<DT> h;
             if constexpr (STAGE == 0)
-                h = ld8<DT>(a.grads[r], i - a.grad_base, cnt);        // each replica its own all-reduced copy
+                h = ld_vals<DT>(a.grads[r], i - a.grad_base, cnt);        // each replica its own all-reduced copy
             else if constexpr (STAGE == 1)
-                h = ld8<DT>(a.grads[owner_of(i, a.shard)], i - a.grad_base, cnt);
+                h = ld_vals<DT>(a.grads[owner_of(i, a.shard)], i - a.grad_base, cnt);
             else
-                h = ld8<DT>(a.reduced, i, cnt);
-            float g[kVec];
+                h = ld_vals<DT>(a.reduced, i, cnt);
+            float g[kVecOf<DT>];
             unscale_group<DT>(h, inv, g);
             if (c != 1.0f) {
 #pragma unroll
-                for (int j = 0; j < kVec; j++)
+                for (int j = 0; j < kVecOf<DT>; j++)
                     g[j] = __fmul_rn(g[j], c);
             }
-            V8<DT> p;
+            Vals<DT> p;
             update_state<DT, OPT>(a, hp, (int64_t)r * a.replica_stride + i, cnt, g, p);
             if constexpr (STAGE == 0) {
-                st8<DT>(a.params16[r], i, p, cnt);
+                st_vals<DT>(a.params16[r], i, p, cnt);
             } else if constexpr (STAGE == 3) {
                 const int o = owner_of(i, a.shard);
-                st8<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
+                st_vals<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
             } else {
                 for (int q = 0; q < a.n_ranks; q++)
-                    st8<DT>(a.params16[q], i, p, cnt);
+                    st_vals<DT>(a.params16[q], i, p, cnt);
             }
         }
     }
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
 template <int STAGE, int DT, bool CLIP, int OPT>
 cudaError_t run_update(const StepArgs& a, cudaStream_t s, bool overlap)
 {
-    const int64_t groups = (a.hi - a.lo + kVec - 1) / kVec;
+    const int64_t groups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     if (groups <= 0) return cudaSuccess;
     const int grid = grid_for((const void*)k_update<STAGE, DT, CLIP, OPT>, groups);
     return launch_step_kernel(k_update<STAGE, DT, CLIP, OPT>, grid, s, overlap, a);

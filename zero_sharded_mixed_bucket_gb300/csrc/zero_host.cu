@@ -83,9 +83,9 @@ zero_status_t check_config(const zero_config_t* c)
     if (c->n_params < 0) return fail(ZERO_EINVAL, "n_params %lld < 0", (long long)c->n_params);
     if (c->n_params > (int64_t(1) << 40))
         return fail(ZERO_EUNSUPPORTED, "n_params %lld exceeds 2^40", (long long)c->n_params);
-    if (c->bucket_elems <= 0 || c->bucket_elems % kVec)
+    if (c->bucket_elems <= 0 || c->bucket_elems % 8)
         return fail(ZERO_EINVAL, "bucket_elems %lld must be a positive multiple of 8", (long long)c->bucket_elems);
-    if (c->align_elems < 0 || c->align_elems % kVec)
+    if (c->align_elems < 0 || c->align_elems % 8)
         return fail(ZERO_EINVAL, "align_elems %lld must be 0 or a positive multiple of 8", (long long)c->align_elems);
     if (c->dtype != ZERO_FP16 && c->dtype != ZERO_BF16 && c->dtype != ZERO_FP32)
         return fail(ZERO_EINVAL, "dtype %d unknown", c->dtype);

@@ -10,7 +10,6 @@ namespace zg {
 
 constexpr int kMaxRanks = ZERO_MAX_RANKS;
 constexpr int kThreads = 128;   // threads per block of every streaming kernel (measured best for k_fused)
-constexpr int kVec = 8;         // consecutive elements per thread and iteration (16 bytes of 16-bit data)
 
 // Workspace layout (caller-provided device memory, zeroed by zero_step_begin).
 namespace ws {
