@@ -1,11 +1,13 @@
 /* A plain C client of libzero_gb300: no Python, no PyTorch.
  *
- * usage: zero_c_client <dir>
+ * usage: zero_c_client <dir> [graph]
  *   reads  <dir>/in.bin:  int64 n, int32 N, int32 steps, float lr, float S,
  *                         then float w0[n], then for each step N x uint16 g[n]
  *   writes <dir>/out.bin: float w[n], float m[n], float v[n], uint16 p16[N][n],
  *                         int64 t, uint32 overflow of the last step
  * Stage 2, fp16, Adam (beta 0.9/0.999, eps 1e-8), bucket 4096, shadow state.
+ * Default: zero_step_stage2 per step.  "graph": the step state in device
+ * memory, two CUDA graphs captured from zero_step_async and replayed.
  * Exit status 0 on success; a message on stderr otherwise. */
 #include <stdint.h>
 #include <stdio.h>
@@ -36,8 +38,9 @@
 
 int main(int argc, char** argv)
 {
-    if (argc != 2) return 2;
+    if (argc != 2 && argc != 3) return 2;
     char path[4096];
+    const int graph_mode = argc > 2 && strcmp(argv[2], "graph") == 0;
     snprintf(path, sizeof path, "%s/in.bin", argv[1]);
     FILE* f = fopen(path, "rb");
     if (!f) return 2;
@@ -92,14 +95,43 @@ int main(int argc, char** argv)
     st.min_loss_scale = 1.0f;
     st.dynamic = 1;
     zero_step_result_t res;
+    memset(&res, 0, sizeof res);
     cudaStream_t stream;
     CK(cudaStreamCreate(&stream));
-    for (int k = 0; k < steps; k++) {
-        for (int r = 0; r < N; r++)
-            CK(cudaMemcpyAsync(grads[r], g + ((size_t)k * N + r) * n, n * 2, cudaMemcpyHostToDevice, stream));
-        ZK(zero_step_stage2(&cfg, &plan, &b, &adam, &st, (void*)stream, &res));
+    if (!graph_mode) {
+        for (int k = 0; k < steps; k++) {
+            for (int r = 0; r < N; r++)
+                CK(cudaMemcpyAsync(grads[r], g + ((size_t)k * N + r) * n, n * 2, cudaMemcpyHostToDevice, stream));
+            ZK(zero_step_stage2(&cfg, &plan, &b, &adam, &st, (void*)stream, &res));
+        }
+        CK(cudaStreamSynchronize(stream));
+    } else {
+        /* step state in device memory; one CUDA graph per value of b.cur
+         * (the fused path alternates the state copies on every call),
+         * replayed alternately with each step's gradients copied in first */
+        void* dev_state;
+        CK(cudaMalloc(&dev_state, sizeof(zero_dev_state_t)));
+        ZK(zero_dev_state_init(dev_state, &adam, &st, (void*)stream));
+        cudaGraphExec_t exec[2];
+        for (int k = 0; k < 2; k++) {
+            cudaGraph_t graph;
+            int32_t launches = 0;
+            CK(cudaStreamBeginCapture(stream, cudaStreamCaptureModeGlobal));
+            ZK(zero_step_async(&cfg, &plan, &b, &adam, dev_state, (void*)stream, &launches));
+            CK(cudaStreamEndCapture(stream, &graph));
+            CK(cudaGraphInstantiate(&exec[k], graph, 0));
+            CK(cudaGraphDestroy(graph));
+        }
+        for (int k = 0; k < steps; k++) {
+            for (int r = 0; r < N; r++)
+                CK(cudaMemcpyAsync(grads[r], g + ((size_t)k * N + r) * n, n * 2, cudaMemcpyHostToDevice, stream));
+            CK(cudaGraphLaunch(exec[k % 2], stream));
+        }
+        ZK(zero_dev_state_read(dev_state, &st, &res, (void*)stream));
+        b.cur = steps % 2;   /* the copy the last replay wrote */
+        for (int k = 0; k < 2; k++) CK(cudaGraphExecDestroy(exec[k]));
+        CK(cudaFree(dev_state));
     }
-    CK(cudaStreamSynchronize(stream));
 
     float* out = malloc(n * 4);
     uint16_t* p = malloc(n * 2);

@@ -312,3 +312,24 @@ def test_device_state_checks_reject_before_any_copy():
     assert step(fb) == zg.ZERO_ENOMEM
     assert step(_FakeBuffers(4), a=one) == zg.ZERO_EINVAL
     assert n.value == -1                       # nothing was launched
+
+
+def test_buffer_allocation_failure_propagates(monkeypatch):
+    """A failing device allocation in the binding surfaces as the allocator's
+    own error; nothing falls back to another memory or another path."""
+    import torch
+    cfg = zg.Config(1000, 2, 2, 64)
+    plan = zg.zero_plan(cfg)
+    calls = []
+    real = torch.zeros
+
+    def failing_zeros(*a, **kw):
+        calls.append(1)
+        if len(calls) == 3:
+            raise torch.OutOfMemoryError("simulated: out of device memory")
+        return real(*a, **{k: v for k, v in kw.items() if k != "device"})
+
+    monkeypatch.setattr(torch, "zeros", failing_zeros)
+    with pytest.raises(torch.OutOfMemoryError):
+        zg.DeviceBuffers(cfg, plan, device="cuda")
+    assert len(calls) == 3

@@ -1,6 +1,8 @@
 """The library used from plain C (tests/c_client/zero_c_client.c): cudaMalloc'd
-buffers, zero_plan and zero_step_stage2 called directly, no Python or
-PyTorch in the client.  Its results must equal the oracle's."""
+buffers, zero_plan and zero_step_stage2 called directly -- or the step state
+in device memory and two CUDA graphs captured from zero_step_async, replayed
+alternately -- no Python or PyTorch in the client.  Its results must equal
+the oracle's."""
 import os
 import subprocess
 
@@ -32,7 +34,8 @@ def test_client_compiles_against_the_header(tmp_path):
 
 
 @pytest.mark.gpu
-def test_c_client_matches_oracle(tmp_path):
+@pytest.mark.parametrize("mode", ["sync", "graph"])
+def test_c_client_matches_oracle(tmp_path, mode):
     n, N, steps, lr, S = 3 * 4096 + 21, 3, 3, 1e-4, 256.0
     w0 = synth.host_normal32(n, 0.02, seed=5, stream=synth.STREAM_WEIGHT)
     grads = [[synth.host_normal16(n, synth.FP16, 1e-3 * S, seed=5, stream=synth.STREAM_GRAD, step=k, rank=r)
@@ -45,7 +48,7 @@ def test_c_client_matches_oracle(tmp_path):
             for r in range(N):
                 f.write(grads[k][r].tobytes())
     exe = build_client(str(tmp_path))
-    subprocess.run([exe, str(tmp_path)], check=True)
+    subprocess.run([exe, str(tmp_path)] + (["graph"] if mode == "graph" else []), check=True)
     raw = open(tmp_path / "out.bin", "rb").read()
     w = np.frombuffer(raw, np.float32, n, 0)
     m = np.frombuffer(raw, np.float32, n, 4 * n)

@@ -15,6 +15,7 @@
 #include <cstring>
 #include <new>
 
+#include "nvtx_ranges.h"
 #include "zero_internal.h"
 
 namespace zg {
@@ -236,6 +237,7 @@ zero_status_t zero_fetcher_init(zero_fetcher_t* f, const zero_config_t* cfg, con
 
 zero_status_t zero_fetch_layer(zero_fetcher_t* f, int32_t pos, void* stream, int64_t* offset)
 {
+    zg::NvtxRange range("zero_fetch_layer", pos);
     Fetcher* F = as_fetcher(f);
     if (!F) return set_error(ZERO_EINVAL, "fetcher not initialised");
     if (pos != F->next_fetch) return set_error(ZERO_EINVAL, "layers must be fetched in the order's sequence");

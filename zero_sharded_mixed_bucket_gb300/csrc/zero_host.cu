@@ -6,6 +6,7 @@
 #include <cstring>
 #include <string>
 
+#include "nvtx_ranges.h"
 #include "zero_internal.h"
 
 namespace zg {
@@ -327,6 +328,7 @@ zero_status_t bucket_impl(const zero_config_t* c, const zero_plan_t* p, const ze
                           const zero_adam_t* adam, const zero_state_t* s, int64_t bucket, void* const* bucket_grads,
                           cudaStream_t st, bool overlap)
 {
+    NvtxRange range("zero_bucket", bucket);
     const Path path = choose_path(c, b, adam);
     const int64_t lo = bucket * c->bucket_elems;
     const int64_t hi = lo + c->bucket_elems < c->n_params ? lo + c->bucket_elems : c->n_params;
@@ -343,6 +345,7 @@ zero_status_t bucket_impl(const zero_config_t* c, const zero_plan_t* p, const ze
 zero_status_t end_impl(const zero_config_t* c, const zero_plan_t* p, zero_buffers_t* b, const zero_adam_t* adam,
                        zero_state_t* s, cudaStream_t st, zero_step_result_t* out)
 {
+    NvtxRange range("zero_step_end");
     const Path path = choose_path(c, b, adam);
     int launches = (int)p->n_buckets;
     cudaError_t e;
@@ -430,6 +433,7 @@ zero_status_t end_impl(const zero_config_t* c, const zero_plan_t* p, zero_buffer
 zero_status_t step_impl(int want_stage, const zero_config_t* c, const zero_plan_t* p, zero_buffers_t* b,
                         const zero_adam_t* adam, zero_state_t* s, void* stream, zero_step_result_t* out)
 {
+    NvtxRange range("zero_step", c ? c->stage : -1);
     zero_status_t st = check_step(c, p, b, adam, s);
     if (st != ZERO_OK) return st;
     if (want_stage >= 0 && c->stage != want_stage)
@@ -598,6 +602,7 @@ zero_status_t zero_step_end(const zero_config_t* c, const zero_plan_t* p, zero_b
 zero_status_t zero_gather_layer(const zero_config_t* c, const zero_plan_t* p, int32_t layer,
                                 void* const* param_shards, void* const* dst, int32_t n_dst, void* stream)
 {
+    NvtxRange range("zero_gather_layer", layer);
     zero_status_t st = check_plan(c, p);
     if (st != ZERO_OK) return st;
     if (c->stage != 3) return fail(ZERO_EINVAL, "layer gathers belong to stage 3 (config has stage %d)", c->stage);
@@ -670,6 +675,7 @@ zero_status_t zero_dev_state_init(void* dev_state, const zero_adam_t* adam, cons
 zero_status_t zero_step_async(const zero_config_t* c, const zero_plan_t* p, zero_buffers_t* b, const zero_adam_t* adam,
                               void* dev_state, void* stream, int32_t* kernel_launches)
 {
+    NvtxRange range("zero_step_async");
     zero_state_t host_view;   // the real step state is on the device; this only passes the host checks
     std::memset(&host_view, 0, sizeof host_view);
     host_view.loss_scale = 1.0f;
@@ -692,6 +698,7 @@ zero_status_t zero_step_async(const zero_config_t* c, const zero_plan_t* p, zero
     if (g_prof_start && (e = cudaEventRecord(g_prof_start, cs)) != cudaSuccess)
         return cuda_fail(e, "recording the profiling start event");
     for (int64_t bk = 0; bk < p->n_buckets; bk++) {
+        NvtxRange bucket_range("zero_bucket", bk);
         StepArgs a = make_args(c, p, b, adam, &host_view, path.fused, b->grads, 0);
         a.dyn = dyn;
         a.lo = bk * c->bucket_elems;
