@@ -432,10 +432,12 @@ def _timed_steps_async(job, steps, warmup, world):
     return ms, launches, kernel, (t0, t1)
 
 
-def e2e_leg(job, steps, warmup, device):
+def e2e_leg(job, steps, warmup, device, world=1):
     """Same step through the C ABI with each step's gradients copied in from
     pinned host memory (bucket by bucket on a copy stream, overlapped with the
-    previous bucket's kernel) and the step result read back by the library."""
+    previous bucket's kernel) and the step result read back by the library.
+    With several ranks all run at once (each GPU has its own host link); the
+    time is the slowest rank's and the value counts every rank's parameters."""
     import torch
     zg = job.zg
     n = N_PARAMS
@@ -474,6 +476,7 @@ def e2e_leg(job, steps, warmup, device):
         for k in range(warmup):
             fn(k)
         torch.cuda.synchronize()
+        barrier(world)
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(job.stream)
         for k in range(steps):
@@ -481,7 +484,9 @@ def e2e_leg(job, steps, warmup, device):
             assert res.overflow == 0
         end.record(job.stream)
         torch.cuda.synchronize()
-        return start.elapsed_time(end) / steps
+        ms = max_over_ranks(start.elapsed_time(end) / steps, world)
+        barrier(world)
+        return ms
 
     import ctypes
     host_ptrs = [(ctypes.c_void_p * N_RANKS)(*[t.data_ptr() for t in hb]) for hb in host]
@@ -498,12 +503,12 @@ def e2e_leg(job, steps, warmup, device):
     h2d = N_RANKS * n * 2
     ms = min(ms_copy, ms_direct)
     mode = "direct" if ms_direct <= ms_copy else "copy"
-    return dict(value=n / (ms * 1e-3) / 1e9, unit=UNIT, h2d_bytes_per_step=h2d, d2h_bytes_per_step=32,
-                ms_per_step=ms, mode=mode,
-                modes={"copy": {"ms_per_step": ms_copy, "value": n / (ms_copy * 1e-3) / 1e9,
+    return dict(value=world * n / (ms * 1e-3) / 1e9, unit=UNIT, h2d_bytes_per_step=world * h2d,
+                d2h_bytes_per_step=world * 32, ms_per_step=ms, mode=mode,
+                modes={"copy": {"ms_per_step": ms_copy, "value": world * n / (ms_copy * 1e-3) / 1e9,
                                 "note": "per-bucket cudaMemcpyAsync from pinned host memory on a second stream, "
                                         "overlapped with the previous bucket's kernel"},
-                       "direct": {"ms_per_step": ms_direct, "value": n / (ms_direct * 1e-3) / 1e9,
+                       "direct": {"ms_per_step": ms_direct, "value": world * n / (ms_direct * 1e-3) / 1e9,
                                   "note": "the fused kernel reads the gradients from pinned host memory over "
                                           "NVLink-C2C"}},
                 note="every step moves the step's 16-bit gradients of all ranks from pinned host memory to the "
@@ -568,50 +573,63 @@ def gpu_arm(args):
                                 "steps)", "sync": "zero_step_stage2 (overflow flag read by the host every step)"
                        }[args.step_api]
     out["clocks"] = clocks_summary(rows, t0, t1)
-    if rank == 0 and args.headline_only:
-        print(json.dumps(out))
-    elif rank == 0 and (args.optimizer != "adam" or dt_name != "fp16"):
+    if args.headline_only:
+        if rank == 0:
+            print(json.dumps(out))
+    elif args.optimizer != "adam" or dt_name != "fp16":
         raise SystemExit("--optimizer other than adam or --dtype other than fp16 needs --headline-only")
-    elif rank == 0:
-        # stages 0 and 1 on the same workload (reported, not the headline).
-        # Stages 0/1 overwrite each rank's gradient with the all-reduce result,
-        # so every step gets a gradient set of its own.
-        other = "sync" if args.step_api == "async" else "async"
-        try:
-            k = max(5, args.steps // 4)
-            oms, _, ok, _ = timed_steps(job, k, 3, 1, api=other)
-            out["other_step_api"] = {"api": other, "steps": k, "ms_per_step": oms / k,
-                                     "value": n_params / (oms / k * 1e-3) / 1e9,
-                                     "kernel_span_ms_per_step": ok["span_ms_per_step"]}
-        except Exception as e:    # reported, never hides the headline
-            out["other_step_api"] = {"api": other, "error": repr(e)}
+    else:
+        if rank == 0:
+            # the other step entry point on the same job (reported, not the headline)
+            other = "sync" if args.step_api == "async" else "async"
+            try:
+                k = max(5, args.steps // 4)
+                oms, _, ok, _ = timed_steps(job, k, 3, 1, api=other)
+                out["other_step_api"] = {"api": other, "steps": k, "ms_per_step": oms / k,
+                                         "value": n_params / (oms / k * 1e-3) / 1e9,
+                                         "kernel_span_ms_per_step": ok["span_ms_per_step"]}
+            except Exception as e:    # reported, never hides the headline
+                out["other_step_api"] = {"api": other, "error": repr(e)}
         del job
         torch.cuda.empty_cache()
-        stages = {}
-        st_steps, st_warm = 5, 3
-        for st in (1, 0):
-            try:
-                j = GpuJob(st, device, ring=st_steps + st_warm)
-                sms, _, sk, _ = timed_steps(j, st_steps, st_warm, 1)
-                stages["stage%d" % st] = {"ms_per_step": sms / st_steps,
-                                          "value": N_PARAMS / (sms / st_steps * 1e-3) / 1e9,
-                                          "kernel_gbs": sk["bytes"] / (sk["total_ms"] * 1e-3) / 1e9,
-                                          "bytes_per_param": bytes_per_param(st), "steps": st_steps}
-                del j
-            except Exception as e:   # reported, never hides the headline
-                stages["stage%d" % st] = {"error": repr(e)}
-            torch.cuda.empty_cache()
-        out["stages"] = stages
-        try:
-            j2 = GpuJob(STAGE, device, ring=2)
-            out["e2e"] = e2e_leg(j2, max(3, args.steps // 2), 3, device)
-            del j2
-        except Exception as e:
-            out["e2e"] = {"error": repr(e)}
-        torch.cuda.empty_cache()
+        # end to end on every rank at once: each GPU has its own host link
+        barrier(world)
         if world == 1:
-            out["cpu_baseline"] = cpu_baseline()
-        print(json.dumps(out))
+            try:
+                j2 = GpuJob(STAGE, device, ring=2)
+                e2e = e2e_leg(j2, max(3, args.steps // 2), 3, device, world)
+                del j2
+            except Exception as e:   # reported, never hides the headline
+                e2e = {"error": repr(e)}
+        else:
+            j2 = GpuJob(STAGE, device, ring=2)
+            e2e = e2e_leg(j2, max(3, args.steps // 2), 3, device, world)
+            del j2
+        torch.cuda.empty_cache()
+        if rank == 0:
+            out["e2e"] = e2e
+            # stages 0 and 1 on the same workload (reported, not the headline).
+            # Stages 0/1 overwrite each rank's gradient with the all-reduce result,
+            # so every step gets a gradient set of its own.
+            stages = {}
+            st_steps, st_warm = 5, 3
+            for st in (1, 0):
+                try:
+                    j = GpuJob(st, device, ring=st_steps + st_warm)
+                    sms, _, sk, _ = timed_steps(j, st_steps, st_warm, 1)
+                    stages["stage%d" % st] = {"ms_per_step": sms / st_steps,
+                                              "value": N_PARAMS / (sms / st_steps * 1e-3) / 1e9,
+                                              "kernel_gbs": sk["bytes"] / (sk["total_ms"] * 1e-3) / 1e9,
+                                              "bytes_per_param": bytes_per_param(st), "steps": st_steps}
+                    del j
+                except Exception as e:   # reported, never hides the headline
+                    stages["stage%d" % st] = {"error": repr(e)}
+                torch.cuda.empty_cache()
+            out["stages"] = stages
+            if world == 1:
+                out["cpu_baseline"] = cpu_baseline()
+            print(json.dumps(out))
+        barrier(world)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
