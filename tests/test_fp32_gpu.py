@@ -70,7 +70,8 @@ def test_bucket_staging(stage):
     job.check(res, job.oracle_step(grads))
 
 
-def test_gathers_and_fetcher():
+@pytest.mark.parametrize("n_dst", [2, 9])
+def test_gathers_and_fetcher(n_dst):
     layers = [1001, 4096, 7, 9000, 3333]
     n, N = sum(layers), 6
     job = Job(n, N, 3, 2048, 8, layers=layers, dtype=FP32, optimizer=zg.ZERO_SGD_MOMENTUM)
@@ -78,7 +79,7 @@ def test_gathers_and_fetcher():
     job.check(res, ref)
     starts = np.cumsum([0] + layers)
     shards = [t.data_ptr() for t in job.bufs.params16]
-    dst = [torch.full((job.plan.max_layer_elems,), -1, dtype=torch.int32, device="cuda") for _ in range(2)]
+    dst = [torch.full((job.plan.max_layer_elems,), -1, dtype=torch.int32, device="cuda") for _ in range(n_dst)]
     for l, ln in enumerate(layers):
         zg.zero_gather_layer(job.cfg, job.plan, l, shards, [d.data_ptr() for d in dst])
         torch.cuda.synchronize()
@@ -86,7 +87,7 @@ def test_gathers_and_fetcher():
             assert np.array_equal(as_bits(d[:ln]), job.p16[starts[l]:starts[l] + ln]), l
     # the fetcher: reverse order under a budget of the two largest layers
     cap = 9000 + 4096 + 16
-    pool = [torch.zeros(cap, dtype=torch.int32, device="cuda") for _ in range(2)]
+    pool = [torch.zeros(cap, dtype=torch.int32, device="cuda") for _ in range(n_dst)]
     side = torch.cuda.Stream()
     order = list(reversed(range(len(layers))))
     f = zg.Fetcher(job.cfg, job.plan, shards, pool, cap, order, 2, side)

@@ -128,9 +128,10 @@ def test_bucket_staging_gather_and_fetch_stay_inside():
         zg.zero_step_bucket(cfg, plan, b, adam, state, bk, [x.ptr() for x in staging], s)
     zg.zero_step_end(cfg, plan, b, adam, state, s)
     shards = [x.ptr() for x in every[N:2 * N]]
-    dst = [Guarded(plan.max_layer_elems, torch.int16) for _ in range(2)]
+    dst = [Guarded(plan.max_layer_elems, torch.int16) for _ in range(9)]
     for l in range(len(layers)):
-        zg.zero_gather_layer(cfg, plan, l, shards, [d.ptr() for d in dst], s)
+        zg.zero_gather_layer(cfg, plan, l, shards, [d.ptr() for d in dst[:2]], s)   # direct stores
+        zg.zero_gather_layer(cfg, plan, l, shards, [d.ptr() for d in dst], s)       # tiles + bulk copies
     cap = 4008 + 2056
     pool = [Guarded(cap, torch.int16) for _ in range(2)]
     side = torch.cuda.Stream()

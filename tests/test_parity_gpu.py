@@ -233,15 +233,17 @@ def test_deterministic_repeat():
 
 
 # --- stage-3 layer gather ------------------------------------------------------
-@pytest.mark.parametrize("A", [8, 2048])
-def test_gather_layers(A):
+@pytest.mark.parametrize("A,n_dst", [(8, 3), (2048, 3), (8, 8), (2048, 17)])
+def test_gather_layers(A, n_dst):
+    """Layers with unaligned starts, ragged ends and several 8192-unit tiles;
+    fewer than 8 destinations take the direct-store kernel, 8 or more the
+    shared-memory tile kernel with bulk copies."""
     layers = [1001, 4096, 7, 20_000, 3333]
     n = sum(layers)
     N = 6
     job = Job(n, N, 3, 2048, A, layers=layers)
     plan = job.plan
     assert plan.max_layer_elems == 20_000
-    n_dst = 3
     dst = [torch.full((plan.max_layer_elems,), -1, dtype=torch.int16, device="cuda") for _ in range(n_dst)]
     shards = [t.data_ptr() for t in job.bufs.params16]
     for step in range(2):

@@ -16,10 +16,31 @@ namespace zg {
 
 namespace {
 
-// Groups of 8 16-bit units (16 bytes) per thread.
-constexpr int kG = 8;
+// The layer is cut into tiles of kTile 16-bit units (16 KB).  A block
+// gathers a tile from the owners' shards into shared memory with ordinary
+// loads (16 bytes per thread where a group of 8 units is aligned and has one
+// owner, else unit by unit), then one thread replicates it into every
+// destination with bulk asynchronous copies shared -> global
+// (cp.async.bulk ... bulk_group), so the n_dst-fold write stream runs on the
+// copy engine of the SM rather than through per-thread stores.  Two tile
+// buffers per block: a buffer is refilled only after the bulk copies that
+// read it two tiles earlier have finished reading it (wait_group.read).
+// Measured on GB300, 64 destinations: 6.70 TB/s with bulk copies against
+// 6.07 with 16-byte stores (8 destinations: 5.94 against 5.88).
+constexpr int kG = 8;                 // units per 16-byte group
+constexpr int kTile = 8192;           // units per tile (16 KB)
+constexpr int kTileGroups = kTile / kG;
 
-__global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ GatherArgs a)
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(gdst), "r"(ssrc), "r"(bytes) : "memory");
+}
+
+// Few destinations: each thread copies its 16-byte group straight to every
+// destination (for one destination this is a copy and measured 5.1 TB/s,
+// against 4.0 through shared memory and a single bulk copy per tile).
+__global__ void __launch_bounds__(kThreads) k_gather_direct(const __grid_constant__ GatherArgs a)
 {
     const int64_t ngroups = (a.len + kG - 1) / kG;
     for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
@@ -28,7 +49,6 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Gat
         const int cnt = (int)min((int64_t)kG, a.len - j0);
         const int64_t i = a.start + j0;
         if (cnt == kG && (i & (kG - 1)) == 0) {
-            // shards are multiples of 8 units: an aligned group has one owner
             const int o = owner_of(i, a.shard);
             const uint4 v = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.shards[o]) +
                                                                   (i - (int64_t)o * a.shard)));
@@ -54,14 +74,84 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Gat
     }
 }
 
+// Destinations from which the tile path with bulk copies is used.
+constexpr int kBulkMinDst = 8;
+
+__global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ GatherArgs a)
+{
+    __shared__ __align__(128) uint4 buf[2][kTileGroups];
+    const int64_t ntiles = (a.len + kTile - 1) / kTile;
+    int b = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, b ^= 1) {
+        // buffer b was last read by the bulk copies committed two tiles ago
+        if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncthreads();
+        const int64_t j_tile = t * kTile;
+        const int64_t units = min((int64_t)kTile, a.len - j_tile);
+        const int groups = (int)((units + kG - 1) / kG);
+        uint16_t* tile16 = reinterpret_cast<uint16_t*>(buf[b]);
+        for (int g = threadIdx.x; g < groups; g += kThreads) {
+            const int64_t j0 = j_tile + (int64_t)g * kG;      // unit index within the layer
+            const int cnt = (int)min((int64_t)kG, a.len - j0);
+            const int64_t i = a.start + j0;                    // flat unit index
+            if (cnt == kG && (i & (kG - 1)) == 0) {
+                // shards are multiples of 8 units: an aligned group has one owner
+                const int o = owner_of(i, a.shard);
+                buf[b][g] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.shards[o]) +
+                                                                   (i - (int64_t)o * a.shard)));
+            } else {
+#pragma unroll
+                for (int j = 0; j < kG; j++) {
+                    uint16_t u = 0;
+                    if (j < cnt) {
+                        const int o = owner_of(i + j, a.shard);
+                        u = static_cast<const uint16_t*>(a.shards[o])[i + j - (int64_t)o * a.shard];
+                    }
+                    tile16[g * kG + j] = u;
+                }
+            }
+        }
+        // make the tile visible to the bulk-copy (async) proxy, then copy it out
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        const uint32_t bulk_bytes = (uint32_t)(units * 2) & ~15u;   // 16-byte multiple
+        if (threadIdx.x == 0) {
+            if (bulk_bytes) {
+                const uint32_t saddr = (uint32_t)__cvta_generic_to_shared(buf[b]);
+                for (int d = 0; d < a.n_dst; d++)
+                    bulk_store(static_cast<uint16_t*>(a.dst[d]) + j_tile, saddr, bulk_bytes);
+            }
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        // the ragged end of the last tile (fewer than 8 units) with plain stores
+        const int rest = (int)(units - bulk_bytes / 2);
+        if (rest > 0) {
+            for (int k = threadIdx.x; k < rest * a.n_dst; k += kThreads) {
+                const int d = k / rest, j = (int)(bulk_bytes / 2) + k % rest;
+                static_cast<uint16_t*>(a.dst[d])[j_tile + j] = tile16[j];
+            }
+        }
+    }
+    // the bulk copies complete before the block exits
+    if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 }  // namespace
 
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s)
 {
-    const int64_t groups = (a.len + kG - 1) / kG;
-    if (groups <= 0) return cudaSuccess;
-    const int grid = grid_for((const void*)k_gather, groups);
-    k_gather<<<grid, kThreads, 0, s>>>(a);
+    if (a.len <= 0) return cudaSuccess;
+    if (a.n_dst < kBulkMinDst) {
+        const int grid = grid_for((const void*)k_gather_direct, (a.len + kG - 1) / kG);
+        k_gather_direct<<<grid, kThreads, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    const int64_t ntiles = (a.len + kTile - 1) / kTile;
+    // two blocks per resident slot: a block's tile loads then overlap another
+    // block's bulk copies (measured 6.5 against 6.1 TB/s with one)
+    const int resident = grid_for((const void*)k_gather, ntiles * kThreads);
+    const int64_t grid = ntiles < 2 * (int64_t)resident ? ntiles : 2 * (int64_t)resident;
+    k_gather<<<(int)grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
