@@ -67,7 +67,8 @@
  *   two-pass  (clipping, or no shadow): pass 1 per bucket reduces and checks
  *             the gradient, materialises it (grads[] in stages 0/1, reduced
  *             in stages 2/3) and accumulates the exact sum of squares; a
- *             one-thread kernel forms the global norm and clip coefficient;
+ *             one-thread kernel forms the global norm and clip coefficient
+ *             (16-bit types only);
  *             pass 2 per bucket updates the state in place, or does nothing
  *             when the flag is set.
  *
