@@ -503,3 +503,23 @@ def test_tiny_partitions_brute_force():
                         job.check(res, ref)
                         count += 1
     assert count == 448
+
+
+# --- pass 2 with the parameters copied out through shared-memory tiles ------
+@pytest.mark.parametrize("stage", [1, 2])
+@pytest.mark.parametrize("N", [8, 16, 33, 64])
+@pytest.mark.parametrize("dtype,optimizer", [(FP16, zg.ZERO_ADAM), (BF16, zg.ZERO_SGD_MOMENTUM),
+                                             (oracle.FP32, zg.ZERO_SGD)])
+def test_two_pass_many_ranks(stage, N, dtype, optimizer):
+    """Stages 1-2 on the two-pass path with many ranks: from 16 ranks the
+    update pass writes every rank's parameters with bulk copies from
+    shared-memory tiles (tiles of 2048 or 1024 elements, buckets with ragged
+    ends, a skipped step in between); 8 ranks keep per-thread stores."""
+    n, B = 3 * 5000 + 3, 5000
+    job = Job(n, N, stage, B, 8, dtype=dtype, shadow=False, optimizer=optimizer,
+              max_norm=1.0 if dtype != oracle.FP32 else 0.0, loss_scale=16.0, dynamic=True)
+    inf = synth.inf_bits(dtype)
+    for t, inject in ((1, ()), (2, ((N - 1, 4999, inf),)), (3, ())):
+        res, ref = job.step(job.make_grads(t, inject))
+        job.check(res, ref)
+        assert res.path == 1 and res.overflow == (1 if inject else 0)

@@ -1,0 +1,13 @@
+// Host-side query: are all of these pointers device memory of the current
+// GPU?  The kernels that copy tiles out with bulk asynchronous copies use
+// them only for destinations in device memory; pinned or other host memory
+// (which the library also accepts) keeps the per-thread store kernels.
+#pragma once
+
+namespace zg {
+
+// Pointer kinds come from cudaPointerGetAttributes; the answer for the last
+// pointer set seen by the calling thread is cached.
+bool device_resident(void* const* ptrs, int n);
+
+}  // namespace zg

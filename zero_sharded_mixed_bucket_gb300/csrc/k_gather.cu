@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "dev_common.cuh"
+#include "host_ptrs.h"
 
 namespace zg {
 
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Gat
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s)
 {
     if (a.len <= 0) return cudaSuccess;
-    if (a.n_dst < kBulkMinDst) {
+    if (a.n_dst < kBulkMinDst || !device_resident(const_cast<void* const*>(a.dst), a.n_dst)) {
         const int grid = grid_for((const void*)k_gather_direct, (a.len + kG - 1) / kG);
         k_gather_direct<<<grid, kThreads, 0, s>>>(a);
         return cudaGetLastError();
@@ -153,6 +154,40 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s)
     const int64_t grid = ntiles < 2 * (int64_t)resident ? ntiles : 2 * (int64_t)resident;
     k_gather<<<(int)grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
+}
+
+bool device_resident(void* const* ptrs, int n)
+{
+    struct Seen {
+        int dev = -1, n = 0;
+        const void* p[kMaxRanks];
+        bool ok = false;
+    };
+    thread_local Seen seen;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (n < 1 || n > kMaxRanks) return false;
+    bool same = seen.dev == dev && seen.n == n;
+    for (int k = 0; same && k < n; k++) same = seen.p[k] == ptrs[k];
+    if (same) return seen.ok;
+    bool ok = true;
+    for (int k = 0; ok && k < n; k++) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, ptrs[k]) != cudaSuccess) {
+            cudaGetLastError();   // not a CUDA pointer: clear the error, answer no
+            ok = false;
+        } else {
+            ok = at.type == cudaMemoryTypeDevice && at.device == dev;
+        }
+    }
+    seen.dev = dev;
+    seen.n = n;
+    for (int k = 0; k < n; k++) seen.p[k] = ptrs[k];
+    seen.ok = ok;
+    return ok;
 }
 
 int grid_for(const void* kernel, int64_t groups)
