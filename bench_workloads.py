@@ -122,12 +122,42 @@ def leg_cfg1(args):
             assert res.overflow == 0
     finally:
         zg.zero_set_profile_events(None, None)
-    ms = sum(walls) / len(walls)
+    ms_sync = sum(walls) / len(walls)
+    # the same step with the step state on the device, replayed from two
+    # captured CUDA graphs (one per state copy): no host round trip per step
+    dev_state = torch.zeros(zg.DEV_STATE_BYTES // 8, dtype=torch.int64, device=dev)
+    zg.zero_dev_state_init(dev_state, adam, state, s)
+    zg.zero_step_async(cfg, plan, bufs, adam, dev_state, s)       # warms the launch-shape cache
+    torch.cuda.synchronize()
+    graphs = []
+    cap = torch.cuda.Stream(dev)
+    for _ in range(2):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            zg.zero_step_async(cfg, plan, bufs, adam, dev_state, torch.cuda.current_stream(dev))
+        graphs.append(g)
+    gwalls = []
+    for k in range(args.warmup + args.steps):
+        flush.fill_(k & 0xff)
+        w0, w1 = _ev(), _ev()
+        w0.record(s)
+        graphs[k % 2].replay()
+        w1.record(s)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            gwalls.append(w0.elapsed_time(w1))
+    st, last = zg.zero_dev_state_read(dev_state, s)
+    assert last.overflow == 0 and st.t == state.t + 1 + args.warmup + args.steps
+    ms_graph = sum(gwalls) / len(gwalls)
+    ms = min(ms_sync, ms_graph)
     out = _base(n / (ms * 1e-3) / 1e9, ms, args.steps, args.warmup,
                 "stage 2, flat 2^20 params, N_d=4, fp16 grads N(0,1e-3) x 1024 static loss scale, one bucket",
                 {"n_params": n, "n_ranks": N, "stage": 2, "l2": "flushed before every step (256 MB write)"})
+    out["modes"] = {"zero_step_stage2": {"ms_per_step": ms_sync, "value": n / (ms_sync * 1e-3) / 1e9},
+                    "graph of zero_step_async": {"ms_per_step": ms_graph, "value": n / (ms_graph * 1e-3) / 1e9}}
+    out["mode"] = "graph of zero_step_async" if ms_graph <= ms_sync else "zero_step_stage2"
     out["roofline"] = _roofline(plan.hbm_bytes_fused, sum(spans) / len(spans), "k_fused<stage 2, fp16>")
-    out["note"] = "42 MB per step: launch latency and the flag read dominate; a parity case, not a bandwidth one"
+    out["note"] = "42 MB per step: launch latency dominates; a parity case, not a bandwidth one"
     return out
 
 

@@ -98,9 +98,11 @@ def test_async_state_round_trip():
     assert last.overflow == 0 and last.grad_norm == -1.0 and last.clip_coef == 1.0
 
 
-@pytest.mark.parametrize("max_norm", [0.0, 1e-3])
-def test_two_captured_graphs_replayed_alternately(max_norm):
-    n, N, B = 6 * 2048 + 17, 8, 2048
+@pytest.mark.parametrize("max_norm,N", [(0.0, 8), (1e-3, 8), (1e-3, 16)])
+def test_two_captured_graphs_replayed_alternately(max_norm, N):
+    """(16 ranks, clipped: the update pass captured is the one that writes
+    the parameters by bulk copies from shared-memory tiles.)"""
+    n, B = 6 * 2048 + 17, 2048
     job = AsyncJob(n, N, 2, B, 8, None, oracle.FP16, loss_scale=1024.0, dynamic=True, growth=3, max_norm=max_norm)
     s = torch.cuda.Stream()
     # one eager step first: it warms the library's launch-shape cache
@@ -115,7 +117,7 @@ def test_two_captured_graphs_replayed_alternately(max_norm):
             job.launch(torch.cuda.current_stream())
         graphs.append(g)
     assert job.bufs.cur == cur0              # two captures flipped it twice (fused) or never (two-pass)
-    inject = {4: (inf_at(job, 3, 5),), 7: (inf_at(job, 7, n - 1),)}
+    inject = {4: (inf_at(job, 3, 5),), 7: (inf_at(job, N - 1, n - 1),)}
     for step in range(2, 12):
         grads = job.make_grads(step, inject.get(step, ()))
         job.load_grads(grads)

@@ -4,10 +4,14 @@
 // (which the library also accepts) keeps the per-thread store kernels.
 #pragma once
 
+#include <cuda_runtime.h>
+
 namespace zg {
 
 // Pointer kinds come from cudaPointerGetAttributes; the answer for the last
-// pointer set seen by the calling thread is cached.
-bool device_resident(void* const* ptrs, int n);
+// pointer set seen by the calling thread is cached.  While `stream` is being
+// captured into a graph no query is made (it could invalidate the capture):
+// the cached answer is used if it is for the same pointers, else no.
+bool device_resident(void* const* ptrs, int n, cudaStream_t stream);
 
 }  // namespace zg

@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Gat
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s)
 {
     if (a.len <= 0) return cudaSuccess;
-    if (a.n_dst < kBulkMinDst || !device_resident(const_cast<void* const*>(a.dst), a.n_dst)) {
+    if (a.n_dst < kBulkMinDst || !device_resident(const_cast<void* const*>(a.dst), a.n_dst, s)) {
         const int grid = grid_for((const void*)k_gather_direct, (a.len + kG - 1) / kG);
         k_gather_direct<<<grid, kThreads, 0, s>>>(a);
         return cudaGetLastError();
@@ -156,7 +156,7 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s)
     return cudaGetLastError();
 }
 
-bool device_resident(void* const* ptrs, int n)
+bool device_resident(void* const* ptrs, int n, cudaStream_t stream)
 {
     struct Seen {
         int dev = -1, n = 0;
@@ -173,6 +173,12 @@ bool device_resident(void* const* ptrs, int n)
     bool same = seen.dev == dev && seen.n == n;
     for (int k = 0; same && k < n; k++) same = seen.p[k] == ptrs[k];
     if (same) return seen.ok;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return false;
     bool ok = true;
     for (int k = 0; ok && k < n; k++) {
         cudaPointerAttributes at;

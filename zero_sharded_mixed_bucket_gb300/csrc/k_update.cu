@@ -167,7 +167,7 @@ cudaError_t run_update(const StepArgs& a, cudaStream_t s, bool overlap)
     const int64_t groups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     if (groups <= 0) return cudaSuccess;
     if constexpr (STAGE == 1 || STAGE == 2) {
-        if (a.n_ranks >= kBulkMinRanks && device_resident(a.params16, a.n_ranks)) {
+        if (a.n_ranks >= kBulkMinRanks && device_resident(a.params16, a.n_ranks, s)) {
             const int64_t tiles = (groups + kThreads * kTileSub - 1) / (kThreads * kTileSub);
             const int grid = grid_for((const void*)k_update_tiled<STAGE, DT, CLIP, OPT>, tiles * kThreads);
             return launch_step_kernel(k_update_tiled<STAGE, DT, CLIP, OPT>, grid, s, overlap, a);
