@@ -395,7 +395,9 @@ zero_status_t zero_step_stage2_noalloc(const zero_config_t* cfg, const zero_plan
 /* Profiling: for the step calls made afterwards on this thread, record
  * start_event (a cudaEvent_t) on the step's stream right after the workspace
  * clear, before the first kernel, and end_event after the step's last kernel,
- * before the overflow flag is read.  The caller creates the events and keeps
+ * before the overflow flag is read (zero_step_async: after its prepare
+ * kernel, and after the last bucket or update kernel, before the restore and
+ * commit).  The caller creates the events and keeps
  * them valid; (NULL, NULL) turns recording off.  Bucket kernels launched
  * back to back inside one call overlap their edges, so the events give the
  * step's kernel span, not per-kernel durations. */
