@@ -360,6 +360,40 @@ def step(grads, w, m, v, *, dtype: int, lr: float, beta1: float, beta2: float, e
 DEFAULT_ALIGN = 2048
 
 
+# ---------------------------------------------------------------------------
+# P_a: partitioned activation checkpoints ([P2] 3.2.1; [P4] "P_a:
+# Partitioned Activation Checkpointing")
+# ---------------------------------------------------------------------------
+def pa_plan(act_elems: int, n_mp: int, value_bytes: int = 2, align_elems: int = 0) -> dict:
+    """Partition of one activation checkpoint of act_elems values across the
+    N_m model-parallel ranks.  Without P_a every rank holds the whole
+    checkpoint (model parallelism replicates a layer's input on every rank);
+    with P_a rank r keeps only the contiguous slice [rP, (r+1)P), P =
+    ceil(act_elems / N_m) rounded up to the alignment, and the slices are
+    all-gathered when backward recomputes the layer; with P_a+cpu the slices
+    live in host memory.  Bytes per rank, and the bytes a rank receives in
+    one all-gather (the other ranks' slices)."""
+    A = align_elems or DEFAULT_ALIGN
+    P = -(-act_elems // n_mp)
+    P = -(-P // A) * A
+    own = [max(0, min(P, act_elems - r * P)) for r in range(n_mp)]
+    return dict(act_elems=act_elems, n_mp=n_mp, shard=P, own=own,
+                mem_per_rank=act_elems * value_bytes,
+                mem_per_rank_pa=P * value_bytes,
+                mem_per_rank_pa_cpu=0,
+                gather_recv_per_rank=[(act_elems - own[r]) * value_bytes for r in range(n_mp)])
+
+
+def pa_partition(replicas, n_mp: int, shard: int):
+    """Rank r keeps the slice [r*shard, (r+1)*shard) of its own replica."""
+    return [np.array(replicas[r][r * shard:(r + 1) * shard]) for r in range(n_mp)]
+
+
+def pa_gather(shards, act_elems: int):
+    """The full checkpoint: the ranks' slices concatenated in rank order."""
+    return np.concatenate(shards)[:act_elems]
+
+
 def plan(n_params: int, n_ranks: int, bucket_elems: int, align_elems: int = 0,
          layer_sizes=None) -> dict:
     """ZeRO-DP partition of a flat parameter vector of n_params elements.
