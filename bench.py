@@ -647,8 +647,9 @@ def main():
                          "e.g. for profiling captures)")
     ap.add_argument("--ring", type=int, default=GRAD_RING, help="distinct per-step gradient sets kept in HBM")
     ap.add_argument("--bucket", type=int, default=BUCKET, help="gradient bucket size in elements")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6],
-                    help="workload: 2 (default) the headline; 1, 3, 4, 5 the others (bench_workloads.py)")
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7],
+                    help="workload: 2 (default) the headline; 1, 3, 4, 5 the others, 6 the optimizer state in host "
+                         "memory, 7 the P_a activation-checkpoint partition and all-gather (bench_workloads.py)")
     ap.add_argument("--ranks", type=int, default=None, help="--config 5: N_d of a single sweep point")
     ap.add_argument("--optimizer", default="adam", choices=sorted(OPTIMIZERS),
                     help="optimizer of the headline step (with --headline-only)")

@@ -447,4 +447,72 @@ def leg_offload(args):
     return out
 
 
-LEGS = {1: leg_cfg1, 3: leg_cfg3, 4: leg_cfg4, 5: leg_cfg5, 6: leg_offload}
+# ---------------------------------------------------------------------------
+def leg_pa(args):
+    """P_a, partitioned activation checkpoints: one layer checkpoint of the
+    1.5B GPT-2 example (batch 32, sequence 1024, hidden 1600; fp16), N_m = 16
+    model-parallel ranks.  Partition (each rank keeps its 1/16 slice) and the
+    all-gather that rebuilds the checkpoint in all 16 ranks' buffers, with
+    the slices in HBM (P_a) and in pinned host memory (P_a+cpu)."""
+    import torch
+
+    import zero_sharded_mixed_bucket_gb300 as zg
+    A, N = 32 * 1024 * 1600, 16
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.current_stream(dev)
+    p = zg.zero_pa_plan(A, N, zg.ZERO_FP16)
+    x = torch.randint(-2 ** 15, 2 ** 15, (A,), dtype=torch.int16, device=dev)
+    replicas = [x.clone() for _ in range(N)]          # model parallelism: the same checkpoint on every rank
+    dst = [torch.empty(A, dtype=torch.int16, device=dev) for _ in range(N)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    steps = max(3, min(args.steps, 20))
+    runs = {}
+    for where in ("hbm", "host"):
+        if where == "hbm":
+            shards = [torch.empty(p.shard_elems, dtype=torch.int16, device=dev) for _ in range(N)]
+        else:
+            shards = [torch.empty(p.shard_elems, dtype=torch.int16).pin_memory() for _ in range(N)]
+        tp, tg = [], []
+        for k in range(args.warmup + steps):
+            flush.fill_(k & 0xff)
+            e0, e1, e2 = _ev(), _ev(), _ev()
+            e0.record(s)
+            zg.zero_pa_partition(p, replicas, shards, s)
+            e1.record(s)
+            flush.fill_((k + 1) & 0xff)
+            e2.record(s)
+            zg.zero_pa_gather(p, shards, dst, s)
+            e3 = _ev()
+            e3.record(s)
+            torch.cuda.synchronize()
+            if k >= args.warmup:
+                tp.append(e0.elapsed_time(e1))
+                tg.append(e2.elapsed_time(e3))
+        assert torch.equal(dst[N - 1], x) and torch.equal(dst[0], x)
+        ms_p, ms_g = sum(tp) / steps, sum(tg) / steps
+        b = 2 * A
+        runs["slices_in_" + where] = {
+            "partition_ms": ms_p, "partition_gbs": 2 * b / (ms_p * 1e-3) / 1e9,
+            "gather_ms": ms_g, "gather_gbs": (1 + N) * b / (ms_g * 1e-3) / 1e9,
+            "note": "partition: each rank reads and writes its slice (2 x 2A bytes in all); gather: the slices "
+                    "read once (2A bytes), the checkpoint written to 16 buffers (16 x 2A)"
+                    + (" -- the slices cross the host link both ways" if where == "host" else "")}
+        del shards
+    hb = runs["slices_in_hbm"]
+    out = _base(A / (hb["gather_ms"] * 1e-3) / 1e9, hb["gather_ms"], steps, args.warmup,
+                "P_a: one activation checkpoint of the 1.5B GPT-2 example (batch 32 x sequence 1024 x hidden 1600, "
+                "fp16), N_m = 16 model-parallel ranks simulated; value = checkpoint values rebuilt per second by the "
+                "all-gather into all 16 ranks",
+                {"act_elems": A, "n_mp": N, "l2": "flushed before each partition and gather (256 MB write)"},
+                dtype="u16")
+    out["unit"] = "Gvalues/s"
+    out["metric"] = "P_a all-gather: checkpoint values rebuilt per second (all 16 ranks)"
+    out["runs"] = runs
+    out["memory_per_rank_bytes"] = {"without_pa": p.mem_per_rank_bytes, "pa": p.mem_per_rank_pa_bytes,
+                                    "pa_cpu_on_gpu": 0}
+    out["gather_bytes_across_ranks"] = p.gather_bytes
+    out["roofline"] = _roofline((1 + N) * 2 * A, hb["gather_ms"], "k_gather (tiles + bulk copies), P_a all-gather")
+    return out
+
+
+LEGS = {1: leg_cfg1, 3: leg_cfg3, 4: leg_cfg4, 5: leg_cfg5, 6: leg_offload, 7: leg_pa}

@@ -392,6 +392,42 @@ zero_status_t zero_step_stage2_noalloc(const zero_config_t* cfg, const zero_plan
                                        const zero_adam_t* adam, zero_state_t* state, void* stream,
                                        zero_step_result_t* out);
 
+/* ---- P_a: partitioned activation checkpoints (ZeRO-R) --------------------
+ * Under model parallelism the input of a layer -- the activation checkpoint
+ * that backward recomputes the layer from -- is replicated on all N_m
+ * model-parallel ranks.  P_a keeps a 1/N_m slice per rank after the forward
+ * pass and rebuilds the checkpoint with an all-gather when backward needs
+ * it; P_a+cpu keeps the slices in host memory ("ZeRO：大模型训练的内存优化
+ * 革命" 3.2.1; SC-2020 ZeRO notes, "P_a: Partitioned Activation
+ * Checkpointing").  The N_m ranks are simulated as buffers, like the
+ * data-parallel ranks.  Slice of rank r: values [r*P, min((r+1)*P, act_elems)),
+ * P = ceil(act_elems / N_m) rounded up to align_elems.  72 bytes. */
+typedef struct zero_pa_plan {
+    int64_t act_elems;              /* values in one checkpoint, >= 0 */
+    int64_t shard_elems;            /* P */
+    int64_t align_elems;            /* 0 -> 2048; a multiple of 8 */
+    int32_t n_mp;                   /* N_m, 1..64 */
+    int32_t dtype;                  /* zero_dtype_t of the activations (2 or 4 bytes) */
+    int64_t mem_per_rank_bytes;     /* without P_a: the whole checkpoint on every rank */
+    int64_t mem_per_rank_pa_bytes;  /* with P_a: one slice (P_a+cpu: none on the GPU) */
+    int64_t gather_bytes;           /* bytes crossing simulated rank boundaries in one all-gather, all ranks */
+    int64_t reserved[2];
+} zero_pa_plan_t;
+
+zero_status_t zero_pa_plan(int64_t act_elems, int32_t n_mp, int32_t dtype, int64_t align_elems,
+                           zero_pa_plan_t* out);
+/* After the forward pass: rank r copies its slice of replicas[r] (the
+ * checkpoint as rank r holds it: act_elems values) to shards[r] (room for
+ * shard_elems values; device or pinned host memory -- P_a+cpu).  Arrays of
+ * n_mp pointers, 16-byte aligned.  One kernel launch, asynchronous. */
+zero_status_t zero_pa_partition(const zero_pa_plan_t* plan, const void* const* replicas, void* const* shards,
+                                void* stream);
+/* Before the layer's recomputation: the all-gather -- the checkpoint rebuilt
+ * from the n_mp slices into each of dst[0..n_dst) (act_elems values each;
+ * n_dst 1..64).  One kernel launch, asynchronous. */
+zero_status_t zero_pa_gather(const zero_pa_plan_t* plan, const void* const* shards, void* const* dst, int32_t n_dst,
+                             void* stream);
+
 /* Profiling: for the step calls made afterwards on this thread, record
  * start_event (a cudaEvent_t) on the step's stream right after the workspace
  * clear, before the first kernel, and end_event after the step's last kernel,

@@ -36,7 +36,7 @@ def test_struct_sizes_match_header():
     text = open(HEADER, encoding="utf-8").read()
     for name, cls in [("zero_config", zg.zero_config_t), ("zero_plan", zg.zero_plan_t), ("zero_adam", zg.zero_adam_t),
                       ("zero_state", zg.zero_state_t), ("zero_buffers", zg.zero_buffers_t),
-                      ("zero_step_result", zg.zero_step_result_t)]:
+                      ("zero_step_result", zg.zero_step_result_t), ("zero_pa_plan", zg.zero_pa_plan_t)]:
         m = re.search(r"(\d+) bytes\. \*/\s*typedef struct %s \{" % name, text)
         assert m, name
         assert ctypes.sizeof(cls) == int(m.group(1)), name
@@ -333,3 +333,34 @@ def test_buffer_allocation_failure_propagates(monkeypatch):
     with pytest.raises(torch.OutOfMemoryError):
         zg.DeviceBuffers(cfg, plan, device="cuda")
     assert len(calls) == 3
+
+
+@pytest.mark.parametrize("A,N,dtype,align", [(0, 1, 0, 0), (1, 1, 0, 0), (7, 3, 1, 8), (32 * 1024 * 1600, 16, 0, 0),
+                                             (100_003, 64, 2, 64), (10, 64, 0, 0)])
+def test_pa_plan_matches_oracle(A, N, dtype, align):
+    p = zg.zero_pa_plan(A, N, dtype, align)
+    b = 4 if dtype == zg.ZERO_FP32 else 2
+    o = oracle.pa_plan(A, N, value_bytes=b, align_elems=align)
+    assert p.shard_elems == o["shard"] and p.n_mp == N and p.act_elems == A
+    assert p.mem_per_rank_bytes == o["mem_per_rank"] and p.mem_per_rank_pa_bytes == o["mem_per_rank_pa"]
+    assert p.gather_bytes == sum(o["gather_recv_per_rank"])
+
+
+def test_pa_argument_checks():
+    for args, status in [((100, 0, 0, 0), zg.ZERO_EUNSUPPORTED), ((100, 65, 0, 0), zg.ZERO_EUNSUPPORTED),
+                         ((100, 4, 3, 0), zg.ZERO_EINVAL), ((100, 4, 0, 12), zg.ZERO_EINVAL),
+                         ((-1, 4, 0, 0), zg.ZERO_EINVAL)]:
+        with pytest.raises(zg.ZeroError) as e:
+            zg.zero_pa_plan(*args)
+        assert e.value.status == status
+    p = zg.zero_pa_plan(10_000, 4)
+    good = [0x10000000 + 0x100000 * r for r in range(4)]
+    L = zg.lib()
+    arr = lambda xs: (ctypes.c_void_p * len(xs))(*xs)
+    assert L.zero_pa_partition(ctypes.byref(p), arr(good), arr(good[:3] + [0x10000008]), None) == zg.ZERO_EALIGN
+    assert L.zero_pa_partition(ctypes.byref(p), arr(good[:3] + [None]), arr(good), None) == zg.ZERO_ENOMEM
+    assert L.zero_pa_gather(ctypes.byref(p), arr(good), arr(good[:1]), 0, None) == zg.ZERO_EUNSUPPORTED
+    assert L.zero_pa_gather(ctypes.byref(p), arr(good), arr([0x10000002]), 1, None) == zg.ZERO_EALIGN
+    forged = zg.zero_pa_plan_t.from_buffer_copy(p)
+    forged.shard_elems += 8
+    assert L.zero_pa_gather(ctypes.byref(forged), arr(good), arr(good[:1]), 1, None) == zg.ZERO_EINVAL

@@ -25,7 +25,7 @@ __all__ = [
     "zero_plan", "zero_plan_bucket", "zero_plan_layer", "zero_model_state_bytes", "zero_comm_bytes",
     "zero_step", "zero_step_stage0", "zero_step_stage1", "zero_step_stage2", "zero_step_stage3",
     "zero_step_stage2_noalloc", "zero_dev_state_init", "zero_step_async", "zero_dev_state_read",
-    "DEV_STATE_BYTES",
+    "DEV_STATE_BYTES", "zero_pa_plan_t", "zero_pa_plan", "zero_pa_partition", "zero_pa_gather",
     "zero_step_begin", "zero_step_bucket", "zero_step_end", "zero_gather_layer", "zero_last_error",
     "zero_version", "zero_set_profile_events", "zero_fetch_schedule", "Fetcher", "DeviceBuffers",
 ]
@@ -74,6 +74,12 @@ class zero_step_result_t(ctypes.Structure):
                 ("new_loss_scale", c_f), ("kernel_launches", c_i32), ("path", c_i32), ("reserved", c_i32)]
 
 
+class zero_pa_plan_t(ctypes.Structure):
+    _fields_ = [("act_elems", c_i64), ("shard_elems", c_i64), ("align_elems", c_i64), ("n_mp", c_i32),
+                ("dtype", c_i32), ("mem_per_rank_bytes", c_i64), ("mem_per_rank_pa_bytes", c_i64),
+                ("gather_bytes", c_i64), ("reserved", c_i64 * 2)]
+
+
 class ZeroError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__("zero status %d: %s" % (status, message))
@@ -113,6 +119,9 @@ def lib():
             "zero_dev_state_init": [c_vp, adam, state, c_vp],
             "zero_step_async": [cfg, plan, bufs, adam, c_vp, c_vp, P(c_i32)],
             "zero_dev_state_read": [c_vp, state, res, c_vp],
+            "zero_pa_plan": [c_i64, c_i32, c_i32, c_i64, P(zero_pa_plan_t)],
+            "zero_pa_partition": [P(zero_pa_plan_t), P(c_vp), P(c_vp), c_vp],
+            "zero_pa_gather": [P(zero_pa_plan_t), P(c_vp), P(c_vp), c_i32, c_vp],
             "zero_step_begin": [cfg, plan, bufs, adam, state, c_vp],
             "zero_step_bucket": [cfg, plan, bufs, adam, state, c_i64, P(c_vp), c_vp],
             "zero_step_end": [cfg, plan, bufs, adam, state, c_vp, res],
@@ -284,6 +293,25 @@ def zero_dev_state_read(dev_state, stream=None):
     st, res = zero_state_t(), zero_step_result_t()
     _check(lib().zero_dev_state_read(_dptr(dev_state), ctypes.byref(st), ctypes.byref(res), _stream(stream)))
     return st, res
+
+
+def zero_pa_plan(act_elems: int, n_mp: int, dtype: int = ZERO_FP16, align_elems: int = 0) -> zero_pa_plan_t:
+    """Partition of one activation checkpoint across N_m model-parallel ranks (P_a)."""
+    p = zero_pa_plan_t()
+    _check(lib().zero_pa_plan(act_elems, n_mp, dtype, align_elems, ctypes.byref(p)))
+    return p
+
+
+def zero_pa_partition(plan: zero_pa_plan_t, replicas, shards, stream=None):
+    """Rank r keeps its slice of replicas[r] in shards[r] (pointers or tensors)."""
+    _check(lib().zero_pa_partition(ctypes.byref(plan), _ptr_array([_dptr(x) for x in replicas]),
+                                   _ptr_array([_dptr(x) for x in shards]), _stream(stream)))
+
+
+def zero_pa_gather(plan: zero_pa_plan_t, shards, dst, stream=None):
+    """All-gather: the checkpoint rebuilt from the slices into every dst."""
+    _check(lib().zero_pa_gather(ctypes.byref(plan), _ptr_array([_dptr(x) for x in shards]),
+                                _ptr_array([_dptr(x) for x in dst]), len(dst), _stream(stream)))
 
 
 def zero_step_begin(cfg, plan, bufs, adam, state, stream=None):
