@@ -433,7 +433,8 @@ zero_status_t zero_pa_gather(const zero_pa_plan_t* plan, const void* const* shar
  * clear, before the first kernel, and end_event after the step's last kernel,
  * before the overflow flag is read (zero_step_async: after its prepare
  * kernel, and after the last bucket or update kernel, before the restore and
- * commit).  The caller creates the events and keeps
+ * commit; those two kernel edges then do not overlap).  The caller creates
+ * the events and keeps
  * them valid; (NULL, NULL) turns recording off.  Bucket kernels launched
  * back to back inside one call overlap their edges, so the events give the
  * step's kernel span, not per-kernel durations. */

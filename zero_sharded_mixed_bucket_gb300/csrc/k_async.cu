@@ -28,6 +28,8 @@ namespace {
 
 __global__ void k_prepare(const PrepArgs a)
 {
+    allow_next_grid();   // the first bucket kernel may launch; it waits for this one
+    wait_prev_grid();    // launched early: the previous step's commit must be complete
     // clear the step's flag and sums (the workspace head) ...
     static_assert(ws::kEnd % 16 == 0, "workspace head is cleared in 16-byte words");
     uint4* head = reinterpret_cast<uint4*>(a.ws);
@@ -85,6 +87,8 @@ __device__ void commit(const CommitArgs& a)
 
 __global__ void k_commit(const CommitArgs a)
 {
+    allow_next_grid();
+    wait_prev_grid();
     if (threadIdx.x == 0) commit(a);
 }
 
@@ -94,6 +98,8 @@ template <int STAGE, int DT, int OPT>
 __global__ void __launch_bounds__(kThreads) k_restore_async(const __grid_constant__ StepArgs a,
                                                              const CommitArgs c)
 {
+    allow_next_grid();
+    wait_prev_grid();    // launched early: every bucket kernel of the step must be complete
     if (blockIdx.x == 0 && threadIdx.x == 0) commit(c);
     if (!*reinterpret_cast<const volatile uint32_t*>(ws_flag(a.ws))) return;   // clean step: nothing to do
     const int64_t ngroups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
@@ -135,54 +141,52 @@ __global__ void __launch_bounds__(kThreads) k_restore_async(const __grid_constan
 }
 
 template <int STAGE, int DT, int OPT>
-cudaError_t run_restore_async(const StepArgs& a, const CommitArgs& c, cudaStream_t s)
+cudaError_t run_restore_async(const StepArgs& a, const CommitArgs& c, cudaStream_t s, bool overlap)
 {
     const int64_t groups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     const int grid = groups > 0 ? grid_for((const void*)k_restore_async<STAGE, DT, OPT>, groups) : 1;
-    k_restore_async<STAGE, DT, OPT><<<grid, kThreads, 0, s>>>(a, c);
-    return cudaGetLastError();
+    return launch_kernel(k_restore_async<STAGE, DT, OPT>, grid, kThreads, s, overlap, a, c);
 }
 
 template <int STAGE, int DT>
-cudaError_t restore_opt(int opt, const StepArgs& a, const CommitArgs& c, cudaStream_t s)
+cudaError_t restore_opt(int opt, const StepArgs& a, const CommitArgs& c, cudaStream_t s, bool overlap)
 {
     switch (opt) {
-    case kSgdm: return run_restore_async<STAGE, DT, kSgdm>(a, c, s);
-    case kSgd: return run_restore_async<STAGE, DT, kSgd>(a, c, s);
-    default: return run_restore_async<STAGE, DT, kAdam>(a, c, s);
+    case kSgdm: return run_restore_async<STAGE, DT, kSgdm>(a, c, s, overlap);
+    case kSgd: return run_restore_async<STAGE, DT, kSgd>(a, c, s, overlap);
+    default: return run_restore_async<STAGE, DT, kAdam>(a, c, s, overlap);
     }
 }
 
 template <int DT>
-cudaError_t restore_stage(int stage, int opt, const StepArgs& a, const CommitArgs& c, cudaStream_t s)
+cudaError_t restore_stage(int stage, int opt, const StepArgs& a, const CommitArgs& c, cudaStream_t s, bool overlap)
 {
     switch (stage) {
-    case 0: return restore_opt<0, DT>(opt, a, c, s);
-    case 1: return restore_opt<1, DT>(opt, a, c, s);
-    case 2: return restore_opt<2, DT>(opt, a, c, s);
-    default: return restore_opt<3, DT>(opt, a, c, s);
+    case 0: return restore_opt<0, DT>(opt, a, c, s, overlap);
+    case 1: return restore_opt<1, DT>(opt, a, c, s, overlap);
+    case 2: return restore_opt<2, DT>(opt, a, c, s, overlap);
+    default: return restore_opt<3, DT>(opt, a, c, s, overlap);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s)
+cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s, bool overlap)
 {
-    k_prepare<<<1, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(k_prepare, 1, kThreads, s, overlap, a);
 }
 
-cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s)
+cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s, bool overlap)
 {
-    k_commit<<<1, 32, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(k_commit, 1, 32, s, overlap, a);
 }
 
 cudaError_t launch_restore_async(int stage, int dtype, int opt, const StepArgs& a, const CommitArgs& c,
-                                 cudaStream_t s)
+                                 cudaStream_t s, bool overlap)
 {
-    if (dtype == kF32) return restore_stage<kF32>(stage, opt, a, c, s);
-    return dtype == kBF16 ? restore_stage<kBF16>(stage, opt, a, c, s) : restore_stage<kF16>(stage, opt, a, c, s);
+    if (dtype == kF32) return restore_stage<kF32>(stage, opt, a, c, s, overlap);
+    return dtype == kBF16 ? restore_stage<kBF16>(stage, opt, a, c, s, overlap)
+                          : restore_stage<kF16>(stage, opt, a, c, s, overlap);
 }
 
 }  // namespace zg

@@ -24,6 +24,11 @@ namespace {
 template <int STAGE, int DT, int OPT>
 __global__ void __launch_bounds__(kThreads, STAGE == 0 ? 5 : 1) k_fused(const __grid_constant__ StepArgs a)
 {
+    // The first bucket kernel of a device-state step is launched early after
+    // the prepare kernel: it waits for it before anything else, and lets the
+    // next bucket kernel launch only then (that one reads the step scalars
+    // without waiting).
+    if (a.wait_first) wait_prev_grid();
     allow_next_grid();
     // Step scalars: from the launch, or from the prepare kernel in a
     // device-state step.

@@ -17,6 +17,7 @@ namespace {
 template <int HDEST, int DT, bool CLIP>
 __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ StepArgs a)
 {
+    if (a.wait_first) wait_prev_grid();   // first bucket of a device-state step (see k_fused)
     allow_next_grid();
     const int win_lo = a.dyn ? a.dyn->win_lo : a.win_lo;
     const int64_t ngroups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;

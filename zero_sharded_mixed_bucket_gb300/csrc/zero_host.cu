@@ -691,8 +691,14 @@ zero_status_t zero_step_async(const zero_config_t* c, const zero_plan_t* p, zero
     Dyn* dyn = reinterpret_cast<Dyn*>(ws_ptr + ws::kDyn);
     DevState* dst = static_cast<DevState*>(dev_state);
     int launches = 0;
+    // Every kernel of the step is a programmatic dependent of the one before
+    // it: prepare, restore/commit and the first bucket kernel wait for their
+    // predecessor at their start, the other bucket kernels at their end.  The
+    // profiling events, when set, sit between the prepare kernel and the
+    // first bucket kernel and after the last bucket or update kernel, so they
+    // time the bucket kernels alone (those two edges then do not overlap).
     PrepArgs pa{dst, dyn, ws_ptr, adam->beta1, adam->beta2, c->n_ranks, c->dtype};
-    cudaError_t e = launch_prepare(pa, cs);   // also clears the workspace head
+    cudaError_t e = launch_prepare(pa, cs, true);   // also clears the workspace head
     if (e != cudaSuccess) return cuda_fail(e, "launching the prepare kernel");
     launches++;
     if (g_prof_start && (e = cudaEventRecord(g_prof_start, cs)) != cudaSuccess)
@@ -701,10 +707,11 @@ zero_status_t zero_step_async(const zero_config_t* c, const zero_plan_t* p, zero
         NvtxRange bucket_range("zero_bucket", bk);
         StepArgs a = make_args(c, p, b, adam, &host_view, path.fused, b->grads, 0);
         a.dyn = dyn;
+        a.wait_first = bk == 0 ? 1 : 0;
         a.lo = bk * c->bucket_elems;
         a.hi = a.lo + c->bucket_elems < c->n_params ? a.lo + c->bucket_elems : c->n_params;
-        e = path.fused ? launch_fused(c->stage, c->dtype, c->optimizer, a, cs, bk > 0)
-                       : launch_reduce(c->stage, c->dtype, path.clip, a, cs, bk > 0);
+        e = path.fused ? launch_fused(c->stage, c->dtype, c->optimizer, a, cs, true)
+                       : launch_reduce(c->stage, c->dtype, path.clip, a, cs, true);
         if (e != cudaSuccess) return cuda_fail(e, "launching a bucket kernel");
         launches++;
     }
@@ -731,7 +738,6 @@ zero_status_t zero_step_async(const zero_config_t* c, const zero_plan_t* p, zero
             launches++;
         }
     }
-    // the profiling span covers the bucket (and update) kernels, as in zero_step
     if (g_prof_end && (e = cudaEventRecord(g_prof_end, cs)) != cudaSuccess)
         return cuda_fail(e, "recording the profiling end event");
     CommitArgs ca{dst, dyn, ws_ptr, path.clip ? 1 : 0};
@@ -740,10 +746,10 @@ zero_status_t zero_step_async(const zero_config_t* c, const zero_plan_t* p, zero
         a.dyn = dyn;
         a.lo = 0;
         a.hi = c->n_params;
-        e = launch_restore_async(c->stage, c->dtype, c->optimizer, a, ca, cs);
+        e = launch_restore_async(c->stage, c->dtype, c->optimizer, a, ca, cs, true);
         if (e != cudaSuccess) return cuda_fail(e, "launching the restore and commit kernel");
     } else {
-        e = launch_commit(ca, cs);
+        e = launch_commit(ca, cs, true);
         if (e != cudaSuccess) return cuda_fail(e, "launching the commit kernel");
     }
     launches++;

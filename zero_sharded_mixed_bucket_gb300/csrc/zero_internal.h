@@ -62,6 +62,7 @@ struct StepArgs {
     AdamHP hp;
     int32_t win_lo;                 // lowest exponent E of the sum-of-squares window
     const Dyn* dyn;                 // device-state step: scalars above come from here (else NULL)
+    int32_t wait_first;             // launched early after the prepare kernel: wait for it before anything else
 };
 
 struct FinalArgs {
@@ -124,10 +125,12 @@ struct CommitArgs {
     const unsigned char* ws;
     int32_t clip;                   // the step clips (norm and coefficient valid)
 };
-cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s);
-cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);
+// All three may be launched as programmatic dependents of the kernel before
+// them (`overlap`): each waits for it to complete before touching memory.
+cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s, bool overlap);
+cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s, bool overlap);
 cudaError_t launch_restore_async(int stage, int dtype, int opt, const StepArgs& a, const CommitArgs& c,
-                                 cudaStream_t s);
+                                 cudaStream_t s, bool overlap);
 
 // Record the thread-local message that zero_last_error() returns; gives back
 // `st`.  For entry points defined outside zero_host.cu.
@@ -135,12 +138,12 @@ zero_status_t set_error(zero_status_t st, const char* msg);
 
 // Launch a bucket kernel taking StepArgs, optionally as a programmatic
 // dependent of the previous kernel in the stream.
-template <typename K>
-inline cudaError_t launch_step_kernel(K kernel, int grid, cudaStream_t s, bool overlap, const StepArgs& a)
+template <typename K, typename... Args>
+inline cudaError_t launch_kernel(K kernel, int grid, int threads, cudaStream_t s, bool overlap, const Args&... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3((unsigned)threads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -148,7 +151,13 @@ inline cudaError_t launch_step_kernel(K kernel, int grid, cudaStream_t s, bool o
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = overlap ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kernel, a);
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <typename K>
+inline cudaError_t launch_step_kernel(K kernel, int grid, cudaStream_t s, bool overlap, const StepArgs& a)
+{
+    return launch_kernel(kernel, grid, kThreads, s, overlap, a);
 }
 
 // Grid for a grid-stride kernel over `groups` work items of kThreads-thread
