@@ -8,10 +8,11 @@
 
 namespace zg {
 
-// Pointer kinds come from cudaPointerGetAttributes; the answer for the last
-// pointer set seen by the calling thread is cached.  While `stream` is being
-// captured into a graph no query is made (it could invalidate the capture):
-// the cached answer is used if it is for the same pointers, else no.
+// Pointer kinds come from cudaPointerGetAttributes and are remembered per
+// thread and pointer value (a pointer is taken to keep its kind while the
+// caller's buffers live).  While `stream` is being captured into a graph no
+// query is made (it could invalidate the capture): remembered answers are
+// used, an unknown pointer counts as not device memory.
 bool device_resident(void* const* ptrs, int n, cudaStream_t stream);
 
 }  // namespace zg

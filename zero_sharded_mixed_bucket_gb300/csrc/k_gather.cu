@@ -158,42 +158,60 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s)
 
 bool device_resident(void* const* ptrs, int n, cudaStream_t stream)
 {
-    struct Seen {
-        int dev = -1, n = 0;
-        const void* p[kMaxRanks];
-        bool ok = false;
+    // A per-thread table of pointers already asked about (open addressing;
+    // cleared when it fills up).
+    constexpr int kSlots = 1024;
+    struct Entry {
+        const void* p;
+        int dev;
+        bool device;
     };
-    thread_local Seen seen;
+    thread_local Entry table[kSlots];
+    thread_local int used = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
-    if (n < 1 || n > kMaxRanks) return false;
-    bool same = seen.dev == dev && seen.n == n;
-    for (int k = 0; same && k < n; k++) same = seen.p[k] == ptrs[k];
-    if (same) return seen.ok;
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    if (cs != cudaStreamCaptureStatusNone) return false;
-    bool ok = true;
-    for (int k = 0; ok && k < n; k++) {
-        cudaPointerAttributes at;
-        if (cudaPointerGetAttributes(&at, ptrs[k]) != cudaSuccess) {
-            cudaGetLastError();   // not a CUDA pointer: clear the error, answer no
-            ok = false;
-        } else {
-            ok = at.type == cudaMemoryTypeDevice && at.device == dev;
+    if (n < 1) return false;
+    bool capturing = false;
+    for (int k = 0; k < n; k++) {
+        const void* p = ptrs[k];
+        if (!p) return false;
+        uint64_t h = reinterpret_cast<uintptr_t>(p) * 0x9E3779B97F4A7C15ull;
+        int slot = (int)(h >> 54);   // 10 bits
+        while (table[slot].p && !(table[slot].p == p && table[slot].dev == dev)) slot = (slot + 1) & (kSlots - 1);
+        if (table[slot].p) {
+            if (!table[slot].device) return false;
+            continue;
         }
+        // not seen yet: ask, unless the stream is being captured (a query could
+        // invalidate the capture)
+        if (!capturing) {
+            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+            if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+                cudaGetLastError();
+                return false;
+            }
+            capturing = cs != cudaStreamCaptureStatusNone;
+        }
+        if (capturing) return false;
+        cudaPointerAttributes at;
+        bool device = false;
+        if (cudaPointerGetAttributes(&at, p) != cudaSuccess)
+            cudaGetLastError();   // not a CUDA pointer: clear the error, answer no
+        else
+            device = at.type == cudaMemoryTypeDevice && at.device == dev;
+        if (used >= kSlots / 2) {   // keep the table sparse
+            for (int j = 0; j < kSlots; j++) table[j].p = nullptr;
+            used = 0;
+            slot = (int)(h >> 54);
+        }
+        table[slot] = Entry{p, dev, device};
+        used++;
+        if (!device) return false;
     }
-    seen.dev = dev;
-    seen.n = n;
-    for (int k = 0; k < n; k++) seen.p[k] = ptrs[k];
-    seen.ok = ok;
-    return ok;
+    return true;
 }
 
 int grid_for(const void* kernel, int64_t groups)
