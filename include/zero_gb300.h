@@ -326,6 +326,20 @@ zero_status_t zero_dev_state_init(void* dev_state, const zero_adam_t* adam, cons
  * (may be NULL) receives the kernels it launched. */
 zero_status_t zero_step_async(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
                               const zero_adam_t* adam, void* dev_state, void* stream, int32_t* kernel_launches);
+/* The same step one bucket at a time (for buckets that become ready during
+ * the backward pass), with the step state on the device: begin (the prepare
+ * kernel), then zero_step_bucket_async for every bucket in any order --
+ * bucket_grads as for zero_step_bucket (stages 2/3 only) -- then end (the
+ * two-pass path's finalize and update kernels, and the commit; on the fused
+ * path bufs->cur flips).  None of them synchronises; the sequence can be
+ * captured in a graph. */
+zero_status_t zero_step_begin_async(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                                    const zero_adam_t* adam, void* dev_state, void* stream);
+zero_status_t zero_step_bucket_async(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                                     const zero_adam_t* adam, int64_t bucket, void* const* bucket_grads,
+                                     void* stream);
+zero_status_t zero_step_end_async(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                                  const zero_adam_t* adam, void* dev_state, void* stream, int32_t* kernel_launches);
 /* Copy the block to the host (synchronises `stream`): the current step state
  * and the last step's outcome (t, overflow, skipped, grad_norm, clip_coef,
  * new_loss_scale; path -1). */

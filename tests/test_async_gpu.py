@@ -128,3 +128,66 @@ def test_two_captured_graphs_replayed_alternately(max_norm, N):
             job.bufs.b.cur = 1 - job.bufs.b.cur   # what the call does on the host, replayed by hand
         job.check(res, ref)
         assert res.overflow == (1 if step in inject else 0)
+
+
+# --- the same step one bucket at a time -----------------------------------------
+@pytest.mark.parametrize("stage,shadow,max_norm,staged", [(2, True, 0.0, False), (2, True, 0.0, True),
+                                                          (2, False, 1e-3, True), (3, True, 0.0, True),
+                                                          (3, False, 0.0, False), (1, True, 0.0, False)])
+def test_per_bucket_async_matches_oracle(stage, shadow, max_norm, staged):
+    """begin_async, the buckets in backward (reverse) order -- from per-rank
+    staging buffers that are refilled for every bucket when `staged` --, then
+    end_async: the oracle's step, bit for bit, through an overflowed step."""
+    n, N, B = 4 * 1024 + 37, 4, 1024
+    job = AsyncJob(n, N, stage, B, 8, None, oracle.FP16, shadow=shadow, loss_scale=64.0, dynamic=True,
+                   max_norm=max_norm)
+    s = torch.cuda.current_stream()
+    staging = [torch.zeros(B, dtype=torch.int16, device="cuda") for _ in range(N)]
+    for step, inject in ((1, ()), (2, ((2, 3 * B + 5, synth.inf_bits(oracle.FP16)),)), (3, ())):
+        grads = job.make_grads(step, inject)
+        job.load_grads(grads)
+        zg.zero_step_begin_async(job.cfg, job.plan, job.bufs, job.adam, job.dev, s)
+        for b in reversed(range(job.plan.n_buckets)):
+            if staged:
+                lo, hi = b * B, min((b + 1) * B, n)
+                for r in range(N):
+                    staging[r][:hi - lo].copy_(torch.from_numpy(grads[r][lo:hi].view(np.int16)))
+            zg.zero_step_bucket_async(job.cfg, job.plan, job.bufs, job.adam, b,
+                                      [t.data_ptr() for t in staging] if staged else None, s)
+        zg.zero_step_end_async(job.cfg, job.plan, job.bufs, job.adam, job.dev, s)
+        res, ref = job.read(), job.oracle_step(grads)
+        job.check(res, ref)
+        assert res.overflow == (1 if inject else 0)
+
+
+def test_per_bucket_async_captured_in_graphs():
+    n, N, B = 3 * 2048 + 11, 4, 2048
+    job = AsyncJob(n, N, 2, B, 8, None, oracle.FP16, loss_scale=32.0, dynamic=True)
+    cap = torch.cuda.Stream()
+
+    def sequence(stream):
+        zg.zero_step_begin_async(job.cfg, job.plan, job.bufs, job.adam, job.dev, stream)
+        for b in reversed(range(job.plan.n_buckets)):
+            zg.zero_step_bucket_async(job.cfg, job.plan, job.bufs, job.adam, b, None, stream)
+        zg.zero_step_end_async(job.cfg, job.plan, job.bufs, job.adam, job.dev, stream)
+
+    grads = job.make_grads(1)
+    job.load_grads(grads)
+    sequence(torch.cuda.current_stream())
+    res, ref = job.read(), job.oracle_step(grads)
+    job.check(res, ref)
+    torch.cuda.synchronize()
+    graphs = []
+    for _ in range(2):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            sequence(torch.cuda.current_stream())
+        graphs.append(g)
+    for step in range(2, 7):
+        grads = job.make_grads(step, ((1, 17, synth.inf_bits(oracle.FP16)),) if step == 4 else ())
+        job.load_grads(grads)
+        graphs[step % 2].replay()
+        torch.cuda.synchronize()
+        res, ref = job.read(), job.oracle_step(grads)
+        job.bufs.b.cur = 1 - job.bufs.b.cur
+        job.check(res, ref)

@@ -25,7 +25,8 @@ __all__ = [
     "zero_plan", "zero_plan_bucket", "zero_plan_layer", "zero_model_state_bytes", "zero_comm_bytes",
     "zero_step", "zero_step_stage0", "zero_step_stage1", "zero_step_stage2", "zero_step_stage3",
     "zero_step_stage2_noalloc", "zero_dev_state_init", "zero_step_async", "zero_dev_state_read",
-    "DEV_STATE_BYTES", "zero_pa_plan_t", "zero_pa_plan", "zero_pa_partition", "zero_pa_gather",
+    "DEV_STATE_BYTES", "zero_step_begin_async", "zero_step_bucket_async", "zero_step_end_async",
+    "zero_pa_plan_t", "zero_pa_plan", "zero_pa_partition", "zero_pa_gather",
     "zero_step_begin", "zero_step_bucket", "zero_step_end", "zero_gather_layer", "zero_last_error",
     "zero_version", "zero_set_profile_events", "zero_fetch_schedule", "Fetcher", "DeviceBuffers",
 ]
@@ -119,6 +120,9 @@ def lib():
             "zero_dev_state_init": [c_vp, adam, state, c_vp],
             "zero_step_async": [cfg, plan, bufs, adam, c_vp, c_vp, P(c_i32)],
             "zero_dev_state_read": [c_vp, state, res, c_vp],
+            "zero_step_begin_async": [cfg, plan, bufs, adam, c_vp, c_vp],
+            "zero_step_bucket_async": [cfg, plan, bufs, adam, c_i64, P(c_vp), c_vp],
+            "zero_step_end_async": [cfg, plan, bufs, adam, c_vp, c_vp, P(c_i32)],
             "zero_pa_plan": [c_i64, c_i32, c_i32, c_i64, P(zero_pa_plan_t)],
             "zero_pa_partition": [P(zero_pa_plan_t), P(c_vp), P(c_vp), c_vp],
             "zero_pa_gather": [P(zero_pa_plan_t), P(c_vp), P(c_vp), c_i32, c_vp],
@@ -285,6 +289,26 @@ def zero_step_async(cfg, plan, bufs, adam, dev_state, stream=None) -> int:
     n = c_i32(0)
     _check(lib().zero_step_async(_cfg(cfg), ctypes.byref(plan), ctypes.byref(b), ctypes.byref(adam),
                                  _dptr(dev_state), _stream(stream), ctypes.byref(n)))
+    return n.value
+
+
+def zero_step_begin_async(cfg, plan, bufs, adam, dev_state, stream=None):
+    b = bufs.b if isinstance(bufs, DeviceBuffers) else bufs
+    _check(lib().zero_step_begin_async(_cfg(cfg), ctypes.byref(plan), ctypes.byref(b), ctypes.byref(adam),
+                                       _dptr(dev_state), _stream(stream)))
+
+
+def zero_step_bucket_async(cfg, plan, bufs, adam, bucket: int, bucket_grads=None, stream=None):
+    b = bufs.b if isinstance(bufs, DeviceBuffers) else bufs
+    _check(lib().zero_step_bucket_async(_cfg(cfg), ctypes.byref(plan), ctypes.byref(b), ctypes.byref(adam), bucket,
+                                        _ptr_array(bucket_grads), _stream(stream)))
+
+
+def zero_step_end_async(cfg, plan, bufs, adam, dev_state, stream=None) -> int:
+    b = bufs.b if isinstance(bufs, DeviceBuffers) else bufs
+    n = c_i32(0)
+    _check(lib().zero_step_end_async(_cfg(cfg), ctypes.byref(plan), ctypes.byref(b), ctypes.byref(adam),
+                                     _dptr(dev_state), _stream(stream), ctypes.byref(n)))
     return n.value
 
 

@@ -459,6 +459,59 @@ zero_status_t set_error(zero_status_t st, const char* msg)
     return st;
 }
 
+// The end of a device-state step after its bucket kernels: the two-pass
+// path's norm finalize and update kernels, then the commit (on the fused
+// path inside the restore kernel, which also undoes an overflowed step).
+// The profiling end event, when set, goes right after the bucket or update
+// kernels.
+zero_status_t async_tail(const zero_config_t* c, const zero_plan_t* p, zero_buffers_t* b, const zero_adam_t* adam,
+                         const zero_state_t* host_view_p, DevState* dst, Dyn* dyn, unsigned char* ws_ptr,
+                         const Path& path, cudaStream_t cs, int* launches_p)
+{
+    const zero_state_t& host_view = *host_view_p;
+    int& launches = *launches_p;
+    cudaError_t e;
+    if (!path.fused) {
+        if (path.clip) {
+            FinalArgs f;
+            f.ws = ws_ptr;
+            f.dtype = c->dtype;
+            f.win_lo = 0;
+            f.inv = 0.0;
+            f.max_norm = (double)adam->max_grad_norm;
+            f.dyn = dyn;
+            e = launch_finalize(f, cs);
+            if (e != cudaSuccess) return cuda_fail(e, "launching the norm finalize kernel");
+            launches++;
+        }
+        for (int64_t bk = 0; bk < p->n_buckets; bk++) {
+            StepArgs a = make_args(c, p, b, adam, &host_view, false, c->stage <= 1 ? b->grads : nullptr, 0);
+            a.dyn = dyn;
+            a.lo = bk * c->bucket_elems;
+            a.hi = a.lo + c->bucket_elems < c->n_params ? a.lo + c->bucket_elems : c->n_params;
+            e = launch_update(c->stage, c->dtype, c->optimizer, path.clip, a, cs, bk > 0);
+            if (e != cudaSuccess) return cuda_fail(e, "launching an update kernel");
+            launches++;
+        }
+    }
+    if (g_prof_end && (e = cudaEventRecord(g_prof_end, cs)) != cudaSuccess)
+        return cuda_fail(e, "recording the profiling end event");
+    CommitArgs ca{dst, dyn, ws_ptr, path.clip ? 1 : 0};
+    if (path.fused) {   // restore on overflow, and the commit, in one kernel
+        StepArgs a = make_args(c, p, b, adam, &host_view, true, nullptr, 0);
+        a.dyn = dyn;
+        a.lo = 0;
+        a.hi = c->n_params;
+        e = launch_restore_async(c->stage, c->dtype, c->optimizer, a, ca, cs, true);
+        if (e != cudaSuccess) return cuda_fail(e, "launching the restore and commit kernel");
+    } else {
+        e = launch_commit(ca, cs, true);
+        if (e != cudaSuccess) return cuda_fail(e, "launching the commit kernel");
+    }
+    launches++;
+    return ZERO_OK;
+}
+
 }  // namespace zg
 
 using namespace zg;
@@ -715,44 +768,89 @@ zero_status_t zero_step_async(const zero_config_t* c, const zero_plan_t* p, zero
         if (e != cudaSuccess) return cuda_fail(e, "launching a bucket kernel");
         launches++;
     }
-    if (!path.fused) {
-        if (path.clip) {
-            FinalArgs f;
-            f.ws = ws_ptr;
-            f.dtype = c->dtype;
-            f.win_lo = 0;
-            f.inv = 0.0;
-            f.max_norm = (double)adam->max_grad_norm;
-            f.dyn = dyn;
-            e = launch_finalize(f, cs);
-            if (e != cudaSuccess) return cuda_fail(e, "launching the norm finalize kernel");
-            launches++;
-        }
-        for (int64_t bk = 0; bk < p->n_buckets; bk++) {
-            StepArgs a = make_args(c, p, b, adam, &host_view, false, c->stage <= 1 ? b->grads : nullptr, 0);
-            a.dyn = dyn;
-            a.lo = bk * c->bucket_elems;
-            a.hi = a.lo + c->bucket_elems < c->n_params ? a.lo + c->bucket_elems : c->n_params;
-            e = launch_update(c->stage, c->dtype, c->optimizer, path.clip, a, cs, bk > 0);
-            if (e != cudaSuccess) return cuda_fail(e, "launching an update kernel");
-            launches++;
-        }
-    }
-    if (g_prof_end && (e = cudaEventRecord(g_prof_end, cs)) != cudaSuccess)
-        return cuda_fail(e, "recording the profiling end event");
-    CommitArgs ca{dst, dyn, ws_ptr, path.clip ? 1 : 0};
-    if (path.fused) {   // restore on overflow, and the commit, in one kernel
-        StepArgs a = make_args(c, p, b, adam, &host_view, true, nullptr, 0);
-        a.dyn = dyn;
-        a.lo = 0;
-        a.hi = c->n_params;
-        e = launch_restore_async(c->stage, c->dtype, c->optimizer, a, ca, cs, true);
-        if (e != cudaSuccess) return cuda_fail(e, "launching the restore and commit kernel");
+    zero_status_t tst = async_tail(c, p, b, adam, &host_view, dst, dyn, ws_ptr, path, cs, &launches);
+    if (tst != ZERO_OK) return tst;
+    if (path.fused) b->cur = 1 - b->cur;   // alternate on every call: an overflow copies the state across
+    if (kernel_launches) *kernel_launches = launches;
+    return ZERO_OK;
+}
+
+// ---- device-state steps, one bucket at a time ---------------------------------
+
+namespace {
+zero_state_t async_host_view()
+{
+    zero_state_t v;   // the real step state is on the device; this only passes the host checks
+    std::memset(&v, 0, sizeof v);
+    v.loss_scale = 1.0f;
+    v.min_loss_scale = 1.0f;
+    return v;
+}
+}  // namespace
+
+zero_status_t zero_step_begin_async(const zero_config_t* c, const zero_plan_t* p, zero_buffers_t* b,
+                                    const zero_adam_t* adam, void* dev_state, void* stream)
+{
+    NvtxRange range("zero_step_begin_async");
+    const zero_state_t host_view = async_host_view();
+    zero_status_t st = check_step(c, p, b, adam, &host_view);
+    if (st != ZERO_OK) return st;
+    if (!dev_state || !aligned16(dev_state)) return fail(ZERO_EALIGN, "dev_state is NULL or not 16-byte aligned");
+    unsigned char* ws_ptr = static_cast<unsigned char*>(b->workspace);
+    PrepArgs pa{static_cast<DevState*>(dev_state), reinterpret_cast<Dyn*>(ws_ptr + ws::kDyn), ws_ptr, adam->beta1,
+                adam->beta2, c->n_ranks, c->dtype};
+    const cudaError_t e = launch_prepare(pa, static_cast<cudaStream_t>(stream), true);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the prepare kernel");
+    return ZERO_OK;
+}
+
+zero_status_t zero_step_bucket_async(const zero_config_t* c, const zero_plan_t* p, zero_buffers_t* b,
+                                     const zero_adam_t* adam, int64_t bucket, void* const* bucket_grads, void* stream)
+{
+    const zero_state_t host_view = async_host_view();
+    zero_status_t st = check_step(c, p, b, adam, &host_view);
+    if (st != ZERO_OK) return st;
+    if (bucket < 0 || bucket >= p->n_buckets)
+        return fail(ZERO_EINVAL, "bucket %lld is outside 0..%lld", (long long)bucket, (long long)p->n_buckets - 1);
+    if (bucket_grads) {
+        if (c->stage < 2)
+            return fail(ZERO_EINVAL, "per-bucket gradient buffers need stage 2 or 3 (stages 0/1 keep full gradients)");
+        st = check_grads(c, bucket_grads, "bucket_grads");
     } else {
-        e = launch_commit(ca, cs, true);
-        if (e != cudaSuccess) return cuda_fail(e, "launching the commit kernel");
+        st = check_grads(c, b->grads, "grads");
     }
-    launches++;
+    if (st != ZERO_OK) return st;
+    NvtxRange range("zero_bucket", bucket);
+    const Path path = choose_path(c, b, adam);
+    const int64_t lo = bucket * c->bucket_elems;
+    StepArgs a = bucket_grads ? make_args(c, p, b, adam, &host_view, path.fused, bucket_grads, lo)
+                              : make_args(c, p, b, adam, &host_view, path.fused, b->grads, 0);
+    a.dyn = reinterpret_cast<const Dyn*>(static_cast<unsigned char*>(b->workspace) + ws::kDyn);
+    a.lo = lo;
+    a.hi = lo + c->bucket_elems < c->n_params ? lo + c->bucket_elems : c->n_params;
+    // the caller may have run work (a staging refill) since the previous kernel: plain stream order
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = path.fused ? launch_fused(c->stage, c->dtype, c->optimizer, a, cs, false)
+                                     : launch_reduce(c->stage, c->dtype, path.clip, a, cs, false);
+    if (e != cudaSuccess) return cuda_fail(e, "launching the bucket kernel");
+    return ZERO_OK;
+}
+
+zero_status_t zero_step_end_async(const zero_config_t* c, const zero_plan_t* p, zero_buffers_t* b,
+                                  const zero_adam_t* adam, void* dev_state, void* stream, int32_t* kernel_launches)
+{
+    NvtxRange range("zero_step_end_async");
+    const zero_state_t host_view = async_host_view();
+    zero_status_t st = check_step(c, p, b, adam, &host_view);
+    if (st != ZERO_OK) return st;
+    if (!dev_state || !aligned16(dev_state)) return fail(ZERO_EALIGN, "dev_state is NULL or not 16-byte aligned");
+    const Path path = choose_path(c, b, adam);
+    unsigned char* ws_ptr = static_cast<unsigned char*>(b->workspace);
+    int launches = 0;
+    st = async_tail(c, p, b, adam, &host_view, static_cast<DevState*>(dev_state),
+                    reinterpret_cast<Dyn*>(ws_ptr + ws::kDyn), ws_ptr, path, static_cast<cudaStream_t>(stream),
+                    &launches);
+    if (st != ZERO_OK) return st;
     if (path.fused) b->cur = 1 - b->cur;   // alternate on every call: an overflow copies the state across
     if (kernel_launches) *kernel_launches = launches;
     return ZERO_OK;
