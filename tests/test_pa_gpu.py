@@ -70,3 +70,10 @@ def test_empty_checkpoint():
     zg.zero_pa_partition(p, x, x)
     zg.zero_pa_gather(p, x, x[:2])
     torch.cuda.synchronize()
+
+
+def test_full_size_checkpoint():
+    """The checkpoint the benchmark uses: batch 32 x sequence 1024 x hidden
+    1600 fp16 (105 MB), N_m = 16, all-gathered into 16 buffers."""
+    p = _run(32 * 1024 * 1600, 16, zg.ZERO_FP16, 16, seed=1)
+    assert p.mem_per_rank_bytes // p.mem_per_rank_pa_bytes == 16
