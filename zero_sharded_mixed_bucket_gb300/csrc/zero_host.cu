@@ -1,5 +1,7 @@
 // Host side of the C ABI: planning, argument checks, the step protocol
-// (begin / bucket / end), the commit-or-skip decision and the loss scaler.
+// (begin / bucket / end), the commit-or-skip decision and the loss scaler;
+// and the device-state steps (zero_step_async and the per-bucket async
+// protocol), whose commit and scaler run on the GPU (k_async.cu).
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
