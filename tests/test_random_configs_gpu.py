@@ -1,0 +1,93 @@
+"""Random combinations of everything the step takes -- stage, N_d, sizes,
+bucket and alignment, value type, optimizer, shadow state or not, clipping,
+loss scaling, staged per-bucket gradients, and the entry point (one call,
+begin/bucket/end, the device-state step, its per-bucket form) -- each run
+for three steps (one of them overflowed) against the oracle, bit for bit.
+The combinations come from a fixed seed, so a failure names a reproducible
+case."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import zero_sharded_mixed_bucket_gb300 as zg
+from tests.gpu_harness import Job, as_signed
+
+pytestmark = pytest.mark.gpu
+
+APIS = ("step", "per_bucket", "async", "per_bucket_async")
+
+
+def _cases(k=96, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < k:
+        stage = int(rng.integers(0, 4))
+        N = int(rng.choice([1, 2, 3, 5, 8, 9, 16, 17, 33]))
+        B = int(rng.choice([8, 64, 512, 2048, 4096]))
+        n = int(rng.integers(1, 6 * B + 50)) if B < 4096 else int(rng.integers(1, 20_000))
+        A = int(rng.choice([8, 64, 2048]))
+        dtype = int(rng.choice([oracle.FP16, oracle.BF16, oracle.FP32]))
+        opt = int(rng.choice([zg.ZERO_ADAM, zg.ZERO_SGD_MOMENTUM, zg.ZERO_SGD]))
+        shadow = bool(rng.integers(0, 2))
+        clip = dtype != oracle.FP32 and bool(rng.integers(0, 3) == 0)
+        api = APIS[int(rng.integers(0, 4))]
+        staged = api in ("per_bucket", "per_bucket_async") and stage >= 2 and bool(rng.integers(0, 2))
+        scale = float(rng.choice([1.0, 8.0, 1024.0]))
+        out.append((stage, N, n, B, A, dtype, opt, shadow, clip, api, staged, scale))
+    return out
+
+
+@pytest.mark.parametrize("case", _cases(), ids=lambda c: "s%d-N%d-n%d-B%d-A%d-dt%d-o%d-sh%d-c%d-%s-st%d" % (
+    c[0], c[1], c[2], c[3], c[4], c[5], c[6], c[7], c[8], c[9], c[10]))
+def test_random_combination(case):
+    stage, N, n, B, A, dtype, opt, shadow, clip, api, staged, scale = case
+    job = Job(n, N, stage, B, A, dtype=dtype, shadow=shadow, optimizer=opt, max_norm=1e-2 if clip else 0.0,
+              loss_scale=scale, dynamic=True, growth=2, sigma=1e-3)
+    dev = None
+    if api in ("async", "per_bucket_async"):
+        dev = torch.zeros(zg.DEV_STATE_BYTES // 8, dtype=torch.int64, device="cuda")
+        zg.zero_dev_state_init(dev, job.adam, job.state)
+    s = torch.cuda.current_stream()
+    vt = torch.int32 if dtype == oracle.FP32 else torch.int16
+    staging = [torch.zeros(B, dtype=vt, device="cuda") for _ in range(N)] if staged else None
+    for step in (1, 2, 3):
+        inject = ((N - 1, n - 1, synth.inf_bits(dtype)),) if step == 2 else ()
+        grads = job.make_grads(step, inject)
+        job.load_grads(grads)
+        two_pass = clip or not shadow
+        if api == "step":
+            fn = [zg.zero_step_stage0, zg.zero_step_stage1, zg.zero_step_stage2, zg.zero_step_stage3][stage]
+            res = fn(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
+        elif api == "async":
+            zg.zero_step_async(job.cfg, job.plan, job.bufs, job.adam, dev, s)
+        else:
+            is_async = api == "per_bucket_async"
+            if is_async:
+                zg.zero_step_begin_async(job.cfg, job.plan, job.bufs, job.adam, dev, s)
+            else:
+                zg.zero_step_begin(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
+            for b in reversed(range(job.plan.n_buckets)):
+                ptrs = None
+                if staged:
+                    lo, hi = b * B, min((b + 1) * B, n)
+                    for r in range(N):
+                        staging[r][:hi - lo].copy_(torch.from_numpy(as_signed(grads[r][lo:hi])))
+                    ptrs = [t.data_ptr() for t in staging]
+                if is_async:
+                    zg.zero_step_bucket_async(job.cfg, job.plan, job.bufs, job.adam, b, ptrs, s)
+                else:
+                    zg.zero_step_bucket(job.cfg, job.plan, job.bufs, job.adam, job.state, b, ptrs, s)
+            if is_async:
+                zg.zero_step_end_async(job.cfg, job.plan, job.bufs, job.adam, dev, s)
+            else:
+                res = zg.zero_step_end(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
+        torch.cuda.synchronize()
+        if dev is not None:
+            st, res = zg.zero_dev_state_read(dev, s)
+            job.state = st
+            res.path = 1 if two_pass else 0
+        ref = job.oracle_step(grads)
+        job.check(res, ref)
+        assert res.overflow == (1 if step == 2 else 0)
