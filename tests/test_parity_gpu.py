@@ -291,11 +291,12 @@ def _transformer_params(vocab, d, layers):
     return vocab * d + layers * (12 * d * d + 4 * d)
 
 
-@pytest.mark.parametrize("stage", [2, 0])
-def test_full_size_sampled(stage):
+@pytest.mark.parametrize("stage,api", [(2, "sync"), (0, "sync"), (2, "async")])
+def test_full_size_sampled(stage, api):
     """The 12-layer d=768 parameter list (123,568,896 params), N_d = 8, bucket
     2^24, inputs generated on the device; 2^16 sampled elements recomputed by
-    the oracle from the host generator, every rank checked at those indices."""
+    the oracle from the host generator, every rank checked at those indices.
+    api "async": through zero_step_async, the entry point the benchmark times."""
     n = _transformer_params(50257, 768, 12)
     assert n == 123_568_896
     N, B = 8, 1 << 24
@@ -316,10 +317,17 @@ def test_full_size_sampled(stage):
                            rank=r, cuda_stream=s.cuda_stream)
     adam = zg.zero_adam_t(**{**dict(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8), "max_grad_norm": 0.0})
     state = zg.zero_state_t(t=0, loss_scale=1.0, min_loss_scale=1.0)
-    fn = zg.zero_step_stage2 if stage == 2 else zg.zero_step_stage0
-    res = fn(cfg, plan, bufs, adam, state, s)
-    torch.cuda.synchronize()
-    assert res.overflow == 0 and res.t == 1 and res.kernel_launches == plan.n_buckets
+    if api == "async":
+        dev = torch.zeros(zg.DEV_STATE_BYTES // 8, dtype=torch.int64, device="cuda")
+        zg.zero_dev_state_init(dev, adam, state, s)
+        launches = zg.zero_step_async(cfg, plan, bufs, adam, dev, s)
+        st, res = zg.zero_dev_state_read(dev, s)
+        assert res.overflow == 0 and st.t == 1 and launches == plan.n_buckets + 2
+    else:
+        fn = zg.zero_step_stage2 if stage == 2 else zg.zero_step_stage0
+        res = fn(cfg, plan, bufs, adam, state, s)
+        torch.cuda.synchronize()
+        assert res.overflow == 0 and res.t == 1 and res.kernel_launches == plan.n_buckets
 
     rng = np.random.default_rng(99)
     idx = np.unique(np.concatenate([rng.integers(0, n, 1 << 16), [0, 1, n - 1, n - 2, B - 1, B, 7 * B - 1]]))
