@@ -616,7 +616,7 @@ def gpu_arm(args):
             for st in (1, 0):
                 try:
                     j = GpuJob(st, device, ring=st_steps + st_warm)
-                    sms, _, sk, _ = timed_steps(j, st_steps, st_warm, 1)
+                    sms, _, sk, _ = timed_steps(j, st_steps, st_warm, 1, api=args.step_api)
                     stages["stage%d" % st] = {"ms_per_step": sms / st_steps,
                                               "value": N_PARAMS / (sms / st_steps * 1e-3) / 1e9,
                                               "kernel_gbs": sk["bytes"] / (sk["total_ms"] * 1e-3) / 1e9,
