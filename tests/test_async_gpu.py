@@ -191,3 +191,15 @@ def test_per_bucket_async_captured_in_graphs():
         res, ref = job.read(), job.oracle_step(grads)
         job.bufs.b.cur = 1 - job.bufs.b.cur
         job.check(res, ref)
+
+
+@pytest.mark.parametrize("shadow", [True, False])
+def test_async_empty_model(shadow):
+    """Zero parameters: the device-state step still commits (t advances), as
+    the synchronising step does."""
+    job = AsyncJob(0, 4, 2, 64, 8, None, oracle.FP16, shadow=shadow)
+    for step in (1, 2):
+        job.load_grads(job.make_grads(step))
+        assert job.launch() == 2
+        st, last = zg.zero_dev_state_read(job.dev)
+        assert st.t == step and last.overflow == 0
