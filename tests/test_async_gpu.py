@@ -196,8 +196,12 @@ def test_per_bucket_async_captured_in_graphs():
 @pytest.mark.parametrize("shadow", [True, False])
 def test_async_empty_model(shadow):
     """Zero parameters: the device-state step still commits (t advances), as
-    the synchronising step does."""
+    the synchronising step does.  (The two-pass path still wants a reduced
+    buffer, even an empty one: a 16-byte placeholder.)"""
     job = AsyncJob(0, 4, 2, 64, 8, None, oracle.FP16, shadow=shadow)
+    placeholder = torch.zeros(8, dtype=torch.int16, device="cuda")
+    if not shadow:
+        job.bufs.b.reduced = placeholder.data_ptr()
     for step in (1, 2):
         job.load_grads(job.make_grads(step))
         assert job.launch() == 2
