@@ -295,7 +295,10 @@ zero_status_t zero_step_end(const zero_config_t* cfg, const zero_plan_t* plan, z
  * buffers dst[d] (capacity max_layer_elems; element j = flat index
  * layer_start + j).  The parameter all-gather that runs before a layer's
  * forward and again before its backward (ZeRO visual reading, communication
- * accounting; "ZeRO：大模型训练的内存优化革命" 3.1.3).  n_dst 1..64. */
+ * accounting; "ZeRO：大模型训练的内存优化革命" 3.1.3).  n_dst 1..64.  With 8
+ * or more destinations in device memory the layer is replicated from
+ * shared-memory tiles by bulk asynchronous copies; otherwise each thread
+ * stores its values to every destination. */
 zero_status_t zero_gather_layer(const zero_config_t* cfg, const zero_plan_t* plan, int32_t layer,
                                 void* const* param_shards, void* const* dst, int32_t n_dst, void* stream);
 
@@ -313,9 +316,11 @@ zero_status_t zero_gather_layer(const zero_config_t* cfg, const zero_plan_t* pla
  * Fused path: the host does not learn the flag, so bufs->cur flips on every
  * call; after an overflow the restore (which also runs the commit) copies
  * the unchanged state into the copy the next step reads and restores the
- * parameters.  A graph
- * captured from one call therefore serves every other step: capture one
- * call per value of bufs->cur and replay them alternately.
+ * parameters.  A graph captured from one call therefore serves every other
+ * step: capture one call per value of bufs->cur and replay them alternately.
+ * The step's kernels are launched as one chain of programmatic dependent
+ * launches (each small kernel, and the first bucket kernel, waits for its
+ * predecessor before it touches memory).
  * The device state block is 64 bytes, 16-byte aligned, caller-owned. */
 typedef struct zero_dev_state { int64_t opaque[8]; } zero_dev_state_t;   /* 64 bytes */
 
