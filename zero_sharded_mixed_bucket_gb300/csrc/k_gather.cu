@@ -20,8 +20,8 @@ namespace {
 // The layer is cut into tiles of kTile 16-bit units (16 KB).  A block
 // gathers a tile from the owners' shards into shared memory with ordinary
 // loads (16 bytes per thread where a group of 8 units is aligned and has one
-// owner, else unit by unit), then one thread replicates it into every
-// destination with bulk asynchronous copies shared -> global
+// owner, else unit by unit), then the lanes of warp 0 replicate it into the
+// destinations, one bulk asynchronous copy shared -> global per destination
 // (cp.async.bulk ... bulk_group), so the n_dst-fold write stream runs on the
 // copy engine of the SM rather than through per-thread stores.  Two tile
 // buffers per block: a buffer is refilled only after the bulk copies that
@@ -84,8 +84,9 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Gat
     const int64_t ntiles = (a.len + kTile - 1) / kTile;
     int b = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, b ^= 1) {
-        // buffer b was last read by the bulk copies committed two tiles ago
-        if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        // buffer b was last read by the bulk copies committed two tiles ago (the
+        // lanes of warp 0 issue them; each waits for its own)
+        if (threadIdx.x < 32) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         __syncthreads();
         const int64_t j_tile = t * kTile;
         const int64_t units = min((int64_t)kTile, a.len - j_tile);
@@ -116,10 +117,10 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Gat
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
         const uint32_t bulk_bytes = (uint32_t)(units * 2) & ~15u;   // 16-byte multiple
-        if (threadIdx.x == 0) {
+        if (threadIdx.x < 32) {   // one destination per lane
             if (bulk_bytes) {
                 const uint32_t saddr = (uint32_t)__cvta_generic_to_shared(buf[b]);
-                for (int d = 0; d < a.n_dst; d++)
+                for (int d = threadIdx.x; d < a.n_dst; d += 32)
                     bulk_store(static_cast<uint16_t*>(a.dst[d]) + j_tile, saddr, bulk_bytes);
             }
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kThreads) k_gather(const __grid_constant__ Gat
         }
     }
     // the bulk copies complete before the block exits
-    if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    if (threadIdx.x < 32) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 }  // namespace

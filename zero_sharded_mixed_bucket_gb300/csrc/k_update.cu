@@ -68,9 +68,9 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
 
 // Stages 1 and 2 with many ranks: the new parameters for every rank are
 // written through shared memory -- a block computes a tile of
-// kTileSub x kThreads groups, then one thread copies it to each rank's
-// parameter buffer with one bulk asynchronous copy (cp.async.bulk shared ->
-// global).  Pass 2 is mostly writes (2 N bytes of parameters per 14 bytes
+// kTileSub x kThreads groups, then the lanes of warp 0 copy it to the ranks'
+// parameter buffers, one bulk asynchronous copy per rank (cp.async.bulk
+// shared -> global).  Pass 2 is mostly writes (2 N bytes of parameters per 14 bytes
 // read); the bulk copies move that replicated stream as the stage-3 gather
 // does.  Two tile buffers: a buffer is rewritten after the copies that read
 // it two tiles earlier have read it (wait_group.read).  The ragged end of a
@@ -106,7 +106,8 @@ __global__ void __launch_bounds__(kThreads) k_update_tiled(const __grid_constant
     const int64_t ntiles = (a.hi - a.lo + kTileElems - 1) / kTileElems;
     int b = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, b ^= 1) {
-        if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        // the lanes of warp 0 issue the copies; each waits for its own
+        if (threadIdx.x < 32) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         __syncthreads();
         const int64_t t0 = a.lo + t * kTileElems;                   // first element of the tile
         const int64_t tel = min(kTileElems, a.hi - t0);              // elements in the tile
@@ -135,10 +136,10 @@ __global__ void __launch_bounds__(kThreads) k_update_tiled(const __grid_constant
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
         const uint32_t bytes = (uint32_t)(tel * kEB) & ~15u;
-        if (threadIdx.x == 0) {
+        if (threadIdx.x < 32) {   // one rank per lane
             if (bytes) {
                 const uint32_t sp = (uint32_t)__cvta_generic_to_shared(&tile[b][0]);
-                for (int r = 0; r < a.n_ranks; r++)
+                for (int r = threadIdx.x; r < a.n_ranks; r += 32)
                     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
                                  :: "l"(static_cast<char*>(a.params16[r]) + t0 * kEB), "r"(sp), "r"(bytes)
                                  : "memory");
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kThreads) k_update_tiled(const __grid_constant
         }
     }
     // the bulk copies complete before the kernel does
-    if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    if (threadIdx.x < 32) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     wait_prev_grid();
 }
 
