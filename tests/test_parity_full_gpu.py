@@ -1,6 +1,6 @@
 """GPU parity at the workloads' full sizes, in the launch configurations that
-bench.py times, on sampled elements the oracle recomputes one by one from the
-host generator (plus properties that hold at any size).
+bench.py times, on about 2^20 sampled elements per test that the oracle
+recomputes from the host generator (plus properties that hold at any size).
 
   * 48-layer d=1600 list (1,555,278,400 params), N_d = 8, bucket 5e8, dynamic
     loss scale: an overflowed step (one inf per 1e9 gradient elements), then a
@@ -28,7 +28,7 @@ def transformer_layers(vocab, d, layers):
     return [vocab * d] + [12 * d * d + 4 * d] * layers
 
 
-def _samples(n, extra, k=1 << 15, seed=7):
+def _samples(n, extra, k=1 << 20, seed=7):
     rng = np.random.default_rng(seed)
     idx = np.concatenate([rng.integers(0, n, k), np.array([i for i in extra if 0 <= i < n], np.int64)])
     return np.unique(idx)
