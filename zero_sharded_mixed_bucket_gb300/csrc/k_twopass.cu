@@ -13,40 +13,88 @@ namespace zg {
 
 namespace {
 
-// HDEST 0: write h to every rank's gradient buffer; 1: to the reduced buffer.
+// One group's reduced values h (from its fp32 rank-order sums s): the
+// overflow test, the exact sum of squares, and the stores.
 template <int HDEST, int DT, bool CLIP>
+__device__ __forceinline__ void finish_group(const StepArgs& a, int64_t i, int64_t gidx, int cnt,
+                                             const float s[kVecOf<DT>], int win_lo, bool& bad, U128& acc,
+                                             unsigned long long* bins)
+{
+    // round to the model precision; elements past cnt are 0 (finite, square 0)
+    Vals<DT> h;
+    bad |= round_group<DT>(s, h) != 0;
+    if constexpr (CLIP) {
+        static_assert(DT != kF32, "no exact sum of squares for binary32 values");
+#pragma unroll
+        for (int p = 0; p < kVecOf<DT> / 2; p++) {
+            sumsq_add<DT>(h.w[p] & 0xffffu, win_lo, acc, bins);
+            sumsq_add<DT>(h.w[p] >> 16, win_lo, acc, bins);
+        }
+    }
+    if constexpr (HDEST == 0) {
+        for (int r = 0; r < a.n_ranks; r++)
+            st_vals<DT>(const_cast<void*>(a.grads[r]), gidx, h, cnt);
+    } else {
+        st_vals<DT>(a.reduced, i, h, cnt);
+    }
+}
+
+// HDEST 0: write h to every rank's gradient buffer; 1: to the reduced buffer.
+// U > 1 (one or two ranks): each thread loads U groups, a grid stride
+// apart, before it sums any, so that enough bytes are in flight per thread
+// when a group is only one or two 16-byte gradient loads.
+template <int HDEST, int DT, bool CLIP, int U>
 __global__ void __launch_bounds__(kThreads) k_reduce(const __grid_constant__ StepArgs a)
 {
     if (a.wait_first) wait_prev_grid();   // first bucket of a device-state step (see k_fused)
     allow_next_grid();
+    constexpr int V = kVecOf<DT>;
     const int win_lo = a.dyn ? a.dyn->win_lo : a.win_lo;
-    const int64_t ngroups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
+    const int64_t ngroups = (a.hi - a.lo + V - 1) / V;
     bool bad = false;
     U128 acc{0ull, 0ull};
     unsigned long long* bins = ws_bins(a.ws);
-    for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
-         gi += (int64_t)gridDim.x * kThreads) {
-        const int64_t i = a.lo + gi * kVecOf<DT>;
-        const int cnt = (int)min((int64_t)kVecOf<DT>, a.hi - i);
-        const int64_t gidx = i - a.grad_base;
-        float s[kVecOf<DT>];
-        reduce_group<DT>(a, gidx, cnt, s);
-        // round to the model precision; elements past cnt are 0 (finite, square 0)
-        Vals<DT> h;
-        bad |= round_group<DT>(s, h) != 0;
-        if constexpr (CLIP) {
-            static_assert(DT != kF32, "no exact sum of squares for binary32 values");
-#pragma unroll
-            for (int p = 0; p < kVecOf<DT> / 2; p++) {
-                sumsq_add<DT>(h.w[p] & 0xffffu, win_lo, acc, bins);
-                sumsq_add<DT>(h.w[p] >> 16, win_lo, acc, bins);
-            }
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    if constexpr (U == 1) {
+        for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups; gi += stride) {
+            const int64_t i = a.lo + gi * V;
+            const int cnt = (int)min((int64_t)V, a.hi - i);
+            const int64_t gidx = i - a.grad_base;
+            float s[V];
+            reduce_group<DT>(a, gidx, cnt, s);
+            finish_group<HDEST, DT, CLIP>(a, i, gidx, cnt, s, win_lo, bad, acc, bins);
         }
-        if constexpr (HDEST == 0) {
-            for (int r = 0; r < a.n_ranks; r++)
-                st_vals<DT>(const_cast<void*>(a.grads[r]), gidx, h, cnt);
-        } else {
-            st_vals<DT>(a.reduced, i, h, cnt);
+    } else {
+        // n_ranks is 1 or 2 here
+        for (int64_t g0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; g0 < ngroups; g0 += stride * U) {
+            Vals<DT> q[U][2];
+#pragma unroll
+            for (int k = 0; k < U; k++) {
+                const int64_t gi = g0 + k * stride;
+                if (gi < ngroups) {
+                    const int64_t i = a.lo + gi * V;
+                    const int cnt = (int)min((int64_t)V, a.hi - i);
+                    q[k][0] = ld_vals<DT>(a.grads[0], i - a.grad_base, cnt);
+                    if (a.n_ranks > 1) q[k][1] = ld_vals<DT>(a.grads[1], i - a.grad_base, cnt);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < U; k++) {
+                const int64_t gi = g0 + k * stride;
+                if (gi < ngroups) {
+                    const int64_t i = a.lo + gi * V;
+                    const int cnt = (int)min((int64_t)V, a.hi - i);
+                    // rank order from 0: s = (0 + g_0) + g_1, as reduce_group
+                    float s[V];
+#pragma unroll
+                    for (int j = 0; j < V; j++) s[j] = __fadd_rn(0.0f, to_f32<DT>(q[k][0].get(j)));
+                    if (a.n_ranks > 1) {
+#pragma unroll
+                        for (int j = 0; j < V; j++) s[j] = __fadd_rn(s[j], to_f32<DT>(q[k][1].get(j)));
+                    }
+                    finish_group<HDEST, DT, CLIP>(a, i, i - a.grad_base, cnt, s, win_lo, bad, acc, bins);
+                }
+            }
         }
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0)
@@ -151,8 +199,12 @@ cudaError_t run_reduce(const StepArgs& a, cudaStream_t s, bool overlap)
 {
     const int64_t groups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     if (groups <= 0) return cudaSuccess;
-    const int grid = grid_for((const void*)k_reduce<HDEST, DT, CLIP>, groups);
-    return launch_step_kernel(k_reduce<HDEST, DT, CLIP>, grid, s, overlap, a);
+    if (a.n_ranks <= 2) {
+        const int grid = grid_for((const void*)k_reduce<HDEST, DT, CLIP, 4>, groups);
+        return launch_step_kernel(k_reduce<HDEST, DT, CLIP, 4>, grid, s, overlap, a);
+    }
+    const int grid = grid_for((const void*)k_reduce<HDEST, DT, CLIP, 1>, groups);
+    return launch_step_kernel(k_reduce<HDEST, DT, CLIP, 1>, grid, s, overlap, a);
 }
 
 template <int DT, bool CLIP>
