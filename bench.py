@@ -505,6 +505,7 @@ def e2e_leg(job, steps, warmup, device, world=1):
     mode = "direct" if ms_direct <= ms_copy else "copy"
     return dict(value=world * n / (ms * 1e-3) / 1e9, unit=UNIT, h2d_bytes_per_step=world * h2d,
                 d2h_bytes_per_step=world * 32, ms_per_step=ms, mode=mode,
+                host_link_gbs_per_gpu=h2d / (ms * 1e-3) / 1e9,
                 modes={"copy": {"ms_per_step": ms_copy, "value": world * n / (ms_copy * 1e-3) / 1e9,
                                 "note": "per-bucket cudaMemcpyAsync from pinned host memory on a second stream, "
                                         "overlapped with the previous bucket's kernel"},

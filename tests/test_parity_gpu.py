@@ -496,6 +496,30 @@ def test_clip_norm_over_full_exponent_range(dtype):
         assert (np.abs(h[h != 0]) < 2.0 ** -40).any() and (np.abs(h) > 2.0 ** 10).any()
 
 
+@pytest.mark.parametrize("S", [1.0, 1024.0])
+def test_clip_norm_bf16_window_edges(S):
+    """bfloat16 squares at both edges of the fixed-point window.  The window
+    starts at E = win_lo = e - 40 (S*N in [2^(e-1), 2^e)); a square enters it
+    at shift 2(E - win_lo) in 0..62 and goes to its exponent bin below 0 and
+    from 64 on.  Rank 1 sends zeros, so the reduced gradient is rank 0's
+    values; the norm and clip coefficient equal the oracle's bit for bit."""
+    import math
+    n, N = 4096 + 45, 2
+    job = Job(n, N, 2, 4096, 8, dtype=BF16, shadow=False, max_norm=1.0, loss_scale=S)
+    win_lo = min(max(math.frexp(S * N)[1] - 40, -133), 88)
+    rng = np.random.default_rng(7)
+    Es = np.array([win_lo + d for d in (-2, -1, 0, 1, 2, 29, 30, 31, 32, 33, 34)], np.float64)
+    E = Es[np.arange(n) % len(Es)]
+    M = rng.integers(128, 256, n).astype(np.float64)
+    x = (rng.choice([-1.0, 1.0], n) * M * 2.0 ** E).astype(np.float32)
+    x[::97] = 0.0
+    g0 = oracle.from_f32(x, BF16)
+    assert np.array_equal(oracle.to_f32(g0, BF16), x)      # every value is exact in bfloat16
+    res, ref = job.step([g0, np.zeros(n, g0.dtype)])
+    assert res.overflow == 0 and ref["overflow"] == 0
+    job.check(res, ref)
+
+
 def test_tiny_partitions_brute_force():
     """Every combination of tiny sizes, rank counts, bucket sizes, alignments
     and stages (448 jobs, one step each) against the oracle: partition

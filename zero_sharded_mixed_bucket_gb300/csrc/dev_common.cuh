@@ -394,7 +394,7 @@ __device__ __forceinline__ void update_state(const StepArgs& a, const AdamHP& hp
 // ---- exact sum of squares --------------------------------------------------
 // A finite 16-bit value is h = M * 2^E with integer M (< 2^11 binary16,
 // < 2^8 bfloat16), so h^2 = M^2 * 2^(2E) exactly.  Terms with
-// 0 <= 2(E - win_lo) <= 64 are added, shifted, into a 128-bit fixed-point
+// 0 <= 2(E - win_lo) <= 63 are added, shifted, into a 128-bit fixed-point
 // accumulator with unit 2^(2 win_lo); the others (rare: a 33-binade window
 // covers every binary16 value and the usual bfloat16 gradient range) go to
 // per-exponent integer bins in the workspace.  Integer sums are exact and
@@ -414,14 +414,15 @@ __device__ __forceinline__ void sumsq_add(uint32_t bits, int win_lo, U128& acc, 
     // Non-finite values are not skipped: they set the step's overflow flag,
     // and an overflowed step discards the norm.
     if constexpr (DT == kBF16) {
+        // in the window when 0 <= sh <= 63: the same two shifts as binary16
+        // below, with no special case (sh = 64 goes to its bin)
         const uint32_t e = (bits >> 7) & 0xffu;
         const uint32_t M = (bits & 0x7fu) | (e ? 0x80u : 0u);
-        const int E = (int)(e ? e : 1u) - 134;
+        const int sh = 2 * ((int)(e ? e : 1u) - 134 - win_lo);
         const unsigned long long m2 = (unsigned long long)(M * M);
-        const int sh = 2 * (E - win_lo);
-        if (sh >= 0 && sh <= 64) {
-            const unsigned long long lo = sh < 64 ? (m2 << sh) : 0ull;
-            const unsigned long long hi = sh == 0 ? 0ull : (sh < 64 ? (m2 >> (64 - sh)) : m2);
+        if ((unsigned)sh <= 63u) {
+            const unsigned long long lo = m2 << sh;
+            const unsigned long long hi = (m2 >> 1) >> (63 - sh);   // 0 when sh == 0
             u128_add(acc, lo, hi);
         } else if (m2) {
             atomicAdd(bins + e, m2);
