@@ -520,6 +520,45 @@ def test_clip_norm_bf16_window_edges(S):
     job.check(res, ref)
 
 
+def test_clip_norm_bf16_group_edges():
+    """bfloat16 squares are summed 8 at a time (one aligned group of 8
+    elements) relative to the group's largest exponent field e_max, down to
+    e_max - 22 or the window's first binade, whichever is higher; a group with
+    a nonzero value below that, or with e_max above the window, is summed
+    value by value.  Groups built on each side of those edges (S*N = 2, so
+    the window's first exponent field is 96 and its last 127), a ragged tail;
+    the norm and clip coefficient equal the oracle's bit for bit."""
+    Z = None   # a zero
+    patterns = [
+        [120, 98, 99, Z, 110, 120, 105, 98],     # down to e_max - 22 exactly
+        [120, 97, 110, 120, Z, 101, 99, 98],     # one value 23 below: per-value path
+        [120, Z, Z, Z, Z, Z, Z, Z],              # zeros below never count
+        [60, 70, 90, 95, 61, 62, 63, 64],        # all below the window: exponent bins
+        [128, 120, 110, 100, 99, 98, 127, 126],  # e_max past the window: per-value path
+        [110, 96, 97, 100, 110, Z, 96, 105],     # base clamped to the window's first exponent
+        [110, 95, 97, 100, 110, Z, 96, 105],     # one value below the window
+        [127, 127, 106, 105, 120, Z, 110, 127],  # e_max at the window's last exponent
+        [120, 0, 110, Z, 100, 0, 99, 98],        # subnormals (field 0, nonzero fraction)
+    ]
+    reps = 40
+    n = 8 * len(patterns) * reps + 5
+    rng = np.random.default_rng(11)
+    bits = np.zeros(n, np.uint16)
+    for g in range(len(patterns) * reps):
+        for j, e in enumerate(patterns[g % len(patterns)]):
+            if e is None:
+                continue
+            f = int(rng.integers(1 if e == 0 else 0, 128))
+            bits[8 * g + j] = (int(rng.integers(0, 2)) << 15) | (e << 7) | f
+    bits[-5:] = np.array([(115 << 7) | 3, 0, (97 << 7) | 1, 1 << 15, (126 << 7)], np.uint16)
+    x = oracle.to_f32(bits, BF16)
+    assert np.isfinite(x).all()
+    job = Job(n, 2, 2, 4096, 8, dtype=BF16, shadow=False, max_norm=1.0, loss_scale=1.0)
+    res, ref = job.step([bits, np.zeros(n, np.uint16)])
+    assert res.overflow == 0 and ref["overflow"] == 0
+    job.check(res, ref)
+
+
 def test_tiny_partitions_brute_force():
     """Every combination of tiny sizes, rank counts, bucket sizes, alignments
     and stages (448 jobs, one step each) against the oracle: partition

@@ -25,10 +25,14 @@ __device__ __forceinline__ void finish_group(const StepArgs& a, int64_t i, int64
     bad |= round_group<DT>(s, h) != 0;
     if constexpr (CLIP) {
         static_assert(DT != kF32, "no exact sum of squares for binary32 values");
+        if constexpr (DT == kBF16) {
+            sumsq_group_bf16(h, win_lo, acc, bins);
+        } else {
 #pragma unroll
-        for (int p = 0; p < kVecOf<DT> / 2; p++) {
-            sumsq_add<DT>(h.w[p] & 0xffffu, win_lo, acc, bins);
-            sumsq_add<DT>(h.w[p] >> 16, win_lo, acc, bins);
+            for (int p = 0; p < kVecOf<DT> / 2; p++) {
+                sumsq_add<DT>(h.w[p] & 0xffffu, win_lo, acc, bins);
+                sumsq_add<DT>(h.w[p] >> 16, win_lo, acc, bins);
+            }
         }
     }
     if constexpr (HDEST == 0) {
