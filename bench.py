@@ -204,7 +204,7 @@ def run_oracle_steps(n_sample, steps, warmup):
     return times
 
 
-def cpu_baseline(n_sample=1 << 24, steps=2):
+def cpu_baseline(n_sample=1 << 26, steps=2):
     times = run_oracle_steps(n_sample, steps, 0)
     sec = sum(times) / len(times)
     return {"value": n_sample / sec / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
