@@ -535,7 +535,8 @@ def gpu_arm(args):
         __graft_entry__.build()      # one builder: concurrent builds would write the same object files
     barrier(world)
     dt_name = args.dtype or "fp16"
-    job = GpuJob(STAGE, device, ring=args.ring, n_params=args.n_params, optimizer=OPTIMIZERS[args.optimizer],
+    stage = args.stage
+    job = GpuJob(stage, device, ring=args.ring, n_params=args.n_params, optimizer=OPTIMIZERS[args.optimizer],
                  dtype=DTYPES[dt_name])
     n_params = job.n
     sampler = ClockSampler(local)
@@ -546,7 +547,7 @@ def gpu_arm(args):
     achieved = kernel["bytes"] / (kernel["total_ms"] * 1e-3) / 1e9
     per_launch = kernel["bytes"] / kernel["launches"]
     # the committed capture is of the fp16 Adam kernel: no counters for the other variants
-    traffic_full = profiled_traffic() if (dt_name, args.optimizer) == ("fp16", "adam") else None
+    traffic_full = profiled_traffic() if (stage, dt_name, args.optimizer) == (2, "fp16", "adam") else None
     # the capture is of a full 2^24-element bucket: scale to the average launch
     traffic = None if traffic_full is None else traffic_full * (n_params / kernel["launches_per_step"]) / (1 << 24)
     step_bytes = job.plan.hbm_bytes_fused
@@ -555,20 +556,23 @@ def gpu_arm(args):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "io_dtype": dt_name, "data": "synthetic",
         "config": {"workload": (WORKLOAD if n_params == N_PARAMS else
-                                "flat parameter vector of %d params, N_d=%d simulated ranks, ZeRO stage %d, bucket "
-                                "2^24 elements, fp16 gradients N(0,1e-3), Adam" % (n_params, N_RANKS, STAGE))
+                                "flat parameter vector of %d params, N_d=%d simulated ranks, ZeRO stage 2, bucket "
+                                "2^24 elements, fp16 gradients N(0,1e-3), Adam" % (n_params, N_RANKS))
+                   .replace("ZeRO stage 2", "ZeRO stage %d" % stage)
                    .replace("fp16 gradients", "%s gradients" % dt_name)
                    .replace("Adam", {"adam": "Adam", "sgdm": "SGD with momentum 0.9", "sgd": "SGD"}[args.optimizer]),
-                   "n_params": n_params, "n_ranks": N_RANKS, "stage": STAGE,
+                   "n_params": n_params, "n_ranks": N_RANKS, "stage": stage,
                    "bucket_elems": BUCKET, "parallelism": "replicas only (simulated ranks inside each GPU)",
                    "l2": "inputs larger than L2: %.2f GB moved per step, %d-step gradient ring of %.1f GB"
                          % (step_bytes / 1e9, args.ring, args.ring * N_RANKS * n_params * 2 / 1e9)},
         "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "k_fused<stage 2, %s, %s>" % (dt_name, args.optimizer),
+        "roofline": {"bound": "hbm",
+                     "kernel": ("k_fused_stage1_tiled<%s, %s>" % (dt_name, args.optimizer) if stage == 1 else
+                                "k_fused<stage %d, %s, %s>" % (stage, dt_name, args.optimizer)),
                      "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes_per_launch": per_launch,
-                     "bytes_per_param": bytes_per_param(STAGE, N_RANKS, STATE_BYTES[job.optimizer], job.e),
+                     "bytes_per_param": bytes_per_param(stage, N_RANKS, STATE_BYTES[job.optimizer], job.e),
                      "launches": kernel["launches"],
                      "avg_launch_ms": kernel["total_ms"] / kernel["launches"],
                      "kernel_span_ms_per_step": kernel["span_ms_per_step"],
@@ -582,7 +586,7 @@ def gpu_arm(args):
     }
     out["optimizer"] = args.optimizer
     out["step_api"] = {"async": "zero_step_async (step state in device memory, no host synchronisation between "
-                                "steps)", "sync": "zero_step_stage2 (overflow flag read by the host every step)"
+                                "steps)", "sync": "zero_step_stage%d (overflow flag read by the host every step)" % stage
                        }[args.step_api]
     out["clocks"] = clocks_summary(rows, t0, t1)
     if args.headline_only:
@@ -673,9 +677,16 @@ def main():
                          "zero_step_stage2")
     ap.add_argument("--headline-only", action="store_true",
                     help="time the stage-2 step only (no stage 0/1, end-to-end or CPU legs)")
+    ap.add_argument("--stage", type=int, default=2, choices=[0, 1, 2, 3],
+                    help="ZeRO stage of the timed step (other than 2: with --headline-only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.stage != 2 and not args.headline_only:
+        ap.error("--stage other than 2 needs --headline-only")
+    if args.stage in (0, 1) and args.ring < args.steps + args.warmup:
+        ap.error("stages 0 and 1 write the all-reduced gradient back into every rank's buffer: give each step "
+                 "a gradient set of its own (--ring >= steps + warmup)")
     if args.impl == "reference":
         return reference_arm(args)
     if args.config != 2:
