@@ -81,8 +81,15 @@
  * Conventions
  * -----------
  *   The caller owns all memory; the library allocates nothing and never
- *   throws.  Between calls it keeps only the thread-local error text and
- *   profiling events; a fetcher's state lives in caller memory.  Every
+ *   throws.  Between calls it keeps only: per process, the resident-block
+ *   count of each kernel on each device (behind a lock); per thread, the
+ *   error text, the profiling events, and whether each pointer it was given
+ *   for a replicated output is device memory of the current device (asked
+ *   once per pointer value with cudaPointerGetAttributes, never during
+ *   stream capture, and assumed to hold for the thread's life: under
+ *   unified addressing device and host allocations never share an
+ *   address).  A fetcher's state lives in caller memory.  Several threads
+ *   may call at once on different jobs and streams.  Every
  *   function returns a zero_status_t; on failure zero_last_error() gives a
  *   message (thread-local).  Kernels run asynchronously on the caller's stream
  *   (a cudaStream_t passed as void*; NULL = legacy default stream).  The
