@@ -92,10 +92,14 @@ __global__ void __launch_bounds__(kThreads, STAGE == 0 ? 5 : 1) k_fused(const __
 // (cp.async.bulk shared -> global), one rank per lane.  Two tile buffers; a
 // buffer is rewritten after the copies that read it two tiles earlier have
 // read it (wait_group.read).  The ragged end of a bucket (less than 16
-// bytes) is stored by the threads.  Measured A/B on the 12-layer d=768
-// list, N_d = 8: stage 1 6352 -> 6595 GB/s, 0.936 -> 0.971 of the copy
-// bandwidth (stage 2, whose replicated output is under a third of its
-// traffic, measured slower this way and keeps per-thread stores).
+// bytes) is stored by the threads.  Two blocks per resident slot: one
+// block's loads and arithmetic overlap another's copies.  Measured A/B on
+// the 12-layer d=768 list, N_d = 8: stage 1 6352 -> 6595 GB/s, 0.936 ->
+// 0.971 of the copy bandwidth with one block per slot, and 1.359-1.362 ->
+// 1.329-1.331 ms per step with two (tiles of 4 x 128 groups: the same).
+// Stage 2, whose replicated output is under a third of its traffic, keeps
+// per-thread stores: through these tiles it measured 1.037-1.042 ms per
+// step against 1.012-1.014.
 constexpr int kTileSub = 2;
 
 template <int DT, int OPT>
@@ -221,7 +225,8 @@ cudaError_t run_fused3(const StepArgs& a, cudaStream_t s, bool overlap)
         if (device_resident(const_cast<void* const*>(a.params16), a.n_ranks, s) &&
             device_resident(const_cast<void* const*>(a.grads), a.n_ranks, s)) {
             const int64_t tiles = (groups + kThreads * kTileSub - 1) / (kThreads * kTileSub);
-            const int grid = grid_for((const void*)k_fused_stage1_tiled<DT, OPT>, tiles * kThreads);
+            const int resident = grid_for((const void*)k_fused_stage1_tiled<DT, OPT>, tiles * kThreads * 4);
+            const int grid = (int)(tiles < 2LL * resident ? tiles : 2LL * resident);
             return launch_step_kernel(k_fused_stage1_tiled<DT, OPT>, grid, s, overlap, a);
         }
     }

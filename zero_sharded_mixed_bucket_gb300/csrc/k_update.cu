@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
     wait_prev_grid();
 }
 
-// Stages 1 and 2 with many ranks: the new parameters for every rank are
+// Stages 1 and 2 with 8 or more ranks: the new parameters for every rank are
 // written through shared memory -- a block computes a tile of
 // kTileSub x kThreads groups, then the lanes of warp 0 copy it to the ranks'
 // parameter buffers, one bulk asynchronous copy per rank (cp.async.bulk
@@ -75,11 +75,14 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
 // does.  Two tile buffers: a buffer is rewritten after the copies that read
 // it two tiles earlier have read it (wait_group.read).  The ragged end of a
 // bucket (less than 16 bytes) is stored by the threads.
-// Measured on the clipped 2^28..2^31 sweep: 32 ranks 0.93 -> 0.95-0.96 of the
-// copy bandwidth; 8 ranks 0.93-0.97 -> 0.91-0.94, so fewer than 16 ranks keep
-// the per-thread stores.
-constexpr int kTileSub = 2;
-constexpr int kBulkMinRanks = 16;
+// Tiles of 4 x 128 groups, two blocks per resident slot (a block's loads and
+// arithmetic then overlap another block's copies).  Measured on GB300, the
+// clipped stage-2 step at 2^28 parameters: 32 ranks 0.947-0.951 of the copy
+// bandwidth with tiles of 2 x 128 groups and one block per slot, 0.985-0.990
+// now (8 x 128: 0.982; three blocks per slot: 0.984); 8 ranks 0.933 / 0.910
+// (fp16 / bf16) with per-thread stores, 0.963 / 0.954 with the tiles.
+constexpr int kTileSub = 4;
+constexpr int kBulkMinRanks = 8;
 
 template <int STAGE, int DT, bool CLIP, int OPT>
 __global__ void __launch_bounds__(kThreads) k_update_tiled(const __grid_constant__ StepArgs a)
@@ -170,7 +173,8 @@ cudaError_t run_update(const StepArgs& a, cudaStream_t s, bool overlap)
     if constexpr (STAGE == 1 || STAGE == 2) {
         if (a.n_ranks >= kBulkMinRanks && device_resident(a.params16, a.n_ranks, s)) {
             const int64_t tiles = (groups + kThreads * kTileSub - 1) / (kThreads * kTileSub);
-            const int grid = grid_for((const void*)k_update_tiled<STAGE, DT, CLIP, OPT>, tiles * kThreads);
+            const int resident = grid_for((const void*)k_update_tiled<STAGE, DT, CLIP, OPT>, tiles * kThreads * 4);
+            const int grid = (int)(tiles < 2LL * resident ? tiles : 2LL * resident);
             return launch_step_kernel(k_update_tiled<STAGE, DT, CLIP, OPT>, grid, s, overlap, a);
         }
     }
