@@ -381,11 +381,31 @@ def sweep_point(n, N, dtype_name, steps, warm):
         gens.append(staging.take_ms() if staging else 0.0)
         norms.append(res.grad_norm)
         assert res.overflow == 0
-    ms = sum(w - g for w, g in zip(walls, gens)) / steps
+    ms_sync = sum(w - g for w, g in zip(walls, gens)) / steps
+    ms, api = ms_sync, "zero_step_stage2"
+    if resident:
+        # the same step with the step state on the device: steps enqueued back
+        # to back, one pair of events around them all, the state read after
+        dev_state = torch.zeros(zg.DEV_STATE_BYTES // 8, dtype=torch.int64, device=dev)
+        zg.zero_dev_state_init(dev_state, adam, state, s)
+        zg.zero_step_async(cfg, plan, bufs, adam, dev_state, s)
+        k_async = max(steps, 10)
+        w0, w1 = _ev(), _ev()
+        w0.record(s)
+        for _ in range(k_async):
+            zg.zero_step_async(cfg, plan, bufs, adam, dev_state, s)
+        w1.record(s)
+        torch.cuda.synchronize()
+        st, last = zg.zero_dev_state_read(dev_state, s)
+        assert st.t == state.t + 1 + k_async and last.overflow == 0
+        assert last.grad_norm == norms[-1]          # the gradients, hence the norm, are the same every step
+        ms_async = w0.elapsed_time(w1) / k_async
+        if ms_async < ms:
+            ms, api = ms_async, "zero_step_async"
     bpp = 28 + 4 * N
     out = {"n_params": n, "n_ranks": N, "dtype": dtype_name, "ms_per_step": ms, "value": n / (ms * 1e-3) / 1e9,
            "hbm_gbs": n * bpp / (ms * 1e-3) / 1e9, "bytes_per_param": bpp, "grad_norm": norms[-1],
-           "clip_coef": res.clip_coef, "t": state.t,
+           "clip_coef": res.clip_coef, "t": state.t, "step_api": api, "ms_per_step_sync": ms_sync,
            "gradients": "resident in HBM" if resident else "generated per bucket into staging (excluded)"}
     del bufs, staging
     torch.cuda.empty_cache()
