@@ -81,7 +81,7 @@ CASES = [
     (1, 3, 2 * 1024 + 7, 1024, 16, 2, False, 0.0, zg.ZERO_SGD_MOMENTUM),
     (2, 4, 5 * 512 + 3, 512, 8, 2, True, 0.0, zg.ZERO_SGD_MOMENTUM),
     (3, 5, 7 * 256 + 1, 256, 8, 2, False, 0.0, zg.ZERO_SGD),
-    # two-pass with 8 or more ranks: parameters written by bulk copies from tiles
+    # two-pass with 2 or more ranks: parameters written by bulk copies from tiles
     (2, 17, 5 * 512 + 3, 512, 8, 0, False, 1.0, zg.ZERO_ADAM),
     (1, 16, 2 * 1024 + 7, 1024, 16, 2, False, 0.0, zg.ZERO_SGD_MOMENTUM),
     (2, 8, 3 * 4096 + 11, 4096, 8, 1, False, 1.0, zg.ZERO_ADAM),

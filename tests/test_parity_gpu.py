@@ -578,15 +578,15 @@ def test_tiny_partitions_brute_force():
 
 # --- pass 2 with the parameters copied out through shared-memory tiles ------
 @pytest.mark.parametrize("stage", [1, 2])
-@pytest.mark.parametrize("N", [4, 8, 16, 33, 64])
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16, 33, 64])
 @pytest.mark.parametrize("dtype,optimizer", [(FP16, zg.ZERO_ADAM), (BF16, zg.ZERO_SGD_MOMENTUM),
                                              (oracle.FP32, zg.ZERO_SGD)])
 def test_two_pass_many_ranks(stage, N, dtype, optimizer):
-    """Stages 1-2 on the two-pass path with many ranks: from 8 ranks the
-    update pass writes every rank's parameters with bulk copies from
-    shared-memory tiles (tiles of 4096 or 2048 elements, so a 5000-element
-    bucket is one full tile and a ragged one, a skipped step in between);
-    4 ranks keep per-thread stores."""
+    """Stages 1-2 on the two-pass path: from 2 ranks the update pass writes
+    every rank's parameters with bulk copies from shared-memory tiles (tiles
+    of 4096 or 2048 elements, so a 5000-element bucket is one full tile and
+    a ragged one, a skipped step in between); 1 rank keeps per-thread
+    stores."""
     n, B = 3 * 5000 + 3, 5000
     job = Job(n, N, stage, B, 8, dtype=dtype, shadow=False, optimizer=optimizer,
               max_norm=1.0 if dtype != oracle.FP32 else 0.0, loss_scale=16.0, dynamic=True)

@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
     wait_prev_grid();
 }
 
-// Stages 1 and 2 with 8 or more ranks: the new parameters for every rank are
+// Stages 1 and 2 with 2 or more ranks: the new parameters for every rank are
 // written through shared memory -- a block computes a tile of
 // kTileSub x kThreads groups, then the lanes of warp 0 copy it to the ranks'
 // parameter buffers, one bulk asynchronous copy per rank (cp.async.bulk
@@ -79,10 +79,12 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
 // arithmetic then overlap another block's copies).  Measured on GB300, the
 // clipped stage-2 step at 2^28 parameters: 32 ranks 0.947-0.951 of the copy
 // bandwidth with tiles of 2 x 128 groups and one block per slot, 0.985-0.990
-// now (8 x 128: 0.982; three blocks per slot: 0.984); 8 ranks 0.933 / 0.910
-// (fp16 / bf16) with per-thread stores, 0.963 / 0.954 with the tiles.
+// now (8 x 128: 0.982; three blocks per slot: 0.984); fp16 / bf16 with
+// per-thread stores against the tiles: 8 ranks 0.933 / 0.910 -> 0.963 /
+// 0.954, 4 ranks 0.919 / 0.863 -> 0.945 / 0.886, 2 ranks 0.893 / 0.865 ->
+// 0.900 / 0.870.  One rank keeps the per-thread stores (a single copy).
 constexpr int kTileSub = 4;
-constexpr int kBulkMinRanks = 8;
+constexpr int kBulkMinRanks = 2;
 
 template <int STAGE, int DT, bool CLIP, int OPT>
 __global__ void __launch_bounds__(kThreads) k_update_tiled(const __grid_constant__ StepArgs a)
