@@ -106,6 +106,22 @@ def test_overflow_other_stages(stage):
     job.check(res, ref)
 
 
+@pytest.mark.parametrize("stage", [1, 2])
+@pytest.mark.parametrize("N,dtype", [(2, FP16), (8, BF16), (33, oracle.FP32), (64, FP16)])
+def test_overflow_restore_tiles(stage, N, dtype):
+    """An overflowed fused step in stages 1-2 with several ranks puts every
+    rank's parameters back through shared-memory tiles and bulk copies
+    (tiles of 4096 16-bit or 2048 binary32 values; a ragged tail of fewer
+    than 16 bytes); then a clean step."""
+    n = 3 * 4096 + 13
+    job = Job(n, N, stage, 5000, 8, dtype=dtype, loss_scale=32.0, dynamic=True)
+    inf = synth.inf_bits(dtype)
+    for t, inject in ((1, ()), (2, ((N // 2, n - 1, inf),)), (3, ())):
+        res, ref = job.step(job.make_grads(t, inject))
+        job.check(res, ref)
+        assert res.path == 0 and res.overflow == (1 if inject else 0)
+
+
 def test_overflow_by_sum():
     """Finite gradients whose rank sum overflows binary16."""
     n = 1000

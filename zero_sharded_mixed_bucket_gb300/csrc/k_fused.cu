@@ -215,6 +215,68 @@ __global__ void __launch_bounds__(kThreads) k_restore(const __grid_constant__ St
     }
 }
 
+// The same restore in stages 1 and 2 with two or more ranks, whose output
+// is the same tile written to every rank: the cast goes to a shared-memory
+// tile of kRestoreTileSub x kThreads groups and the lanes of warp 0 copy it
+// to the ranks with bulk asynchronous copies, as the two-pass update does
+// (two tile buffers, two blocks per resident slot).
+constexpr int kRestoreTileSub = 4;
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) k_restore_tiled(const __grid_constant__ StepArgs a)
+{
+    constexpr int V = kVecOf<DT>;
+    constexpr int kEB = DT == kF32 ? 4 : 2;                        // bytes per value
+    constexpr int kTileGroups = kThreads * kRestoreTileSub;
+    constexpr int64_t kTileElems = (int64_t)kTileGroups * V;
+    __shared__ __align__(128) Vals<DT> tile[2][kTileGroups];
+    const int64_t ntiles = (a.hi - a.lo + kTileElems - 1) / kTileElems;
+    int b = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, b ^= 1) {
+        if (threadIdx.x < 32) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncthreads();
+        const int64_t t0 = a.lo + t * kTileElems;
+        const int64_t tel = min(kTileElems, a.hi - t0);
+        for (int k = 0; k < kRestoreTileSub; k++) {
+            const int gl = k * kThreads + threadIdx.x;
+            const int64_t i = t0 + (int64_t)gl * V;
+            if (i >= a.hi) break;
+            const int cnt = (int)min((int64_t)V, a.hi - i);
+            float w[V];
+            ld_f<V>(a.w_in, i, cnt, w);
+            Vals<DT> p;
+#pragma unroll
+            for (int j = 0; j < V; j++)
+                p.set(j, from_f32<DT>(w[j]));
+            tile[b][gl] = p;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        const uint32_t bytes = (uint32_t)(tel * kEB) & ~15u;
+        if (threadIdx.x < 32) {   // one rank per lane
+            if (bytes) {
+                const uint32_t sp = (uint32_t)__cvta_generic_to_shared(&tile[b][0]);
+                for (int r = threadIdx.x; r < a.n_ranks; r += 32)
+                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                                 :: "l"(static_cast<char*>(a.params16[r]) + t0 * kEB), "r"(sp), "r"(bytes)
+                                 : "memory");
+            }
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        const int done = (int)(bytes / kEB);
+        const int rest = (int)(tel - done);                          // < 16 bytes' worth
+        for (int q = threadIdx.x; q < rest * a.n_ranks; q += kThreads) {
+            const int r = q / rest, j = done + q % rest;
+            const uint32_t pv = tile[b][j / V].get(j % V);
+            if constexpr (kEB == 4)
+                static_cast<uint32_t*>(a.params16[r])[t0 + j] = pv;
+            else
+                static_cast<uint16_t*>(a.params16[r])[t0 + j] = (uint16_t)pv;
+        }
+    }
+    if (threadIdx.x < 32) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 template <int STAGE, int DT, int OPT>
 cudaError_t run_fused3(const StepArgs& a, cudaStream_t s, bool overlap)
 {
@@ -249,6 +311,15 @@ cudaError_t run_restore(const StepArgs& a, cudaStream_t s)
 {
     const int64_t groups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     if (groups <= 0) return cudaSuccess;
+    if constexpr (STAGE == 1 || STAGE == 2) {
+        if (a.n_ranks >= 2 && device_resident(a.params16, a.n_ranks, s)) {
+            const int64_t tiles = (groups + kThreads * kRestoreTileSub - 1) / (kThreads * kRestoreTileSub);
+            const int resident = grid_for((const void*)k_restore_tiled<DT>, tiles * kThreads * 4);
+            const int grid = (int)(tiles < 2LL * resident ? tiles : 2LL * resident);
+            k_restore_tiled<DT><<<grid, kThreads, 0, s>>>(a);
+            return cudaGetLastError();
+        }
+    }
     const int grid = grid_for((const void*)k_restore<STAGE, DT>, groups);
     k_restore<STAGE, DT><<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
