@@ -4,7 +4,9 @@ loss scaling, staged per-bucket gradients, and the entry point (one call,
 begin/bucket/end, the device-state step, its per-bucket form) -- each run
 for three steps (one of them overflowed) against the oracle, bit for bit.
 The combinations come from a fixed seed, so a failure names a reproducible
-case."""
+case; ZG_RANDOM_SEED and ZG_RANDOM_CASES draw another set (a longer soak)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -39,7 +41,8 @@ def _cases(k=96, seed=2024):
     return out
 
 
-@pytest.mark.parametrize("case", _cases(), ids=lambda c: "s%d-N%d-n%d-B%d-A%d-dt%d-o%d-sh%d-c%d-%s-st%d" % (
+@pytest.mark.parametrize("case", _cases(int(os.environ.get("ZG_RANDOM_CASES", "96")),
+                                         int(os.environ.get("ZG_RANDOM_SEED", "2024"))), ids=lambda c: "s%d-N%d-n%d-B%d-A%d-dt%d-o%d-sh%d-c%d-%s-st%d" % (
     c[0], c[1], c[2], c[3], c[4], c[5], c[6], c[7], c[8], c[9], c[10]))
 def test_random_combination(case):
     stage, N, n, B, A, dtype, opt, shadow, clip, api, staged, scale = case
