@@ -440,6 +440,25 @@ __device__ __forceinline__ void sumsq_add(uint32_t bits, int win_lo, U128& acc, 
     }
 }
 
+// The two binary16 squares of a packed word, as sumsq_add<kF16> for each
+// half, with the field extraction done by multiplications (the integer
+// multiplier, not the shift and logic unit the rest of this work keeps
+// busy): x >> k as the high word of x * 2^(32 - k); the hidden bit as
+// (e + 31) >> 5, which is 1 exactly when e > 0; max(e, 1) - 1 as e - hidden.
+__device__ __forceinline__ void sumsq_add_f16x2(uint32_t w, U128& acc)
+{
+    const uint32_t e[2] = {__umulhi(w & 0x00007c00u, 1u << 22), __umulhi(w & 0x7c000000u, 1u << 6)};
+    const uint32_t f[2] = {w & 0x000003ffu, __umulhi(w & 0x03ff0000u, 1u << 16)};
+#pragma unroll
+    for (int k = 0; k < 2; k++) {
+        const uint32_t hid = __umulhi(e[k] + 31u, 1u << 27);
+        const uint32_t M = f[k] + hid * 0x400u;
+        const int sh = 2 * (int)(e[k] - hid);
+        const unsigned long long m2 = (unsigned long long)(M * M);
+        u128_add(acc, m2 << sh, (m2 >> 1) >> (63 - sh));
+    }
+}
+
 // The squares of one group of 8 bfloat16 values.  Each square is m2 *
 // 2^(2(e - 134)) with m2 = M^2 < 2^16 and e = max(exponent field, 1); in
 // units of 2^(2(base - 134)), with base = max(e_max - 22, the window's first

@@ -29,10 +29,8 @@ __device__ __forceinline__ void finish_group(const StepArgs& a, int64_t i, int64
             sumsq_group_bf16(h, win_lo, acc, bins);
         } else {
 #pragma unroll
-            for (int p = 0; p < kVecOf<DT> / 2; p++) {
-                sumsq_add<DT>(h.w[p] & 0xffffu, win_lo, acc, bins);
-                sumsq_add<DT>(h.w[p] >> 16, win_lo, acc, bins);
-            }
+            for (int p = 0; p < kVecOf<DT> / 2; p++)
+                sumsq_add_f16x2(h.w[p], acc);
         }
     }
     if constexpr (HDEST == 0) {
