@@ -481,11 +481,15 @@ __device__ __forceinline__ void sumsq_group_bf16(const H16<8>& h, int win_lo, U1
     int emax = 1;
 #pragma unroll
     for (int j = 0; j < 8; j++) {
-        const uint32_t bits = h.get(j);
-        const uint32_t e = (bits >> 7) & 0xffu;
-        const uint32_t M = (bits & 0x7fu) + min(e, 1u) * 0x80u;
+        // fields by multiplications, as in sumsq_add_f16x2: x >> k as the
+        // high word of x * 2^(32 - k), the hidden bit as (e + 255) >> 8
+        const uint32_t w = h.w[j >> 1];
+        const uint32_t e = (j & 1) ? __umulhi(w & 0x7f800000u, 1u << 9) : __umulhi(w & 0x00007f80u, 1u << 25);
+        const uint32_t f = (j & 1) ? __umulhi(w & 0x007f0000u, 1u << 16) : (w & 0x0000007fu);
+        const uint32_t hid = __umulhi(e + 255u, 1u << 24);
+        const uint32_t M = f + hid * 0x80u;
         m2[j] = M * M;
-        ex[j] = (int)max(e, 1u);
+        ex[j] = (int)(e + 1u - hid);                 // max(e, 1)
         emax = max(emax, ex[j]);
     }
     const int base = max(emax - kD, first);
