@@ -567,8 +567,10 @@ def gpu_arm(args):
                          % (step_bytes / 1e9, args.ring, args.ring * N_RANKS * n_params * 2 / 1e9)},
         "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm",
-                     "kernel": ("k_fused_stage1_tiled<%s, %s>" % (dt_name, args.optimizer) if stage == 1 else
-                                "k_fused<stage %d, %s, %s>" % (stage, dt_name, args.optimizer)),
+                     "kernel": "%s<stage %d, %s, %s>" % (
+                         "k_fused_tiled" if stage == 1 or (stage == 2 and (args.optimizer != "adam" or
+                                                                           dt_name == "fp32")) else "k_fused",
+                         stage, dt_name, args.optimizer),
                      "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes_per_launch": per_launch,

@@ -85,31 +85,42 @@ __global__ void __launch_bounds__(kThreads, STAGE == 0 ? 5 : 1) k_fused(const __
     wait_prev_grid();
 }
 
-// Stage 1 with its two replicated outputs -- the all-reduced gradient and
-// the new parameters, each written to every rank -- through shared memory:
-// a block computes a tile of kTileSub x kThreads groups, then the lanes of
-// warp 0 copy both tiles to each rank with bulk asynchronous copies
-// (cp.async.bulk shared -> global), one rank per lane.  Two tile buffers; a
-// buffer is rewritten after the copies that read it two tiles earlier have
-// read it (wait_group.read).  The ragged end of a bucket (less than 16
-// bytes) is stored by the threads.  Two blocks per resident slot: one
-// block's loads and arithmetic overlap another's copies.  Measured A/B on
-// the 12-layer d=768 list, N_d = 8: stage 1 6352 -> 6595 GB/s, 0.936 ->
+// Stages 1 and 2 with their replicated outputs -- the new parameters, and in
+// stage 1 the all-reduced gradient, each written to every rank -- through
+// shared memory: a block computes a tile of kTileSub x kThreads groups, then
+// the lanes of warp 0 copy the tile(s) to each rank with bulk asynchronous
+// copies (cp.async.bulk shared -> global), one rank per lane.  Two tile
+// buffers; a buffer is rewritten after the copies that read it two tiles
+// earlier have read it (wait_group.read).  The ragged end of a bucket (less
+// than 16 bytes) is stored by the threads.  Two blocks per resident slot:
+// one block's loads and arithmetic overlap another's copies.  Measured A/B
+// on the 12-layer d=768 list, N_d = 8: stage 1 6352 -> 6595 GB/s, 0.936 ->
 // 0.971 of the copy bandwidth with one block per slot, and 1.359-1.362 ->
 // 1.329-1.331 ms per step with two (tiles of 4 x 128 groups: the same).
-// Stage 2, whose replicated output is under a third of its traffic, keeps
-// per-thread stores: through these tiles it measured 1.037-1.042 ms per
-// step against 1.012-1.014.
+// Stage 2 takes the tiles where the replicated parameters are a large share
+// of the traffic: SGD and SGD with momentum (16 of 40 and of 48 bytes per
+// parameter; fp16 0.746 -> 0.730 and 0.896 -> 0.873 ms per step, fp32
+// 1.331 -> 1.316 and 1.480 -> 1.461) and binary32 Adam (32 of 88; 1.613 ->
+// 1.599).  16-bit Adam (16 of 56) keeps per-thread stores: through the
+// tiles it measured 1.037-1.042 ms per step against 1.012-1.014.
 constexpr int kTileSub = 2;
 
-template <int DT, int OPT>
-__global__ void __launch_bounds__(kThreads) k_fused_stage1_tiled(const __grid_constant__ StepArgs a)
+template <int STAGE, int DT, int OPT>
+constexpr bool tiled_step()
 {
+    return STAGE == 1 || (STAGE == 2 && (OPT != kAdam || DT == kF32));
+}
+
+template <int STAGE, int DT, int OPT>
+__global__ void __launch_bounds__(kThreads) k_fused_tiled(const __grid_constant__ StepArgs a)
+{
+    static_assert(STAGE == 1 || STAGE == 2, "outputs replicated to every rank: stages 1 and 2");
     constexpr int V = kVecOf<DT>;
     constexpr int kEB = DT == kF32 ? 4 : 2;                        // bytes per value
+    constexpr int kArrays = STAGE == 1 ? 2 : 1;                    // parameters (, gradient)
     constexpr int kTileGroups = kThreads * kTileSub;
     constexpr int64_t kTileElems = (int64_t)kTileGroups * V;
-    __shared__ __align__(128) Vals<DT> tile[2][2][kTileGroups];    // [buffer][parameters, gradient]
+    __shared__ __align__(128) Vals<DT> tile[2][kArrays][kTileGroups];
     if (a.wait_first) wait_prev_grid();
     allow_next_grid();
     float inv = a.inv;
@@ -141,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) k_fused_stage1_tiled(const __grid_co
             Vals<DT> p;
             update_state<DT, OPT>(a, hp, i, cnt, g, p);
             tile[b][0][gl] = p;
-            tile[b][1][gl] = h;
+            if constexpr (STAGE == 1) tile[b][kArrays - 1][gl] = h;
         }
         // make the tiles visible to the bulk-copy (async) proxy, then copy them out
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -150,15 +161,17 @@ __global__ void __launch_bounds__(kThreads) k_fused_stage1_tiled(const __grid_co
         if (threadIdx.x < 32) {   // one rank per lane
             if (bytes) {
                 const uint32_t sp = (uint32_t)__cvta_generic_to_shared(&tile[b][0][0]);
-                const uint32_t sg = (uint32_t)__cvta_generic_to_shared(&tile[b][1][0]);
+                const uint32_t sg = (uint32_t)__cvta_generic_to_shared(&tile[b][kArrays - 1][0]);
                 for (int r = threadIdx.x; r < a.n_ranks; r += 32) {
                     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
                                  :: "l"(static_cast<char*>(a.params16[r]) + t0 * kEB), "r"(sp), "r"(bytes)
                                  : "memory");
-                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                                 :: "l"(static_cast<char*>(const_cast<void*>(a.grads[r])) + (t0 - a.grad_base) * kEB),
-                                 "r"(sg), "r"(bytes)
-                                 : "memory");
+                    if constexpr (STAGE == 1)
+                        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                                     :: "l"(static_cast<char*>(const_cast<void*>(a.grads[r])) +
+                                            (t0 - a.grad_base) * kEB),
+                                     "r"(sg), "r"(bytes)
+                                     : "memory");
                 }
             }
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
@@ -167,13 +180,16 @@ __global__ void __launch_bounds__(kThreads) k_fused_stage1_tiled(const __grid_co
         const int rest = (int)(tel - done);                          // < 16 bytes' worth
         for (int q = threadIdx.x; q < rest * a.n_ranks; q += kThreads) {
             const int r = q / rest, j = done + q % rest;
-            const uint32_t pv = tile[b][0][j / V].get(j % V), hv = tile[b][1][j / V].get(j % V);
+            const uint32_t pv = tile[b][0][j / V].get(j % V);
+            const uint32_t hv = tile[b][kArrays - 1][j / V].get(j % V);
             if constexpr (kEB == 4) {
                 static_cast<uint32_t*>(a.params16[r])[t0 + j] = pv;
-                static_cast<uint32_t*>(const_cast<void*>(a.grads[r]))[t0 - a.grad_base + j] = hv;
+                if constexpr (STAGE == 1)
+                    static_cast<uint32_t*>(const_cast<void*>(a.grads[r]))[t0 - a.grad_base + j] = hv;
             } else {
                 static_cast<uint16_t*>(a.params16[r])[t0 + j] = (uint16_t)pv;
-                static_cast<uint16_t*>(const_cast<void*>(a.grads[r]))[t0 - a.grad_base + j] = (uint16_t)hv;
+                if constexpr (STAGE == 1)
+                    static_cast<uint16_t*>(const_cast<void*>(a.grads[r]))[t0 - a.grad_base + j] = (uint16_t)hv;
             }
         }
     }
@@ -282,14 +298,15 @@ cudaError_t run_fused3(const StepArgs& a, cudaStream_t s, bool overlap)
 {
     const int64_t groups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     if (groups <= 0) return cudaSuccess;
-    if constexpr (STAGE == 1) {
-        // the bulk copies write the ranks' parameters and gradients: device memory only
-        if (device_resident(const_cast<void* const*>(a.params16), a.n_ranks, s) &&
-            device_resident(const_cast<void* const*>(a.grads), a.n_ranks, s)) {
+    if constexpr (tiled_step<STAGE, DT, OPT>()) {
+        // device memory only (the bulk copies write the ranks' parameters, and
+        // in stage 1 their gradients); stage 2 from two ranks
+        if ((STAGE == 1 || a.n_ranks >= 2) && device_resident(const_cast<void* const*>(a.params16), a.n_ranks, s) &&
+            (STAGE == 2 || device_resident(const_cast<void* const*>(a.grads), a.n_ranks, s))) {
             const int64_t tiles = (groups + kThreads * kTileSub - 1) / (kThreads * kTileSub);
-            const int resident = grid_for((const void*)k_fused_stage1_tiled<DT, OPT>, tiles * kThreads * 4);
+            const int resident = grid_for((const void*)k_fused_tiled<STAGE, DT, OPT>, tiles * kThreads * 4);
             const int grid = (int)(tiles < 2LL * resident ? tiles : 2LL * resident);
-            return launch_step_kernel(k_fused_stage1_tiled<DT, OPT>, grid, s, overlap, a);
+            return launch_step_kernel(k_fused_tiled<STAGE, DT, OPT>, grid, s, overlap, a);
         }
     }
     const int grid = grid_for((const void*)k_fused<STAGE, DT, OPT>, groups);
