@@ -85,10 +85,10 @@
  *   count of each kernel on each device (behind a lock); per thread, the
  *   error text, the profiling events, and whether each pointer it was given
  *   for a replicated output is device memory of the current device (asked
- *   once per pointer value with cudaPointerGetAttributes, never during
- *   stream capture, and assumed to hold for the thread's life: under
- *   unified addressing device and host allocations never share an
- *   address).  A fetcher's state lives in caller memory.  Several threads
+ *   of the driver on every call outside stream capture, so a freed address
+ *   that later holds host or managed memory is seen as such; while a stream
+ *   is captured no query is made and the answer last seen on the thread
+ *   stands, an unknown pointer counting as not device memory).  A fetcher's state lives in caller memory.  Several threads
  *   may call at once on different jobs and streams.  Every
  *   function returns a zero_status_t; on failure zero_last_error() gives a
  *   message (thread-local).  Kernels run asynchronously on the caller's stream
@@ -231,15 +231,30 @@ typedef struct zero_step_result {
 /* ---- planning (host only, no CUDA calls) ------------------------------ */
 
 /* Partition, bucket table sizes, buffer sizes and the paper's accounting for
- * cfg.  Errors: ZERO_EINVAL (bad field), ZERO_EUNSUPPORTED (n_ranks). */
+ * cfg.  Source: the shard rule -- each of the N_d ranks keeps one contiguous
+ * 1/N_d of the flattened states, per stage (ZeRO visual reading, stage list;
+ * "ZeRO：大模型训练的内存优化革命" 3.1.1-3.1.3) -- the constant-size gradient
+ * buckets (same page, 3.2.2, C_B; SC-2020 ZeRO notes, "Deep Dive into
+ * ZeRO-R") and the per-stage memory and communication formulas (ZeRO visual
+ * reading, stage formulas and communication accounting).  The shard is padded
+ * to align_elems (a layout choice the pages leave open).  cfg and out are
+ * caller memory; nothing is kept.  Errors: ZERO_EINVAL (bad field or NULL),
+ * ZERO_EUNSUPPORTED (n_ranks outside 1..64, n_params above 2^40). */
 zero_status_t zero_plan(const zero_config_t* cfg, zero_plan_t* out);
 
 /* Segments of bucket b: for each rank owning part of it, in rank order,
  * seg[3k] = rank, seg[3k+1] = offset inside that rank's shard, seg[3k+2] =
- * length.  seg must hold 3*n_ranks entries; *n_seg receives the count. */
+ * length -- where the reduce-scatter of one fusion bucket sends its
+ * elements ("ZeRO：大模型训练的内存优化革命" 3.1.2 and 3.2.2; ZeRO visual
+ * reading, stage list: the owner of a gradient shard reduces it).  seg must
+ * hold 3*n_ranks entries; *n_seg receives the count.  Errors: ZERO_EINVAL
+ * (b outside 0..n_buckets-1, NULL output), as zero_plan for cfg. */
 zero_status_t zero_plan_bucket(const zero_config_t* cfg, int64_t b, int64_t* seg, int32_t* n_seg);
 
-/* Flat start and length of stage-3 layer `layer`. */
+/* Flat start and length of stage-3 layer `layer`: the unit that stage 3
+ * gathers before the layer runs and releases after it
+ * ("ZeRO：大模型训练的内存优化革命" 3.1.3; ZeRO visual reading, stage-3
+ * section).  Errors: ZERO_EINVAL (layer out of range, NULL output). */
 zero_status_t zero_plan_layer(const zero_config_t* cfg, int32_t layer, int64_t* start, int64_t* len);
 
 /* Per-rank model-state bytes of the paper's accounting (ZeRO visual reading,
@@ -263,7 +278,23 @@ zero_status_t zero_comm_bytes(int64_t n_params, int32_t n_ranks, int32_t stage, 
 /* ---- the step (device) --------------------------------------------------- */
 
 /* One complete optimizer step over all buckets: begin, every bucket, end.
- * zero_step dispatches on cfg->stage; zero_step_stageK requires stage K. */
+ * zero_step dispatches on cfg->stage; zero_step_stageK requires stage K
+ * (ZERO_EINVAL otherwise).  Sources, per stage: stage 0 is plain data
+ * parallelism (every rank keeps every state, gradients all-reduced); stage 1
+ * partitions the optimizer state (P_os), stage 2 also the gradients
+ * (P_os+g), stage 3 also the parameters (P_os+g+p)
+ * ("ZeRO：大模型训练的内存优化革命" 3.1.1-3.1.3; ZeRO visual reading, stage
+ * list and communication accounting: reduce-scatter, update of the owned
+ * shard, all-gather).  The update itself is the mixed-precision one: fp32
+ * master weights and optimizer state updated from the 16-bit gradient, then
+ * cast back to 16 bits (SC-2020 ZeRO notes, "Where Did All the Memory Go? /
+ * Model States"; "AI论文陪读·ZeRO" section 01).  Adam is Kingma & Ba,
+ * Algorithm 1 (the pages name Adam but do not print it).  The buffers are the
+ * caller's (layout above); the call returns after reading the step's
+ * overflow flag (one synchronisation of `stream`).  Errors: ZERO_EINVAL,
+ * ZERO_EALIGN, ZERO_ENOMEM (missing buffer), ZERO_ECUDA (a launch or the
+ * synchronisation failed; the message has the CUDA error), ZERO_EUNSUPPORTED.
+ * On any error before the first launch nothing on the device has changed. */
 zero_status_t zero_step(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
                         const zero_adam_t* adam, zero_state_t* state, void* stream,
                         zero_step_result_t* out);
@@ -281,7 +312,9 @@ zero_status_t zero_step_stage3(const zero_config_t* cfg, const zero_plan_t* plan
                                zero_step_result_t* out);
 
 /* The same step, bucket by bucket, for gradients that arrive one bucket at a
- * time (backward hooks filling a constant-size bucket).  Call begin, then
+ * time (backward hooks filling a constant-size bucket: the fused buffer of
+ * "ZeRO：大模型训练的内存优化革命" 3.2.2 and the SC-2020 ZeRO notes, "Deep
+ * Dive into ZeRO-R", C_B).  Call begin, then
  * zero_step_bucket exactly once for every bucket b in any order, then end,
  * all on one stream with unchanged arguments.
  * bucket_grads: NULL to read bufs->grads, or (stages 2 and 3 only) a host
@@ -408,7 +441,9 @@ zero_status_t zero_fetch_schedule(const int64_t* layer_sizes, int32_t n_layers, 
  * bufs->reduced and the shadow copies bufs->w/m/v[1-cur] are ignored; the
  * step always takes the two-pass path and updates the [cur] state in place
  * (clipping allowed).  The caller still passes the gradients, parameters and
- * fp32 state.  The first call on each device looks up the array's device
+ * fp32 state.  The array used is the current device's, so `stream` must
+ * belong to the current device (ZERO_EINVAL otherwise; NULL is the current
+ * device's legacy default stream).  The first call on each device looks up the array's device
  * address (cudaGetSymbolAddress, with that device current); make that first
  * call before any stream capture.  Each call clears the array's workspace
  * part before use; the rest keeps the last call's contents.  All calls share
@@ -466,8 +501,12 @@ zero_status_t zero_pa_gather(const zero_pa_plan_t* plan, const void* const* shar
  * step's kernel span, not per-kernel durations. */
 zero_status_t zero_set_profile_events(void* start_event, void* end_event);
 
-/* Thread-local message of the last failed call ("" if none). */
+/* Thread-local message of the last failed call ("" if none).  No
+ * counterpart on the pages: error reporting of this C ABI.  The string is
+ * owned by the library and stays valid until the thread's next failing
+ * call. */
 const char* zero_last_error(void);
+/* ZERO_GB300_VERSION of the loaded library (no counterpart on the pages). */
 int32_t zero_version(void);
 
 #ifdef __cplusplus
