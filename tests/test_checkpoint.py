@@ -43,6 +43,26 @@ def test_round_trip_files_cpu(tmp_path, stage, optimizer):
                         zg.zero_plan(zg.Config(10_003, 3, stage, 2048, 8, None, zg.ZERO_FP16, optimizer)), b, st2)
 
 
+def test_resume_rejects_another_layer_split(tmp_path):
+    """Same size, stage, ranks and partition, but another split into layers:
+    the stage-3 gather units and the fetch offsets would no longer match the
+    saved job, so resuming is refused."""
+    layers = [4000, 3000, 3003]
+    cfg = zg.Config(10_003, 3, 3, 1024, 8, layers)
+    plan = zg.zero_plan(cfg)
+    a = zg.DeviceBuffers(cfg, plan, device="cpu")
+    st = zg.zero_state_t(t=1, loss_scale=1.0, min_loss_scale=1.0)
+    save_checkpoint(str(tmp_path), cfg, plan, a, st)
+    load_checkpoint(str(tmp_path), cfg, plan, zg.DeviceBuffers(cfg, plan, device="cpu"), zg.zero_state_t())
+    for other in ([4000, 3003, 3000], None):
+        cfg2 = zg.Config(10_003, 3, 3, 1024, 8, other)
+        plan2 = zg.zero_plan(cfg2)
+        assert plan2.shard_elems == plan.shard_elems
+        with pytest.raises(ValueError, match="layer sizes"):
+            load_checkpoint(str(tmp_path), cfg2, plan2, zg.DeviceBuffers(cfg2, plan2, device="cpu"),
+                            zg.zero_state_t())
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("stage", [1, 3])
 def test_resume_continues_bit_for_bit(tmp_path, stage):

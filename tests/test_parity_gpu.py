@@ -276,6 +276,33 @@ def test_gather_layers(A, n_dst):
             start += ln
 
 
+def test_gather_destinations_change_kind():
+    """The library asks the driver what each destination is on every call:
+    the same job gathers into device buffers (tile kernel with bulk copies),
+    then, after those are freed, into pinned host buffers (per-thread
+    stores), then into device buffers again; every result equals the
+    oracle's parameters."""
+    layers = [3001, 20_000, 17]
+    n = sum(layers)
+    job = Job(n, 4, 3, 4096, layers=layers)
+    plan = job.plan
+    shards = [t.data_ptr() for t in job.bufs.params16]
+    for kind in ("device", "host", "device"):
+        if kind == "device":
+            dst = [torch.full((plan.max_layer_elems,), -1, dtype=torch.int16, device="cuda") for _ in range(8)]
+        else:
+            dst = [torch.full((plan.max_layer_elems,), -1, dtype=torch.int16).pin_memory() for _ in range(8)]
+        start = 0
+        for l, ln in enumerate(layers):
+            zg.zero_gather_layer(job.cfg, plan, l, shards, [d.data_ptr() for d in dst])
+            torch.cuda.synchronize()
+            for d in dst:
+                assert np.array_equal(d[:ln].cpu().numpy().view(np.uint16), job.p16[start:start + ln]), (kind, l)
+            start += ln
+        del dst
+        torch.cuda.empty_cache()
+
+
 def test_gather_max_destinations():
     layers = [5000, 5000]
     job = Job(10_000, 4, 3, 1024, 8, layers=layers)

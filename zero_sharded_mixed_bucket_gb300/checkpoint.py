@@ -62,7 +62,8 @@ def save_checkpoint(path: str, cfg, plan, bufs, state: zero_state_t) -> None:
 
 def load_checkpoint(path: str, cfg, plan, bufs, state: zero_state_t) -> None:
     """Restore into bufs' current state copy and into `state`.  The config
-    must describe the same job (sizes, stage, ranks, dtype, optimizer)."""
+    must describe the same job (sizes, layer split, stage, ranks, dtype,
+    optimizer); ValueError otherwise."""
     import torch
     c = _c(cfg)
     with open(os.path.join(path, "manifest.json")) as f:
@@ -72,6 +73,11 @@ def load_checkpoint(path: str, cfg, plan, bufs, state: zero_state_t) -> None:
             raise ValueError("checkpoint was written for %s=%r, the config has %r" % (key, val, getattr(c, key)))
     if man["shard_elems"] != plan.shard_elems:
         raise ValueError("checkpoint partition differs from the plan")
+    # the layer split fixes the stage-3 gather units and the fetch offsets
+    layers = [int(c.layer_sizes[i]) for i in range(c.n_layers)] if c.n_layers else None
+    if man.get("layer_sizes") != layers:
+        raise ValueError("checkpoint was written for layer sizes %r, the config has %r"
+                         % (man.get("layer_sizes"), layers))
     arrays = _ARRAYS[c.optimizer]
     k = bufs.cur
     for r in range(c.n_ranks):

@@ -8,11 +8,11 @@
 
 namespace zg {
 
-// Pointer kinds come from cudaPointerGetAttributes and are remembered per
-// thread and pointer value (a pointer is taken to keep its kind while the
-// caller's buffers live).  While `stream` is being captured into a graph no
-// query is made (it could invalidate the capture): remembered answers are
-// used, an unknown pointer counts as not device memory.
+// Pointer kinds are asked of the driver on every call (an address the
+// caller freed may later be host or managed memory) and remembered per
+// thread for stream capture: while `stream` is being captured into a graph
+// no query is made (it could invalidate the capture), remembered answers
+// are used and an unknown pointer counts as not device memory.
 bool device_resident(void* const* ptrs, int n, cudaStream_t stream);
 
 }  // namespace zg

@@ -8,6 +8,8 @@
 // 3.1.3; ZeRO visual reading, communication accounting: the second all-gather
 // that makes stage 3 cost 3 Psi; SC-2020 ZeRO notes, C_B constant-size
 // buffers).
+#include <cuda.h>
+
 #include <mutex>
 
 #include "dev_common.cuh"
@@ -157,10 +159,58 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s)
     return cudaGetLastError();
 }
 
+namespace {
+
+// cuPointerGetAttributes through the runtime's driver entry-point lookup (no
+// link against the driver library).  Unlike the one-attribute query it
+// succeeds for pointers the driver does not know, reporting them as memory
+// type 0.
+using PointerAttrsFn = CUresult (*)(unsigned int, CUpointer_attribute*, void**, CUdeviceptr);
+
+PointerAttrsFn pointer_attrs_fn()
+{
+    static const PointerAttrsFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuPointerGetAttributes", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return (PointerAttrsFn) nullptr;
+        }
+        return reinterpret_cast<PointerAttrsFn>(f);
+    }();
+    return fn;
+}
+
+// Is p plain (not managed) device memory of device `dev`?  Asked of the
+// driver each time: an address freed by the caller may later belong to host
+// or managed memory.
+bool query_device_memory(const void* p, int dev, bool* ok)
+{
+    *ok = false;
+    const PointerAttrsFn fn = pointer_attrs_fn();
+    if (!fn) return false;
+    unsigned int type = 0;
+    unsigned int managed = 0;
+    int ordinal = -1;
+    CUpointer_attribute attrs[3] = {CU_POINTER_ATTRIBUTE_MEMORY_TYPE, CU_POINTER_ATTRIBUTE_IS_MANAGED,
+                                    CU_POINTER_ATTRIBUTE_DEVICE_ORDINAL};
+    void* data[3] = {&type, &managed, &ordinal};
+    if (fn(3, attrs, data, (CUdeviceptr) reinterpret_cast<uintptr_t>(p)) != CUDA_SUCCESS) return false;
+    *ok = true;
+    return type == CU_MEMORYTYPE_DEVICE && !managed && ordinal == dev;
+}
+
+}  // namespace
+
 bool device_resident(void* const* ptrs, int n, cudaStream_t stream)
 {
-    // A per-thread table of pointers already asked about (open addressing;
-    // cleared when it fills up).
+    // Outside stream capture every pointer is asked of the driver on every
+    // call.  A per-thread table keeps the answers (open addressing; cleared
+    // when it fills up) for use while a stream is captured, when no query is
+    // made: there a remembered answer stands and an unknown pointer counts
+    // as not device memory.
     constexpr int kSlots = 1024;
     struct Entry {
         const void* p;
@@ -175,41 +225,34 @@ bool device_resident(void* const* ptrs, int n, cudaStream_t stream)
         return false;
     }
     if (n < 1) return false;
-    bool capturing = false;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    const bool capturing = cs != cudaStreamCaptureStatusNone;
     for (int k = 0; k < n; k++) {
         const void* p = ptrs[k];
         if (!p) return false;
-        uint64_t h = reinterpret_cast<uintptr_t>(p) * 0x9E3779B97F4A7C15ull;
+        const uint64_t h = reinterpret_cast<uintptr_t>(p) * 0x9E3779B97F4A7C15ull;
         int slot = (int)(h >> 54);   // 10 bits
         while (table[slot].p && !(table[slot].p == p && table[slot].dev == dev)) slot = (slot + 1) & (kSlots - 1);
-        if (table[slot].p) {
-            if (!table[slot].device) return false;
+        if (capturing) {
+            if (!table[slot].p || !table[slot].device) return false;
             continue;
         }
-        // not seen yet: ask, unless the stream is being captured (a query could
-        // invalidate the capture)
-        if (!capturing) {
-            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-            if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
-                cudaGetLastError();
-                return false;
+        bool ok = false;
+        const bool device = query_device_memory(p, dev, &ok);
+        if (!ok) return false;
+        if (!table[slot].p) {
+            if (used >= kSlots / 2) {   // keep the table sparse
+                for (int j = 0; j < kSlots; j++) table[j].p = nullptr;
+                used = 0;
+                slot = (int)(h >> 54);
             }
-            capturing = cs != cudaStreamCaptureStatusNone;
-        }
-        if (capturing) return false;
-        cudaPointerAttributes at;
-        bool device = false;
-        if (cudaPointerGetAttributes(&at, p) != cudaSuccess)
-            cudaGetLastError();   // not a CUDA pointer: clear the error, answer no
-        else
-            device = at.type == cudaMemoryTypeDevice && at.device == dev;
-        if (used >= kSlots / 2) {   // keep the table sparse
-            for (int j = 0; j < kSlots; j++) table[j].p = nullptr;
-            used = 0;
-            slot = (int)(h >> 54);
+            used++;
         }
         table[slot] = Entry{p, dev, device};
-        used++;
         if (!device) return false;
     }
     return true;

@@ -33,13 +33,11 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
 
-// Device address of the static scratch on the current device, looked up once
-// per device (the first call on a device does this set-up).
-cudaError_t scratch_address(void** out)
+// Device address of the static scratch on device `dev` (the current device),
+// looked up once per device (the first call on a device does this set-up).
+cudaError_t scratch_address(int dev, void** out)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_addr[dev]) {
@@ -77,8 +75,31 @@ extern "C" zero_status_t zero_step_stage2_noalloc(const zero_config_t* cfg, cons
                       (long long)fresh.padded_elems, (long long)kNoAllocMaxReduced);
         return zg::set_error(ZERO_EUNSUPPORTED, msg);
     }
+    // The scratch address belongs to the current device, and the kernels run
+    // on `stream`: both must be the same GPU.
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        std::snprintf(msg, sizeof msg, "zero_step_stage2_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+        return zg::set_error(ZERO_ECUDA, msg);
+    }
+    if (stream) {
+        int sdev = -1;
+        e = cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev);
+        if (e != cudaSuccess) {
+            std::snprintf(msg, sizeof msg, "zero_step_stage2_noalloc: cudaStreamGetDevice: %s",
+                          cudaGetErrorString(e));
+            return zg::set_error(ZERO_ECUDA, msg);
+        }
+        if (sdev != dev) {
+            std::snprintf(msg, sizeof msg,
+                          "zero_step_stage2_noalloc: the stream belongs to device %d, the current device is %d "
+                          "(make the stream's device current)", sdev, dev);
+            return zg::set_error(ZERO_EINVAL, msg);
+        }
+    }
     void* scratch = nullptr;
-    const cudaError_t e = scratch_address(&scratch);
+    e = scratch_address(dev, &scratch);
     if (e != cudaSuccess) {
         std::snprintf(msg, sizeof msg, "zero_step_stage2_noalloc: cudaGetSymbolAddress of the static scratch: %s",
                       cudaGetErrorString(e));
