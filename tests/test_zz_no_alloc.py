@@ -5,11 +5,13 @@ Its scratch comes from a static array inside the library, so the caller
 passes no workspace and no reduced-gradient buffer.
 
 The GPU test runs the new entry point and the regular zero_step_stage2 on
-identical inputs, several calls in a row, and requires identical results
-(the same bar as the parity tests: bit-exact 16-bit parameters and flags,
-fp32 state within 1e-6 relative -- here bit-identical, since both run the
-same kernels).  The file is collected last so that a run stopping at the
-first failure has already run every other test.
+identical inputs, several calls in a row (clean and overflowed steps, with
+and without clipping), and requires identical results; every call is also
+compared with the CPU oracle's unpartitioned step on the same inputs, at
+the parity tests' bar (bit-exact 16-bit parameters, flag, norm, clip
+coefficient and loss scale; the fp32 state here bit-identical too).  The
+file is collected last so that a run stopping at the first failure has
+already run every other test.
 """
 import ctypes
 
@@ -76,6 +78,9 @@ def test_noalloc_matches_regular_step(max_norm):
         ra = zg.zero_step_stage2(ref.cfg, ref.plan, ref.bufs, ref.adam, ref.state, s)
         rb = zg.zero_step_stage2_noalloc(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
         torch.cuda.synchronize()
+        # against the oracle: the job's reduced-gradient buffer is not used
+        # (that scratch is the library's static array), everything else is
+        job.check(rb, job.oracle_step(grads), reduced=False)
         assert (rb.overflow, rb.skipped, rb.t, rb.path) == (ra.overflow, ra.skipped, ra.t, ra.path)
         assert rb.overflow == (1 if inject else 0)
         assert rb.new_loss_scale == ra.new_loss_scale
