@@ -1,22 +1,31 @@
 """Benchmark: ZeRO sharded mixed-precision Adam step on GB300.
 
-Workload (default): the parameter list of a 12-layer d=768 transformer
-(embedding 50257 x 768, per layer 4 d^2 attention + 8 d^2 MLP + 4 d
-LayerNorm vectors: 123,568,896 parameters), N_d = 8 simulated data-parallel
-ranks, ZeRO stage 2, gradient bucket 2^24 elements, fp16 gradients
-N(0, 1e-3), loss scale 1, Adam (lr 1e-4, betas 0.9/0.999, eps 1e-8).  A
-step is one pass of the whole hot path: every bucket's fused
-reduce-scatter + overflow check + unscale + Adam + cast + all-gather kernel,
-then the flag read and commit.  Stages 0 and 1 on the same workload are
-timed after the headline and reported under "stages".
+Workload (default, the largest single-GPU configuration): ZeRO stage 3 on
+the parameter list of a 32-layer d=4096 transformer (embedding 50257 x
+4096, per layer 4 d^2 attention + 8 d^2 MLP + 4 d LayerNorm vectors:
+6,648,827,904 parameters), N_d = 64 simulated data-parallel ranks, bucket
+2^24 elements, fp16 gradients N(0, 1e-3) x 1024 (static loss scale 1024),
+Adam (lr 1e-4, betas 0.9/0.999, eps 1e-8).  A step is one pass of the whole
+hot path: every layer gathered from the 64 owners' shards into 64
+constant-size buffers for the forward pass, and again, in reverse order,
+for the backward pass, where each bucket's 64 gradient copies are
+reduce-scattered, checked, unscaled, applied by Adam to the owned fp32
+shard and cast back into the owner's 16-bit shard; then the commit.  Each
+bucket's gradients come from a ring of pre-generated gradient sets in HBM
+(generation is not part of the step).  Also reported, each with its own
+roofline: the stage-2 step on a 12-layer d=768 list (N_d = 8) and the
+clipped stage-2 steps at 2^31 parameters (N_d = 2 and 32, bf16).
 
 Output: one JSON line (rank 0).  `value` is parameters updated per second
 over all GPUs with inputs resident in HBM; `e2e` is the same through the C
-ABI with gradients arriving from pinned host memory every step; `roofline`
-is the fused kernel's algorithmic bytes per launch over its CUDA-event
-duration against the measured HBM copy bandwidth.
+ABI with every bucket's gradients copied in from pinned host memory inside
+the timed region; `roofline` is the dominant kernel's (the layer gather's)
+algorithmic bytes per launch over its CUDA-event duration against the
+measured HBM copy bandwidth, with the other kernel and the whole step
+beside it.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py --config K          the other workloads (bench_workloads.py)
 
 With --gpus N > 1 (under torchrun) each rank runs an independent replica of
 the job on its own GPU: the simulated ranks live inside one GPU, so there is
@@ -49,10 +58,20 @@ SIGMA = 1e-3
 ADAM = dict(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8)
 GRAD_RING = 10          # distinct per-step gradient sets ("10 steps, fresh seeds per step")
 FALLBACK_HBM_GBS = 6800.0
+# GB300's nominal HBM3e bandwidth: NVIDIA's GB300 NVL72 specification gives
+# 576 TB/s over its 72 GPUs, 8 TB/s per GPU.  Reported beside the fraction of
+# the measured copy bandwidth, which is the roofline's denominator.
+CHIP_HBM_GBS = 8000.0
+CHIP_HBM_SOURCE = "NVIDIA GB300 NVL72 specification: 576 TB/s HBM3e over 72 GPUs = 8 TB/s per GPU (nominal)"
 KERNEL_SOURCES = ["zero_sharded_mixed_bucket_gb300/csrc/k_fused.cu",
                   "zero_sharded_mixed_bucket_gb300/csrc/dev_common.cuh",
                   "zero_sharded_mixed_bucket_gb300/csrc/zero_internal.h"]
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "k_fused_stage2_fp16_n8.md")
+GATHER_SOURCES = ["zero_sharded_mixed_bucket_gb300/csrc/k_gather.cu",
+                  "zero_sharded_mixed_bucket_gb300/csrc/dev_common.cuh",
+                  "zero_sharded_mixed_bucket_gb300/csrc/zero_internal.h"]
+GATHER_SUMMARY = os.path.join(ROOT, "profiles", "k_gather_stage3_n64.md")
+S3_LAYERS, S3_D, S3_RANKS, S3_SCALE = 32, 4096, 64, 1024.0
 
 
 def bytes_per_param(stage, n=N_RANKS, sb=12, e=2):
@@ -72,6 +91,10 @@ def layer_sizes(vocab=VOCAB, d=D_MODEL, layers=N_LAYERS):
 
 
 N_PARAMS = sum(layer_sizes())
+S3_N_PARAMS = sum(layer_sizes(VOCAB, S3_D, S3_LAYERS))
+S3_WORKLOAD = ("ZeRO stage 3, 32-layer d=4096 transformer parameter list (%d params), N_d=64 simulated ranks, "
+               "bucket 2^24 elements, two all-gathers per layer into 64 constant-size buffers, fp16 gradients "
+               "N(0,1e-3) x 1024 static loss scale, Adam" % S3_N_PARAMS)
 WORKLOAD = ("12-layer d=768 transformer parameter list (%d params), N_d=%d simulated ranks, ZeRO stage %d, "
             "bucket 2^24 elements, fp16 gradients N(0,1e-3), Adam" % (N_PARAMS, N_RANKS, STAGE))
 
@@ -79,9 +102,11 @@ WORKLOAD = ("12-layer d=768 transformer parameter list (%d params), N_d=%d simul
 # ---------------------------------------------------------------------------
 # helpers
 # ---------------------------------------------------------------------------
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
+    """First 16 hex digits of the SHA-256 of a kernel's source files: an ncu
+    summary records it, and its counters are used only while it matches."""
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -97,18 +122,32 @@ def measured_peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic():
-    """dram bytes per launch of the fused kernel from the committed ncu
-    summary, if it was taken on the current kernel source (else None)."""
+def profiled_value(key, summary=PROFILE_SUMMARY, sources=None):
+    """A number recorded as `key: value` in a committed ncu summary, if the
+    summary's kernel_source_hash matches the current kernel source (counters
+    taken on other code do not count); else None."""
     try:
-        text = open(PROFILE_SUMMARY, encoding="utf-8").read()
+        text = open(summary, encoding="utf-8").read()
     except OSError:
         return None
     m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
-    m_bytes = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    m_val = re.search(re.escape(key) + r":\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_val or m_hash.group(1) != kernel_source_hash(sources):
         return None
-    return float(m_bytes.group(1))
+    return float(m_val.group(1))
+
+
+def profiled_traffic():
+    """dram bytes per full-bucket launch of the stage-2 fused kernel from its
+    committed ncu summary (None when it was taken on other code)."""
+    return profiled_value("dram_bytes_per_full_launch")
+
+
+def traffic_source(summary, sources):
+    return {"summary": os.path.relpath(summary, ROOT), "kernel_source_hash": kernel_source_hash(sources),
+            "note": "dram__bytes_read.sum + dram__bytes_write.sum of one ncu capture of a smaller launch, scaled "
+                    "to the average launch by its elements; writes read below the algorithmic count when dirty "
+                    "L2 lines are written back after the captured kernel ends"}
 
 
 class ClockSampler:
@@ -176,27 +215,28 @@ def clocks_summary(rows, t0, t1):
 # ---------------------------------------------------------------------------
 # CPU oracle legs
 # ---------------------------------------------------------------------------
-def oracle_sample_step(n_sample, seed_step):
+def oracle_sample_step(n_sample, seed_step, ranks=S3_RANKS, scale=S3_SCALE):
+    """Inputs of the oracle on the first n_sample parameters: every rank's
+    fp16 gradients N(0, 1e-3) x scale, master weights N(0, 0.02), m = v = 0."""
     import numpy as np
 
-    import oracle
     import synth
-    grads = [synth.host_normal16(n_sample, synth.FP16, SIGMA, seed=0, stream=synth.STREAM_GRAD, step=seed_step,
-                                 rank=r) for r in range(N_RANKS)]
+    grads = [synth.host_normal16(n_sample, synth.FP16, SIGMA * scale, seed=0, stream=synth.STREAM_GRAD,
+                                 step=seed_step, rank=r) for r in range(ranks)]
     w = synth.host_normal32(n_sample, 0.02, seed=0, stream=synth.STREAM_WEIGHT)
     m = np.zeros(n_sample, np.float32)
     v = np.zeros(n_sample, np.float32)
     return grads, w, m, v
 
 
-def run_oracle_steps(n_sample, steps, warmup):
+def run_oracle_steps(n_sample, steps, warmup, ranks=S3_RANKS, scale=S3_SCALE):
     import oracle
-    grads, w, m, v = oracle_sample_step(n_sample, 1)
+    grads, w, m, v = oracle_sample_step(n_sample, 1, ranks, scale)
     t = 0
     times = []
     for k in range(warmup + steps):
         t0 = time.perf_counter()
-        r = oracle.step(grads, w, m, v, dtype=oracle.FP16, t=t, loss_scale=1.0, **ADAM)
+        r = oracle.step(grads, w, m, v, dtype=oracle.FP16, t=t, loss_scale=scale, **ADAM)
         dt = time.perf_counter() - t0
         t = r["t"]
         if k >= warmup:
@@ -204,12 +244,19 @@ def run_oracle_steps(n_sample, steps, warmup):
     return times
 
 
-def cpu_baseline(n_sample=1 << 26, steps=2):
-    times = run_oracle_steps(n_sample, steps, 0)
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+def cpu_baseline(n_sample=1 << 21, steps=3, ranks=S3_RANKS, scale=S3_SCALE):
+    """The oracle as it is (single-threaded C: one of the host's cores) on
+    the first n_sample parameters of the workload."""
+    times = run_oracle_steps(n_sample, steps, 0, ranks, scale)
     sec = sum(times) / len(times)
-    return {"value": n_sample / sec / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "%d contiguous parameters of the workload, N_d=%d ranks, %d steps, single-threaded C oracle "
-                      "(unpartitioned step; stage 2 computes the same numbers)" % (n_sample, N_RANKS, steps),
+    return {"value": n_sample / sec / 1e9, "unit": UNIT, "cores": 1, "host_cores": host_cores(), "kind": "oracle",
+            "sample": "%d contiguous parameters of the workload, N_d=%d ranks, loss scale %g, %d steps, "
+                      "single-threaded C oracle (the unpartitioned step: every stage computes the same numbers; "
+                      "the stage-3 gathers are copies of its 16-bit result)" % (n_sample, ranks, scale, steps),
             "seconds": sum(times)}
 
 
@@ -217,18 +264,18 @@ def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    n_sample = 1 << 22
+    n_sample = 1 << 19
     times = run_oracle_steps(n_sample, args.steps, args.warmup)
     sec = sum(times) / len(times)
     value = n_sample / sec / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "n_params": N_PARAMS, "n_ranks": N_RANKS, "stage": STAGE,
+            "config": {"workload": S3_WORKLOAD, "n_params": S3_N_PARAMS, "n_ranks": S3_RANKS, "stage": 3,
                        "bucket_elems": BUCKET, "sample_params": n_sample},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": "%d parameters of the workload per step, N_d=%d, single-threaded C oracle"
-                                       % (n_sample, N_RANKS)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "host_cores": host_cores(), "kind": "oracle",
+                             "sample": "%d parameters of the workload per step, N_d=%d, loss scale %g, "
+                                       "single-threaded C oracle" % (n_sample, S3_RANKS, S3_SCALE)},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -645,7 +692,7 @@ def gpu_arm(args):
                 torch.cuda.empty_cache()
             out["stages"] = stages
             if world == 1:
-                out["cpu_baseline"] = cpu_baseline()
+                out["cpu_baseline"] = cpu_baseline(1 << 26, 2, N_RANKS, 1.0)
             print(json.dumps(out))
         barrier(world)
     if world > 1:
@@ -654,10 +701,247 @@ def gpu_arm(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# the default line: the stage-3 step at 6.65B parameters
+# ---------------------------------------------------------------------------
+def stage3_e2e(job, steps, warmup, device, world=1):
+    """The stage-3 step through the C ABI with each bucket's 64 gradient
+    copies arriving from pinned host memory inside the timed region: two
+    pinned host sets of N_d x 2^24 values, one cudaMemcpyAsync per bucket
+    on a copy stream into one of two device sets, double-buffered (a set is
+    refilled once the bucket kernel that read it has run), and the step's
+    result read back by the host (zero_dev_state_read, 64 bytes) after every
+    step."""
+    import torch
+    zg = job.zg
+    assert len(job.ring) >= 2
+    host = [torch.empty(job.N * job.B, dtype=torch.int16).pin_memory() for _ in range(2)]
+    for k in range(2):
+        host[k].copy_(job.ring[k])
+    copy_stream = torch.cuda.Stream(device)
+    free = [None, None]            # per device set: event after the bucket kernel that last read it
+
+    def before(b):
+        k = b % 2
+        with torch.cuda.stream(copy_stream):
+            if free[k] is not None:
+                copy_stream.wait_event(free[k])
+            job.ring[k].copy_(host[k], non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(copy_stream)
+        job.stream.wait_event(e)
+
+    def after(b):
+        e = torch.cuda.Event()
+        e.record(job.stream)
+        free[b % 2] = e
+
+    def one():
+        job.step(grad_ptrs=lambda b: job.ring_ptrs[b % 2], before_bucket=before, after_bucket=after)
+        st, last = zg.zero_dev_state_read(job.dev_state, job.stream)       # the step's result, to the host
+        assert last.overflow == 0
+        return st
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(job.stream)
+    copy_stream.wait_event(start)
+    for _ in range(steps):
+        one()
+    end.record(job.stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(end) / steps, world)
+    barrier(world)
+    nb = job.plan.n_buckets
+    h2d = nb * job.N * job.B * 2
+    return dict(value=world * job.n / (ms * 1e-3) / 1e9, unit=UNIT, h2d_bytes_per_step=world * h2d,
+                d2h_bytes_per_step=world * zg.DEV_STATE_BYTES, ms_per_step=ms, steps=steps, warmup=warmup,
+                host_link_gbs_per_gpu=h2d / (ms * 1e-3) / 1e9,
+                note="every bucket's 64 gradient copies (64 x 2^24 fp16 values, one 2.1 GB cudaMemcpyAsync) copied "
+                     "from pinned host memory on a second stream, double-buffered against the bucket kernels; the "
+                     "step's result block read back after every step; the host link sets the pace")
+
+
+def stage3_arm(args):
+    import torch
+    world, rank, local = dist_setup(args)
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()      # one builder: concurrent builds would write the same object files
+    barrier(world)
+    import bench_workloads as bw
+    import zero_sharded_mixed_bucket_gb300 as zg
+    job = bw.Stage3Job(device, ring=args.ring3, n_layers=args.s3_layers, d=args.s3_d)
+    n = job.n
+    for _ in range(args.warmup):
+        job.step()
+    nsched = len(job.schedule)
+    prof = {k: [torch.cuda.Event(enable_timing=True) for _ in range(nsched + 1)]
+            for k in range(0, args.steps, PROFILE_EVERY)}
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(job.stream)
+    for k in range(args.steps):
+        job.step(events=prof.get(k))
+    end.record(job.stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    rows = sampler.stop()
+    st, last = zg.zero_dev_state_read(job.dev_state, job.stream)
+    assert st.t == args.warmup + args.steps and last.overflow == 0, "a step overflowed"
+    ms = start.elapsed_time(end)
+    ms_per_step, value = aggregate(ms, n, args.steps, world)
+    peak, peak_kind = measured_peak_hbm()
+    # per-kernel durations from the profiled steps' events
+    g_ms = b_ms = 0.0
+    for evs in prof.values():
+        g, b = job.kernel_times(evs)
+        g_ms += g
+        b_ms += b
+    n_prof = len(prof)
+    n_gathers = sum(1 for kind, _ in job.schedule if kind == "gather")
+    g_bytes = n_prof * 2 * n * (2 + 2 * job.N)
+    f_bytes = n_prof * n * bench_bytes(3, job.N)
+    g_launch = g_bytes / (n_prof * n_gathers)
+    g_ach = g_bytes / (g_ms * 1e-3) / 1e9
+    f_ach = f_bytes / (b_ms * 1e-3) / 1e9
+    step_bytes = n * job.bytes_per_param()
+    g_units = profiled_value("dram_bytes_per_gathered_element", GATHER_SUMMARY, GATHER_SOURCES)
+    g_traffic = None if g_units is None else g_units * (2 * n / n_gathers)
+    layers = "%d-layer d=%d" % (args.s3_layers, args.s3_d)
+    workload = S3_WORKLOAD if (args.s3_layers, args.s3_d) == (S3_LAYERS, S3_D) else \
+        S3_WORKLOAD.replace("32-layer d=4096", layers).replace("(%d params)" % S3_N_PARAMS, "(%d params)" % n)
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "io_dtype": "fp16", "data": "synthetic",
+        "config": {"workload": workload, "n_params": n, "n_ranks": job.N, "stage": 3, "bucket_elems": job.B,
+                   "n_layers": len(job.layers), "gather_capacity_elems": job.plan.max_layer_elems,
+                   "loss_scale": job.S, "parallelism": "replicas only (simulated ranks inside each GPU)",
+                   "gradients": "each bucket's %d gradient copies read from a ring of %d pre-generated bucket-sized "
+                                "gradient sets in HBM (bucket b reads set b mod %d; %.1f GB); generated before the "
+                                "timed region, so no generation is inside a step" % (
+                                    job.N, len(job.ring), len(job.ring), len(job.ring) * job.N * job.B * 2 / 1e9),
+                   "l2": "inputs larger than L2: %.0f GB moved per step; each gradient set 2.1 GB"
+                         % (step_bytes / 1e9)},
+        "hbm_gbs_step": step_bytes / (ms_per_step * 1e-3) / 1e9,
+        "step_roofline": {"bytes_per_param": job.bytes_per_param(), "bytes_per_step": step_bytes,
+                          "achieved": step_bytes / (ms_per_step * 1e-3) / 1e9, "peak": peak,
+                          "frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / peak,
+                          "frac_of_chip_nominal": step_bytes / (ms_per_step * 1e-3) / 1e9 / CHIP_HBM_GBS},
+        "roofline": {"bound": "hbm", "kernel": "k_gather (stage-3 layer all-gather, 64 destinations)",
+                     "achieved": g_ach, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": g_ach / peak,
+                     "traffic": g_traffic,
+                     "traffic_source": traffic_source(GATHER_SUMMARY, GATHER_SOURCES) if g_traffic else None,
+                     "algorithmic_bytes_per_launch": g_launch, "bytes_per_element": 2 + 2 * job.N,
+                     "launches": n_prof * n_gathers, "avg_launch_ms": g_ms / (n_prof * n_gathers),
+                     "share_of_step_bytes": 2 * (2 + 2 * job.N) / job.bytes_per_param(),
+                     "frac_of_chip_nominal": g_ach / CHIP_HBM_GBS, "chip_nominal_gbs": CHIP_HBM_GBS,
+                     "chip_nominal_source": CHIP_HBM_SOURCE,
+                     "timing": "CUDA events recorded on the step's stream between consecutive launches on every "
+                               "%dth timed step (%d of %d); each interval holds one kernel" % (
+                                   PROFILE_EVERY, n_prof, args.steps)},
+        "kernels": {"k_fused<stage 3, fp16, adam>": {
+            "achieved": f_ach, "frac": f_ach / peak, "bytes_per_param": bench_bytes(3, job.N),
+            "launches": n_prof * job.plan.n_buckets, "avg_launch_ms": b_ms / (n_prof * job.plan.n_buckets),
+            "algorithmic_bytes_per_launch": f_bytes / (n_prof * job.plan.n_buckets)}},
+        "gpu_launches": args.steps * job.launches_per_step(),
+        "step_api": "zero_step_begin_async / zero_gather_layer / zero_step_bucket_async / zero_step_end_async "
+                    "(step state in device memory, steps enqueued back to back)",
+    }
+    out["clocks"] = clocks_summary(rows, t0, t1)
+    if args.headline_only:
+        if rank == 0:
+            print(json.dumps(out))
+        return _finish(world)
+    # end to end on every rank at once: each GPU has its own host link
+    try:
+        out["e2e"] = stage3_e2e(job, args.e2e_steps, 1, device, world)
+    except Exception as e:         # reported, never hides the headline
+        if world > 1:
+            raise
+        out["e2e"] = {"error": repr(e)}
+    del job
+    torch.cuda.empty_cache()
+    if rank == 0:
+        out["legs"] = other_legs(args, device)
+        if world == 1:
+            out["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(out))
+    barrier(world)
+    return _finish(world)
+
+
+def bench_bytes(stage, n_ranks):
+    return bytes_per_param(stage, n_ranks)
+
+
+def _finish(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def other_legs(args, device):
+    """The stage-2 step on the 12-layer d=768 list (N_d = 8) and the clipped
+    stage-2 steps at 2^31 parameters (N_d = 2 and 32, bf16), each with its
+    own roofline; reported beside the headline, never hiding it."""
+    import torch
+
+    import bench_workloads as bw
+    legs = {}
+    try:
+        job = GpuJob(2, device, ring=GRAD_RING)
+        k = max(10, args.steps)
+        ms, launches, kernel, _ = timed_steps(job, k, args.warmup, 1, api="async")
+        peak, kind = measured_peak_hbm()
+        ach = kernel["bytes"] / (kernel["total_ms"] * 1e-3) / 1e9
+        tr = profiled_traffic()
+        legs["workload2_stage2"] = {
+            "workload": WORKLOAD, "n_params": N_PARAMS, "steps": k, "ms_per_step": ms / k,
+            "value": N_PARAMS / (ms / k * 1e-3) / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "k_fused<stage 2, fp16, adam>", "achieved": ach, "peak": peak,
+                         "peak_kind": kind, "unit": "GB/s", "frac": ach / peak,
+                         "traffic": None if tr is None else tr * (N_PARAMS / job.plan.n_buckets) / (1 << 24),
+                         "traffic_source": traffic_source(PROFILE_SUMMARY, KERNEL_SOURCES) if tr else None,
+                         "bytes_per_param": bytes_per_param(2), "launches": kernel["launches"],
+                         "avg_launch_ms": kernel["total_ms"] / kernel["launches"],
+                         "timing": "library-recorded events around a step's bucket kernels (kernel span) on every "
+                                   "%dth step" % PROFILE_EVERY}}
+        del job
+    except Exception as e:
+        legs["workload2_stage2"] = {"error": repr(e)}
+    torch.cuda.empty_cache()
+    peak, kind = measured_peak_hbm()
+    for n_ranks, dt in ((2, "bf16"), (32, "bf16")):
+        name = "clip_2p31_n%d_%s" % (n_ranks, dt)
+        try:
+            r = bw.sweep_point(1 << 31, n_ranks, dt, max(2, min(args.steps, 4)), 1)
+            r["roofline"] = {"bound": "hbm", "kernel": "k_reduce + k_finalize + k_update (two-pass, clipping)",
+                             "achieved": r["hbm_gbs"], "peak": peak, "peak_kind": kind, "unit": "GB/s",
+                             "frac": r["hbm_gbs"] / peak, "traffic": None,
+                             "timing": "whole clipped step (CUDA events); generation of staged gradients "
+                                       "subtracted where gradients are staged"}
+            legs[name] = r
+        except Exception as e:
+            legs[name] = {"error": repr(e)}
+        torch.cuda.empty_cache()
+    return legs
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--n-params", type=int, default=None,
@@ -665,9 +949,22 @@ def main():
                          "e.g. for profiling captures)")
     ap.add_argument("--ring", type=int, default=GRAD_RING, help="distinct per-step gradient sets kept in HBM")
     ap.add_argument("--bucket", type=int, default=BUCKET, help="gradient bucket size in elements")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7],
-                    help="workload: 2 (default) the headline; 1, 3, 4, 5 the others, 6 the optimizer state in host "
-                         "memory, 7 the P_a activation-checkpoint partition and all-gather (bench_workloads.py)")
+    ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5, 6, 7, 8],
+                    help="workload: 4 (default) the stage-3 step at 6.65B parameters; 2 the stage-2 step on the "
+                         "12-layer d=768 list (the options --stage, --optimizer, --dtype, --step-api, --n-params "
+                         "apply to it); 1, 3, 5 the others, 6 the optimizer state in host memory, 7 the P_a "
+                         "activation-checkpoint partition and all-gather, 8 stage-3 layer gathers alone "
+                         "(bench_workloads.py)")
+    ap.add_argument("--ring3", type=int, default=4, help="--config 4: pre-generated bucket gradient sets in HBM")
+    ap.add_argument("--s3-layers", type=int, default=S3_LAYERS, help="--config 4: transformer layers")
+    ap.add_argument("--s3-d", type=int, default=S3_D, help="--config 4: model width d")
+    ap.add_argument("--e2e-steps", type=int, default=2, help="--config 4: timed steps of the end-to-end leg")
+    ap.add_argument("--with-generation", action="store_true",
+                    help="--config 4: instead, the step with each bucket's gradients generated into a staging "
+                         "area right before its kernel (generation timed and subtracted), and the prefetching "
+                         "fetcher run")
+    ap.add_argument("--layer-elems", type=int, default=1 << 24, help="--config 8: elements per layer")
+    ap.add_argument("--n-layers", type=int, default=2, help="--config 8: layers")
     ap.add_argument("--ranks", type=int, default=None, help="--config 5: N_d of a single sweep point")
     ap.add_argument("--optimizer", default="adam", choices=sorted(OPTIMIZERS),
                     help="optimizer of the headline step (with --headline-only)")
@@ -678,19 +975,21 @@ def main():
                     help="entry point of the timed steps: zero_step_async (default) or the synchronising "
                          "zero_step_stage2")
     ap.add_argument("--headline-only", action="store_true",
-                    help="time the stage-2 step only (no stage 0/1, end-to-end or CPU legs)")
+                    help="time the workload's step only (no other legs, end-to-end or CPU legs)")
     ap.add_argument("--stage", type=int, default=2, choices=[0, 1, 2, 3],
                     help="ZeRO stage of the timed step (other than 2: with --headline-only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
-    if args.stage != 2 and not args.headline_only:
-        ap.error("--stage other than 2 needs --headline-only")
+    if args.stage != 2 and not (args.headline_only and args.config == 2):
+        ap.error("--stage other than 2 needs --config 2 --headline-only")
     if args.stage in (0, 1) and args.ring < args.steps + args.warmup:
         ap.error("stages 0 and 1 write the all-reduced gradient back into every rank's buffer: give each step "
                  "a gradient set of its own (--ring >= steps + warmup)")
     if args.impl == "reference":
         return reference_arm(args)
+    if args.config == 4 and not args.with_generation:
+        return stage3_arm(args)
     if args.config != 2:
         import torch
 

@@ -85,6 +85,121 @@ class StagedGrads:
 
 
 # ---------------------------------------------------------------------------
+class Stage3Job:
+    """ZeRO stage 3 on a transformer parameter list (default: 32 layers,
+    d = 4096, 6,648,827,904 parameters), N_d = 64 simulated ranks, bucket
+    2^24, fp16 gradients N(0, 1e-3) x 1024 (static loss scale 1024), Adam,
+    step state in device memory.
+
+    One step, as a stage-3 data-parallel step runs it: the forward pass
+    gathers every layer's 16-bit parameters from the owners' shards into 64
+    constant-size buffers (one per rank, each the size of the largest
+    layer); the backward pass, in reverse layer order, gathers the layer
+    again, then reduces, updates and writes back to the owners' shards every
+    bucket whose lowest element lies in that layer.  Each bucket's 64
+    gradient copies come from a ring of `ring` bucket-sized gradient sets
+    generated in HBM when the job is built (bucket b reads set b mod ring):
+    no input is generated inside a step, and every set (N_d x 2^24 x 2 B =
+    2.1 GB) is far larger than L2.  Set k holds the generator's gradients of
+    step k+1 at offsets 0..2^24 of each rank's stream."""
+
+    def __init__(self, device, ring=4, n_layers=32, d=4096, vocab=50257, ranks=64, bucket=1 << 24, scale=1024.0):
+        import torch
+
+        import synth
+        import zero_sharded_mixed_bucket_gb300 as zg
+        self.zg, self.torch = zg, torch
+        self.layers = transformer_layers(vocab, d, n_layers)
+        self.n = sum(self.layers)
+        self.N, self.B, self.S = ranks, bucket, scale
+        self.cfg = zg.Config(self.n, ranks, 3, bucket, 0, self.layers)
+        self.plan = zg.zero_plan(self.cfg)
+        self.bufs = zg.DeviceBuffers(self.cfg, self.plan, device=device, grads=False, reduced=False)
+        self.stream = torch.cuda.current_stream(device)
+        s = self.stream.cuda_stream
+        synth.dev_normal32(self.bufs.w[0].data_ptr(), self.n, 0.02, seed=0, stream=synth.STREAM_WEIGHT, cuda_stream=s)
+        self.ring = [torch.empty(ranks * bucket, dtype=torch.int16, device=device) for _ in range(ring)]
+        for k, t in enumerate(self.ring):
+            for r in range(ranks):
+                synth.dev_normal16(t.data_ptr() + 2 * r * bucket, bucket, synth.FP16, bench.SIGMA * scale, seed=0,
+                                   stream=synth.STREAM_GRAD, step=k + 1, rank=r, cuda_stream=s)
+        self.ring_ptrs = [zg.ptr_array([t.data_ptr() + 2 * r * bucket for r in range(ranks)]) for t in self.ring]
+        self.dst = [torch.empty(self.plan.max_layer_elems, dtype=torch.int16, device=device) for _ in range(ranks)]
+        self.dst_ptrs = zg.ptr_array([t.data_ptr() for t in self.dst])
+        self.shard_ptrs = zg.ptr_array([t.data_ptr() for t in self.bufs.params16])
+        self.adam = zg.zero_adam_t(max_grad_norm=0.0, **ADAM)
+        self.state = zg.zero_state_t(t=0, loss_scale=scale, min_loss_scale=1.0)
+        self.dev_state = torch.zeros(zg.DEV_STATE_BYTES // 8, dtype=torch.int64, device=device)
+        zg.zero_dev_state_init(self.dev_state, self.adam, self.state, self.stream)
+        starts = [0]
+        for ln in self.layers:
+            starts.append(starts[-1] + ln)
+        self.starts = starts
+        # the step's launches in order: forward gathers, then per layer
+        # (reversed) its gather and the buckets that start inside it
+        sched = [("gather", l) for l in range(len(self.layers))]
+        nxt = self.plan.n_buckets - 1
+        for l in reversed(range(len(self.layers))):
+            sched.append(("gather", l))
+            while nxt >= 0 and nxt * bucket >= starts[l]:
+                sched.append(("bucket", nxt))
+                nxt -= 1
+        assert nxt == -1
+        self.schedule = sched
+        torch.cuda.synchronize(device)
+
+    def bucket_len(self, b):
+        lo = b * self.B
+        return min(lo + self.B, self.n) - lo
+
+    def bytes_per_param(self):
+        """Algorithmic HBM bytes per parameter of one step: two gathers (the
+        shard read once, 64 destinations written: 2 + 2 N_d each) and the
+        fused stage-3 update (N_d gradient reads, 12 B of state read and
+        written, the owner's 16-bit parameter written: 2 N_d + 24 + 2)."""
+        return 2 * (2 + 2 * self.N) + bench.bytes_per_param(3, self.N)
+
+    def launches_per_step(self):
+        return 2 + len(self.schedule)      # prepare, gathers and buckets, restore/commit
+
+    def step(self, events=None, grad_ptrs=None, before_bucket=None, after_bucket=None):
+        """Enqueue one step on the job's stream; never synchronises.
+        events: None, or len(schedule)+1 CUDA events recorded between the
+        launches (event k before schedule entry k).  grad_ptrs(b): the 64
+        gradient pointers of bucket b (default: ring set b mod ring);
+        before_bucket(b) / after_bucket(b): stream hooks around bucket b's
+        kernel (end-to-end copies)."""
+        zg, s = self.zg, self.stream
+        zg.zero_step_begin_async(self.cfg, self.plan, self.bufs, self.adam, self.dev_state, s)
+        for k, (kind, x) in enumerate(self.schedule):
+            if events is not None:
+                events[k].record(s)
+            if kind == "gather":
+                zg.zero_gather_layer(self.cfg, self.plan, x, self.shard_ptrs, self.dst_ptrs, s)
+            else:
+                if before_bucket:
+                    before_bucket(x)
+                ptrs = grad_ptrs(x) if grad_ptrs else self.ring_ptrs[x % len(self.ring_ptrs)]
+                zg.zero_step_bucket_async(self.cfg, self.plan, self.bufs, self.adam, x, ptrs, s)
+                if after_bucket:
+                    after_bucket(x)
+        if events is not None:
+            events[len(self.schedule)].record(s)
+        zg.zero_step_end_async(self.cfg, self.plan, self.bufs, self.adam, self.dev_state, s)
+
+    def kernel_times(self, events):
+        """(gather ms, bucket ms) of one profiled step from its events."""
+        g = b = 0.0
+        for k, (kind, _) in enumerate(self.schedule):
+            ms = events[k].elapsed_time(events[k + 1])
+            if kind == "gather":
+                g += ms
+            else:
+                b += ms
+        return g, b
+
+
+# ---------------------------------------------------------------------------
 def leg_cfg1(args):
     import torch
 
@@ -538,4 +653,53 @@ def leg_pa(args):
     return out
 
 
-LEGS = {1: leg_cfg1, 3: leg_cfg3, 4: leg_cfg4, 5: leg_cfg5, 6: leg_offload, 7: leg_pa}
+# ---------------------------------------------------------------------------
+def leg_gather(args):
+    """Stage-3 layer gathers alone: a model of --n-layers layers of
+    --layer-elems elements each, N_d = 64 owner shards, every call gathering
+    one layer (in turn) into 64 destination buffers.  The case the k_gather
+    ncu summary captures (small enough for a profiler: 2 x 2^24 elements
+    hold about 4.4 GB of device memory)."""
+    import torch
+
+    import zero_sharded_mixed_bucket_gb300 as zg
+    N, le, nl = 64, args.layer_elems, args.n_layers
+    layers = [le] * nl
+    n = le * nl
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.current_stream(dev)
+    cfg = zg.Config(n, N, 3, 1 << 24, 0, layers)
+    plan = zg.zero_plan(cfg)
+    P = plan.shard_elems
+    flat = torch.randint(-2 ** 15, 2 ** 15, (N * P,), dtype=torch.int16, device=dev)
+    shards = [flat[r * P:(r + 1) * P] for r in range(N)]
+    dst = [torch.empty(plan.max_layer_elems, dtype=torch.int16, device=dev) for _ in range(N)]
+    sp = zg.ptr_array([t.data_ptr() for t in shards])
+    dp = zg.ptr_array([t.data_ptr() for t in dst])
+    steps = max(1, args.steps)
+    times = []
+    for k in range(args.warmup + steps):
+        e0, e1 = _ev(), _ev()
+        e0.record(s)
+        zg.zero_gather_layer(cfg, plan, k % nl, sp, dp, s)
+        e1.record(s)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    last = (args.warmup + steps - 1) % nl
+    assert torch.equal(dst[N - 1][:le], flat[last * le:(last + 1) * le])
+    assert torch.equal(dst[0][:le], flat[last * le:(last + 1) * le])
+    ms = sum(times) / steps
+    bpe = 2 + 2 * N
+    out = _base(le / (ms * 1e-3) / 1e9, ms, steps, args.warmup,
+                "stage-3 layer gather alone: %d layers of %d elements, N_d=64 owner shards, 64 destination buffers"
+                % (nl, le), {"n_params": n, "n_ranks": N, "stage": 3, "layer_elems": le}, dtype="u16")
+    out["unit"] = "Gelements/s"
+    out["metric"] = "stage-3 layer gather: elements gathered per second into all 64 destinations"
+    out["roofline"] = _roofline(le * bpe, ms, "k_gather (tiles + bulk copies, 64 destinations)")
+    out["bytes_per_element"] = bpe
+    out["l2"] = "each call writes %.1f GB: far larger than L2" % (le * 2 * N / 1e9)
+    return out
+
+
+LEGS = {1: leg_cfg1, 3: leg_cfg3, 4: leg_cfg4, 5: leg_cfg5, 6: leg_offload, 7: leg_pa, 8: leg_gather}

@@ -54,19 +54,31 @@ def test_warmup_below_three_is_refused():
 
 @pytest.mark.gpu
 def test_gpu_arm_line():
-    d = _run(["--steps", "8", "--warmup", "3"], timeout=900)
-    _check_base(d, 8, 3)
+    """The default line: the stage-3 step at 6.65B parameters (about 210 GB
+    of device memory, in a child process), its legs, end to end and the CPU
+    baseline."""
+    import torch
+    torch.cuda.empty_cache()
+    d = _run(["--steps", "4", "--warmup", "3", "--e2e-steps", "1"], timeout=1200)
+    _check_base(d, 4, 3)
+    assert d["config"]["n_params"] == 6_648_827_904 and d["config"]["stage"] == 3
+    assert d["config"]["n_ranks"] == 64
     r = d["roofline"]
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] > 0
     assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
-    assert r["traffic"] is None or r["traffic"] > 0
+    assert r["traffic"] is None or (r["traffic"] > 0 and r["traffic_source"]["summary"])
+    assert 0.5 < r["share_of_step_bytes"] < 0.7
+    assert d["step_roofline"]["bytes_per_param"] == 414
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     cb = d["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["host_cores"] >= 1 and cb["value"] > 0
     c = d["clocks"]
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(c)
-    # 8 bucket kernels per step of the 123.6M-parameter list, plus the step's
-    # prepare and restore/commit kernels; profile events on steps 0 and 4
-    assert d["gpu_launches"] == 8 * (8 + 2)
-    assert r["launches"] == 2 * 8
+    # per step: prepare, 2 x 33 gathers, 397 bucket kernels, restore/commit
+    assert d["gpu_launches"] == 4 * (1 + 66 + 397 + 1)
+    assert r["launches"] == 1 * 66
+    legs = d["legs"]
+    for name in ("workload2_stage2", "clip_2p31_n2_bf16", "clip_2p31_n32_bf16"):
+        assert "error" not in legs[name], legs[name]
+        assert legs[name]["roofline"]["frac"] > 0

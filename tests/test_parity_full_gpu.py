@@ -6,7 +6,9 @@ recomputes from the host generator (plus properties that hold at any size).
     loss scale: an overflowed step (one inf per 1e9 gradient elements), then a
     clean one.
   * 32-layer d=4096 list (6,648,827,904 params), stage 3, N_d = 64, bucket
-    2^24, gradients staged per bucket, layer gathers.
+    2^24, gradients staged per bucket, layer gathers; and the same step as
+    the default benchmark runs it (gradients from the ring of pre-generated
+    sets, device-state protocol, two gathers per layer).
   * 2^31 flat params, N_d = 32, bf16, clipping path with c < 1, staged
     gradients; the exact norm over all 2^31 reduced values.
 """
@@ -146,6 +148,53 @@ def test_cfg4_stage3_staged_with_gathers():
         assert sel.any()
         for d in dst:
             assert np.array_equal(as_u16(_at(d, idx[sel] - starts[l])), ref["p16"][sel])
+
+
+def test_cfg4_as_the_benchmark_runs_it():
+    """The default benchmark's stage-3 step exactly as bench.py times it
+    (bench_workloads.Stage3Job: the device-state protocol, two gathers per
+    layer into 64 constant-size buffers, each bucket's 64 gradient copies
+    from the ring of pre-generated sets), two steps.  Sampled elements
+    against the oracle, which regenerates each sampled element's gradients
+    from the ring set its bucket reads; the 64 gather buffers hold layer 0
+    as gathered by the second step's backward pass, i.e. after step 1."""
+    import bench_workloads as bw
+    job = bw.Stage3Job(torch.device("cuda", 0), ring=4)
+    n, N, B, S = job.n, job.N, job.B, job.S
+    assert n == 6_648_827_904 and N == 64 and B == 1 << 24
+    for _ in range(2):
+        job.step()
+    st, last = zg.zero_dev_state_read(job.dev_state, job.stream)
+    assert st.t == 2 and last.overflow == 0 and last.skipped == 0
+    P = job.plan.shard_elems
+    idx = _samples(n, [0, n - 1, P - 1, P, 63 * P, B - 1, B, 3 * B, 4 * B - 1, job.starts[1], job.starts[1] - 1])
+    sets = (idx // B) % len(job.ring)
+    grads = []
+    for r in range(N):
+        g = np.empty(idx.size, np.uint16)
+        for k in range(len(job.ring)):
+            sel = sets == k
+            g[sel] = synth.host_normal16_at(idx[sel] % B, synth.FP16, 1e-3 * S, seed=0, stream=synth.STREAM_GRAD,
+                                            step=k + 1, rank=r)
+        grads.append(g)
+    w = synth.host_normal32_at(idx, 0.02, seed=0, stream=synth.STREAM_WEIGHT)
+    m, v = np.zeros_like(w), np.zeros_like(w)
+    ref1 = oracle.step(grads, w, m, v, dtype=oracle.FP16, t=0, loss_scale=S, **ADAM)
+    ref2 = oracle.step(grads, w, m, v, dtype=oracle.FP16, t=1, loss_scale=S, **ADAM)
+    assert ref1["overflow"] == 0 and ref2["overflow"] == 0 and ref2["t"] == 2
+    gw, gm, gv = job.bufs.state()
+    assert np.array_equal(as_u32(_at(gw, idx)), as_u32(w))
+    assert np.array_equal(as_u32(_at(gm, idx)), as_u32(m))
+    assert np.array_equal(as_u32(_at(gv, idx)), as_u32(v))
+    owners = idx // P
+    for o in np.unique(owners):
+        sel = owners == o
+        got = as_u16(_at(job.bufs.params16[int(o)], idx[sel] - o * P))
+        assert np.array_equal(got, ref2["p16"][sel]), int(o)
+    sel = idx < job.starts[1]
+    assert sel.sum() > 1000
+    for d in (0, 31, 63):
+        assert np.array_equal(as_u16(_at(job.dst[d], idx[sel])), ref1["p16"][sel]), d
 
 
 def test_sweep_2p31_n32_bf16_clip_path():

@@ -28,7 +28,7 @@ __all__ = [
     "DEV_STATE_BYTES", "zero_step_begin_async", "zero_step_bucket_async", "zero_step_end_async",
     "zero_pa_plan_t", "zero_pa_plan", "zero_pa_partition", "zero_pa_gather",
     "zero_step_begin", "zero_step_bucket", "zero_step_end", "zero_gather_layer", "zero_last_error",
-    "zero_version", "zero_set_profile_events", "zero_fetch_schedule", "Fetcher", "DeviceBuffers",
+    "zero_version", "zero_set_profile_events", "zero_fetch_schedule", "Fetcher", "DeviceBuffers", "ptr_array",
 ]
 
 ZERO_OK, ZERO_EINVAL, ZERO_EALIGN, ZERO_ENOMEM, ZERO_ECUDA, ZERO_ETIMEOUT, ZERO_EUNSUPPORTED = range(7)
@@ -345,8 +345,17 @@ def zero_step_begin(cfg, plan, bufs, adam, state, stream=None):
 
 
 def _ptr_array(ptrs):
+    """A host array of pointers: None, a ctypes array of c_void_p (passed as
+    it is, so callers can build one once and reuse it), or a sequence of ints."""
     if ptrs is None:
         return None
+    if isinstance(ptrs, ctypes.Array) and ptrs._type_ is c_vp:
+        return ptrs
+    return (c_vp * len(ptrs))(*[int(p) for p in ptrs])
+
+
+def ptr_array(ptrs):
+    """A reusable host array of device pointers for the calls that take one."""
     return (c_vp * len(ptrs))(*[int(p) for p in ptrs])
 
 
