@@ -297,7 +297,7 @@ def leg_cfg3(args):
                            cuda_stream=s.cuda_stream)
         adam = zg.zero_adam_t(max_grad_norm=0.0, **ADAM)
         state = zg.zero_state_t(t=0, loss_scale=1024.0, min_loss_scale=1.0, dynamic=1, growth_interval=0)
-        walls, skipped, scales = [], 0, []
+        walls, skipped, scales, skipped_bytes = [], 0, [], []
         for k in range(steps):
             step_no = k + 1
             S = state.loss_scale
@@ -315,11 +315,15 @@ def leg_cfg3(args):
             walls.append(w0.elapsed_time(w1))
             skipped += res.skipped
             scales.append(res.new_loss_scale)
+            if res.skipped:
+                skipped_bytes.append(res.hbm_bytes)
         ms = sum(walls) / len(walls)
         runs[run] = {"ms_per_step": ms, "value": n / (ms * 1e-3) / 1e9, "steps": steps, "skipped": skipped,
                      "loss_scales": scales, "t": state.t,
                      "hbm_bytes_per_clean_step": plan.hbm_bytes_fused,
-                     "hbm_bytes_per_skipped_step": plan.hbm_bytes_fused + n * (4 + 2 * N)}
+                     "hbm_bytes_per_skipped_step": (sum(skipped_bytes) / len(skipped_bytes)) if skipped_bytes
+                     else None,
+                     "hbm_bytes_per_skipped_step_without_skipping": plan.hbm_bytes_fused + n * (4 + 2 * N)}
     main = runs["odd_steps"]
     out = _base(main["value"], main["ms_per_step"], steps, 0,
                 "stage 2, 48-layer d=1600 parameter list (%d params), N_d=8, bucket 5e8, fp16 grads N(0,1e-3) x S, "
@@ -327,8 +331,10 @@ def leg_cfg3(args):
                 {"n_params": n, "n_ranks": N, "stage": 2, "bucket_elems": B, "injection": "value: odd steps only; "
                  "runs.literal: every step (12 infs over 1.24e10 gradient elements)"})
     out["runs"] = runs
-    out["note"] = ("a skipped step also runs the parameter restore kernel (cast of the unchanged master weights "
-                   "to every rank); step times are CUDA events around the whole library call")
+    out["note"] = ("bucket kernels that start after the step's flag is raised do nothing; a skipped step then "
+                   "restores the parameters of the window the other kernels wrote (cast of the unchanged master "
+                   "weights to every rank); hbm_bytes_per_skipped_step is the library's count of what moved; step "
+                   "times are CUDA events around the whole library call")
     return out
 
 

@@ -63,7 +63,12 @@
  *   fused     (no clipping and shadow state given): one kernel per bucket,
  *             state read from [cur] and written to [1-cur].  On overflow the
  *             step is discarded and each written 16-bit parameter is restored
- *             to the cast of the unchanged master weights.
+ *             to the cast of the unchanged master weights.  In stages 2 and 3
+ *             a bucket kernel that starts after the step's flag is raised
+ *             writes nothing, and only the window the others wrote is
+ *             restored (hbm_bytes counts what really moved); so the 16-bit
+ *             parameters must hold the cast of the current master weights
+ *             when a step starts, as every step leaves them.
  *   two-pass  (clipping, or no shadow): pass 1 per bucket reduces and checks
  *             the gradient, materialises it (grads[] in stages 0/1, reduced
  *             in stages 2/3) and accumulates the exact sum of squares; a

@@ -57,6 +57,12 @@ def test_cfg3_overflow_then_clean():
     plan = zg.zero_plan(cfg)
     bufs = zg.DeviceBuffers(cfg, plan, device="cuda")
     synth.dev_normal32(bufs.w[0].data_ptr(), n, 0.02, seed=0, stream=synth.STREAM_WEIGHT, cuda_stream=s.cuda_stream)
+    # every rank's 16-bit parameters start as the cast of the master weights
+    # (torch's binary32 -> binary16 conversion rounds to nearest even)
+    p16 = bufs.w[0][:n].to(torch.float16).view(torch.int16)
+    for r in range(N):
+        bufs.params16[r][:n].copy_(p16)
+    del p16
     adam = zg.zero_adam_t(max_grad_norm=0.0, **ADAM)
     state = zg.zero_state_t(t=0, loss_scale=1024.0, min_loss_scale=1.0, dynamic=1)
     inj = synth.inf_positions(n, N, seed=0, step=1)

@@ -101,9 +101,73 @@ def test_overflow_other_stages(stage):
     res, ref = job.step(job.make_grads(1, inject=[(0, 17, 0x7E00)]))   # NaN
     assert res.overflow == 1
     job.check(res, ref)
-    assert res.hbm_bytes == job.plan.hbm_bytes_fused + n * oracle.hbm_bytes_per_param(2, stage, "restore")
+    full = job.plan.hbm_bytes_fused + n * oracle.hbm_bytes_per_param(2, stage, "restore")
+    if stage <= 1:     # every bucket writes the all-reduced gradient back: nothing is skipped
+        assert res.hbm_bytes == full
+    else:              # later bucket kernels may skip once the flag is up
+        assert 0 < res.hbm_bytes <= full
     res, ref = job.step(job.make_grads(2))
     job.check(res, ref)
+
+
+@pytest.mark.parametrize("stage,optimizer", [(2, zg.ZERO_ADAM), (2, zg.ZERO_SGD), (3, zg.ZERO_ADAM)])
+@pytest.mark.parametrize("where", ["first", "middle", "last"])
+@pytest.mark.parametrize("order", ["forward", "backward"])
+def test_overflow_skips_later_buckets(stage, optimizer, where, order):
+    """Buckets launched one at a time (plain stream order) after the flag is
+    raised do nothing; the restore covers only the window the kernels that
+    ran wrote.  State and parameters equal the oracle's (state unchanged,
+    loss scale halved, t unchanged), and hbm_bytes counts exactly the buckets
+    that ran (fused bytes) and their window (restore bytes).  Stage 2 with
+    SGD takes the tile kernel."""
+    n, B, N = 8 * 4096 + 101, 4096, 4
+    nb = 9
+    job = Job(n, N, stage, B, 8, loss_scale=1024.0, dynamic=True, optimizer=optimizer)
+    res, ref = job.step(job.make_grads(1))
+    job.check(res, ref)
+    kb = {"first": 0, "middle": 4, "last": nb - 1}[where]
+    i = min(kb * B + 1000, n - 1)
+    grads = job.make_grads(2, inject=[(1, i, synth.inf_bits(job.dtype))])
+    job.load_grads(grads)
+    s = torch.cuda.current_stream()
+    buckets = list(range(nb)) if order == "forward" else list(reversed(range(nb)))
+    zg.zero_step_begin(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
+    for b in buckets:
+        zg.zero_step_bucket(job.cfg, job.plan, job.bufs, job.adam, job.state, b, None, s)
+    res = zg.zero_step_end(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
+    torch.cuda.synchronize()
+    ref = job.oracle_step(grads)
+    assert res.overflow == 1 and res.skipped == 1 and res.new_loss_scale == 512.0
+    job.check(res, ref)
+    ran = buckets[:buckets.index(kb) + 1]
+    updated = sum(min((b + 1) * B, n) - b * B for b in ran)
+    window = min((max(ran) + 1) * B, n) - min(ran) * B
+    sb = {zg.ZERO_ADAM: 12, zg.ZERO_SGD: 4}[optimizer]
+    assert res.hbm_bytes == (updated * oracle.hbm_bytes_per_param(N, stage, "fused", sb)
+                             + window * oracle.hbm_bytes_per_param(N, stage, "restore", sb))
+    res, ref = job.step(job.make_grads(3))
+    assert res.overflow == 0
+    job.check(res, ref)
+
+
+@pytest.mark.parametrize("stage", [2, 3])
+@pytest.mark.parametrize("where", ["first", "middle", "last"])
+def test_overflow_anywhere_whole_step(stage, where):
+    """The whole-step entry point (bucket kernels chained by programmatic
+    dependent launch, so how many skip depends on timing) with the inf in the
+    first, a middle or the last of 17 buckets: bit-exact against the oracle,
+    and the bytes reported are positive and at most the full step plus a
+    full restore."""
+    n, B, N = 16 * 8192 + 77, 8192, 8
+    job = Job(n, N, stage, B, 8, loss_scale=256.0, dynamic=True)
+    kb = {"first": 0, "middle": 8, "last": 16}[where]
+    for t, inject in ((1, []), (2, [(N - 1, min(kb * B + 5, n - 1), 0x7C00)]), (3, [])):
+        res, ref = job.step(job.make_grads(t, inject))
+        job.check(res, ref)
+        if inject:
+            fb = oracle.hbm_bytes_per_param(N, stage, "fused")
+            rb = oracle.hbm_bytes_per_param(N, stage, "restore")
+            assert 0 < res.hbm_bytes <= n * (fb + rb)
 
 
 @pytest.mark.parametrize("stage", [1, 2])

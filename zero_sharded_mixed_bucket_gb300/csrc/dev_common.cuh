@@ -553,6 +553,65 @@ __device__ __forceinline__ unsigned long long* ws_bins(unsigned char* ws)
     return reinterpret_cast<unsigned long long*>(ws + ws::kBins);
 }
 
+// ---- overflowed steps ----------------------------------------------------------
+// An overflowed step is discarded whatever its other buckets hold.  In stages
+// 2 and 3 the fused bucket kernels write nothing that outlives a discarded
+// step except the 16-bit parameters, so a block that finds the step's flag
+// already raised when it starts does nothing at all; a thread raises the flag
+// as soon as it meets a non-finite value, so later blocks see it early.  The
+// blocks that do run record, in the workspace, their bucket's element window
+// (the host then restores parameters only there) and how many elements they
+// updated (the bytes the step really moved).
+__device__ __forceinline__ bool flag_raised(const unsigned char* ws)
+{
+    return *reinterpret_cast<const volatile uint32_t*>(ws + ws::kFlag) != 0u;
+}
+
+// Raise the step's flag at the first non-finite value this thread meets.
+__device__ __forceinline__ void raise_flag(unsigned char* ws, uint32_t nonfinite, bool& raised)
+{
+    if (nonfinite && !raised) {
+        atomicOr(reinterpret_cast<uint32_t*>(ws + ws::kFlag), 1u);
+        raised = true;
+    }
+}
+
+// Elements of the window [lo, hi), cut into groups of V, that this block
+// covers when the grid strides over the groups kThreads at a time: block b
+// takes groups b*kThreads + t + k*S (t < kThreads, S = gridDim.x*kThreads).
+__device__ __forceinline__ int64_t block_elems_grid_stride(int64_t lo, int64_t hi, int V)
+{
+    const int64_t ng = (hi - lo + V - 1) / V;
+    const int64_t base = (int64_t)blockIdx.x * kThreads;
+    if (ng <= base) return 0;
+    const int64_t S = (int64_t)gridDim.x * kThreads;
+    const int64_t q = (ng - base) / S, r = (ng - base) % S;
+    int64_t elems = (q * kThreads + (r < kThreads ? r : (int64_t)kThreads)) * V;
+    const int64_t last = (ng - 1) % S;                      // the window's last group, maybe short
+    if (last >= base && last < base + kThreads) elems -= ng * V - (hi - lo);
+    return elems;
+}
+
+// The same for a grid striding over tiles of T elements one per block.
+__device__ __forceinline__ int64_t block_elems_tile_stride(int64_t lo, int64_t hi, int64_t T)
+{
+    const int64_t nt = (hi - lo + T - 1) / T;
+    const int64_t b = blockIdx.x;
+    if (nt <= b) return 0;
+    int64_t elems = ((nt - 1 - b) / gridDim.x + 1) * T;
+    if ((nt - 1) % gridDim.x == b) elems -= nt * T - (hi - lo);
+    return elems;
+}
+
+// One thread per block: this block updated `elems` elements of [lo, hi).
+__device__ __forceinline__ void note_updated(unsigned char* ws, int64_t lo, int64_t hi, int64_t elems)
+{
+    if (elems <= 0) return;
+    atomicAdd(reinterpret_cast<unsigned long long*>(ws + ws::kUpdated), (unsigned long long)elems);
+    atomicMax(reinterpret_cast<unsigned long long*>(ws + ws::kWroteLoC), ~(unsigned long long)lo);
+    atomicMax(reinterpret_cast<unsigned long long*>(ws + ws::kWroteHi), (unsigned long long)hi);
+}
+
 // Stage 3: owner rank of a flat index and the index inside its shard.
 __device__ __forceinline__ int owner_of(int64_t i, int64_t shard)
 {

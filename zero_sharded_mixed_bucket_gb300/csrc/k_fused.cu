@@ -31,6 +31,14 @@ __global__ void __launch_bounds__(kThreads, STAGE == 0 ? 5 : 1) k_fused(const __
     // without waiting).
     if (a.wait_first) wait_prev_grid();
     allow_next_grid();
+    // Stages 2 and 3: nothing to do once the step has overflowed (the flag
+    // was cleared before the step's first bucket kernel started).
+    if constexpr (STAGE >= 2) {
+        if (flag_raised(a.ws)) {
+            wait_prev_grid();
+            return;
+        }
+    }
     // Step scalars: from the launch, or from the prepare kernel in a
     // device-state step.
     float inv = a.inv;
@@ -53,7 +61,7 @@ __global__ void __launch_bounds__(kThreads, STAGE == 0 ? 5 : 1) k_fused(const __
 
         // round to the model precision (elements past cnt are 0: finite, no effect)
         Vals<DT> h;
-        bad |= round_group<DT>(s, h) != 0;
+        raise_flag(a.ws, round_group<DT>(s, h), bad);
         float g[kVecOf<DT>];
         unscale_group<DT>(h, inv, g);
 
@@ -80,8 +88,9 @@ __global__ void __launch_bounds__(kThreads, STAGE == 0 ? 5 : 1) k_fused(const __
             }
         }
     }
-    if (__syncthreads_or(bad) && threadIdx.x == 0)
-        atomicOr(ws_flag(a.ws), 1u);
+    if constexpr (STAGE >= 2) {
+        if (threadIdx.x == 0) note_updated(a.ws, a.lo, a.hi, block_elems_grid_stride(a.lo, a.hi, kVecOf<DT>));
+    }
     wait_prev_grid();
 }
 
@@ -123,6 +132,12 @@ __global__ void __launch_bounds__(kThreads) k_fused_tiled(const __grid_constant_
     __shared__ __align__(128) Vals<DT> tile[2][kArrays][kTileGroups];
     if (a.wait_first) wait_prev_grid();
     allow_next_grid();
+    if constexpr (STAGE == 2) {   // nothing to do once the step has overflowed (as k_fused)
+        if (flag_raised(a.ws)) {
+            wait_prev_grid();
+            return;
+        }
+    }
     float inv = a.inv;
     AdamHP hp = a.hp;
     if (a.dyn) {
@@ -146,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) k_fused_tiled(const __grid_constant_
             float s[V];
             reduce_group<DT>(a, i - a.grad_base, cnt, s);
             Vals<DT> h;
-            bad |= round_group<DT>(s, h) != 0;
+            raise_flag(a.ws, round_group<DT>(s, h), bad);
             float g[V];
             unscale_group<DT>(h, inv, g);
             Vals<DT> p;
@@ -193,8 +208,9 @@ __global__ void __launch_bounds__(kThreads) k_fused_tiled(const __grid_constant_
             }
         }
     }
-    if (__syncthreads_or(bad) && threadIdx.x == 0)
-        atomicOr(ws_flag(a.ws), 1u);
+    if constexpr (STAGE == 2) {
+        if (threadIdx.x == 0) note_updated(a.ws, a.lo, a.hi, block_elems_tile_stride(a.lo, a.hi, kTileElems));
+    }
     // the bulk copies complete before the kernel does
     if (threadIdx.x < 32) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     wait_prev_grid();

@@ -378,7 +378,11 @@ zero_status_t end_impl(const zero_config_t* c, const zero_plan_t* p, zero_buffer
         if (e != cudaSuccess) return cuda_fail(e, "recording the profiling end event");
     }
     unsigned char head[ws::kAcc];
+    uint64_t wrote[3];   // ~lowest written index, end of the highest written window, elements updated
     e = cudaMemcpyAsync(head, b->workspace, sizeof head, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(wrote, static_cast<unsigned char*>(b->workspace) + ws::kWroteLoC, sizeof wrote,
+                            cudaMemcpyDeviceToHost, st);
     if (e != cudaSuccess) return cuda_fail(e, "reading the overflow flag");
     e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "synchronising the step");
@@ -390,10 +394,20 @@ zero_status_t end_impl(const zero_config_t* c, const zero_plan_t* p, zero_buffer
     std::memcpy(&clip, head + ws::kClip, 4);
     const bool overflow = flag != 0;
 
-    if (overflow && path.fused && c->n_params > 0) {
+    // After an overflowed fused step the 16-bit parameters the bucket kernels
+    // wrote are put back.  In stages 2 and 3 the kernels record the window
+    // they wrote (kernels that started after the flag was raised wrote
+    // nothing); stages 0 and 1 write everywhere.
+    const bool skips = path.fused && c->stage >= 2;
+    int64_t rlo = 0, rhi = overflow && path.fused ? c->n_params : 0;
+    if (overflow && skips) {
+        rlo = wrote[0] ? (int64_t)~wrote[0] : 0;
+        rhi = wrote[0] ? (int64_t)wrote[1] : 0;
+    }
+    if (rhi > rlo) {
         StepArgs a = make_args(c, p, b, adam, s, false, nullptr, 0);
-        a.lo = 0;
-        a.hi = c->n_params;
+        a.lo = rlo;
+        a.hi = rhi;
         e = launch_restore(c->stage, c->dtype, a, st);
         if (e != cudaSuccess) return cuda_fail(e, "launching the parameter restore kernel");
         launches++;
@@ -410,7 +424,11 @@ zero_status_t end_impl(const zero_config_t* c, const zero_plan_t* p, zero_buffer
     r.hbm_bytes = path.fused ? p->hbm_bytes_fused : p->hbm_bytes_two_pass;
     r.comm_counted_bytes = p->comm_counted_bytes;
     if (overflow) {
-        if (path.fused) r.hbm_bytes += c->n_params * restore_bytes_per_param(c->stage, c->n_ranks, value_bytes(c->dtype));
+        // the elements the bucket kernels really updated, and the restore
+        if (skips)
+            r.hbm_bytes = (int64_t)wrote[2] * bytes_per_param(c->stage, c->n_ranks, true, state_bytes(c->optimizer),
+                                                               value_bytes(c->dtype));
+        r.hbm_bytes += (rhi - rlo) * restore_bytes_per_param(c->stage, c->n_ranks, value_bytes(c->dtype));
         if (s->dynamic) {
             float h = s->loss_scale * 0.5f;
             s->loss_scale = h > s->min_loss_scale ? h : s->min_loss_scale;

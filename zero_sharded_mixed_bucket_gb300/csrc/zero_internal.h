@@ -18,9 +18,17 @@ constexpr size_t kNorm = 8;     // double: ||g||_2 (two-pass with clipping)
 constexpr size_t kClip = 16;    // float: clip coefficient
 constexpr size_t kAcc = 32;     // 4 x uint64: 32-bit limbs of the fixed-point sum of squares
 constexpr size_t kBins = 64;    // 256 x uint64: sum of M^2 per exponent field, outside the window
-constexpr size_t kEnd = kBins + 256 * 8;
+// Fused step, stages 2 and 3: what the bucket kernels that ran wrote (an
+// overflowed step restores parameters only there) -- the complement of the
+// lowest written flat index (0: nothing written), the end of the highest
+// written window, and the number of elements updated.
+constexpr size_t kWroteLoC = kBins + 256 * 8;   // uint64: ~lo
+constexpr size_t kWroteHi = kWroteLoC + 8;      // uint64: hi
+constexpr size_t kUpdated = kWroteHi + 8;       // uint64: elements updated
+constexpr size_t kEnd = kUpdated + 16;          // end of the part cleared before every step (16-byte multiple)
 constexpr size_t kDyn = 2176;   // Dyn: per-step scalars of a device-state step (written by the prepare kernel)
 constexpr int64_t kBytes = 4096;
+static_assert(kEnd % 16 == 0 && kEnd <= kDyn, "workspace head");
 }  // namespace ws
 
 // Per-step scalars of a step whose loss scale and step count live on the
