@@ -248,7 +248,7 @@ def host_cores() -> int:
     return len(os.sched_getaffinity(0))
 
 
-def cpu_baseline(n_sample=1 << 21, steps=3, ranks=S3_RANKS, scale=S3_SCALE):
+def cpu_baseline(n_sample=1 << 22, steps=3, ranks=S3_RANKS, scale=S3_SCALE):
     """The oracle as it is (single-threaded C: one of the host's cores) on
     the first n_sample parameters of the workload."""
     times = run_oracle_steps(n_sample, steps, 0, ranks, scale)
@@ -704,20 +704,27 @@ def gpu_arm(args):
 # ---------------------------------------------------------------------------
 # the default line: the stage-3 step at 6.65B parameters
 # ---------------------------------------------------------------------------
-def stage3_e2e(job, steps, warmup, device, world=1):
-    """The stage-3 step through the C ABI with each bucket's 64 gradient
-    copies arriving from pinned host memory inside the timed region: two
-    pinned host sets of N_d x 2^24 values, one cudaMemcpyAsync per bucket
-    on a copy stream into one of two device sets, double-buffered (a set is
-    refilled once the bucket kernel that read it has run), and the step's
-    result read back by the host (zero_dev_state_read, 64 bytes) after every
-    step."""
+def stage3_e2e(job, steps, warmup, device, world=1, mode="direct"):
+    """The stage-3 step through the C ABI with every bucket's 64 gradient
+    copies crossing from pinned host memory to the GPU inside the timed
+    region, and the step's result read back by the host after every step
+    (zero_dev_state_read, 64 bytes).  Two pinned host sets of N_d x 2^24
+    values serve the buckets alternately.
+
+    mode "direct": each bucket kernel loads its 64 gradient windows straight
+    from pinned host memory over NVLink-C2C (the library accepts any pointer
+    the GPU can load from).  mode "copy": one cudaMemcpyAsync per bucket (the
+    whole 2.1 GB set) on a second stream into one of two device sets,
+    double-buffered against the bucket kernels.  Measured on GB300: direct
+    199 GB/s on the host link; copy 140-160 GB/s, single 2.1 GB copies taking
+    10 to 94 ms."""
     import torch
     zg = job.zg
     assert len(job.ring) >= 2
     host = [torch.empty(job.N * job.B, dtype=torch.int16).pin_memory() for _ in range(2)]
     for k in range(2):
         host[k].copy_(job.ring[k])
+    host_ptrs = [zg.ptr_array([h.data_ptr() + 2 * r * job.B for r in range(job.N)]) for h in host]
     copy_stream = torch.cuda.Stream(device)
     free = [None, None]            # per device set: event after the bucket kernel that last read it
 
@@ -737,7 +744,10 @@ def stage3_e2e(job, steps, warmup, device, world=1):
         free[b % 2] = e
 
     def one():
-        job.step(grad_ptrs=lambda b: job.ring_ptrs[b % 2], before_bucket=before, after_bucket=after)
+        if mode == "direct":
+            job.step(grad_ptrs=lambda b: host_ptrs[b % 2])
+        else:
+            job.step(grad_ptrs=lambda b: job.ring_ptrs[b % 2], before_bucket=before, after_bucket=after)
         st, last = zg.zero_dev_state_read(job.dev_state, job.stream)       # the step's result, to the host
         assert last.overflow == 0
         return st
@@ -756,13 +766,16 @@ def stage3_e2e(job, steps, warmup, device, world=1):
     ms = max_over_ranks(start.elapsed_time(end) / steps, world)
     barrier(world)
     nb = job.plan.n_buckets
-    h2d = nb * job.N * job.B * 2
+    # bytes that cross the host link per step: direct, each bucket's windows
+    # (N_d x bucket length); copy, the whole set per bucket
+    h2d = job.N * job.n * 2 if mode == "direct" else nb * job.N * job.B * 2
     return dict(value=world * job.n / (ms * 1e-3) / 1e9, unit=UNIT, h2d_bytes_per_step=world * h2d,
                 d2h_bytes_per_step=world * zg.DEV_STATE_BYTES, ms_per_step=ms, steps=steps, warmup=warmup,
-                host_link_gbs_per_gpu=h2d / (ms * 1e-3) / 1e9,
-                note="every bucket's 64 gradient copies (64 x 2^24 fp16 values, one 2.1 GB cudaMemcpyAsync) copied "
-                     "from pinned host memory on a second stream, double-buffered against the bucket kernels; the "
-                     "step's result block read back after every step; the host link sets the pace")
+                mode=mode, host_link_gbs_per_gpu=h2d / (ms * 1e-3) / 1e9,
+                note="every step's 64 x 6.65e9 fp16 gradient values cross from pinned host memory to the GPU "
+                     + ("(the bucket kernels load them over NVLink-C2C)" if mode == "direct" else
+                        "(one cudaMemcpyAsync per bucket on a second stream, double-buffered)")
+                     + "; the step's result block is read back after every step; the host link sets the pace")
 
 
 def stage3_arm(args):
@@ -864,7 +877,7 @@ def stage3_arm(args):
         return _finish(world)
     # end to end on every rank at once: each GPU has its own host link
     try:
-        out["e2e"] = stage3_e2e(job, args.e2e_steps, 1, device, world)
+        out["e2e"] = stage3_e2e(job, args.e2e_steps, 1, device, world, args.e2e_mode)
     except Exception as e:         # reported, never hides the headline
         if world > 1:
             raise
@@ -959,6 +972,8 @@ def main():
     ap.add_argument("--s3-layers", type=int, default=S3_LAYERS, help="--config 4: transformer layers")
     ap.add_argument("--s3-d", type=int, default=S3_D, help="--config 4: model width d")
     ap.add_argument("--e2e-steps", type=int, default=2, help="--config 4: timed steps of the end-to-end leg")
+    ap.add_argument("--e2e-mode", default="direct", choices=["direct", "copy"],
+                    help="--config 4: gradients read by the kernels from pinned host memory, or copied per bucket")
     ap.add_argument("--with-generation", action="store_true",
                     help="--config 4: instead, the step with each bucket's gradients generated into a staging "
                          "area right before its kernel (generation timed and subtracted), and the prefetching "
