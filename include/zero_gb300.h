@@ -126,7 +126,7 @@ typedef enum {
     ZERO_EALIGN = 2,         /* a device pointer is not 16-byte aligned */
     ZERO_ENOMEM = 3,         /* a caller-provided buffer is missing or too small */
     ZERO_ECUDA = 4,          /* a CUDA runtime call failed (message has the CUDA error) */
-    ZERO_ETIMEOUT = 5,       /* reserved: no kernel here spins on a flag another kernel sets */
+    ZERO_ETIMEOUT = 5,       /* a kernel's bounded wait on its own copies ran out (seconds); the step was not applied */
     ZERO_EUNSUPPORTED = 6    /* n_ranks outside 1..64, or another unsupported size */
 } zero_status_t;
 
@@ -392,7 +392,9 @@ zero_status_t zero_step_end_async(const zero_config_t* cfg, const zero_plan_t* p
                                   const zero_adam_t* adam, void* dev_state, void* stream, int32_t* kernel_launches);
 /* Copy the block to the host (synchronises `stream`): the current step state
  * and the last step's outcome (t, overflow, skipped, grad_norm, clip_coef,
- * new_loss_scale; path -1). */
+ * new_loss_scale; path -1).  Returns ZERO_ETIMEOUT (outputs still filled) if
+ * a bounded wait inside the last step's kernels ran out; that step was not
+ * applied and the loss scaler was left as it was. */
 zero_status_t zero_dev_state_read(const void* dev_state, zero_state_t* state, zero_step_result_t* last, void* stream);
 
 /* ---- stage 3: gathers ahead of use under a live-parameter budget ---------

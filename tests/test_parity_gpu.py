@@ -702,3 +702,59 @@ def test_two_pass_many_ranks(stage, N, dtype, optimizer):
         res, ref = job.step(job.make_grads(t, inject))
         job.check(res, ref)
         assert res.path == 1 and res.overflow == (1 if inject else 0)
+
+
+@pytest.mark.parametrize("N", [1, 2])
+@pytest.mark.parametrize("stage", [2, 3])
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("max_norm", [0.0, 1.0])
+def test_staged_pass1_one_or_two_ranks(N, stage, dtype, max_norm):
+    """Pass 1 with one or two ranks in stages 2 and 3 streams the gradient
+    tiles into shared memory (bulk copies on mbarriers, 4096-element tiles,
+    each block striding over several): buckets of several tiles with a
+    ragged last tile and a last group shorter than 8, a bucket smaller than
+    one tile, an overflowed step and clean steps after it, against the
+    oracle bit for bit (reduced gradient, norm, clip coefficient, state)."""
+    n, B = 5 * 40960 + 4096 + 5, 40960           # 6 buckets; the last of 4101 elements
+    job = Job(n, N, stage, B, 8, dtype=dtype, shadow=False, loss_scale=64.0, dynamic=True, max_norm=max_norm,
+              sigma=0.02)
+    inf = synth.inf_bits(dtype)
+    for t, inject in ((1, ()), (2, ((N - 1, n - 3, inf),)), (3, ()), (4, ())):
+        res, ref = job.step(job.make_grads(t, inject))
+        assert res.path == 1 and res.overflow == (1 if inject else 0)
+        job.check(res, ref)
+        if max_norm > 0 and not inject:
+            assert 0.0 < res.clip_coef < 1.0
+
+
+@pytest.mark.parametrize("N", [1, 2])
+def test_staged_pass1_many_tiles_per_block_and_staging(N):
+    """One bucket of 2^24 + 8 * 1000 + 3 elements -- more tiles than blocks
+    resident at once, so every block cycles its stage ring several times --
+    through the per-bucket protocol with gradient windows in separate staging
+    buffers, clipped; then the same through the device-state step."""
+    n, B = (1 << 24) + 8 * 1000 + 3, 1 << 24
+    job = Job(n, N, 2, B, 8, dtype=FP16, shadow=False, loss_scale=1.0, max_norm=1.0)
+    s = torch.cuda.current_stream()
+    grads = job.make_grads(1)
+    staging = [torch.empty(B, dtype=torch.int16, device="cuda") for _ in range(N)]
+    zg.zero_step_begin(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
+    for b in range(job.plan.n_buckets):
+        lo, hi = b * B, min((b + 1) * B, n)
+        for r in range(N):
+            staging[r][:hi - lo].copy_(torch.from_numpy(grads[r][lo:hi].view(np.int16)))
+        zg.zero_step_bucket(job.cfg, job.plan, job.bufs, job.adam, job.state, b, [t.data_ptr() for t in staging], s)
+    res = zg.zero_step_end(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
+    torch.cuda.synchronize()
+    job.check(res, job.oracle_step(grads))
+    assert 0.0 < res.clip_coef < 1.0
+    dev = torch.zeros(zg.DEV_STATE_BYTES // 8, dtype=torch.int64, device="cuda")
+    zg.zero_dev_state_init(dev, job.adam, job.state, s)
+    grads = job.make_grads(2)
+    job.load_grads(grads)
+    zg.zero_step_async(job.cfg, job.plan, job.bufs, job.adam, dev, s)
+    st, last = zg.zero_dev_state_read(dev, s)
+    job.state = st
+    ref = job.oracle_step(grads)
+    last.path = 1
+    job.check(last, ref)

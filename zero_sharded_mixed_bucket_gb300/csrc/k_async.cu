@@ -61,6 +61,16 @@ __device__ void commit(const CommitArgs& a)
 {
     DevState* st = a.st;
     const uint32_t flag = *reinterpret_cast<const volatile uint32_t*>(a.ws + ws::kFlag);
+    if (*reinterpret_cast<const volatile uint32_t*>(a.ws + ws::kErr)) {
+        // a kernel gave up a bounded wait (and raised the flag, so nothing was
+        // updated): the step is not applied and the scaler keeps its state;
+        // bit 1 of last_overflow tells zero_dev_state_read
+        st->last_overflow = 3u;
+        st->last_skipped = 1;
+        st->last_grad_norm = __longlong_as_double(0x7ff8000000000000ll);   // NaN
+        st->last_clip_coef = 1.0f;
+        return;
+    }
     if (flag) {
         if (st->dynamic) {
             const float h = __fmul_rn(st->loss_scale, 0.5f);

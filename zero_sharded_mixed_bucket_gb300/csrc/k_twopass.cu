@@ -7,7 +7,10 @@
 //                                   exact integer sum of squares.
 //   once                k_finalize: exact sum -> fp64 -> ||g||, clip coefficient.
 //   pass 2, per bucket  k_update:   optimizer update in place (k_update.cu).
+#include <mutex>
+
 #include "dev_common.cuh"
+#include "host_ptrs.h"
 
 namespace zg {
 
@@ -110,6 +113,221 @@ __global__ void __launch_bounds__(kThreads, (CLIP && U > 1) ? 4 : 1) k_reduce(co
     wait_prev_grid();
 }
 
+// ---- pass 1 for one or two ranks (stages 2 and 3), staged ---------------------
+// With one or two ranks a group of 8 elements is only one or two 16-byte
+// gradient loads, while the exact sum of squares costs a dozen integer
+// instructions per value: the per-thread kernel above has to keep many
+// groups' loads in flight in registers (124 of them, four blocks per SM) and
+// then runs out of warps to hide its integer chains (ALU pipe 58 %, DRAM 33 %
+// on GB300).  Here the two jobs are split: in each block one lane of a
+// producer warp streams every rank's part of a tile into a ring of
+// shared-memory stages with bulk asynchronous copies (cp.async.bulk global ->
+// shared, completing on the stage's "full" mbarrier), and eight consumer warps
+// do the arithmetic from shared memory and release the stage on its "empty"
+// mbarrier.  The bytes in flight no longer depend on how many warps are
+// resident.  Grid: at most the blocks that fit at once, each striding over
+// the bucket's tiles.  Every wait is bounded: past kWaitNs of global time a
+// thread records ZERO_ETIMEOUT's cause in the workspace, raises the overflow
+// flag (so the update pass skips the step) and stops.
+namespace staged {
+constexpr int kWarps = 8;                              // consumer warps
+constexpr int kConsumers = kWarps * 32;
+constexpr int kBlockThreads = kConsumers + 32;         // and one producer warp
+constexpr int kGroupsPerThread = 2;
+constexpr int kTileElems = kConsumers * kGroupsPerThread * 8;   // 4096 elements: 8 KB per rank
+constexpr int kStages = 4;
+constexpr uint64_t kWaitNs = 2000000000ull;            // 2 s
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Wait for the completion of the barrier's phase with parity `parity`;
+// false once kWaitNs have passed without it.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
+{
+    const uint32_t addr = smem_addr(bar);
+    uint64_t t0 = 0;
+    for (uint32_t k = 0;; k++) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done) : "r"(addr), "r"(parity) : "memory");
+        if (done) return true;
+        if ((k & 63) == 0) {
+            const uint64_t now = global_ns();
+            if (k == 0) t0 = now;
+            else if (now - t0 > kWaitNs) return false;
+        }
+    }
+}
+
+// Global -> shared bulk copy of `bytes` (a multiple of 16, both addresses
+// 16-byte aligned), completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(smem_addr(sdst)), "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void report_timeout(unsigned char* ws)
+{
+    atomicOr(reinterpret_cast<uint32_t*>(ws + ws::kErr), 1u);
+    atomicOr(reinterpret_cast<uint32_t*>(ws + ws::kFlag), 1u);
+}
+}  // namespace staged
+
+template <int DT, bool CLIP, int NR>
+__global__ void __launch_bounds__(staged::kBlockThreads, 2) k_reduce_staged(const __grid_constant__ StepArgs a)
+{
+    using namespace staged;
+    static_assert(NR == 1 || NR == 2, "one or two ranks");
+    static_assert(DT != kF32, "16-bit values: groups of 8");
+    extern __shared__ __align__(128) unsigned char sm[];   // [kStages][NR][kTileElems] 16-bit values
+    __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
+    __shared__ unsigned long long red_lo[kWarps], red_hi[kWarps];
+    if (a.wait_first) wait_prev_grid();   // first bucket of a device-state step (see k_fused)
+    allow_next_grid();
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int st = 0; st < kStages; st++) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], kWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int64_t ntiles = (a.hi - a.lo + kTileElems - 1) / kTileElems;
+    uint16_t* stage_base = reinterpret_cast<uint16_t*>(sm);
+    if (tid >= kConsumers) {
+        if (tid == kConsumers) {   // the producer lane
+            int k = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, k++) {
+                const int st = k % kStages;
+                if (!mbar_wait(&empty[st], ((k / kStages) & 1) ^ 1)) {   // released by the consumers
+                    ok = false;
+                    break;
+                }
+                const int64_t t0 = a.lo + t * kTileElems;
+                const int64_t tel = min((int64_t)kTileElems, a.hi - t0);
+                const uint32_t bytes = (uint32_t)(tel * 2) & ~15u;       // whole groups; a short last group is loaded by its thread
+                mbar_arrive_expect_tx(&full[st], NR * bytes);
+                if (bytes) {
+#pragma unroll
+                    for (int r = 0; r < NR; r++)
+                        bulk_load(stage_base + (size_t)(st * NR + r) * kTileElems,
+                                  static_cast<const uint16_t*>(a.grads[r]) + (t0 - a.grad_base), bytes, &full[st]);
+                }
+            }
+            if (!ok) report_timeout(a.ws);
+            // the last fill of every stage has landed before the block exits
+            for (int j = k - kStages < 0 ? 0 : k - kStages; j < k; j++)
+                if (!mbar_wait(&full[j % kStages], (j / kStages) & 1)) {
+                    report_timeout(a.ws);
+                    break;
+                }
+        }
+    } else {
+        const int win_lo = a.dyn ? a.dyn->win_lo : a.win_lo;
+        bool bad = false;
+        U128 acc{0ull, 0ull};
+        unsigned long long* bins = ws_bins(a.ws);
+        int k = 0;
+        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, k++) {
+            const int st = k % kStages;
+            if (!mbar_wait(&full[st], (k / kStages) & 1)) {
+                report_timeout(a.ws);
+                break;
+            }
+            const int64_t t0 = a.lo + t * kTileElems;
+#pragma unroll
+            for (int g = 0; g < kGroupsPerThread; g++) {
+                const int gl = g * kConsumers + tid;                 // group within the tile
+                const int64_t i = t0 + (int64_t)gl * 8;
+                if (i < a.hi) {
+                    const int cnt = (int)min((int64_t)8, a.hi - i);
+                    H16<8> q[NR];
+#pragma unroll
+                    for (int r = 0; r < NR; r++) {
+                        if (cnt == 8) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(
+                                stage_base + (size_t)(st * NR + r) * kTileElems + gl * 8);
+                            q[r].w[0] = v.x; q[r].w[1] = v.y; q[r].w[2] = v.z; q[r].w[3] = v.w;
+                        } else {
+                            q[r] = ld_h16<8>(a.grads[r], i - a.grad_base, cnt);
+                        }
+                    }
+                    // rank order from 0: s = (0 + g_0) + g_1, as reduce_group
+                    float s[8];
+#pragma unroll
+                    for (int p = 0; p < 4; p++) {
+                        const float2 f = to_f32x2<DT>(q[0].w[p]);
+                        s[2 * p] = __fadd_rn(0.0f, f.x);
+                        s[2 * p + 1] = __fadd_rn(0.0f, f.y);
+                        if constexpr (NR == 2) {
+                            const float2 f1 = to_f32x2<DT>(q[1].w[p]);
+                            s[2 * p] = __fadd_rn(s[2 * p], f1.x);
+                            s[2 * p + 1] = __fadd_rn(s[2 * p + 1], f1.y);
+                        }
+                    }
+                    finish_group<1, DT, CLIP>(a, i, i - a.grad_base, cnt, s, win_lo, bad, acc, bins);
+                }
+            }
+            __syncwarp();
+            if ((tid & 31) == 0) mbar_arrive(&empty[st]);
+        }
+        if (bad) atomicOr(ws_flag(a.ws), 1u);
+        if constexpr (CLIP) {
+            // consumer warps only (named barrier 1): one 128-bit sum per block
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const unsigned long long lo = __shfl_down_sync(0xffffffffu, acc.lo, off);
+                const unsigned long long hi = __shfl_down_sync(0xffffffffu, acc.hi, off);
+                u128_add(acc, lo, hi);
+            }
+            if ((tid & 31) == 0) {
+                red_lo[tid >> 5] = acc.lo;
+                red_hi[tid >> 5] = acc.hi;
+            }
+            asm volatile("bar.sync 1, %0;" :: "r"(kConsumers) : "memory");
+            if (tid == 0) {
+                U128 sum{0ull, 0ull};
+                for (int w = 0; w < kWarps; w++)
+                    u128_add(sum, red_lo[w], red_hi[w]);
+                const unsigned long long l[4] = {sum.lo & 0xffffffffull, sum.lo >> 32, sum.hi & 0xffffffffull,
+                                                 sum.hi >> 32};
+                unsigned long long* limbs = ws_acc(a.ws);
+#pragma unroll
+                for (int j = 0; j < 4; j++)
+                    if (l[j]) atomicAdd(limbs + j, l[j]);
+            }
+        }
+    }
+    wait_prev_grid();
+}
+
 // ---- finalize: exact integer -> nearest fp64 -------------------------------
 constexpr int kBigWords = 10;   // 640 bits: covers 2^(2*(-133)) .. 2^(2*127 + 64)
 
@@ -200,11 +418,65 @@ __global__ void k_finalize(const FinalArgs a)
     *clip_out = __double2float_rn(q < 1.0 ? q : 1.0);
 }
 
+// Launch the staged pass 1: dynamic shared memory for the stage ring, grid
+// at most the blocks resident at once.
+template <int DT, bool CLIP, int NR>
+cudaError_t run_reduce_staged(const StepArgs& a, cudaStream_t s, bool overlap)
+{
+    using namespace staged;
+    auto kernel = k_reduce_staged<DT, CLIP, NR>;
+    const int smem = kStages * NR * kTileElems * 2;
+    struct Entry {
+        int dev;
+        int resident;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int n_cache = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int resident = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int k = 0; k < n_cache; k++)
+            if (cache[k].dev == dev) resident = cache[k].resident;
+        if (!resident) {
+            e = cudaFuncSetAttribute((const void*)kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            int sms = 0, per_sm = 0;
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, (const void*)kernel, kBlockThreads, smem);
+            resident = (sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+            if (n_cache < 64) cache[n_cache++] = Entry{dev, resident};
+        }
+    }
+    const int64_t tiles = (a.hi - a.lo + kTileElems - 1) / kTileElems;
+    const int grid = (int)(tiles < resident ? tiles : resident);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)kBlockThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 template <int HDEST, int DT, bool CLIP>
 cudaError_t run_reduce(const StepArgs& a, cudaStream_t s, bool overlap)
 {
     const int64_t groups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     if (groups <= 0) return cudaSuccess;
+    if constexpr (HDEST == 1 && DT != kF32) {
+        // stages 2/3, one or two ranks, gradients in this GPU's memory: staged
+        if (a.n_ranks <= 2 && device_resident(const_cast<void* const*>(a.grads), a.n_ranks, s))
+            return a.n_ranks == 2 ? run_reduce_staged<DT, CLIP, 2>(a, s, overlap)
+                                  : run_reduce_staged<DT, CLIP, 1>(a, s, overlap);
+    }
     if (a.n_ranks <= 2) {
         const int grid = grid_for((const void*)k_reduce<HDEST, DT, CLIP, 4>, groups);
         return launch_step_kernel(k_reduce<HDEST, DT, CLIP, 4>, grid, s, overlap, a);

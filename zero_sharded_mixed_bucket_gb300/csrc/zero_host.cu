@@ -386,12 +386,15 @@ zero_status_t end_impl(const zero_config_t* c, const zero_plan_t* p, zero_buffer
     if (e != cudaSuccess) return cuda_fail(e, "reading the overflow flag");
     e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "synchronising the step");
-    uint32_t flag;
+    uint32_t flag, err;
     double norm;
     float clip;
     std::memcpy(&flag, head + ws::kFlag, 4);
+    std::memcpy(&err, head + ws::kErr, 4);
     std::memcpy(&norm, head + ws::kNorm, 8);
     std::memcpy(&clip, head + ws::kClip, 4);
+    if (err)   // a kernel gave up a bounded wait; it also raised the flag, so no update ran
+        return fail(ZERO_ETIMEOUT, "a bounded wait inside a step kernel ran out; the step was not applied");
     const bool overflow = flag != 0;
 
     // After an overflowed fused step the 16-bit parameters the bucket kernels
@@ -895,13 +898,15 @@ zero_status_t zero_dev_state_read(const void* dev_state, zero_state_t* s, zero_s
     if (last) {
         std::memset(last, 0, sizeof *last);
         last->t = d.t;
-        last->overflow = d.last_overflow;
+        last->overflow = d.last_overflow & 1u;
         last->skipped = d.last_skipped;
         last->grad_norm = d.last_grad_norm;
         last->clip_coef = d.last_clip_coef;
         last->new_loss_scale = d.loss_scale;
         last->path = -1;
     }
+    if (d.last_overflow & 2u)
+        return fail(ZERO_ETIMEOUT, "a bounded wait inside the last step's kernels ran out; that step was not applied");
     return ZERO_OK;
 }
 

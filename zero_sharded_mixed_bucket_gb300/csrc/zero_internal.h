@@ -14,6 +14,7 @@ constexpr int kThreads = 128;   // threads per block of every streaming kernel (
 // Workspace layout (caller-provided device memory, zeroed by zero_step_begin).
 namespace ws {
 constexpr size_t kFlag = 0;     // uint32: 1 once any reduced gradient element is inf/NaN
+constexpr size_t kErr = 4;      // uint32: 1 if a kernel gave up a bounded wait (the step is then skipped)
 constexpr size_t kNorm = 8;     // double: ||g||_2 (two-pass with clipping)
 constexpr size_t kClip = 16;    // float: clip coefficient
 constexpr size_t kAcc = 32;     // 4 x uint64: 32-bit limbs of the fixed-point sum of squares
