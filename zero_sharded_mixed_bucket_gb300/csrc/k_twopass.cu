@@ -386,9 +386,32 @@ __device__ double big_to_double(const unsigned long long big[kBigWords], int sca
     return scalbn((double)mant, exp + scale_exp);
 }
 
+// One warp: the lanes read the sum's limbs and the 256 exponent bins at once
+// (8 bins each) and mark the non-zero bins by ballot; lane 0 then folds the
+// limbs and only those bins into the big integer, in exponent order.
+// Launched as a programmatic dependent of the step's last pass-1 kernel: it
+// waits for that kernel (hence every pass-1 kernel) to complete first.
 __global__ void k_finalize(const FinalArgs a)
 {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    allow_next_grid();   // the first update kernel may launch; it waits for this one
+    wait_prev_grid();
+    if (blockIdx.x != 0) return;
+    __shared__ unsigned long long sbins[256];
+    __shared__ uint32_t nonzero[8];
+    const int lane = threadIdx.x;
+    const unsigned long long* bins = reinterpret_cast<const unsigned long long*>(a.ws + ws::kBins);
+    unsigned long long b[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++)
+        b[k] = bins[k * 32 + lane];
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        sbins[k * 32 + lane] = b[k];
+        const uint32_t m = __ballot_sync(0xffffffffu, b[k] != 0ull);
+        if (lane == 0) nonzero[k] = m;
+    }
+    __syncwarp();
+    if (lane != 0) return;
     const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(a.ws + ws::kFlag);
     double* norm_out = reinterpret_cast<double*>(a.ws + ws::kNorm);
     float* clip_out = reinterpret_cast<float*>(a.ws + ws::kClip);
@@ -405,11 +428,12 @@ __global__ void k_finalize(const FinalArgs a)
     const unsigned long long* limbs = reinterpret_cast<const unsigned long long*>(a.ws + ws::kAcc);
     for (int k = 0; k < 4; k++)
         big_add(big, limbs[k], 2 * (win_lo - emin) + 32 * k);
-    const unsigned long long* bins = reinterpret_cast<const unsigned long long*>(a.ws + ws::kBins);
-    for (int e = 0; e < 256; e++) {
-        if (!bins[e]) continue;
-        const int E = a.dtype == kBF16 ? (e ? e : 1) - 134 : (e ? e : 1) - 25;
-        big_add(big, bins[e], 2 * (E - emin));
+    for (int k = 0; k < 8; k++) {
+        for (uint32_t m = nonzero[k]; m; m &= m - 1u) {
+            const int e = k * 32 + __ffs(m) - 1;
+            const int E = a.dtype == kBF16 ? (e ? e : 1) - 134 : (e ? e : 1) - 25;
+            big_add(big, sbins[e], 2 * (E - emin));
+        }
     }
     const double sumsq = big_to_double(big, 2 * emin);
     const double norm = __dmul_rn(__dsqrt_rn(sumsq), inv);
@@ -502,10 +526,9 @@ cudaError_t launch_reduce(int stage, int dtype, bool clip, const StepArgs& a, cu
     return clip ? reduce_dt<kF16, true>(stage, a, s, overlap) : reduce_dt<kF16, false>(stage, a, s, overlap);
 }
 
-cudaError_t launch_finalize(const FinalArgs& a, cudaStream_t s)
+cudaError_t launch_finalize(const FinalArgs& a, cudaStream_t s, bool overlap)
 {
-    k_finalize<<<1, 32, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(k_finalize, 1, 32, s, overlap, a);
 }
 
 }  // namespace zg

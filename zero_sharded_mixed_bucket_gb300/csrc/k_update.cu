@@ -11,9 +11,12 @@ namespace {
 template <int STAGE, int DT, bool CLIP, int OPT>
 __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ StepArgs a)
 {
-    // The first update kernel of a step is launched in plain stream order after
-    // the pass-1 kernels and the finalize, so the flag and the clip
-    // coefficient are final before any update kernel starts.
+    // The first update kernel of a step is a programmatic dependent of the
+    // finalize (or, without clipping, of the last pass-1 kernel): it waits for
+    // it before reading the flag and the clip coefficient, and only then lets
+    // the next update kernel launch, so those values are final for every
+    // update kernel.
+    if (a.wait_first) wait_prev_grid();
     allow_next_grid();
     if (*reinterpret_cast<volatile uint32_t*>(ws_flag(a.ws))) {
         wait_prev_grid();
@@ -95,6 +98,7 @@ __global__ void __launch_bounds__(kThreads) k_update_tiled(const __grid_constant
     constexpr int kTileGroups = kThreads * kTileSub;
     constexpr int64_t kTileElems = (int64_t)kTileGroups * V;
     __shared__ __align__(128) Vals<DT> tile[2][kTileGroups];
+    if (a.wait_first) wait_prev_grid();   // as k_update
     allow_next_grid();
     if (*reinterpret_cast<volatile uint32_t*>(ws_flag(a.ws))) {
         wait_prev_grid();

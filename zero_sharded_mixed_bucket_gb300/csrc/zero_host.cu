@@ -360,7 +360,7 @@ zero_status_t end_impl(const zero_config_t* c, const zero_plan_t* p, zero_buffer
             f.inv = (double)(float)(1.0 / ((double)s->loss_scale * (double)c->n_ranks));
             f.max_norm = (double)adam->max_grad_norm;
             f.dyn = nullptr;
-            e = launch_finalize(f, st);
+            e = launch_finalize(f, st, true);
             if (e != cudaSuccess) return cuda_fail(e, "launching the norm finalize kernel");
             launches++;
         }
@@ -368,7 +368,8 @@ zero_status_t end_impl(const zero_config_t* c, const zero_plan_t* p, zero_buffer
             StepArgs a = make_args(c, p, b, adam, s, false, c->stage <= 1 ? b->grads : nullptr, 0);
             a.lo = bk * c->bucket_elems;
             a.hi = a.lo + c->bucket_elems < c->n_params ? a.lo + c->bucket_elems : c->n_params;
-            e = launch_update(c->stage, c->dtype, c->optimizer, path.clip, a, st, bk > 0);
+            a.wait_first = bk == 0 ? 1 : 0;
+            e = launch_update(c->stage, c->dtype, c->optimizer, path.clip, a, st, true);
             if (e != cudaSuccess) return cuda_fail(e, "launching the update kernel");
             launches++;
         }
@@ -503,7 +504,7 @@ zero_status_t async_tail(const zero_config_t* c, const zero_plan_t* p, zero_buff
             f.inv = 0.0;
             f.max_norm = (double)adam->max_grad_norm;
             f.dyn = dyn;
-            e = launch_finalize(f, cs);
+            e = launch_finalize(f, cs, true);
             if (e != cudaSuccess) return cuda_fail(e, "launching the norm finalize kernel");
             launches++;
         }
@@ -512,7 +513,8 @@ zero_status_t async_tail(const zero_config_t* c, const zero_plan_t* p, zero_buff
             a.dyn = dyn;
             a.lo = bk * c->bucket_elems;
             a.hi = a.lo + c->bucket_elems < c->n_params ? a.lo + c->bucket_elems : c->n_params;
-            e = launch_update(c->stage, c->dtype, c->optimizer, path.clip, a, cs, bk > 0);
+            a.wait_first = bk == 0 ? 1 : 0;
+            e = launch_update(c->stage, c->dtype, c->optimizer, path.clip, a, cs, true);
             if (e != cudaSuccess) return cuda_fail(e, "launching an update kernel");
             launches++;
         }

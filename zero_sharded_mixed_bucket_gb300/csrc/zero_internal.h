@@ -71,7 +71,9 @@ struct StepArgs {
     AdamHP hp;
     int32_t win_lo;                 // lowest exponent E of the sum-of-squares window
     const Dyn* dyn;                 // device-state step: scalars above come from here (else NULL)
-    int32_t wait_first;             // launched early after the prepare kernel: wait for it before anything else
+    int32_t wait_first;             // launched early after a kernel whose results it reads (the prepare kernel
+                                    // before a step's first bucket, the finalize or the last pass-1 kernel
+                                    // before the first update): wait for it before anything else
 };
 
 struct FinalArgs {
@@ -111,7 +113,7 @@ struct GatherArgs {
 // step pass, launched by the library itself.
 cudaError_t launch_fused(int stage, int dtype, int opt, const StepArgs& a, cudaStream_t s, bool overlap);
 cudaError_t launch_reduce(int stage, int dtype, bool clip, const StepArgs& a, cudaStream_t s, bool overlap);
-cudaError_t launch_finalize(const FinalArgs& a, cudaStream_t s);
+cudaError_t launch_finalize(const FinalArgs& a, cudaStream_t s, bool overlap);
 cudaError_t launch_update(int stage, int dtype, int opt, bool clip, const StepArgs& a, cudaStream_t s,
                           bool overlap);
 cudaError_t launch_restore(int stage, int dtype, const StepArgs& a, cudaStream_t s);
