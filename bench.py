@@ -822,7 +822,7 @@ def stage3_arm(args):
     n_prof = len(prof)
     n_gathers = sum(1 for kind, _ in job.schedule if kind == "gather")
     g_bytes = n_prof * 2 * n * (2 + 2 * job.N)
-    f_bytes = n_prof * n * bench_bytes(3, job.N)
+    f_bytes = n_prof * n * bench_bytes(3, job.N)    # every bucket kernel of a profiled step
     g_launch = g_bytes / (n_prof * n_gathers)
     g_ach = g_bytes / (g_ms * 1e-3) / 1e9
     f_ach = f_bytes / (b_ms * 1e-3) / 1e9
@@ -859,16 +859,16 @@ def stage3_arm(args):
                      "share_of_step_bytes": 2 * (2 + 2 * job.N) / job.bytes_per_param(),
                      "frac_of_chip_nominal": g_ach / CHIP_HBM_GBS, "chip_nominal_gbs": CHIP_HBM_GBS,
                      "chip_nominal_source": CHIP_HBM_SOURCE,
-                     "timing": "CUDA events recorded on the step's stream between consecutive launches on every "
-                               "%dth timed step (%d of %d); each interval holds one kernel" % (
-                                   PROFILE_EVERY, n_prof, args.steps)},
+                     "timing": "CUDA events recorded on the step's stream between consecutive library calls on "
+                               "every %dth timed step (%d of %d); each gather interval holds one gather kernel, each "
+                               "run interval one layer's bucket kernels" % (PROFILE_EVERY, n_prof, args.steps)},
         "kernels": {"k_fused<stage 3, fp16, adam>": {
             "achieved": f_ach, "frac": f_ach / peak, "bytes_per_param": bench_bytes(3, job.N),
             "launches": n_prof * job.plan.n_buckets, "avg_launch_ms": b_ms / (n_prof * job.plan.n_buckets),
             "algorithmic_bytes_per_launch": f_bytes / (n_prof * job.plan.n_buckets)}},
         "gpu_launches": args.steps * job.launches_per_step(),
-        "step_api": "zero_step_begin_async / zero_gather_layer / zero_step_bucket_async / zero_step_end_async "
-                    "(step state in device memory, steps enqueued back to back)",
+        "step_api": "zero_step_begin_async / zero_gather_layer / zero_step_buckets_async (one run of buckets per "
+                    "layer) / zero_step_end_async (step state in device memory, steps enqueued back to back)",
     }
     out["clocks"] = clocks_summary(rows, t0, t1)
     if args.headline_only:

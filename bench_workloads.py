@@ -84,6 +84,52 @@ class StagedGrads:
         return ms
 
 
+def copy_ceiling(nbytes, reps=20, flush=None, graph=False):
+    """Milliseconds of one device copy moving `nbytes` in all (nbytes/2 read,
+    nbytes/2 written) -- the floor of any kernel with that traffic, measured
+    the way the step beside it is: back to back (one pair of events around
+    `reps` copies), or, given a flush buffer, one copy per flush with events
+    around the copy alone; graph=True replays the copy from a captured CUDA
+    graph, as the step it is compared with is."""
+    import torch
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.current_stream(dev)
+    half = max(16, (nbytes // 2) // 16 * 16)
+    src = torch.empty(half, dtype=torch.uint8, device=dev)
+    dst = torch.empty(half, dtype=torch.uint8, device=dev)
+    src.fill_(1)
+    run = lambda: dst.copy_(src)
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(s)
+        with torch.cuda.graph(g, stream=cap):
+            dst.copy_(src)
+        s.wait_stream(cap)
+        run = g.replay
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    if flush is None:
+        e0, e1 = _ev(), _ev()
+        e0.record(s)
+        for _ in range(reps):
+            run()
+        e1.record(s)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+    times = []
+    for k in range(reps):
+        flush.fill_(k & 0xff)
+        e0, e1 = _ev(), _ev()
+        e0.record(s)
+        run()
+        e1.record(s)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return sum(times) / reps
+
+
 # ---------------------------------------------------------------------------
 class Stage3Job:
     """ZeRO stage 3 on a transformer parameter list (default: 32 layers,
@@ -135,18 +181,32 @@ class Stage3Job:
         for ln in self.layers:
             starts.append(starts[-1] + ln)
         self.starts = starts
-        # the step's launches in order: forward gathers, then per layer
-        # (reversed) its gather and the buckets that start inside it
+        # the step's library calls in order: forward gathers, then per layer
+        # (reversed) its gather and one run of the buckets that start inside it
         sched = [("gather", l) for l in range(len(self.layers))]
         nxt = self.plan.n_buckets - 1
         for l in reversed(range(len(self.layers))):
             sched.append(("gather", l))
+            run = []
             while nxt >= 0 and nxt * bucket >= starts[l]:
-                sched.append(("bucket", nxt))
+                run.append(nxt)
                 nxt -= 1
+            if run:
+                sched.append(("buckets", run))
         assert nxt == -1
         self.schedule = sched
+        self.n_bucket_kernels = self.plan.n_buckets
+        self._runs = {}           # run index -> (indices, flat gradient pointers) for the ring
+        for k, (kind, x) in enumerate(sched):
+            if kind == "buckets":
+                self._runs[k] = self._run_arrays(x, lambda b: self.ring_ptrs[b % len(self.ring_ptrs)])
         torch.cuda.synchronize(device)
+
+    def _run_arrays(self, run, grad_ptrs):
+        import ctypes
+        idx = (ctypes.c_int64 * len(run))(*run)
+        flat = self.zg.ptr_array([p for b in run for p in list(grad_ptrs(b))])
+        return idx, flat
 
     def bucket_len(self, b):
         lo = b * self.B
@@ -160,15 +220,18 @@ class Stage3Job:
         return 2 * (2 + 2 * self.N) + bench.bytes_per_param(3, self.N)
 
     def launches_per_step(self):
-        return 2 + len(self.schedule)      # prepare, gathers and buckets, restore/commit
+        # prepare, the gathers, the bucket kernels, restore/commit
+        return 2 + sum(1 for kind, _ in self.schedule if kind == "gather") + self.n_bucket_kernels
 
     def step(self, events=None, grad_ptrs=None, before_bucket=None, after_bucket=None):
         """Enqueue one step on the job's stream; never synchronises.
         events: None, or len(schedule)+1 CUDA events recorded between the
-        launches (event k before schedule entry k).  grad_ptrs(b): the 64
-        gradient pointers of bucket b (default: ring set b mod ring);
-        before_bucket(b) / after_bucket(b): stream hooks around bucket b's
-        kernel (end-to-end copies)."""
+        library calls (event k before schedule entry k).  grad_ptrs(b): the
+        64 gradient pointers of bucket b (default: ring set b mod ring).
+        Each layer's buckets go to the library as one run
+        (zero_step_buckets_async: consecutive kernels overlap their edges),
+        unless before_bucket(b) / after_bucket(b) stream hooks are given
+        (end-to-end copies): then one call per bucket, in plain stream order."""
         zg, s = self.zg, self.stream
         zg.zero_step_begin_async(self.cfg, self.plan, self.bufs, self.adam, self.dev_state, s)
         for k, (kind, x) in enumerate(self.schedule):
@@ -176,13 +239,17 @@ class Stage3Job:
                 events[k].record(s)
             if kind == "gather":
                 zg.zero_gather_layer(self.cfg, self.plan, x, self.shard_ptrs, self.dst_ptrs, s)
+            elif before_bucket or after_bucket:
+                for b in x:
+                    if before_bucket:
+                        before_bucket(b)
+                    ptrs = grad_ptrs(b) if grad_ptrs else self.ring_ptrs[b % len(self.ring_ptrs)]
+                    zg.zero_step_bucket_async(self.cfg, self.plan, self.bufs, self.adam, b, ptrs, s)
+                    if after_bucket:
+                        after_bucket(b)
             else:
-                if before_bucket:
-                    before_bucket(x)
-                ptrs = grad_ptrs(x) if grad_ptrs else self.ring_ptrs[x % len(self.ring_ptrs)]
-                zg.zero_step_bucket_async(self.cfg, self.plan, self.bufs, self.adam, x, ptrs, s)
-                if after_bucket:
-                    after_bucket(x)
+                idx, flat = self._runs[k] if grad_ptrs is None else self._run_arrays(x, grad_ptrs)
+                zg.zero_step_buckets_async(self.cfg, self.plan, self.bufs, self.adam, idx, flat, s)
         if events is not None:
             events[len(self.schedule)].record(s)
         zg.zero_step_end_async(self.cfg, self.plan, self.bufs, self.adam, self.dev_state, s)
@@ -265,6 +332,7 @@ def leg_cfg1(args):
     assert last.overflow == 0 and st.t == state.t + 1 + args.warmup + args.steps
     ms_graph = sum(gwalls) / len(gwalls)
     ms = min(ms_sync, ms_graph)
+    ceil_ms = copy_ceiling(plan.hbm_bytes_fused, reps=args.steps, flush=flush, graph=True)
     out = _base(n / (ms * 1e-3) / 1e9, ms, args.steps, args.warmup,
                 "stage 2, flat 2^20 params, N_d=4, fp16 grads N(0,1e-3) x 1024 static loss scale, one bucket",
                 {"n_params": n, "n_ranks": N, "stage": 2, "l2": "flushed before every step (256 MB write)"})
@@ -272,6 +340,9 @@ def leg_cfg1(args):
                     "graph of zero_step_async": {"ms_per_step": ms_graph, "value": n / (ms_graph * 1e-3) / 1e9}}
     out["mode"] = "graph of zero_step_async" if ms_graph <= ms_sync else "zero_step_stage2"
     out["roofline"] = _roofline(plan.hbm_bytes_fused, sum(spans) / len(spans), "k_fused<stage 2, fp16>")
+    out["copy_ceiling"] = {"ms": ceil_ms, "step_over_copy": ms / ceil_ms,
+                           "note": "one device copy of the step's %d bytes (half read, half written), replayed from a "
+                                   "CUDA graph after the same 256 MB flush" % plan.hbm_bytes_fused}
     out["note"] = "42 MB per step: launch latency dominates; a parity case, not a bandwidth one"
     return out
 
@@ -528,6 +599,12 @@ def sweep_point(n, N, dtype_name, steps, warm):
            "hbm_gbs": n * bpp / (ms * 1e-3) / 1e9, "bytes_per_param": bpp, "grad_norm": norms[-1],
            "clip_coef": res.clip_coef, "t": state.t, "step_api": api, "ms_per_step_sync": ms_sync,
            "gradients": "resident in HBM" if resident else "generated per bucket into staging (excluded)"}
+    if resident and n * bpp <= 4 << 30:
+        # the same bytes as one device copy, back to back like the steps above
+        c = copy_ceiling(n * bpp, reps=20)
+        out["copy_ceiling"] = {"ms": c, "step_over_copy": ms / c,
+                               "note": "one device copy moving the step's %d bytes (half read, half written), "
+                                       "timed back to back like the steps" % (n * bpp)}
     del bufs, staging
     torch.cuda.empty_cache()
     return out

@@ -334,6 +334,17 @@ zero_status_t zero_step_bucket(const zero_config_t* cfg, const zero_plan_t* plan
 zero_status_t zero_step_end(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
                             const zero_adam_t* adam, zero_state_t* state, void* stream,
                             zero_step_result_t* out);
+/* Several buckets of the same step in one call: buckets[0..count), in that
+ * order, each exactly once in the step as for zero_step_bucket.
+ * bucket_grads: NULL, or (stages 2 and 3) count*N device pointers, bucket k's
+ * N windows at bucket_grads[k*N .. k*N+N).  The first kernel follows plain
+ * stream order; each later one is a programmatic dependent of the one before
+ * (it may start while its predecessor drains, as inside zero_step), so every
+ * window must hold its gradients before the call's first kernel runs.  Same
+ * errors as zero_step_bucket (ZERO_EINVAL for an index out of range). */
+zero_status_t zero_step_buckets(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                                const zero_adam_t* adam, const zero_state_t* state, const int64_t* buckets,
+                                int32_t count, void* const* bucket_grads, void* stream);
 
 /* Stage 3: copy layer `layer`'s 16-bit parameters from the owners' shards
  * (param_shards[r], P elements each) into each of the n_dst destination
@@ -388,6 +399,11 @@ zero_status_t zero_step_begin_async(const zero_config_t* cfg, const zero_plan_t*
 zero_status_t zero_step_bucket_async(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
                                      const zero_adam_t* adam, int64_t bucket, void* const* bucket_grads,
                                      void* stream);
+/* zero_step_buckets for the device-state protocol (between begin_async and
+ * end_async). */
+zero_status_t zero_step_buckets_async(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
+                                      const zero_adam_t* adam, const int64_t* buckets, int32_t count,
+                                      void* const* bucket_grads, void* stream);
 zero_status_t zero_step_end_async(const zero_config_t* cfg, const zero_plan_t* plan, zero_buffers_t* bufs,
                                   const zero_adam_t* adam, void* dev_state, void* stream, int32_t* kernel_launches);
 /* Copy the block to the host (synchronises `stream`): the current step state

@@ -364,3 +364,38 @@ def test_pa_argument_checks():
     forged = zg.zero_pa_plan_t.from_buffer_copy(p)
     forged.shard_elems += 8
     assert L.zero_pa_gather(ctypes.byref(forged), arr(good), arr(good[:1]), 1, None) == zg.ZERO_EINVAL
+
+
+def test_bucket_runs_checked_before_any_launch():
+    """zero_step_buckets / zero_step_buckets_async refuse a bad run on the host
+    (made-up device addresses: nothing is launched)."""
+    L = zg.lib()
+    cfg = zg.Config(1000, 4, 2, 64)
+    plan = zg.zero_plan(cfg)
+    fb = _FakeBuffers(4)
+    adam = zg.zero_adam_t(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8)
+    state = zg.zero_state_t(t=0, loss_scale=1.0, min_loss_scale=1.0)
+    idx = lambda xs: (ctypes.c_int64 * max(1, len(xs)))(*xs)
+    good = [0x70000000 + 0x100000 * r for r in range(8)]
+    grads = (ctypes.c_void_p * 8)(*good)
+
+    def both(buckets, count, g, stage_cfg=cfg, stage_plan=plan):
+        a = L.zero_step_buckets(ctypes.byref(stage_cfg.c), ctypes.byref(stage_plan), ctypes.byref(fb.b),
+                                ctypes.byref(adam), ctypes.byref(state), buckets, count, g, None)
+        b = L.zero_step_buckets_async(ctypes.byref(stage_cfg.c), ctypes.byref(stage_plan), ctypes.byref(fb.b),
+                                      ctypes.byref(adam), buckets, count, g, None)
+        return a, b
+
+    assert both(idx([0, 16]), 2, None) == (zg.ZERO_EINVAL, zg.ZERO_EINVAL)      # 16 buckets: 0..15
+    assert "outside 0..15" in zg.zero_last_error()
+    assert both(idx([-1]), 1, None) == (zg.ZERO_EINVAL, zg.ZERO_EINVAL)
+    assert both(None, 3, None) == (zg.ZERO_EINVAL, zg.ZERO_EINVAL)
+    assert both(idx([0]), -1, None) == (zg.ZERO_EINVAL, zg.ZERO_EINVAL)
+    assert both(idx([]), 0, None) == (zg.ZERO_OK, zg.ZERO_OK)                    # an empty run launches nothing
+    bad = (ctypes.c_void_p * 8)(*(good[:5] + [0x70000008] + good[6:]))        # bucket 1, rank 1 misaligned
+    assert both(idx([2, 3]), 2, bad) == (zg.ZERO_EALIGN, zg.ZERO_EALIGN)
+    assert "bucket_grads[1]" in zg.zero_last_error()
+    cfg1 = zg.Config(1000, 4, 1, 64)
+    plan1 = zg.zero_plan(cfg1)
+    assert both(idx([0, 1]), 2, grads, cfg1, plan1) == (zg.ZERO_EINVAL, zg.ZERO_EINVAL)
+    assert "stage 2 or 3" in zg.zero_last_error()

@@ -758,3 +758,49 @@ def test_staged_pass1_many_tiles_per_block_and_staging(N):
     ref = job.oracle_step(grads)
     last.path = 1
     job.check(last, ref)
+
+
+@pytest.mark.parametrize("stage,shadow,max_norm,api", [(2, True, 0.0, "sync"), (3, True, 0.0, "async"),
+                                                       (2, False, 1.0, "async"), (1, True, 0.0, "sync"),
+                                                       (3, False, 0.0, "sync")])
+def test_bucket_runs(stage, shadow, max_norm, api):
+    """Buckets given to the library in runs (zero_step_buckets and its
+    device-state twin): runs of 1-3 buckets in an arbitrary order, whose
+    consecutive kernels overlap their edges; stages 2/3 from separate
+    windows per bucket (the flat pointer table), stage 1 from the full
+    gradient buffers.  Two steps, each against the oracle bit for bit."""
+    n, N, B = 7 * 3000 + 13, 4, 3000
+    job = Job(n, N, stage, B, 8, shadow=shadow, max_norm=max_norm, loss_scale=16.0)
+    s = torch.cuda.current_stream()
+    runs = [[6, 5], [0], [3, 1, 2], [4, 7]]
+    dev = None
+    if api == "async":
+        dev = torch.zeros(zg.DEV_STATE_BYTES // 8, dtype=torch.int64, device="cuda")
+        zg.zero_dev_state_init(dev, job.adam, job.state, s)
+    for t in (1, 2):
+        grads = job.make_grads(t)
+        if stage >= 2:
+            win = [[torch.from_numpy(grads[r][b * B:min((b + 1) * B, n)].view(np.int16).copy()).cuda()
+                    for r in range(N)] for b in range(job.plan.n_buckets)]
+        else:
+            job.load_grads(grads)
+        if api == "sync":
+            zg.zero_step_begin(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
+        else:
+            zg.zero_step_begin_async(job.cfg, job.plan, job.bufs, job.adam, dev, s)
+        for run in runs:
+            table = [[w.data_ptr() for w in win[b]] for b in run] if stage >= 2 else None
+            if api == "sync":
+                zg.zero_step_buckets(job.cfg, job.plan, job.bufs, job.adam, job.state, run, table, s)
+            else:
+                zg.zero_step_buckets_async(job.cfg, job.plan, job.bufs, job.adam, run, table, s)
+        if api == "sync":
+            res = zg.zero_step_end(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
+        else:
+            zg.zero_step_end_async(job.cfg, job.plan, job.bufs, job.adam, dev, s)
+            st, res = zg.zero_dev_state_read(dev, s)
+            job.state = st
+            res.path = 0 if (shadow and max_norm == 0) else 1
+        torch.cuda.synchronize()
+        ref = job.oracle_step(grads)
+        job.check(res, ref)

@@ -28,6 +28,7 @@ __all__ = [
     "DEV_STATE_BYTES", "zero_step_begin_async", "zero_step_bucket_async", "zero_step_end_async",
     "zero_pa_plan_t", "zero_pa_plan", "zero_pa_partition", "zero_pa_gather",
     "zero_step_begin", "zero_step_bucket", "zero_step_end", "zero_gather_layer", "zero_last_error",
+    "zero_step_buckets", "zero_step_buckets_async",
     "zero_version", "zero_set_profile_events", "zero_fetch_schedule", "Fetcher", "DeviceBuffers", "ptr_array",
 ]
 
@@ -123,6 +124,8 @@ def lib():
             "zero_step_begin_async": [cfg, plan, bufs, adam, c_vp, c_vp],
             "zero_step_bucket_async": [cfg, plan, bufs, adam, c_i64, P(c_vp), c_vp],
             "zero_step_end_async": [cfg, plan, bufs, adam, c_vp, c_vp, P(c_i32)],
+            "zero_step_buckets": [cfg, plan, bufs, adam, state, P(c_i64), c_i32, P(c_vp), c_vp],
+            "zero_step_buckets_async": [cfg, plan, bufs, adam, P(c_i64), c_i32, P(c_vp), c_vp],
             "zero_pa_plan": [c_i64, c_i32, c_i32, c_i64, P(zero_pa_plan_t)],
             "zero_pa_partition": [P(zero_pa_plan_t), P(c_vp), P(c_vp), c_vp],
             "zero_pa_gather": [P(zero_pa_plan_t), P(c_vp), P(c_vp), c_i32, c_vp],
@@ -364,6 +367,33 @@ def zero_step_bucket(cfg, plan, bufs, adam, state, bucket: int, bucket_grads=Non
     b = bufs.b if isinstance(bufs, DeviceBuffers) else bufs
     _check(lib().zero_step_bucket(_cfg(cfg), ctypes.byref(plan), ctypes.byref(b), ctypes.byref(adam),
                                   ctypes.byref(state), bucket, _ptr_array(bucket_grads), _stream(stream)))
+
+
+def _bucket_run(buckets, bucket_grads):
+    """(int64 array of indices, count, flat pointer array or None) of a run of buckets;
+    bucket_grads: None, a prebuilt ctypes pointer array (count*N), or one pointer list per bucket."""
+    idx = buckets if isinstance(buckets, ctypes.Array) else (c_i64 * len(buckets))(*[int(x) for x in buckets])
+    if bucket_grads is None or isinstance(bucket_grads, ctypes.Array):
+        g = bucket_grads
+    else:
+        g = _ptr_array([int(p) for ptrs in bucket_grads for p in ptrs])
+    return idx, len(idx), g
+
+
+def zero_step_buckets(cfg, plan, bufs, adam, state, buckets, bucket_grads=None, stream=None):
+    """Several buckets of one step in one call, consecutive kernels overlapping their edges."""
+    b = bufs.b if isinstance(bufs, DeviceBuffers) else bufs
+    idx, n, g = _bucket_run(buckets, bucket_grads)
+    _check(lib().zero_step_buckets(_cfg(cfg), ctypes.byref(plan), ctypes.byref(b), ctypes.byref(adam),
+                                   ctypes.byref(state), idx, n, g, _stream(stream)))
+
+
+def zero_step_buckets_async(cfg, plan, bufs, adam, buckets, bucket_grads=None, stream=None):
+    """zero_step_buckets between zero_step_begin_async and zero_step_end_async."""
+    b = bufs.b if isinstance(bufs, DeviceBuffers) else bufs
+    idx, n, g = _bucket_run(buckets, bucket_grads)
+    _check(lib().zero_step_buckets_async(_cfg(cfg), ctypes.byref(plan), ctypes.byref(b), ctypes.byref(adam), idx,
+                                         n, g, _stream(stream)))
 
 
 def zero_step_end(cfg, plan, bufs, adam, state, stream=None) -> zero_step_result_t:

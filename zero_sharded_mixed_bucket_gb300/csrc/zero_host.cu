@@ -665,6 +665,47 @@ zero_status_t zero_step_bucket(const zero_config_t* c, const zero_plan_t* p, zer
     return bucket_impl(c, p, b, adam, s, bucket, bucket_grads, static_cast<cudaStream_t>(stream), false);
 }
 
+namespace {
+// Arguments of a run of buckets: indices in range, gradient pointers valid.
+zero_status_t check_run(const zero_config_t* c, const zero_plan_t* p, const zero_buffers_t* b,
+                        const int64_t* buckets, int32_t count, void* const* bucket_grads)
+{
+    if (count < 0) return fail(ZERO_EINVAL, "count %d < 0", count);
+    if (count > 0 && !buckets) return fail(ZERO_EINVAL, "buckets is NULL");
+    for (int32_t k = 0; k < count; k++)
+        if (buckets[k] < 0 || buckets[k] >= p->n_buckets)
+            return fail(ZERO_EINVAL, "buckets[%d] = %lld is outside 0..%lld", k, (long long)buckets[k],
+                        (long long)p->n_buckets - 1);
+    if (!bucket_grads) return count ? check_grads(c, b->grads, "grads") : ZERO_OK;
+    if (c->stage < 2)
+        return fail(ZERO_EINVAL, "per-bucket gradient buffers need stage 2 or 3 (stages 0/1 keep full gradients)");
+    for (int32_t k = 0; k < count; k++) {
+        zero_status_t st = check_grads(c, bucket_grads + (size_t)k * c->n_ranks, "bucket_grads");
+        if (st != ZERO_OK) return st;
+    }
+    return ZERO_OK;
+}
+}  // namespace
+
+zero_status_t zero_step_buckets(const zero_config_t* c, const zero_plan_t* p, zero_buffers_t* b,
+                                const zero_adam_t* adam, const zero_state_t* s, const int64_t* buckets,
+                                int32_t count, void* const* bucket_grads, void* stream)
+{
+    zero_status_t st = check_step(c, p, b, adam, s);
+    if (st != ZERO_OK) return st;
+    st = check_run(c, p, b, buckets, count, bucket_grads);
+    if (st != ZERO_OK) return st;
+    // the first kernel in plain stream order after whatever the caller ran;
+    // the rest of the run overlap their edges
+    for (int32_t k = 0; k < count; k++) {
+        st = bucket_impl(c, p, b, adam, s, buckets[k],
+                         bucket_grads ? bucket_grads + (size_t)k * c->n_ranks : nullptr,
+                         static_cast<cudaStream_t>(stream), k > 0);
+        if (st != ZERO_OK) return st;
+    }
+    return ZERO_OK;
+}
+
 zero_status_t zero_step_end(const zero_config_t* c, const zero_plan_t* p, zero_buffers_t* b, const zero_adam_t* adam,
                             zero_state_t* s, void* stream, zero_step_result_t* out)
 {
@@ -858,6 +899,34 @@ zero_status_t zero_step_bucket_async(const zero_config_t* c, const zero_plan_t* 
     const cudaError_t e = path.fused ? launch_fused(c->stage, c->dtype, c->optimizer, a, cs, false)
                                      : launch_reduce(c->stage, c->dtype, path.clip, a, cs, false);
     if (e != cudaSuccess) return cuda_fail(e, "launching the bucket kernel");
+    return ZERO_OK;
+}
+
+zero_status_t zero_step_buckets_async(const zero_config_t* c, const zero_plan_t* p, zero_buffers_t* b,
+                                      const zero_adam_t* adam, const int64_t* buckets, int32_t count,
+                                      void* const* bucket_grads, void* stream)
+{
+    const zero_state_t host_view = async_host_view();
+    zero_status_t st = check_step(c, p, b, adam, &host_view);
+    if (st != ZERO_OK) return st;
+    st = check_run(c, p, b, buckets, count, bucket_grads);
+    if (st != ZERO_OK) return st;
+    const Path path = choose_path(c, b, adam);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    for (int32_t k = 0; k < count; k++) {
+        NvtxRange range("zero_bucket", buckets[k]);
+        const int64_t lo = buckets[k] * c->bucket_elems;
+        void* const* g = bucket_grads ? bucket_grads + (size_t)k * c->n_ranks : nullptr;
+        StepArgs a = g ? make_args(c, p, b, adam, &host_view, path.fused, g, lo)
+                       : make_args(c, p, b, adam, &host_view, path.fused, b->grads, 0);
+        a.dyn = reinterpret_cast<const Dyn*>(static_cast<unsigned char*>(b->workspace) + ws::kDyn);
+        a.lo = lo;
+        a.hi = lo + c->bucket_elems < c->n_params ? lo + c->bucket_elems : c->n_params;
+        // the first kernel in plain stream order, the rest overlap their edges
+        const cudaError_t e = path.fused ? launch_fused(c->stage, c->dtype, c->optimizer, a, cs, k > 0)
+                                         : launch_reduce(c->stage, c->dtype, path.clip, a, cs, k > 0);
+        if (e != cudaSuccess) return cuda_fail(e, "launching a bucket kernel");
+    }
     return ZERO_OK;
 }
 
