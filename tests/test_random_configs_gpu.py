@@ -1,8 +1,10 @@
 """Random combinations of everything the step takes -- stage, N_d, sizes,
 bucket and alignment, value type, optimizer, shadow state or not, clipping,
 loss scaling, staged per-bucket gradients, and the entry point (one call,
-begin/bucket/end, the device-state step, its per-bucket form) -- each run
-for three steps (one of them overflowed) against the oracle, bit for bit.
+begin/bucket/end, the device-state step, its per-bucket form, and runs of
+buckets in a random order, plain and device-state) -- each run for three
+steps (the second overflowed by an inf at a random rank and element, so
+the buckets after it may skip) against the oracle, bit for bit.
 The combinations come from a fixed seed, so a failure names a reproducible
 case; ZG_RANDOM_SEED and ZG_RANDOM_CASES draw another set (a longer soak)."""
 import os
@@ -18,7 +20,7 @@ from tests.gpu_harness import Job, as_signed
 
 pytestmark = pytest.mark.gpu
 
-APIS = ("step", "per_bucket", "async", "per_bucket_async")
+APIS = ("step", "per_bucket", "async", "per_bucket_async", "runs", "runs_async")
 
 
 def _cases(k=96, seed=2024):
@@ -34,29 +36,43 @@ def _cases(k=96, seed=2024):
         opt = int(rng.choice([zg.ZERO_ADAM, zg.ZERO_SGD_MOMENTUM, zg.ZERO_SGD]))
         shadow = bool(rng.integers(0, 2))
         clip = dtype != oracle.FP32 and bool(rng.integers(0, 3) == 0)
-        api = APIS[int(rng.integers(0, 4))]
-        staged = api in ("per_bucket", "per_bucket_async") and stage >= 2 and bool(rng.integers(0, 2))
+        api = APIS[int(rng.integers(0, len(APIS)))]
+        staged = api != "step" and api != "async" and stage >= 2 and bool(rng.integers(0, 2))
         scale = float(rng.choice([1.0, 8.0, 1024.0]))
-        out.append((stage, N, n, B, A, dtype, opt, shadow, clip, api, staged, scale))
+        inj = (int(rng.integers(0, N)), int(rng.integers(0, n)))
+        order = int(rng.integers(0, 2 ** 31))       # seed of the bucket order and runs
+        out.append((stage, N, n, B, A, dtype, opt, shadow, clip, api, staged, scale, inj, order))
     return out
 
 
+def _runs(nb, seed):
+    """The buckets in a random order, cut into runs of 1 to 4."""
+    rng = np.random.default_rng(seed)
+    perm = [int(b) for b in rng.permutation(nb)]
+    runs = []
+    while perm:
+        k = int(rng.integers(1, 5))
+        runs.append(perm[:k])
+        perm = perm[k:]
+    return runs
+
+
 @pytest.mark.parametrize("case", _cases(int(os.environ.get("ZG_RANDOM_CASES", "96")),
-                                         int(os.environ.get("ZG_RANDOM_SEED", "2024"))), ids=lambda c: "s%d-N%d-n%d-B%d-A%d-dt%d-o%d-sh%d-c%d-%s-st%d" % (
-    c[0], c[1], c[2], c[3], c[4], c[5], c[6], c[7], c[8], c[9], c[10]))
+                                         int(os.environ.get("ZG_RANDOM_SEED", "2024"))), ids=lambda c: "s%d-N%d-n%d-B%d-A%d-dt%d-o%d-sh%d-c%d-%s-st%d-i%d.%d" % (
+    c[0], c[1], c[2], c[3], c[4], c[5], c[6], c[7], c[8], c[9], c[10], c[12][0], c[12][1]))
 def test_random_combination(case):
-    stage, N, n, B, A, dtype, opt, shadow, clip, api, staged, scale = case
+    stage, N, n, B, A, dtype, opt, shadow, clip, api, staged, scale, inj, order = case
     job = Job(n, N, stage, B, A, dtype=dtype, shadow=shadow, optimizer=opt, max_norm=1e-2 if clip else 0.0,
               loss_scale=scale, dynamic=True, growth=2, sigma=1e-3)
     dev = None
-    if api in ("async", "per_bucket_async"):
+    if api in ("async", "per_bucket_async", "runs_async"):
         dev = torch.zeros(zg.DEV_STATE_BYTES // 8, dtype=torch.int64, device="cuda")
         zg.zero_dev_state_init(dev, job.adam, job.state)
     s = torch.cuda.current_stream()
     vt = torch.int32 if dtype == oracle.FP32 else torch.int16
     staging = [torch.zeros(B, dtype=vt, device="cuda") for _ in range(N)] if staged else None
     for step in (1, 2, 3):
-        inject = ((N - 1, n - 1, synth.inf_bits(dtype)),) if step == 2 else ()
+        inject = ((inj[0], inj[1], synth.inf_bits(dtype)),) if step == 2 else ()
         grads = job.make_grads(step, inject)
         job.load_grads(grads)
         two_pass = clip or not shadow
@@ -65,6 +81,30 @@ def test_random_combination(case):
             res = fn(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
         elif api == "async":
             zg.zero_step_async(job.cfg, job.plan, job.bufs, job.adam, dev, s)
+        elif api in ("runs", "runs_async"):
+            is_async = api == "runs_async"
+            if is_async:
+                zg.zero_step_begin_async(job.cfg, job.plan, job.bufs, job.adam, dev, s)
+            else:
+                zg.zero_step_begin(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
+            windows = []                       # every bucket its own windows: a run's kernels overlap
+            for run in _runs(job.plan.n_buckets, order + step):
+                table = None
+                if staged:
+                    table = []
+                    for b in run:
+                        lo, hi = b * B, min((b + 1) * B, n)
+                        w = [torch.from_numpy(as_signed(grads[r][lo:hi]).copy()).cuda() for r in range(N)]
+                        windows.append(w)
+                        table.append([t.data_ptr() for t in w])
+                if is_async:
+                    zg.zero_step_buckets_async(job.cfg, job.plan, job.bufs, job.adam, run, table, s)
+                else:
+                    zg.zero_step_buckets(job.cfg, job.plan, job.bufs, job.adam, job.state, run, table, s)
+            if is_async:
+                zg.zero_step_end_async(job.cfg, job.plan, job.bufs, job.adam, dev, s)
+            else:
+                res = zg.zero_step_end(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
         else:
             is_async = api == "per_bucket_async"
             if is_async:
