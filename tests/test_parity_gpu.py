@@ -804,3 +804,51 @@ def test_bucket_runs(stage, shadow, max_norm, api):
         torch.cuda.synchronize()
         ref = job.oracle_step(grads)
         job.check(res, ref)
+
+
+def test_staged_wait_that_runs_out_reports_etimeout(monkeypatch):
+    """The staged pass 1's waits are bounded.  With the test hook
+    ZERO_TEST_WITHHOLD_TILE set, block 0 announces its first tile's bytes to
+    the stage's mbarrier but issues no copy, so its consumers' wait for that
+    tile, and its producer's wait for the stage's release, run out after 2 s
+    of global time.  The step is not applied and returns ZERO_ETIMEOUT (the
+    device-state step: zero_dev_state_read does), t and the loss scale
+    unchanged.  With the hook cleared the next steps run on the same context
+    and match the oracle."""
+    n, B, N = 3 * 40960 + 5, 40960, 2
+    job = Job(n, N, 2, B, 8, shadow=False, max_norm=1.0, loss_scale=64.0, dynamic=True)
+    s = torch.cuda.current_stream()
+    res, ref = job.step(job.make_grads(1))
+    job.check(res, ref)
+    before = [as_u32(t[:n]).copy() for t in job.bufs.state()]
+    p_before = as_u16(job.bufs.params16[1][:n]).copy()
+    grads = job.make_grads(2)
+    job.load_grads(grads)
+    monkeypatch.setenv("ZERO_TEST_WITHHOLD_TILE", "1")
+    with pytest.raises(zg.ZeroError) as e:
+        zg.zero_step_stage2(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
+    assert e.value.status == zg.ZERO_ETIMEOUT and "bounded wait" in str(e.value)
+    monkeypatch.delenv("ZERO_TEST_WITHHOLD_TILE")
+    assert job.state.t == 1 and job.state.loss_scale == 64.0
+    for a, b in zip(before, job.bufs.state()):
+        assert np.array_equal(a, as_u32(b[:n]))
+    assert np.array_equal(p_before, as_u16(job.bufs.params16[1][:n]))
+    res, ref = job.step(grads)                       # the same step again, now normally
+    job.check(res, ref)
+    # the device-state step
+    dev = torch.zeros(zg.DEV_STATE_BYTES // 8, dtype=torch.int64, device="cuda")
+    zg.zero_dev_state_init(dev, job.adam, job.state, s)
+    grads = job.make_grads(3)
+    job.load_grads(grads)
+    monkeypatch.setenv("ZERO_TEST_WITHHOLD_TILE", "1")
+    zg.zero_step_async(job.cfg, job.plan, job.bufs, job.adam, dev, s)
+    monkeypatch.delenv("ZERO_TEST_WITHHOLD_TILE")
+    with pytest.raises(zg.ZeroError) as e:
+        zg.zero_dev_state_read(dev, s)
+    assert e.value.status == zg.ZERO_ETIMEOUT
+    zg.zero_step_async(job.cfg, job.plan, job.bufs, job.adam, dev, s)
+    st, last = zg.zero_dev_state_read(dev, s)
+    assert st.t == 3 and st.loss_scale == 64.0
+    job.state = st
+    last.path = 1
+    job.check(last, job.oracle_step(grads))

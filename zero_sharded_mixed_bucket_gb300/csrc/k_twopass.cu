@@ -234,7 +234,9 @@ __global__ void __launch_bounds__(staged::kBlockThreads, 2) k_reduce_staged(cons
                 const int64_t tel = min((int64_t)kTileElems, a.hi - t0);
                 const uint32_t bytes = (uint32_t)(tel * 2) & ~15u;       // whole groups; a short last group is loaded by its thread
                 mbar_arrive_expect_tx(&full[st], NR * bytes);
-                if (bytes) {
+                // test hook: block 0's first tile announced but never copied
+                const bool withhold = a.withhold_tile && blockIdx.x == 0 && k == 0;
+                if (bytes && !withhold) {
 #pragma unroll
                     for (int r = 0; r < NR; r++)
                         bulk_load(stage_base + (size_t)(st * NR + r) * kTileElems,
@@ -243,11 +245,9 @@ __global__ void __launch_bounds__(staged::kBlockThreads, 2) k_reduce_staged(cons
             }
             if (!ok) report_timeout(a.ws);
             // the last fill of every stage has landed before the block exits
+            // (each wait bounded; one that runs out does not end the others)
             for (int j = k - kStages < 0 ? 0 : k - kStages; j < k; j++)
-                if (!mbar_wait(&full[j % kStages], (j / kStages) & 1)) {
-                    report_timeout(a.ws);
-                    break;
-                }
+                if (!mbar_wait(&full[j % kStages], (j / kStages) & 1)) report_timeout(a.ws);
         }
     } else {
         const int win_lo = a.dyn ? a.dyn->win_lo : a.win_lo;

@@ -71,6 +71,9 @@ struct StepArgs {
     AdamHP hp;
     int32_t win_lo;                 // lowest exponent E of the sum-of-squares window
     const Dyn* dyn;                 // device-state step: scalars above come from here (else NULL)
+    int32_t withhold_tile;          // test hook (environment ZERO_TEST_WITHHOLD_TILE): the staged pass 1's
+                                    // block 0 announces its first tile but issues no copy, so its bounded
+                                    // waits run out and the step reports ZERO_ETIMEOUT
     int32_t wait_first;             // launched early after a kernel whose results it reads (the prepare kernel
                                     // before a step's first bucket, the finalize or the last pass-1 kernel
                                     // before the first update): wait for it before anything else
