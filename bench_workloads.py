@@ -720,6 +720,9 @@ def leg_pa(args):
                     + (" -- the slices cross the host link both ways" if where == "host" else "")}
         del shards
     hb = runs["slices_in_hbm"]
+    # a copy of the all-gather's bytes after the same flush, for the ceiling
+    hb["gather_copy_ceiling_ms"] = copy_ceiling((1 + N) * 2 * A, reps=steps, flush=flush)
+    hb["gather_over_copy"] = hb["gather_ms"] / hb["gather_copy_ceiling_ms"]
     out = _base(A / (hb["gather_ms"] * 1e-3) / 1e9, hb["gather_ms"], steps, args.warmup,
                 "P_a: one activation checkpoint of the 1.5B GPT-2 example (batch 32 x sequence 1024 x hidden 1600, "
                 "fp16), N_m = 16 model-parallel ranks simulated; value = checkpoint values rebuilt per second by the "
