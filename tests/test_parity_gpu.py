@@ -226,6 +226,29 @@ def test_empty_model():
     assert res.kernel_launches == 0 and res.overflow == 0 and res.t == 1
 
 
+@pytest.mark.parametrize("api", ["sync", "async"])
+def test_empty_model_clipped(api):
+    """Zero parameters with clipping: the norm finalize runs with no pass-1
+    kernel before it (after the workspace clear, or the prepare kernel of a
+    device-state step); the norm is 0 and the coefficient 1."""
+    job = Job(0, 4, 2, 64, shadow=False, max_norm=1.0)
+    placeholder = torch.zeros(8, dtype=torch.int16, device="cuda")
+    job.bufs.b.reduced = placeholder.data_ptr()
+    s = torch.cuda.current_stream()
+    if api == "sync":
+        for t in (1, 2):
+            res = zg.zero_step_stage2(job.cfg, job.plan, job.bufs, job.adam, job.state, s)
+            assert res.kernel_launches == 1 and res.overflow == 0 and res.t == t
+            assert res.grad_norm == 0.0 and res.clip_coef == 1.0
+    else:
+        dev = torch.zeros(zg.DEV_STATE_BYTES // 8, dtype=torch.int64, device="cuda")
+        zg.zero_dev_state_init(dev, job.adam, job.state, s)
+        for t in (1, 2):
+            assert zg.zero_step_async(job.cfg, job.plan, job.bufs, job.adam, dev, s) == 3
+            st, last = zg.zero_dev_state_read(dev, s)
+            assert st.t == t and last.overflow == 0 and last.grad_norm == 0.0 and last.clip_coef == 1.0
+
+
 @pytest.mark.parametrize("stage", [2, 3])
 @pytest.mark.parametrize("shadow", [True, False])
 def test_per_bucket_protocol(stage, shadow):
