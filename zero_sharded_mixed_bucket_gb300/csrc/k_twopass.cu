@@ -44,6 +44,40 @@ __device__ __forceinline__ void finish_group(const StepArgs& a, int64_t i, int64
     }
 }
 
+// The reduced values of one group of one or two ranks' 16-bit gradients as
+// packed 16-bit additions: h = (g_0 [+ g_1]) + 0, two values per instruction.
+// This equals the rank-order fp32 sum (0 + g_0) + g_1 rounded once to 16 bits:
+// the fp32 sum of two 16-bit values is exact when their significands (11 bits
+// for binary16, 8 for bfloat16) fit together in fp32's 24, and otherwise the
+// smaller one lies below a quarter of the larger one's 16-bit ulp, so the
+// correctly rounded 16-bit sum and the rounded fp32 sum are both the larger
+// value; a single value is rounded exactly.  The trailing + 0 gives -0 + -0 the
+// +0 that (0 + -0) + -0 has.  Returns nonzero if any h is inf or NaN.
+template <int DT, int NR>
+__device__ __forceinline__ uint32_t sum16_group(const H16<8> q[NR], H16<8>& h)
+{
+    static_assert(NR == 1 || NR == 2, "one or two ranks");
+    uint32_t nf = 0;
+#pragma unroll
+    for (int p = 0; p < 4; p++) {
+        uint32_t w;
+        if constexpr (DT == kBF16) {
+            __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&q[0].w[p]);
+            if constexpr (NR == 2) x = __hadd2(x, *reinterpret_cast<const __nv_bfloat162*>(&q[1].w[p]));
+            x = __hadd2(x, __float2bfloat162_rn(0.0f));
+            w = *reinterpret_cast<const uint32_t*>(&x);
+        } else {
+            __half2 x = *reinterpret_cast<const __half2*>(&q[0].w[p]);
+            if constexpr (NR == 2) x = __hadd2(x, *reinterpret_cast<const __half2*>(&q[1].w[p]));
+            x = __hadd2(x, __float2half2_rn(0.0f));
+            w = *reinterpret_cast<const uint32_t*>(&x);
+        }
+        h.w[p] = w;
+        nf |= nonfinite_x2<DT>(w);
+    }
+    return nf;
+}
+
 // HDEST 0: write h to every rank's gradient buffer; 1: to the reduced buffer.
 // U > 1 (one or two ranks): each thread loads U groups, a grid stride
 // apart, before it sums any, so that enough bytes are in flight per thread
@@ -279,20 +313,19 @@ __global__ void __launch_bounds__(staged::kBlockThreads, 2) k_reduce_staged(cons
                             q[r] = ld_h16<8>(a.grads[r], i - a.grad_base, cnt);
                         }
                     }
-                    // rank order from 0: s = (0 + g_0) + g_1, as reduce_group
-                    float s[8];
+                    // h = round16((0 + g_0) + g_1), as packed 16-bit additions
+                    H16<8> h;
+                    bad |= sum16_group<DT, NR>(q, h) != 0;
+                    if constexpr (CLIP) {
+                        if constexpr (DT == kBF16) {
+                            sumsq_group_bf16(h, win_lo, acc, bins);
+                        } else {
 #pragma unroll
-                    for (int p = 0; p < 4; p++) {
-                        const float2 f = to_f32x2<DT>(q[0].w[p]);
-                        s[2 * p] = __fadd_rn(0.0f, f.x);
-                        s[2 * p + 1] = __fadd_rn(0.0f, f.y);
-                        if constexpr (NR == 2) {
-                            const float2 f1 = to_f32x2<DT>(q[1].w[p]);
-                            s[2 * p] = __fadd_rn(s[2 * p], f1.x);
-                            s[2 * p + 1] = __fadd_rn(s[2 * p + 1], f1.y);
+                            for (int p = 0; p < 4; p++)
+                                sumsq_add_f16x2(h.w[p], acc);
                         }
                     }
-                    finish_group<1, DT, CLIP>(a, i, i - a.grad_base, cnt, s, win_lo, bad, acc, bins);
+                    st_h16<8>(a.reduced, i, h, cnt);
                 }
             }
             __syncwarp();
