@@ -459,24 +459,79 @@ __device__ __forceinline__ void sumsq_add_f16x2(uint32_t w, U128& acc)
     }
 }
 
-// The squares of one group of 8 bfloat16 values.  Each square is m2 *
-// 2^(2(e - 134)) with m2 = M^2 < 2^16 and e = max(exponent field, 1); in
-// units of 2^(2(base - 134)), with base = max(e_max - 22, the window's first
-// exponent), a square is m2 << 2(e - base) < 2^60, and the group's 8 of them
-// add up exactly in 64 bits.  The sum then goes into the 128-bit accumulator
+// Nonzero (in bit 15 or 31) if a binary16 value of the packed pair has an
+// exponent field of 20 or more -- |h| >= 32, inf or NaN: adding 12 to the
+// masked field carries into the half's top bit exactly then, never across the
+// halves.
+__device__ __forceinline__ uint32_t f16x2_exp_ge20(uint32_t w)
+{
+    return ((w & 0x7c007c00u) + 0x30003000u) & 0x80008000u;
+}
+
+// The squares of one group of 8 binary16 values, when no exponent field is 20
+// or more (f16x2_exp_ge20 of every word is 0; the caller checks).  A value
+// with exponent field e and mantissa f is h = X * 2^-24 with X = M << E',
+// M = f + 1024 [e > 0], E' = max(e, 1) - 1, so h^2 = X^2 * 2^-48 in the
+// accumulator's unit.  With e <= 19, X < 2^29 and X^2 < 2^58: the group's
+// eight squares add up in 64 bits, one multiply-add each on the integer
+// multiplier, then one 128-bit add.  The same integer as sumsq_add_f16x2.
+__device__ __forceinline__ void sumsq_group_f16_small(const H16<8>& h, U128& acc)
+{
+    unsigned long long s = 0ull;
+#pragma unroll
+    for (int p = 0; p < 4; p++) {
+        const uint32_t w = h.w[p];
+        // fields by multiplications, as in sumsq_add_f16x2
+        const uint32_t e[2] = {__umulhi(w & 0x00007c00u, 1u << 22), __umulhi(w & 0x7c000000u, 1u << 6)};
+        const uint32_t f[2] = {w & 0x000003ffu, __umulhi(w & 0x03ff0000u, 1u << 16)};
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+            const uint32_t hid = min(e[k], 1u);
+            const uint32_t X = (f[k] + hid * 0x400u) << (e[k] - hid);
+            asm("mad.wide.u32 %0, %1, %1, %0;" : "+l"(s) : "r"(X));
+        }
+    }
+    u128_add(acc, s, 0ull);
+}
+
+// The squares of one group of 8 binary16 values into the accumulator; sets
+// `bad` if one is inf or NaN.  Groups whose values all lie below 32 in
+// magnitude (gradients almost always do) take sumsq_group_f16_small; the
+// others the per-value path and the inf/NaN test.
+__device__ __forceinline__ void sumsq_group_f16(const H16<8>& h, U128& acc, bool& bad)
+{
+    uint32_t big = 0;
+#pragma unroll
+    for (int p = 0; p < 4; p++)
+        big |= f16x2_exp_ge20(h.w[p]);
+    if (!big) {
+        sumsq_group_f16_small(h, acc);
+        return;
+    }
+#pragma unroll
+    for (int p = 0; p < 4; p++) {
+        bad |= nonfinite_x2<kF16>(h.w[p]) != 0;
+        sumsq_add_f16x2(h.w[p], acc);
+    }
+}
+
+// The squares of one group of 8 bfloat16 values.  Each square is M^2 *
+// 2^(2(e - 134)) with M < 2^8 and e = max(exponent field, 1); in units of
+// 2^(2(base - 134)), with base = max(e_max - 22, the window's first
+// exponent), a square is (M << (e - base))^2 < 2^60, and the group's 8 of
+// them add up exactly in 64 bits.  The sum then goes into the 128-bit accumulator
 // with one shifted add, at window shift 2(base - first) <= 62.  A group with
 // a nonzero value below base, or whose largest value lies above the window,
 // takes the per-value path above instead (the same exact integer).  Fewer
 // integer instructions per value than the per-value bfloat16 path, whose
 // window test and shifted 128-bit adds form one dependent chain: measured on
 // GB300, N_d = 2, clipped two-pass step, 0.846 -> 0.864 of the copy
-// bandwidth.  (For binary16 the same scheme measured 0.885 against 0.890 for
-// the per-value path, which has no window test there.)
+// bandwidth (binary16 groups have their own form, sumsq_group_f16).
 __device__ __forceinline__ void sumsq_group_bf16(const H16<8>& h, int win_lo, U128& acc, unsigned long long* bins)
 {
     constexpr int kD = 22;                           // binades below the group's largest value
     const int first = win_lo + 134;                  // e of the window's first binade
-    uint32_t m2[8];
+    uint32_t Mv[8];
     int ex[8];
     int emax = 1;
 #pragma unroll
@@ -487,21 +542,23 @@ __device__ __forceinline__ void sumsq_group_bf16(const H16<8>& h, int win_lo, U1
         const uint32_t e = (j & 1) ? __umulhi(w & 0x7f800000u, 1u << 9) : __umulhi(w & 0x00007f80u, 1u << 25);
         const uint32_t f = (j & 1) ? __umulhi(w & 0x007f0000u, 1u << 16) : (w & 0x0000007fu);
         const uint32_t hid = __umulhi(e + 255u, 1u << 24);
-        const uint32_t M = f + hid * 0x80u;
-        m2[j] = M * M;
+        Mv[j] = f + hid * 0x80u;
         ex[j] = (int)(e + 1u - hid);                 // max(e, 1)
         emax = max(emax, ex[j]);
     }
     const int base = max(emax - kD, first);
-    // sign bit set iff some nonzero square lies below base
+    // a square relative to base is X^2 with X = M << (ex - base) < 2^30, so
+    // X^2 < 2^60 and the eight add up in 64 bits: one multiply-add each on
+    // the integer multiplier.  The sign bit of `below` is set iff some
+    // nonzero value lies below base.
     int below = 0;
-    unsigned long long b0 = 0ull, b1 = 0ull;
+    unsigned long long b = 0ull;
 #pragma unroll
     for (int j = 0; j < 8; j++) {
-        const int sh = 2 * (ex[j] - base);
-        below |= sh & -(int)m2[j];
-        const unsigned long long t = (unsigned long long)m2[j] << max(sh, 0);
-        if (j & 1) b1 += t; else b0 += t;
+        const int d = ex[j] - base;
+        below |= d & -(int)Mv[j];
+        const uint32_t X = Mv[j] << max(d, 0);
+        asm("mad.wide.u32 %0, %1, %1, %0;" : "+l"(b) : "r"(X));
     }
     const int top = 2 * (emax - first);              // window shift of the largest square
     if (below < 0 || top > 62) {
@@ -510,7 +567,6 @@ __device__ __forceinline__ void sumsq_group_bf16(const H16<8>& h, int win_lo, U1
             sumsq_add<kBF16>(h.get(j), win_lo, acc, bins);
         return;
     }
-    const unsigned long long b = b0 + b1;
     const int t = 2 * (base - first);                // 0..62
     u128_add(acc, b << t, (b >> 1) >> (63 - t));
 }

@@ -28,13 +28,10 @@ __device__ __forceinline__ void finish_group(const StepArgs& a, int64_t i, int64
     bad |= round_group<DT>(s, h) != 0;
     if constexpr (CLIP) {
         static_assert(DT != kF32, "no exact sum of squares for binary32 values");
-        if constexpr (DT == kBF16) {
+        if constexpr (DT == kBF16)
             sumsq_group_bf16(h, win_lo, acc, bins);
-        } else {
-#pragma unroll
-            for (int p = 0; p < kVecOf<DT> / 2; p++)
-                sumsq_add_f16x2(h.w[p], acc);
-        }
+        else
+            sumsq_group_f16(h, acc, bad);
     }
     if constexpr (HDEST == 0) {
         for (int r = 0; r < a.n_ranks; r++)
@@ -53,7 +50,7 @@ __device__ __forceinline__ void finish_group(const StepArgs& a, int64_t i, int64
 // correctly rounded 16-bit sum and the rounded fp32 sum are both the larger
 // value; a single value is rounded exactly.  The trailing + 0 gives -0 + -0 the
 // +0 that (0 + -0) + -0 has.  Returns nonzero if any h is inf or NaN.
-template <int DT, int NR>
+template <int DT, int NR, bool TEST = true>
 __device__ __forceinline__ uint32_t sum16_group(const H16<8> q[NR], H16<8>& h)
 {
     static_assert(NR == 1 || NR == 2, "one or two ranks");
@@ -73,7 +70,7 @@ __device__ __forceinline__ uint32_t sum16_group(const H16<8> q[NR], H16<8>& h)
             w = *reinterpret_cast<const uint32_t*>(&x);
         }
         h.w[p] = w;
-        nf |= nonfinite_x2<DT>(w);
+        if constexpr (TEST) nf |= nonfinite_x2<DT>(w);
     }
     return nf;
 }
@@ -313,17 +310,16 @@ __global__ void __launch_bounds__(staged::kBlockThreads, 2) k_reduce_staged(cons
                             q[r] = ld_h16<8>(a.grads[r], i - a.grad_base, cnt);
                         }
                     }
-                    // h = round16((0 + g_0) + g_1), as packed 16-bit additions
+                    // h = round16((0 + g_0) + g_1), as packed 16-bit additions;
+                    // clipped binary16 tests for inf/NaN inside the sum of squares
                     H16<8> h;
-                    bad |= sum16_group<DT, NR>(q, h) != 0;
+                    constexpr bool kSumsqTests = CLIP && DT == kF16;
+                    bad |= sum16_group<DT, NR, !kSumsqTests>(q, h) != 0;
                     if constexpr (CLIP) {
-                        if constexpr (DT == kBF16) {
+                        if constexpr (DT == kBF16)
                             sumsq_group_bf16(h, win_lo, acc, bins);
-                        } else {
-#pragma unroll
-                            for (int p = 0; p < 4; p++)
-                                sumsq_add_f16x2(h.w[p], acc);
-                        }
+                        else
+                            sumsq_group_f16(h, acc, bad);
                     }
                     st_h16<8>(a.reduced, i, h, cnt);
                 }
