@@ -875,3 +875,40 @@ def test_staged_wait_that_runs_out_reports_etimeout(monkeypatch):
     job.state = st
     last.path = 1
     job.check(last, job.oracle_step(grads))
+
+
+@pytest.mark.parametrize("N,stage", [(1, 2), (2, 2), (2, 0), (4, 3)])
+def test_clip_norm_f16_fast_path_edges(N, stage):
+    """The binary16 sum of squares adds a group's eight squares with integer
+    multiply-adds when no exponent field reaches 20 (|h| < 32).  Groups at
+    that edge: eight times the largest such value (31.98: the largest 64-bit
+    group sum), one value at 32 among small ones (the per-value path),
+    subnormals, zeros, mixed signs; one or two ranks (the staged pass 1), and
+    the per-thread pass 1 (stage 0, four ranks).  Norm, clip coefficient and
+    state equal the oracle's bit for bit."""
+    kinds = [0x4FFF, 0xCFFF, 0x5000, 0x0001, 0x8003, 0x0000, 0x3C00, 0x4BFF]
+    rng = np.random.default_rng(N * 10 + stage)
+    groups = []
+    for g in range(4096):
+        c = g % 5
+        if c == 0:
+            grp = [kinds[int(rng.integers(0, 2))]] * 8             # all at the largest fast-path magnitude
+        elif c == 1:
+            grp = [int(rng.integers(0, 0x4FFF + 1)) | (0x8000 if rng.integers(0, 2) else 0) for _ in range(8)]
+        elif c == 2:                                               # one value at 32: the per-value path
+            grp = [int(rng.integers(0, 0x3000)) for _ in range(8)]
+            grp[int(rng.integers(0, 8))] = 0x5000
+        elif c == 3:
+            grp = [int(rng.choice(kinds)) for _ in range(8)]
+        else:
+            grp = [int(rng.integers(0, 0x0400)) for _ in range(8)]  # subnormals and zero
+        groups.extend(grp)
+    n = len(groups) + 5
+    h = np.array(groups + [0x4FFF] * 5, np.uint16)
+    job = Job(n, N, stage, 8192, 8, dtype=FP16, shadow=False, max_norm=1.0, loss_scale=1.0)
+    # rank 0 carries h, the others +0, so the reduced gradient is h itself
+    grads = [h.copy()] + [np.zeros(n, np.uint16) for _ in range(N - 1)]
+    res, ref = job.step(grads)
+    assert res.overflow == 0 and res.path == 1
+    job.check(res, ref)
+    assert 0.0 < res.clip_coef < 1.0
