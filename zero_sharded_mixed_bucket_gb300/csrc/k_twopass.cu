@@ -7,6 +7,7 @@
 //                                   exact integer sum of squares.
 //   once                k_finalize: exact sum -> fp64 -> ||g||, clip coefficient.
 //   pass 2, per bucket  k_update:   optimizer update in place (k_update.cu).
+#include <cstdlib>
 #include <mutex>
 
 #include "dev_common.cuh"
@@ -506,6 +507,9 @@ cudaError_t run_reduce_staged(const StepArgs& a, cudaStream_t s, bool overlap)
     }
     const int64_t tiles = (a.hi - a.lo + kTileElems - 1) / kTileElems;
     const int grid = (int)(tiles < resident ? tiles : resident);
+    // the test hook that withholds a tile (see StepArgs::withhold_tile)
+    StepArgs args = a;
+    args.withhold_tile = std::getenv("ZERO_TEST_WITHHOLD_TILE") ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3((unsigned)kBlockThreads);
@@ -516,7 +520,7 @@ cudaError_t run_reduce_staged(const StepArgs& a, cudaStream_t s, bool overlap)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = overlap ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kernel, a);
+    return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
 template <int HDEST, int DT, bool CLIP>

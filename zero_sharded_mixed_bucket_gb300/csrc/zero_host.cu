@@ -5,7 +5,6 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
-#include <cstdlib>
 #include <cstring>
 #include <string>
 
@@ -313,7 +312,6 @@ StepArgs make_args(const zero_config_t* c, const zero_plan_t* p, const zero_buff
     }
     a.hp.mu = adam->momentum;
     a.win_lo = window_lo(c->dtype, s->loss_scale, N);
-    a.withhold_tile = std::getenv("ZERO_TEST_WITHHOLD_TILE") ? 1 : 0;
     return a;
 }
 
