@@ -652,14 +652,20 @@ def test_clip_norm_bf16_window_edges(S):
 
 def test_clip_norm_bf16_group_edges():
     """bfloat16 squares are summed 8 at a time (one aligned group of 8
-    elements) relative to the group's largest exponent field e_max, down to
-    e_max - 22 or the window's first binade, whichever is higher; a group with
-    a nonzero value below that, or with e_max above the window, is summed
-    value by value.  Groups built on each side of those edges (S*N = 2, so
-    the window's first exponent field is 96 and its last 127), a ragged tail;
-    the norm and clip coefficient equal the oracle's bit for bit."""
+    elements): first against a fixed window, the top 23 binades of the
+    accumulator's (exponent fields 105..127 here); a group with a nonzero
+    value outside it is summed relative to its largest exponent field e_max,
+    down to e_max - 22 or the window's first binade, whichever is higher; a
+    group with a nonzero value below that, or with e_max above the window, is
+    summed value by value.  Groups built on each side of those edges (S*N = 2,
+    so the window's first exponent field is 96 and its last 127), a ragged
+    tail; the norm and clip coefficient equal the oracle's bit for bit."""
     Z = None   # a zero
     patterns = [
+        [105, 127, 105, 126, Z, 110, 105, 127],  # the fixed window's both ends
+        [104, 127, 105, 126, Z, 110, 105, 120],  # one value just below it
+        [105, 106, 107, 108, 109, 110, 111, 105],
+        [Z, Z, Z, Z, Z, Z, Z, Z],                # all zero
         [120, 98, 99, Z, 110, 120, 105, 98],     # down to e_max - 22 exactly
         [120, 97, 110, 120, Z, 101, 99, 98],     # one value 23 below: per-value path
         [120, Z, Z, Z, Z, Z, Z, Z],              # zeros below never count

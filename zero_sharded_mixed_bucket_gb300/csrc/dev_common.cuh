@@ -531,6 +531,35 @@ __device__ __forceinline__ void sumsq_group_bf16(const H16<8>& h, int win_lo, U1
 {
     constexpr int kD = 22;                           // binades below the group's largest value
     const int first = win_lo + 134;                  // e of the window's first binade
+    {
+        // First a fixed window: when every nonzero value of the group has e
+        // in [first + 9, first + 31] -- the top 23 binades of the
+        // accumulator's window, which is placed by S * N_d so that these
+        // hold mean gradients of magnitude about 2^-23 to 1 -- each square
+        // is X^2 * 2^18 units with X = M << (e - first - 9) < 2^30: one
+        // multiply-add per value, no group maximum, one add at a constant
+        // shift.  Subnormals (e = 0, first >= 1) and inf and NaN (e = 255,
+        // first <= 222) always lie outside it.
+        const int fbase = first + 9;
+        unsigned long long b = 0ull;
+        uint32_t outside = 0;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const uint32_t w = h.w[j >> 1];
+            const uint32_t e = (j & 1) ? __umulhi(w & 0x7f800000u, 1u << 9) : __umulhi(w & 0x00007f80u, 1u << 25);
+            const uint32_t f = (j & 1) ? __umulhi(w & 0x007f0000u, 1u << 16) : (w & 0x0000007fu);
+            const uint32_t hid = min(e, 1u);
+            const uint32_t M = f + hid * 0x80u;
+            const uint32_t d = e + 1u - hid - (uint32_t)fbase;   // e - fbase for e >= 1
+            outside |= d > 22u ? M : 0u;                          // a nonzero value outside the window
+            const uint32_t X = M << (d & 31u);
+            asm("mad.wide.u32 %0, %1, %1, %0;" : "+l"(b) : "r"(X));
+        }
+        if (!outside) {
+            u128_add(acc, b << 18, b >> 46);
+            return;
+        }
+    }
     uint32_t Mv[8];
     int ex[8];
     int emax = 1;
