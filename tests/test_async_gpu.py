@@ -98,11 +98,12 @@ def test_async_state_round_trip():
     assert last.overflow == 0 and last.grad_norm == -1.0 and last.clip_coef == 1.0
 
 
-@pytest.mark.parametrize("max_norm,N", [(0.0, 8), (1e-3, 8), (1e-3, 16)])
-def test_two_captured_graphs_replayed_alternately(max_norm, N):
+@pytest.mark.parametrize("max_norm,N,B", [(0.0, 8, 2048), (1e-3, 8, 2048), (1e-3, 16, 2048), (0.0, 8, 1 << 16)])
+def test_two_captured_graphs_replayed_alternately(max_norm, N, B):
     """(16 ranks, clipped: the update pass captured is the one that writes
-    the parameters by bulk copies from shared-memory tiles.)"""
-    n, B = 6 * 2048 + 17, 2048
+    the parameters by bulk copies from shared-memory tiles.  One bucket of
+    2^16: the model is a single bucket.)"""
+    n = 6 * 2048 + 17
     job = AsyncJob(n, N, 2, B, 8, None, oracle.FP16, loss_scale=1024.0, dynamic=True, growth=3, max_norm=max_norm)
     s = torch.cuda.Stream()
     # one eager step first: it warms the library's launch-shape cache
@@ -128,6 +129,36 @@ def test_two_captured_graphs_replayed_alternately(max_norm, N):
             job.bufs.b.cur = 1 - job.bufs.b.cur   # what the call does on the host, replayed by hand
         job.check(res, ref)
         assert res.overflow == (1 if step in inject else 0)
+
+
+# --- a model that is one bucket ---------------------------------------------------
+ONE = [
+    # stage, N, n, dtype, optimizer
+    (2, 4, 1 << 20, oracle.FP16, zg.ZERO_ADAM),            # the 2^20-parameter, 4-rank workload
+    (2, 1, 1, oracle.FP16, zg.ZERO_ADAM),
+    (2, 3, 1005, oracle.BF16, zg.ZERO_SGD_MOMENTUM),
+    (2, 2, 1_200_003, oracle.FP16, zg.ZERO_ADAM),          # more groups than one wave of blocks
+    (2, 4, 300_001, oracle.FP32, zg.ZERO_ADAM),
+    (3, 5, 12_345, oracle.FP16, zg.ZERO_SGD),
+    (3, 8, 70_001, oracle.BF16, zg.ZERO_ADAM),
+    (3, 64, 65_536, oracle.FP16, zg.ZERO_ADAM),
+]
+
+
+@pytest.mark.parametrize("case", ONE, ids=lambda c: "s%d-N%d-n%d-dt%d-o%d" % c)
+def test_one_bucket_steps_match_oracle(case):
+    """Stages 2-3, the model one bucket (sizes up to more groups than one
+    wave of blocks): equal to the oracle bit for bit through overflows at the
+    first and the last element and loss-scale growth."""
+    stage, N, n, dtype, opt = case
+    job = AsyncJob(n, N, stage, 1 << 22, 8, None, dtype, loss_scale=256.0, dynamic=True, growth=2, optimizer=opt)
+    assert job.plan.n_buckets == 1
+    plan = [(), (), (inf_at(job, 0, 0),), (), (), (inf_at(job, N - 1, n - 1),), (), ()]
+    for step, inject in enumerate(plan, start=1):
+        res, ref = job.step(job.make_grads(step, inject))
+        job.check(res, ref)
+        assert res.overflow == (1 if inject else 0)
+    assert job.state.t == 6 and job.state.loss_scale == ref["loss_scale"]
 
 
 # --- the same step one bucket at a time -----------------------------------------

@@ -10,7 +10,7 @@ near 1.0 and about half of the steps are clipped.  The device-state runs take
 the fused path (speculative, with shadow state) and the clipped two-pass path
 through 100 steps with a dynamic loss scale, overflows injected every 17th
 step and growth every 10 clean steps (two ranks: pass 1 staged through
-shared memory)."""
+shared memory; and a model that is one bucket)."""
 import math
 
 import numpy as np
@@ -42,10 +42,11 @@ def test_clipped_trajectory(N, dtype):
     assert 0 < clipped < STEPS, clipped
 
 
-@pytest.mark.parametrize("shadow,max_norm,dtype,N", [(True, 0.0, oracle.FP16, 8), (False, 1.0, oracle.BF16, 8),
-                                                     (False, 1.0, oracle.FP16, 2)])
-def test_device_state_trajectory(shadow, max_norm, dtype, N):
-    n, B = 5 * 2048 + 19, 2048
+@pytest.mark.parametrize("shadow,max_norm,dtype,N,B", [(True, 0.0, oracle.FP16, 8, 2048), (False, 1.0, oracle.BF16, 8, 2048),
+                                                       (False, 1.0, oracle.FP16, 2, 2048),
+                                                       (True, 0.0, oracle.BF16, 4, 1 << 14)])
+def test_device_state_trajectory(shadow, max_norm, dtype, N, B):
+    n = 5 * 2048 + 19
     job = AsyncJob(n, N, 2, B, 8, None, dtype, shadow=shadow, loss_scale=1024.0, dynamic=True, growth=10,
                    max_norm=max_norm, sigma=0.03 if max_norm else 1e-3)
     skipped = 0
