@@ -885,6 +885,12 @@ def stage3_arm(args):
     del job
     torch.cuda.empty_cache()
     if rank == 0:
+        # the gather writes 64 of every 65 bytes it moves: beside the copy
+        # bandwidth (half read, half written), the write-only ceiling
+        w = bw.write_ceiling_gbs()
+        out["roofline"]["write_only_ceiling"] = {
+            "gbs": w, "frac": g_ach / w,
+            "how": "torch fill_ of one 8 GiB fp32 buffer on this GPU after the timed steps, median of 5"}
         out["legs"] = other_legs(args, device)
         if world == 1:
             out["cpu_baseline"] = cpu_baseline()

@@ -84,6 +84,31 @@ class StagedGrads:
         return ms
 
 
+def write_ceiling_gbs(nbytes=8 << 30, reps=5):
+    """GB/s of a write-only stream on this GPU: a fill of one fp32 buffer of
+    `nbytes` (median of `reps`).  The measured copy bandwidth moves half its
+    bytes each way; a kernel that mostly writes (the stage-3 gather writes
+    64 bytes for every one it reads) is bounded by this instead."""
+    import torch
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.current_stream(dev)
+    buf = torch.empty(nbytes // 4, dtype=torch.float32, device=dev)
+    buf.fill_(0.0)
+    torch.cuda.synchronize()
+    times = []
+    for k in range(reps):
+        e0, e1 = _ev(), _ev()
+        e0.record(s)
+        buf.fill_(float(k + 1))
+        e1.record(s)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    times.sort()
+    del buf
+    torch.cuda.empty_cache()
+    return nbytes / (times[len(times) // 2] * 1e-3) / 1e9
+
+
 def copy_ceiling(nbytes, reps=20, flush=None, graph=False):
     """Milliseconds of one device copy moving `nbytes` in all (nbytes/2 read,
     nbytes/2 written) -- the floor of any kernel with that traffic, measured
@@ -735,7 +760,7 @@ def leg_pa(args):
     out["memory_per_rank_bytes"] = {"without_pa": p.mem_per_rank_bytes, "pa": p.mem_per_rank_pa_bytes,
                                     "pa_cpu_on_gpu": 0}
     out["gather_bytes_across_ranks"] = p.gather_bytes
-    out["roofline"] = _roofline((1 + N) * 2 * A, hb["gather_ms"], "k_gather (tiles + bulk copies), P_a all-gather")
+    out["roofline"] = _roofline((1 + N) * 2 * A, hb["gather_ms"], "k_gather (chunk by chunk, destination by destination), P_a all-gather")
     return out
 
 
@@ -782,7 +807,7 @@ def leg_gather(args):
                 % (nl, le), {"n_params": n, "n_ranks": N, "stage": 3, "layer_elems": le}, dtype="u16")
     out["unit"] = "Gelements/s"
     out["metric"] = "stage-3 layer gather: elements gathered per second into all 64 destinations"
-    out["roofline"] = _roofline(le * bpe, ms, "k_gather (tiles + bulk copies, 64 destinations)")
+    out["roofline"] = _roofline(le * bpe, ms, "k_gather (chunk by chunk, destination by destination, 64 destinations)")
     out["bytes_per_element"] = bpe
     out["l2"] = "each call writes %.1f GB: far larger than L2" % (le * 2 * N / 1e9)
     return out

@@ -1,7 +1,8 @@
 """P_a (partitioned activation checkpoints) on the GPU against the oracle, bit
 for bit: partition of every rank's replica into its slice, all-gather into
-one or many destinations (direct stores below 8, shared-memory tiles with
-bulk copies from 8), slices in device memory or in pinned host memory
+one or many destinations (direct stores below 8, or with the slices in
+host memory; from 8, chunk by chunk, destination by destination), slices in
+device memory or in pinned host memory
 (P_a+cpu), ragged sizes, 16-bit and binary32 activations, guard regions."""
 import numpy as np
 import pytest

@@ -338,9 +338,10 @@ def test_deterministic_repeat():
 # --- stage-3 layer gather ------------------------------------------------------
 @pytest.mark.parametrize("A,n_dst", [(8, 3), (2048, 3), (8, 8), (2048, 17)])
 def test_gather_layers(A, n_dst):
-    """Layers with unaligned starts, ragged ends and several 8192-unit tiles;
-    fewer than 8 destinations take the direct-store kernel, 8 or more the
-    shared-memory tile kernel with bulk copies."""
+    """Layers with unaligned starts, ragged ends and several 8192-unit
+    segments, shards smaller than a segment; fewer than 8 destinations take
+    the direct-store kernel, 8 or more the chunked one (destination by
+    destination)."""
     layers = [1001, 4096, 7, 20_000, 3333]
     n = sum(layers)
     N = 6
@@ -363,9 +364,37 @@ def test_gather_layers(A, n_dst):
             start += ln
 
 
+@pytest.mark.parametrize("n_dst", [8, 64])
+def test_gather_layers_of_several_chunks(n_dst):
+    """The chunked gather on layers longer than its 2 MB chunks: 64 shards,
+    a layer ending mid-group, one of exactly two chunks and a group, a tiny
+    one; every destination equals the oracle's parameters."""
+    layers = [2_500_003, 2 * (1 << 20) + 8, 9]
+    n = sum(layers)
+    job = Job(n, 64, 3, 1 << 20, 8, layers=layers)
+    plan = job.plan
+    dst = [torch.full((plan.max_layer_elems,), -1, dtype=torch.int16, device="cuda") for _ in range(n_dst)]
+    shards = [t.data_ptr() for t in job.bufs.params16]
+    for step in range(2):
+        if step:
+            res, ref = job.step(job.make_grads(1))
+            job.check(res, ref)
+        start = 0
+        for l, ln in enumerate(layers):
+            for d in dst:
+                d.fill_(-1)
+            zg.zero_gather_layer(job.cfg, plan, l, shards, [d.data_ptr() for d in dst])
+            torch.cuda.synchronize()
+            want = job.p16[start:start + ln]
+            for d in dst:
+                assert np.array_equal(as_u16(d[:ln]), want), (step, l)
+                assert (d[ln:] == -1).all()
+            start += ln
+
+
 def test_gather_destinations_change_kind():
     """The library asks the driver what each destination is on every call:
-    the same job gathers into device buffers (tile kernel with bulk copies),
+    the same job gathers into device buffers (the chunked kernel),
     then, after those are freed, into pinned host buffers (per-thread
     stores), then into device buffers again; every result equals the
     oracle's parameters."""

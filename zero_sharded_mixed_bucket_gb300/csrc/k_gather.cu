@@ -69,12 +69,14 @@ constexpr int kChunkMinDst = 8;
 // fastest, so the device writes the destinations one after another, chunk by
 // chunk: each destination's part of a chunk is one sequential sweep, and
 // the chunk's source, read from the owners' shards once, stays in L2 for the
-// other destinations.  Measured on GB300, 64 destinations: 7.34 TB/s on
-// 201 M-unit layers and 7.13 on 2^24-unit ones (algorithmic bytes), against
+// other destinations.  Measured on GB300, 64 destinations (algorithmic
+// bytes): 7.53 TB/s on 201 M-unit layers and 7.20 on 2^24-unit ones, against
 // 6.77 and 6.43 when each block gathered a tile into shared memory and
 // copied it to every destination with bulk copies (many interleaved write
 // streams at once), and 6.4-6.5 for per-thread stores without the chunks;
-// chunks of 2-4 MB measured the same, 8 MB 7.15, 16 MB 6.47.
+// chunks of 2-4 MB measured the same, 8 MB 2 % less, 16 MB 12 % less.  Eight
+// blocks per SM (32 registers): with the owner found by a 64-bit division
+// per group, or at 4 blocks per SM, the same order reached only 6.3-6.5.
 constexpr int kSegThreads = 256;
 constexpr int kPer = 4;                                            // groups per thread
 constexpr int64_t kSeg = (int64_t)kSegThreads * kPer * kG;         // 8192 units
@@ -165,12 +167,19 @@ __global__ void __launch_bounds__(kSegThreads, 8) k_gather(const __grid_constant
         if (k < nv) dp[k * (kStride / kG)] = v[k];
 }
 
+int owner_of_host(int64_t i, int64_t shard) { return (int)(i / shard); }
+
 }  // namespace
 
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s)
 {
     if (a.len <= 0) return cudaSuccess;
-    if (a.n_dst < kChunkMinDst || !device_resident(const_cast<void* const*>(a.dst), a.n_dst, s)) {
+    // k_gather reads each chunk's source once per destination (from L2 after
+    // the first): only for sources, as well as destinations, in this GPU's
+    // memory; a source in host memory would cross the host link n_dst times
+    const int o_first = owner_of_host(a.start, a.shard), o_last = owner_of_host(a.start + a.len - 1, a.shard);
+    if (a.n_dst < kChunkMinDst || !device_resident(const_cast<void* const*>(a.dst), a.n_dst, s) ||
+        !device_resident(const_cast<void* const*>(a.shards) + o_first, o_last - o_first + 1, s)) {
         const int grid = grid_for((const void*)k_gather_direct, (a.len + kG - 1) / kG);
         k_gather_direct<<<grid, kThreads, 0, s>>>(a);
         return cudaGetLastError();
