@@ -1,7 +1,9 @@
 // Host-side query: are all of these pointers device memory of the current
 // GPU?  The kernels that copy tiles out with bulk asynchronous copies use
-// them only for destinations in device memory; pinned or other host memory
-// (which the library also accepts) keeps the per-thread store kernels.
+// them only for destinations in device memory, and the layer gather's
+// chunked order (which reads each chunk's source once per destination) only
+// for sources and destinations there; pinned or other host memory (which
+// the library also accepts) keeps the per-thread store kernels.
 #pragma once
 
 #include <cuda_runtime.h>
