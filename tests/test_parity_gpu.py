@@ -392,6 +392,47 @@ def test_gather_layers_of_several_chunks(n_dst):
             start += ln
 
 
+def _gather_cases(k=40, seed=77):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(k):
+        N = int(rng.choice([1, 2, 3, 8, 17, 64]))
+        n = int(rng.integers(1, 3_000_000))
+        cuts = sorted(set(int(c) for c in rng.integers(1, n, int(rng.integers(0, 5))))) if n > 1 else []
+        layers = [b - a for a, b in zip([0] + cuts, cuts + [n])]
+        A = int(rng.choice([8, 64, 2048]))
+        n_dst = int(rng.choice([1, 5, 8, 9, 17, 33, 64]))
+        out.append((N, n, layers, A, n_dst))
+    return out
+
+
+@pytest.mark.parametrize("case", _gather_cases(), ids=lambda c: "N%d-n%d-L%d-A%d-d%d" % (c[0], c[1], len(c[2]), c[3], c[4]))
+def test_gather_random_layouts(case):
+    """Seeded random layer splits (unaligned starts, layers from one element
+    to several 2 MB chunks), shard sizes from below a 16 KB segment to
+    millions of elements, 1-64 destinations: every destination holds the
+    layer's slice of the flat parameter vector (the shards laid end to end),
+    bit for bit, and nothing past it."""
+    N, n, layers, A, n_dst = case
+    cfg = zg.Config(n, N, 3, 1 << 20, A, layers)
+    plan = zg.zero_plan(cfg)
+    P = plan.shard_elems
+    gen = torch.Generator(device="cuda").manual_seed(n * 31 + N)
+    shards = [torch.randint(-32768, 32767, (P,), dtype=torch.int16, device="cuda", generator=gen) for _ in range(N)]
+    flat = torch.cat(shards)[:n]
+    dst = [torch.empty(plan.max_layer_elems, dtype=torch.int16, device="cuda") for _ in range(n_dst)]
+    start = 0
+    for l, ln in enumerate(layers):
+        for d in dst:
+            d.fill_(-1)
+        zg.zero_gather_layer(cfg, plan, l, [t.data_ptr() for t in shards], [d.data_ptr() for d in dst])
+        torch.cuda.synchronize()
+        for d in dst:
+            assert torch.equal(d[:ln], flat[start:start + ln]), l
+            assert (d[ln:] == -1).all(), l
+        start += ln
+
+
 def test_gather_destinations_change_kind():
     """The library asks the driver what each destination is on every call:
     the same job gathers into device buffers (the chunked kernel),
