@@ -619,6 +619,30 @@ def sweep_point(n, N, dtype_name, steps, warm):
         ms_async = w0.elapsed_time(w1) / k_async
         if ms_async < ms:
             ms, api = ms_async, "zero_step_async"
+        if n * (28 + 4 * N) <= 4 << 30:
+            # a small step is bound by launches: the same step captured once in
+            # a CUDA graph (the two-pass path keeps one state copy, so one
+            # graph serves every step) and replayed back to back
+            t_before = zg.zero_dev_state_read(dev_state, s)[0].t
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(s)
+            with torch.cuda.graph(g, stream=cap):
+                zg.zero_step_async(cfg, plan, bufs, adam, dev_state, torch.cuda.current_stream(dev))
+            s.wait_stream(cap)
+            for _ in range(3):
+                g.replay()
+            w0, w1 = _ev(), _ev()
+            w0.record(s)
+            for _ in range(k_async):
+                g.replay()
+            w1.record(s)
+            torch.cuda.synchronize()
+            st, last = zg.zero_dev_state_read(dev_state, s)
+            assert st.t == t_before + 3 + k_async and last.overflow == 0 and last.grad_norm == norms[-1]
+            ms_graph = w0.elapsed_time(w1) / k_async
+            if ms_graph < ms:
+                ms, api = ms_graph, "graph of zero_step_async"
     bpp = 28 + 4 * N
     out = {"n_params": n, "n_ranks": N, "dtype": dtype_name, "ms_per_step": ms, "value": n / (ms * 1e-3) / 1e9,
            "hbm_gbs": n * bpp / (ms * 1e-3) / 1e9, "bytes_per_param": bpp, "grad_norm": norms[-1],

@@ -36,13 +36,25 @@ class AsyncJob(Job):
         self.state = st
         return res
 
+    def two_kernels(self):
+        """The library's rule: a two-pass step (clipping, or no shadow state)
+        of a model that is one bucket, in stages 2-3, whose gradients,
+        reduced gradient, state and parameters (n x (2 N e + 2 e + 24) bytes)
+        fit in 64 MiB, runs as two kernels."""
+        e = 4 if self.dtype == oracle.FP32 else 2
+        return (self.two_pass and self.plan.n_buckets == 1 and self.stage >= 2
+                and self.n * (2 * self.N * e + 2 * e + 24) <= 64 << 20)
+
     def step(self, grads):
         self.load_grads(grads)
         n = self.launch()
         per_bucket = 2 if self.two_pass else 1
         # prepare, the bucket kernels (and the finalize and updates), then the
-        # commit (joined with the restore on the fused path)
-        assert n == 2 + per_bucket * self.plan.n_buckets + (1 if self.max_norm > 0 else 0)
+        # commit (joined with the restore on the fused path); or pass 1 and pass 2
+        if self.two_kernels():
+            assert n == 2
+        else:
+            assert n == 2 + per_bucket * self.plan.n_buckets + (1 if self.max_norm > 0 else 0)
         return self.read(), self.oracle_step(grads)
 
 
@@ -98,11 +110,13 @@ def test_async_state_round_trip():
     assert last.overflow == 0 and last.grad_norm == -1.0 and last.clip_coef == 1.0
 
 
-@pytest.mark.parametrize("max_norm,N,B", [(0.0, 8, 2048), (1e-3, 8, 2048), (1e-3, 16, 2048), (0.0, 8, 1 << 16)])
+@pytest.mark.parametrize("max_norm,N,B", [(0.0, 8, 2048), (1e-3, 8, 2048), (1e-3, 16, 2048), (0.0, 8, 1 << 16),
+                                         (1e-3, 8, 1 << 16)])
 def test_two_captured_graphs_replayed_alternately(max_norm, N, B):
     """(16 ranks, clipped: the update pass captured is the one that writes
     the parameters by bulk copies from shared-memory tiles.  One bucket of
-    2^16: the model is a single bucket.)"""
+    2^16: the model is a single bucket; clipped, the step captured is two
+    kernels.)"""
     n = 6 * 2048 + 17
     job = AsyncJob(n, N, 2, B, 8, None, oracle.FP16, loss_scale=1024.0, dynamic=True, growth=3, max_norm=max_norm)
     s = torch.cuda.Stream()
@@ -153,6 +167,39 @@ def test_one_bucket_steps_match_oracle(case):
     stage, N, n, dtype, opt = case
     job = AsyncJob(n, N, stage, 1 << 22, 8, None, dtype, loss_scale=256.0, dynamic=True, growth=2, optimizer=opt)
     assert job.plan.n_buckets == 1
+    plan = [(), (), (inf_at(job, 0, 0),), (), (), (inf_at(job, N - 1, n - 1),), (), ()]
+    for step, inject in enumerate(plan, start=1):
+        res, ref = job.step(job.make_grads(step, inject))
+        job.check(res, ref)
+        assert res.overflow == (1 if inject else 0)
+    assert job.state.t == 6 and job.state.loss_scale == ref["loss_scale"]
+
+
+TWO = [
+    # stage, N, n, dtype, max_norm, optimizer, shadow
+    (2, 8, 1 << 20, oracle.FP16, 1.0, zg.ZERO_ADAM, False),      # the 2^20-parameter point of the clipping sweep
+    (2, 2, 300_001, oracle.BF16, 1e-2, zg.ZERO_ADAM, False),
+    (2, 1, 1, oracle.FP16, 1e-2, zg.ZERO_SGD_MOMENTUM, False),
+    (3, 5, 70_001, oracle.BF16, 1e-3, zg.ZERO_ADAM, False),
+    (3, 64, 65_536, oracle.FP16, 1e-2, zg.ZERO_SGD, False),
+    (2, 4, 100_003, oracle.FP32, 0.0, zg.ZERO_ADAM, False),      # binary32 without a shadow: two-pass, no clipping
+    (2, 3, 1005, oracle.FP16, 0.0, zg.ZERO_ADAM, False),
+    (2, 8, 1 << 20, oracle.FP16, 1.0, zg.ZERO_ADAM, True),       # clipping with the shadow state given
+    (2, 32, 1 << 20, oracle.FP16, 1.0, zg.ZERO_ADAM, False),     # one bucket above 64 MiB: five kernels
+]
+
+
+@pytest.mark.parametrize("case", TWO, ids=lambda c: "s%d-N%d-n%d-dt%d-c%g-o%d-sh%d" % c)
+def test_one_bucket_two_pass_steps_match_oracle(case):
+    """Two-pass device-state steps of a model that is one bucket: when small,
+    pass 1 (whose last block derives the step's scalars and finishes the
+    norm) and pass 2 (whose last block commits) are the whole step.  Equal to
+    the oracle bit for bit, norm and clip coefficient included, through
+    overflows at the first and the last element and loss-scale growth."""
+    stage, N, n, dtype, max_norm, opt, shadow = case
+    job = AsyncJob(n, N, stage, 1 << 22, 8, None, dtype, shadow=shadow, loss_scale=256.0, dynamic=True, growth=2,
+                   max_norm=max_norm, optimizer=opt, sigma=0.03 if max_norm >= 1.0 else 1e-3)
+    assert job.plan.n_buckets == 1 and job.two_pass
     plan = [(), (), (inf_at(job, 0, 0),), (), (), (inf_at(job, N - 1, n - 1),), (), ()]
     for step, inject in enumerate(plan, start=1):
         res, ref = job.step(job.make_grads(step, inject))

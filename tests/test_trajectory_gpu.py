@@ -44,7 +44,8 @@ def test_clipped_trajectory(N, dtype):
 
 @pytest.mark.parametrize("shadow,max_norm,dtype,N,B", [(True, 0.0, oracle.FP16, 8, 2048), (False, 1.0, oracle.BF16, 8, 2048),
                                                        (False, 1.0, oracle.FP16, 2, 2048),
-                                                       (True, 0.0, oracle.BF16, 4, 1 << 14)])
+                                                       (True, 0.0, oracle.BF16, 4, 1 << 14),
+                                                       (False, 1.0, oracle.FP16, 8, 1 << 14)])
 def test_device_state_trajectory(shadow, max_norm, dtype, N, B):
     n = 5 * 2048 + 19
     job = AsyncJob(n, N, 2, B, 8, None, dtype, shadow=shadow, loss_scale=1024.0, dynamic=True, growth=10,

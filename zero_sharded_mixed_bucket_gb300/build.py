@@ -19,7 +19,7 @@ LIB = os.path.join(BUILD_DIR, "libzero_gb300.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["zero_host.cu", "k_fused.cu", "k_twopass.cu", "k_update.cu", "k_gather.cu", "k_noalloc.cu", "zero_fetch.cu", "k_async.cu", "zero_pa.cu"]
-HEADERS = ["zero_internal.h", "dev_common.cuh", "nvtx_ranges.h", "host_ptrs.h"]
+HEADERS = ["zero_internal.h", "dev_common.cuh", "dev_state.cuh", "nvtx_ranges.h", "host_ptrs.h"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC,-Wall",
          "-I" + INCLUDE, "-I" + CSRC]
 

@@ -6,7 +6,7 @@
 //                    corrections for step t+1, 1/(S*N), the sum-of-squares
 //                    window) from the state block into the workspace, where
 //                    the bucket kernels read them;
-//   commit           one thread: the step's outcome into the state block --
+//   commit           (dev_state.cuh) one thread: the step's outcome into the state block --
 //                    t and the beta powers advance on a clean step, the loss
 //                    scaler halves on overflow or grows after a run of clean
 //                    steps -- and the last step's flag, norm and coefficient;
@@ -20,7 +20,7 @@
 // The arithmetic matches the host-synchronised step exactly: beta^t is kept
 // as the same sequence of fp64 multiplications, 1/(S*N) and the scaler use
 // the same fp64 and fp32 operations.
-#include "dev_common.cuh"
+#include "dev_state.cuh"
 
 namespace zg {
 
@@ -36,63 +36,7 @@ __global__ void k_prepare(const PrepArgs a)
     for (int k = threadIdx.x; k < (int)(ws::kEnd / 16); k += blockDim.x)
         head[k] = make_uint4(0u, 0u, 0u, 0u);
     // ... and derive the step's scalars from the state block
-    if (threadIdx.x != 0) return;
-    const DevState* st = a.st;
-    Dyn d;
-    d.beta1_pow_next = __dmul_rn(st->beta1_pow, (double)a.beta1);
-    d.beta2_pow_next = __dmul_rn(st->beta2_pow, (double)a.beta2);
-    d.bc1 = __double2float_rn(__dsub_rn(1.0, d.beta1_pow_next));
-    d.bc2 = __double2float_rn(__dsub_rn(1.0, d.beta2_pow_next));
-    const double sn = __dmul_rn((double)st->loss_scale, (double)a.n_ranks);
-    d.inv = __double2float_rn(__ddiv_rn(1.0, sn));
-    d.inv_d = (double)d.inv;
-    if (a.dtype == kF16) {
-        d.win_lo = -24;
-    } else {
-        int e = 0;
-        frexp(sn, &e);
-        int lo = -40 + e;
-        d.win_lo = lo < -133 ? -133 : (lo > 88 ? 88 : lo);
-    }
-    *a.dyn = d;
-}
-
-__device__ void commit(const CommitArgs& a)
-{
-    DevState* st = a.st;
-    const uint32_t flag = *reinterpret_cast<const volatile uint32_t*>(a.ws + ws::kFlag);
-    if (*reinterpret_cast<const volatile uint32_t*>(a.ws + ws::kErr)) {
-        // a kernel gave up a bounded wait (and raised the flag, so nothing was
-        // updated): the step is not applied and the scaler keeps its state;
-        // bit 1 of last_overflow tells zero_dev_state_read
-        st->last_overflow = 3u;
-        st->last_skipped = 1;
-        st->last_grad_norm = __longlong_as_double(0x7ff8000000000000ll);   // NaN
-        st->last_clip_coef = 1.0f;
-        return;
-    }
-    if (flag) {
-        if (st->dynamic) {
-            const float h = __fmul_rn(st->loss_scale, 0.5f);
-            st->loss_scale = h > st->min_loss_scale ? h : st->min_loss_scale;
-        }
-        st->good_steps = 0;
-    } else {
-        st->t += 1;
-        st->beta1_pow = a.dyn->beta1_pow_next;
-        st->beta2_pow = a.dyn->beta2_pow_next;
-        st->good_steps += 1;
-        if (st->dynamic && st->growth_interval > 0 && st->good_steps >= st->growth_interval) {
-            st->loss_scale = __fmul_rn(st->loss_scale, 2.0f);
-            st->good_steps = 0;
-        }
-    }
-    st->last_overflow = flag ? 1u : 0u;
-    st->last_skipped = flag ? 1 : 0;
-    const double norm = *reinterpret_cast<const double*>(a.ws + ws::kNorm);
-    const float clip = *reinterpret_cast<const float*>(a.ws + ws::kClip);
-    st->last_grad_norm = a.clip ? (flag ? __longlong_as_double(0x7ff0000000000000ll) : norm) : -1.0;
-    st->last_clip_coef = a.clip && !flag ? clip : 1.0f;
+    if (threadIdx.x == 0) *a.dyn = derive_dyn(a.st, a.beta1, a.beta2, a.n_ranks, a.dtype);
 }
 
 __global__ void k_commit(const CommitArgs a)
@@ -112,42 +56,8 @@ __global__ void __launch_bounds__(kThreads) k_restore_async(const __grid_constan
     wait_prev_grid();    // launched early: every bucket kernel of the step must be complete
     if (blockIdx.x == 0 && threadIdx.x == 0) commit(c);
     if (!*reinterpret_cast<const volatile uint32_t*>(ws_flag(a.ws))) return;   // clean step: nothing to do
-    const int64_t ngroups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
-    const int reps = STAGE == 0 ? a.n_ranks : 1;
-    for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
-         gi += (int64_t)gridDim.x * kThreads) {
-        const int64_t i = a.lo + gi * kVecOf<DT>;
-        const int cnt = (int)min((int64_t)kVecOf<DT>, a.hi - i);
-        for (int r = 0; r < reps; r++) {
-            const int64_t si = (int64_t)r * a.replica_stride + i;
-            float w[kVecOf<DT>];
-            ld_f<kVecOf<DT>>(a.w_in, si, cnt, w);
-            st_f<kVecOf<DT>>(a.w_out, si, cnt, w);
-            if constexpr (OPT != kSgd) {
-                float m[kVecOf<DT>];
-                ld_f<kVecOf<DT>>(a.m_in, si, cnt, m);
-                st_f<kVecOf<DT>>(a.m_out, si, cnt, m);
-            }
-            if constexpr (OPT == kAdam) {
-                float v[kVecOf<DT>];
-                ld_f<kVecOf<DT>>(a.v_in, si, cnt, v);
-                st_f<kVecOf<DT>>(a.v_out, si, cnt, v);
-            }
-            Vals<DT> p;
-#pragma unroll
-            for (int j = 0; j < kVecOf<DT>; j++)
-                p.set(j, from_f32<DT>(w[j]));
-            if constexpr (STAGE == 0) {
-                st_vals<DT>(a.params16[r], i, p, cnt);
-            } else if constexpr (STAGE == 3) {
-                const int o = owner_of(i, a.shard);
-                st_vals<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
-            } else {
-                for (int q = 0; q < a.n_ranks; q++)
-                    st_vals<DT>(a.params16[q], i, p, cnt);
-            }
-        }
-    }
+    restore_async_groups<STAGE, DT, OPT>(a, (int64_t)blockIdx.x * kThreads + threadIdx.x,
+                                         (int64_t)gridDim.x * kThreads);
 }
 
 template <int STAGE, int DT, int OPT>

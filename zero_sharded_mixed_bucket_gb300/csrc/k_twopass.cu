@@ -10,7 +10,7 @@
 #include <cstdlib>
 #include <mutex>
 
-#include "dev_common.cuh"
+#include "dev_state.cuh"
 #include "host_ptrs.h"
 
 namespace zg {
@@ -416,20 +416,16 @@ __device__ double big_to_double(const unsigned long long big[kBigWords], int sca
     return scalbn((double)mant, exp + scale_exp);
 }
 
-// One warp: the lanes read the sum's limbs and the 256 exponent bins at once
-// (8 bins each) and mark the non-zero bins by ballot; lane 0 then folds the
-// limbs and only those bins into the big integer, in exponent order.
-// Launched as a programmatic dependent of the step's last pass-1 kernel: it
-// waits for that kernel (hence every pass-1 kernel) to complete first.
-__global__ void k_finalize(const FinalArgs a)
+// One warp (lanes 0..31 of the calling block): the lanes read the 256
+// exponent bins at once (8 each) and mark the non-zero ones by ballot; lane 0
+// then folds the sum's limbs and only those bins into the big integer, in
+// exponent order, and writes the norm and the clip coefficient.
+__device__ void finalize_norm(unsigned char* ws, int dtype, int win_lo, double inv, double max_norm)
 {
-    allow_next_grid();   // the first update kernel may launch; it waits for this one
-    wait_prev_grid();
-    if (blockIdx.x != 0) return;
     __shared__ unsigned long long sbins[256];
     __shared__ uint32_t nonzero[8];
     const int lane = threadIdx.x;
-    const unsigned long long* bins = reinterpret_cast<const unsigned long long*>(a.ws + ws::kBins);
+    const unsigned long long* bins = reinterpret_cast<const unsigned long long*>(ws + ws::kBins);
     unsigned long long b[8];
 #pragma unroll
     for (int k = 0; k < 8; k++)
@@ -442,34 +438,91 @@ __global__ void k_finalize(const FinalArgs a)
     }
     __syncwarp();
     if (lane != 0) return;
-    const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(a.ws + ws::kFlag);
-    double* norm_out = reinterpret_cast<double*>(a.ws + ws::kNorm);
-    float* clip_out = reinterpret_cast<float*>(a.ws + ws::kClip);
+    const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(ws + ws::kFlag);
+    double* norm_out = reinterpret_cast<double*>(ws + ws::kNorm);
+    float* clip_out = reinterpret_cast<float*>(ws + ws::kClip);
     if (flag) {
         *norm_out = __longlong_as_double(0x7ff0000000000000ll);   // +inf
         *clip_out = 1.0f;
         return;
     }
-    const int emin = a.dtype == kBF16 ? -133 : -24;   // E of the smallest subnormal
-    const int win_lo = a.dyn ? a.dyn->win_lo : a.win_lo;
-    const double inv = a.dyn ? a.dyn->inv_d : a.inv;
+    const int emin = dtype == kBF16 ? -133 : -24;   // E of the smallest subnormal
     unsigned long long big[kBigWords];
     for (int k = 0; k < kBigWords; k++) big[k] = 0ull;
-    const unsigned long long* limbs = reinterpret_cast<const unsigned long long*>(a.ws + ws::kAcc);
+    const unsigned long long* limbs = reinterpret_cast<const unsigned long long*>(ws + ws::kAcc);
     for (int k = 0; k < 4; k++)
         big_add(big, limbs[k], 2 * (win_lo - emin) + 32 * k);
     for (int k = 0; k < 8; k++) {
         for (uint32_t m = nonzero[k]; m; m &= m - 1u) {
             const int e = k * 32 + __ffs(m) - 1;
-            const int E = a.dtype == kBF16 ? (e ? e : 1) - 134 : (e ? e : 1) - 25;
+            const int E = dtype == kBF16 ? (e ? e : 1) - 134 : (e ? e : 1) - 25;
             big_add(big, sbins[e], 2 * (E - emin));
         }
     }
     const double sumsq = big_to_double(big, 2 * emin);
     const double norm = __dmul_rn(__dsqrt_rn(sumsq), inv);
-    const double q = __ddiv_rn(a.max_norm, __dadd_rn(norm, 1e-6));
+    const double q = __ddiv_rn(max_norm, __dadd_rn(norm, 1e-6));
     *norm_out = norm;
     *clip_out = __double2float_rn(q < 1.0 ? q : 1.0);
+}
+
+// Launched as a programmatic dependent of the step's last pass-1 kernel: it
+// waits for that kernel (hence every pass-1 kernel) to complete first.
+__global__ void k_finalize(const FinalArgs a)
+{
+    allow_next_grid();   // the first update kernel may launch; it waits for this one
+    wait_prev_grid();
+    if (blockIdx.x != 0) return;
+    finalize_norm(a.ws, a.dtype, a.dyn ? a.dyn->win_lo : a.win_lo, a.dyn ? a.dyn->inv_d : a.inv, a.max_norm);
+}
+
+// Pass 1 of a device-state two-pass step whose model is one bucket,
+// launched right after the workspace head was cleared (no prepare kernel,
+// no finalize kernel): each thread takes the sum-of-squares window from the
+// state block's loss scale itself, and the block that finishes last (a
+// completion count in the workspace) derives the step's scalars into the
+// workspace for pass 2 and the commit and, when clipping, folds the exact
+// sum of squares into the norm and the clip coefficient (one warp, as
+// k_finalize).  A small step is bound by its kernel boundaries: five
+// kernels (prepare, pass 1, finalize, pass 2, commit) become two.
+template <int DT, bool CLIP>
+__global__ void __launch_bounds__(kThreads) k_reduce_one(const __grid_constant__ StepArgs a, const PrepArgs p,
+                                                          double max_norm)
+{
+    __shared__ int last;
+    allow_next_grid();   // pass 2 may launch; it waits for this kernel to complete
+    constexpr int V = kVecOf<DT>;
+    const int win_lo = CLIP ? window_lo_of(p.st->loss_scale, p.n_ranks, DT) : 0;
+    const int64_t ngroups = (a.hi - a.lo + V - 1) / V;
+    bool bad = false;
+    U128 acc{0ull, 0ull};
+    unsigned long long* bins = ws_bins(a.ws);
+    for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups; gi += (int64_t)gridDim.x * kThreads) {
+        const int64_t i = a.lo + gi * V;
+        const int cnt = (int)min((int64_t)V, a.hi - i);
+        const int64_t gidx = i - a.grad_base;
+        float s[V];
+        reduce_group<DT>(a, gidx, cnt, s);
+        finish_group<1, DT, CLIP>(a, i, gidx, cnt, s, win_lo, bad, acc, bins);
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0)
+        atomicOr(ws_flag(a.ws), 1u);
+    if constexpr (CLIP)
+        sumsq_flush(acc, ws_acc(a.ws));
+    // Count the block done.  The barrier orders its threads' writes (the
+    // flag, the bins) before thread 0's device-wide fence, so they are
+    // visible before the count is.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        last = atomicAdd(reinterpret_cast<unsigned int*>(a.ws + ws::kDone), 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last || threadIdx.x >= 32) return;
+    __threadfence();   // every other block's sums and flag are seen from here on
+    const Dyn d = derive_dyn(p.st, p.beta1, p.beta2, p.n_ranks, DT);
+    if (threadIdx.x == 0) *p.dyn = d;
+    if constexpr (CLIP) finalize_norm(a.ws, DT, d.win_lo, d.inv_d, max_norm);
 }
 
 // Launch the staged pass 1: dynamic shared memory for the stage ring, grid
@@ -562,6 +615,26 @@ cudaError_t launch_reduce(int stage, int dtype, bool clip, const StepArgs& a, cu
 cudaError_t launch_finalize(const FinalArgs& a, cudaStream_t s, bool overlap)
 {
     return launch_kernel(k_finalize, 1, 32, s, overlap, a);
+}
+
+namespace {
+template <int DT, bool CLIP>
+cudaError_t run_reduce_one(const StepArgs& a, const PrepArgs& p, double max_norm, cudaStream_t s)
+{
+    const int64_t groups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
+    if (groups <= 0) return cudaErrorInvalidValue;
+    const int grid = grid_for((const void*)k_reduce_one<DT, CLIP>, groups);
+    return launch_kernel(k_reduce_one<DT, CLIP>, grid, kThreads, s, false, a, p, max_norm);
+}
+}  // namespace
+
+cudaError_t launch_reduce_one(int dtype, bool clip, const StepArgs& a, const PrepArgs& p, double max_norm,
+                              cudaStream_t s)
+{
+    if (dtype == kBF16) return clip ? run_reduce_one<kBF16, true>(a, p, max_norm, s)
+                                    : run_reduce_one<kBF16, false>(a, p, max_norm, s);
+    if (dtype == kF32) return clip ? cudaErrorNotSupported : run_reduce_one<kF32, false>(a, p, max_norm, s);
+    return clip ? run_reduce_one<kF16, true>(a, p, max_norm, s) : run_reduce_one<kF16, false>(a, p, max_norm, s);
 }
 
 }  // namespace zg

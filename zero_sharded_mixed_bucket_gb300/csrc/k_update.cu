@@ -1,12 +1,50 @@
 // Two-pass step, pass 2 (see k_twopass.cu for pass 1 and the finalize): per
 // bucket, the optimizer update in place on the current state, unless the
 // step's overflow flag is set, then the model-precision cast and the all-gather.
-#include "dev_common.cuh"
+#include "dev_state.cuh"
 #include "host_ptrs.h"
 
 namespace zg {
 
 namespace {
+
+// One group of pass 2 at flat element i: the reduced gradient unscaled
+// (and, with clipping, multiplied by c when c < 1: g * 1 == g for every
+// finite g, so both forms give the same bits), the update, the cast and the
+// stage's parameter writes.
+template <int STAGE, int DT, int OPT>
+__device__ __forceinline__ void update_group(const StepArgs& a, int64_t i, float c, float inv, const AdamHP& hp)
+{
+    const int cnt = (int)min((int64_t)kVecOf<DT>, a.hi - i);
+    const int reps = STAGE == 0 ? a.n_ranks : 1;
+    for (int r = 0; r < reps; r++) {
+        Vals<DT> h;
+        if constexpr (STAGE == 0)
+            h = ld_vals<DT>(a.grads[r], i - a.grad_base, cnt);        // each replica its own all-reduced copy
+        else if constexpr (STAGE == 1)
+            h = ld_vals<DT>(a.grads[owner_of(i, a.shard)], i - a.grad_base, cnt);
+        else
+            h = ld_vals<DT>(a.reduced, i, cnt);
+        float g[kVecOf<DT>];
+        unscale_group<DT>(h, inv, g);
+        if (c != 1.0f) {
+#pragma unroll
+            for (int j = 0; j < kVecOf<DT>; j++)
+                g[j] = __fmul_rn(g[j], c);
+        }
+        Vals<DT> p;
+        update_state<DT, OPT>(a, hp, (int64_t)r * a.replica_stride + i, cnt, g, p);
+        if constexpr (STAGE == 0) {
+            st_vals<DT>(a.params16[r], i, p, cnt);
+        } else if constexpr (STAGE == 3) {
+            const int o = owner_of(i, a.shard);
+            st_vals<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
+        } else {
+            for (int q = 0; q < a.n_ranks; q++)
+                st_vals<DT>(a.params16[q], i, p, cnt);
+        }
+    }
+}
 
 template <int STAGE, int DT, bool CLIP, int OPT>
 __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ StepArgs a)
@@ -22,8 +60,6 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
         wait_prev_grid();
         return;   // overflow: the whole step is skipped
     }
-    // With clipping on, multiply by c only when c < 1: g * 1 == g for every
-    // finite g, so both forms give the same bits.
     const float c = CLIP ? *reinterpret_cast<const float*>(a.ws + ws::kClip) : 1.0f;
     float inv = a.inv;
     AdamHP hp = a.hp;
@@ -34,39 +70,41 @@ __global__ void __launch_bounds__(kThreads) k_update(const __grid_constant__ Ste
     }
     const int64_t ngroups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
     for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
-         gi += (int64_t)gridDim.x * kThreads) {
-        const int64_t i = a.lo + gi * kVecOf<DT>;
-        const int cnt = (int)min((int64_t)kVecOf<DT>, a.hi - i);
-        const int reps = STAGE == 0 ? a.n_ranks : 1;
-        for (int r = 0; r < reps; r++) {
-            Vals<DT> h;
-            if constexpr (STAGE == 0)
-                h = ld_vals<DT>(a.grads[r], i - a.grad_base, cnt);        // each replica its own all-reduced copy
-            else if constexpr (STAGE == 1)
-                h = ld_vals<DT>(a.grads[owner_of(i, a.shard)], i - a.grad_base, cnt);
-            else
-                h = ld_vals<DT>(a.reduced, i, cnt);
-            float g[kVecOf<DT>];
-            unscale_group<DT>(h, inv, g);
-            if (c != 1.0f) {
-#pragma unroll
-                for (int j = 0; j < kVecOf<DT>; j++)
-                    g[j] = __fmul_rn(g[j], c);
-            }
-            Vals<DT> p;
-            update_state<DT, OPT>(a, hp, (int64_t)r * a.replica_stride + i, cnt, g, p);
-            if constexpr (STAGE == 0) {
-                st_vals<DT>(a.params16[r], i, p, cnt);
-            } else if constexpr (STAGE == 3) {
-                const int o = owner_of(i, a.shard);
-                st_vals<DT>(a.params16[o], i - (int64_t)o * a.shard, p, cnt);
-            } else {
-                for (int q = 0; q < a.n_ranks; q++)
-                    st_vals<DT>(a.params16[q], i, p, cnt);
-            }
-        }
-    }
+         gi += (int64_t)gridDim.x * kThreads)
+        update_group<STAGE, DT, OPT>(a, a.lo + gi * kVecOf<DT>, c, inv, hp);
     wait_prev_grid();
+}
+
+// Pass 2 of the two-kernel step of a model that is one bucket (k_reduce_one
+// is pass 1): as k_update, with the scalars the last pass-1 block wrote, and
+// the block that finishes last (the second completion count) commits the
+// step.
+template <int STAGE, int DT, bool CLIP, int OPT>
+__global__ void __launch_bounds__(kThreads) k_update_one(const __grid_constant__ StepArgs a, const CommitArgs cm)
+{
+    __shared__ int last;
+    wait_prev_grid();   // pass 1, its last block's scalars, norm and clip coefficient among it
+    if (!*reinterpret_cast<volatile uint32_t*>(ws_flag(a.ws))) {
+        const float c = CLIP ? *reinterpret_cast<const float*>(a.ws + ws::kClip) : 1.0f;
+        AdamHP hp = a.hp;
+        hp.bc1 = a.dyn->bc1;
+        hp.bc2 = a.dyn->bc2;
+        const float inv = a.dyn->inv;
+        const int64_t ngroups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
+        for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < ngroups;
+             gi += (int64_t)gridDim.x * kThreads)
+            update_group<STAGE, DT, OPT>(a, a.lo + gi * kVecOf<DT>, c, inv, hp);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        last = atomicAdd(reinterpret_cast<unsigned int*>(a.ws + ws::kDone) + 1, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (last && threadIdx.x == 0) {
+        __threadfence();
+        commit(cm);
+    }
 }
 
 // Stages 1 and 2 with 2 or more ranks: the new parameters for every rank are
@@ -226,6 +264,44 @@ cudaError_t launch_update(int stage, int dtype, int opt, bool clip, const StepAr
     if (dtype == kF32) return update_opt<kF32>(stage, opt, clip, a, s, overlap);
     return dtype == kBF16 ? update_opt<kBF16>(stage, opt, clip, a, s, overlap)
                           : update_opt<kF16>(stage, opt, clip, a, s, overlap);
+}
+
+namespace {
+template <int STAGE, int DT, bool CLIP, int OPT>
+cudaError_t run_update_one(const StepArgs& a, const CommitArgs& c, cudaStream_t s)
+{
+    const int64_t groups = (a.hi - a.lo + kVecOf<DT> - 1) / kVecOf<DT>;
+    if (groups <= 0) return cudaErrorInvalidValue;
+    const int grid = grid_for((const void*)k_update_one<STAGE, DT, CLIP, OPT>, groups);
+    return launch_kernel(k_update_one<STAGE, DT, CLIP, OPT>, grid, kThreads, s, true, a, c);
+}
+
+template <int STAGE, int DT, bool CLIP>
+cudaError_t update_one_opt(int opt, const StepArgs& a, const CommitArgs& c, cudaStream_t s)
+{
+    switch (opt) {
+    case kSgdm: return run_update_one<STAGE, DT, CLIP, kSgdm>(a, c, s);
+    case kSgd: return run_update_one<STAGE, DT, CLIP, kSgd>(a, c, s);
+    default: return run_update_one<STAGE, DT, CLIP, kAdam>(a, c, s);
+    }
+}
+
+template <int DT, bool CLIP>
+cudaError_t update_one_stage(int stage, int opt, const StepArgs& a, const CommitArgs& c, cudaStream_t s)
+{
+    if (stage == 2) return update_one_opt<2, DT, CLIP>(opt, a, c, s);
+    if (stage == 3) return update_one_opt<3, DT, CLIP>(opt, a, c, s);
+    return cudaErrorInvalidValue;
+}
+}  // namespace
+
+cudaError_t launch_update_one(int stage, int dtype, int opt, bool clip, const StepArgs& a, const CommitArgs& c,
+                              cudaStream_t s)
+{
+    if (dtype == kF32) return clip ? cudaErrorNotSupported : update_one_stage<kF32, false>(stage, opt, a, c, s);
+    if (dtype == kBF16) return clip ? update_one_stage<kBF16, true>(stage, opt, a, c, s)
+                                    : update_one_stage<kBF16, false>(stage, opt, a, c, s);
+    return clip ? update_one_stage<kF16, true>(stage, opt, a, c, s) : update_one_stage<kF16, false>(stage, opt, a, c, s);
 }
 
 }  // namespace zg

@@ -163,6 +163,19 @@ struct Path {
     bool fused;
 };
 
+// A two-pass device-state step of a model that is one bucket (stages 2 and
+// 3) runs as two kernels (pass 1 finishing the norm, pass 2 committing)
+// when it is small -- its gradients, reduced gradient, state and parameters
+// within 64 MiB -- since such a step is bound by its kernel boundaries.
+constexpr int64_t kTwoKernelBytes = int64_t(64) << 20;
+
+bool two_kernel_step(const zero_config_t* c, const zero_plan_t* p, const Path& path)
+{
+    if (path.fused || p->n_buckets != 1 || c->stage < 2) return false;
+    const int64_t e = c->dtype == ZERO_FP32 ? 4 : 2;
+    return c->n_params * (2 * (int64_t)c->n_ranks * e + 2 * e + 24) <= kTwoKernelBytes;
+}
+
 // Number of fp32 state arrays the optimizer uses: w; w, m; w, m, v.
 int state_arrays(int optimizer) { return optimizer == ZERO_SGD ? 1 : (optimizer == ZERO_SGD_MOMENTUM ? 2 : 3); }
 
@@ -810,14 +823,39 @@ zero_status_t zero_step_async(const zero_config_t* c, const zero_plan_t* p, zero
     Dyn* dyn = reinterpret_cast<Dyn*>(ws_ptr + ws::kDyn);
     DevState* dst = static_cast<DevState*>(dev_state);
     int launches = 0;
+    PrepArgs pa{dst, dyn, ws_ptr, adam->beta1, adam->beta2, c->n_ranks, c->dtype};
+    cudaError_t e;
+    if (two_kernel_step(c, p, path)) {
+        // the workspace head cleared, then pass 1 and pass 2 (the profiling
+        // events, when set, around the two)
+        e = cudaMemsetAsync(ws_ptr, 0, ws::kEnd, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace");
+        if (g_prof_start && (e = cudaEventRecord(g_prof_start, cs)) != cudaSuccess)
+            return cuda_fail(e, "recording the profiling start event");
+        StepArgs a1 = make_args(c, p, b, adam, &host_view, false, b->grads, 0);
+        a1.lo = 0;
+        a1.hi = c->n_params;
+        e = launch_reduce_one(c->dtype, path.clip, a1, pa, (double)adam->max_grad_norm, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "launching the one-bucket pass-1 kernel");
+        StepArgs a2 = make_args(c, p, b, adam, &host_view, false, nullptr, 0);
+        a2.dyn = dyn;
+        a2.lo = 0;
+        a2.hi = c->n_params;
+        const CommitArgs ca{dst, dyn, ws_ptr, path.clip ? 1 : 0};
+        e = launch_update_one(c->stage, c->dtype, c->optimizer, path.clip, a2, ca, cs);
+        if (e != cudaSuccess) return cuda_fail(e, "launching the one-bucket pass-2 kernel");
+        if (g_prof_end && (e = cudaEventRecord(g_prof_end, cs)) != cudaSuccess)
+            return cuda_fail(e, "recording the profiling end event");
+        if (kernel_launches) *kernel_launches = 2;
+        return ZERO_OK;
+    }
     // Every kernel of the step is a programmatic dependent of the one before
     // it: prepare, restore/commit and the first bucket kernel wait for their
     // predecessor at their start, the other bucket kernels at their end.  The
     // profiling events, when set, sit between the prepare kernel and the
     // first bucket kernel and after the last bucket or update kernel, so they
     // time the bucket kernels alone (those two edges then do not overlap).
-    PrepArgs pa{dst, dyn, ws_ptr, adam->beta1, adam->beta2, c->n_ranks, c->dtype};
-    cudaError_t e = launch_prepare(pa, cs, true);   // also clears the workspace head
+    e = launch_prepare(pa, cs, true);   // also clears the workspace head
     if (e != cudaSuccess) return cuda_fail(e, "launching the prepare kernel");
     launches++;
     if (g_prof_start && (e = cudaEventRecord(g_prof_start, cs)) != cudaSuccess)

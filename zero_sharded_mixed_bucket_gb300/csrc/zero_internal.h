@@ -26,7 +26,8 @@ constexpr size_t kBins = 64;    // 256 x uint64: sum of M^2 per exponent field, 
 constexpr size_t kWroteLoC = kBins + 256 * 8;   // uint64: ~lo
 constexpr size_t kWroteHi = kWroteLoC + 8;      // uint64: hi
 constexpr size_t kUpdated = kWroteHi + 8;       // uint64: elements updated
-constexpr size_t kEnd = kUpdated + 16;          // end of the part cleared before every step (16-byte multiple)
+constexpr size_t kDone = kUpdated + 8;          // 2 x uint32: blocks of a one-bucket step's passes 1, 2 that finished
+constexpr size_t kEnd = kDone + 8;              // end of the part cleared before every step (16-byte multiple)
 constexpr size_t kDyn = 2176;   // Dyn: per-step scalars of a device-state step (written by the prepare kernel)
 constexpr int64_t kBytes = 4096;
 static_assert(kEnd % 16 == 0 && kEnd <= kDyn, "workspace head");
@@ -145,6 +146,15 @@ cudaError_t launch_prepare(const PrepArgs& a, cudaStream_t s, bool overlap);
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s, bool overlap);
 cudaError_t launch_restore_async(int stage, int dtype, int opt, const StepArgs& a, const CommitArgs& c,
                                  cudaStream_t s, bool overlap);
+// The two-pass device-state step of a model that is one bucket (stages 2
+// and 3) as two kernels, after the workspace head was cleared: pass 1, whose
+// last block to finish derives the step's scalars into p.dyn and, when
+// clipping, the norm and clip coefficient; pass 2 (a programmatic dependent
+// of pass 1), whose last block commits the step.
+cudaError_t launch_reduce_one(int dtype, bool clip, const StepArgs& a, const PrepArgs& p, double max_norm,
+                              cudaStream_t s);
+cudaError_t launch_update_one(int stage, int dtype, int opt, bool clip, const StepArgs& a, const CommitArgs& c,
+                              cudaStream_t s);
 
 // Record the thread-local message that zero_last_error() returns; gives back
 // `st`.  For entry points defined outside zero_host.cu.
