@@ -377,7 +377,12 @@ zero_status_t zero_gather_layer(const zero_config_t* cfg, const zero_plan_t* pla
  * step: capture one call per value of bufs->cur and replay them alternately.
  * The step's kernels are launched as one chain of programmatic dependent
  * launches (each small kernel, and the first bucket kernel, waits for its
- * predecessor before it touches memory).
+ * predecessor before it touches memory).  A two-pass step (clipping, or no
+ * shadow state) of a model that is one bucket, in stages 2-3, moving at
+ * most 64 MiB (n x (2 N e + 2 e + 24) bytes, e the value size) is two
+ * kernels after a memset of the workspace head: pass 1, whose last block
+ * derives the scalars and finishes the norm, and pass 2, whose last block
+ * commits.
  * The device state block is 64 bytes, 16-byte aligned, caller-owned. */
 typedef struct zero_dev_state { int64_t opaque[8]; } zero_dev_state_t;   /* 64 bytes */
 
