@@ -7,6 +7,8 @@ partition offsets bit-exact; fp32 master weights, momentum and variance within
 evaluate the same IEEE operations in the same order (and a single differing
 fp32 ulp would flip 16-bit roundings).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -406,13 +408,16 @@ def _gather_cases(k=40, seed=77):
     return out
 
 
-@pytest.mark.parametrize("case", _gather_cases(), ids=lambda c: "N%d-n%d-L%d-A%d-d%d" % (c[0], c[1], len(c[2]), c[3], c[4]))
+@pytest.mark.parametrize("case", _gather_cases(int(os.environ.get("ZG_GATHER_CASES", "40")),
+                                         int(os.environ.get("ZG_GATHER_SEED", "77"))),
+                         ids=lambda c: "N%d-n%d-L%d-A%d-d%d" % (c[0], c[1], len(c[2]), c[3], c[4]))
 def test_gather_random_layouts(case):
     """Seeded random layer splits (unaligned starts, layers from one element
     to several 2 MB chunks), shard sizes from below a 16 KB segment to
     millions of elements, 1-64 destinations: every destination holds the
     layer's slice of the flat parameter vector (the shards laid end to end),
-    bit for bit, and nothing past it."""
+    bit for bit, and nothing past it.  ZG_GATHER_SEED and ZG_GATHER_CASES
+    draw another set (a longer soak)."""
     N, n, layers, A, n_dst = case
     cfg = zg.Config(n, N, 3, 1 << 20, A, layers)
     plan = zg.zero_plan(cfg)
