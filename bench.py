@@ -968,12 +968,12 @@ def main():
                          "e.g. for profiling captures)")
     ap.add_argument("--ring", type=int, default=GRAD_RING, help="distinct per-step gradient sets kept in HBM")
     ap.add_argument("--bucket", type=int, default=BUCKET, help="gradient bucket size in elements")
-    ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5, 6, 7, 8],
+    ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9],
                     help="workload: 4 (default) the stage-3 step at 6.65B parameters; 2 the stage-2 step on the "
                          "12-layer d=768 list (the options --stage, --optimizer, --dtype, --step-api, --n-params "
                          "apply to it); 1, 3, 5 the others, 6 the optimizer state in host memory, 7 the P_a "
-                         "activation-checkpoint partition and all-gather, 8 stage-3 layer gathers alone "
-                         "(bench_workloads.py)")
+                         "activation-checkpoint partition and all-gather, 8 stage-3 layer gathers alone, 9 the "
+                         "clipped step split into its passes (bench_workloads.py)")
     ap.add_argument("--ring3", type=int, default=4, help="--config 4: pre-generated bucket gradient sets in HBM")
     ap.add_argument("--s3-layers", type=int, default=S3_LAYERS, help="--config 4: transformer layers")
     ap.add_argument("--s3-d", type=int, default=S3_D, help="--config 4: model width d")
@@ -986,7 +986,7 @@ def main():
                          "fetcher run")
     ap.add_argument("--layer-elems", type=int, default=1 << 24, help="--config 8: elements per layer")
     ap.add_argument("--n-layers", type=int, default=2, help="--config 8: layers")
-    ap.add_argument("--ranks", type=int, default=None, help="--config 5: N_d of a single sweep point")
+    ap.add_argument("--ranks", type=int, default=None, help="--config 5, 9: N_d of a single point")
     ap.add_argument("--optimizer", default="adam", choices=sorted(OPTIMIZERS),
                     help="optimizer of the headline step (with --headline-only)")
     ap.add_argument("--dtype", default=None, choices=["fp16", "bf16", "fp32"],

@@ -681,6 +681,75 @@ def leg_cfg5(args):
     return out
 
 
+def leg_pass_split(args):
+    """The clipped two-pass stage-2 step split into its passes by CUDA
+    events: pass 1 (the buckets' reduce, flag and exact sum of squares, sent
+    as one run through zero_step_buckets) and pass 2 (the norm finalize and
+    the update kernels, up to the library's end event), each against its
+    algorithmic bytes (pass 1: 2 N + 2 B per parameter; pass 2: 2 + 24 + 2 N
+    B).  Points: --n-params/--ranks/--dtype, else 2^28 and 2^31 parameters,
+    two ranks, fp16 and bf16."""
+    import torch
+
+    import synth
+    import zero_sharded_mixed_bucket_gb300 as zg
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.current_stream(dev)
+    peak, kind = bench.measured_peak_hbm()
+    if args.n_params:
+        points = [(args.n_params, args.ranks or 2, args.dtype or "bf16")]
+    else:
+        points = [(1 << 28, 2, "fp16"), (1 << 28, 2, "bf16"), (1 << 31, 2, "bf16"), (1 << 31, 2, "fp16")]
+    steps = max(args.steps, 3)
+    res = []
+    for n, N, dt in points:
+        dtype = zg.ZERO_BF16 if dt == "bf16" else zg.ZERO_FP16
+        cfg = zg.Config(n, N, 2, 1 << 24, 0, None, dtype)
+        plan = zg.zero_plan(cfg)
+        bufs = zg.DeviceBuffers(cfg, plan, device=dev, shadow=False)
+        synth.dev_normal32(bufs.w[0].data_ptr(), n, 0.02, seed=0, stream=synth.STREAM_WEIGHT,
+                           cuda_stream=s.cuda_stream)
+        for r in range(N):
+            synth.dev_normal16(bufs.grads[r].data_ptr(), n, dtype, 1e-3, seed=0, stream=synth.STREAM_GRAD, step=1,
+                               rank=r, cuda_stream=s.cuda_stream)
+        adam = zg.zero_adam_t(max_grad_norm=1.0, **ADAM)
+        state = zg.zero_state_t(t=0, loss_scale=1.0, min_loss_scale=1.0)
+        p1 = p2 = 0.0
+        for k in range(args.warmup + steps):
+            c0, c1, mid = _ev(), _ev(), _ev()
+            c0.record(s)
+            c1.record(s)            # materialised: the library records them by handle
+            zg.zero_set_profile_events(c0, c1)    # c0 after the workspace clear, c1 after the update kernels
+            try:
+                zg.zero_step_begin(cfg, plan, bufs, adam, state, s)
+                zg.zero_step_buckets(cfg, plan, bufs, adam, state, list(range(plan.n_buckets)), None, s)
+                mid.record(s)
+                zg.zero_step_end(cfg, plan, bufs, adam, state, s)
+            finally:
+                zg.zero_set_profile_events(None, None)
+            torch.cuda.synchronize()
+            if k >= args.warmup:
+                p1 += c0.elapsed_time(mid)
+                p2 += mid.elapsed_time(c1)
+        p1 /= steps
+        p2 /= steps
+        b1, b2 = n * (2 * N + 2), n * (2 + 24 + 2 * N)
+        res.append({"n_params": n, "n_ranks": N, "dtype": dt, "pass1_ms": p1, "pass1_frac": b1 / (p1 * 1e-3) / 1e9 / peak,
+                    "pass2_ms": p2, "pass2_frac": b2 / (p2 * 1e-3) / 1e9 / peak, "step_ms": p1 + p2,
+                    "step_frac": (b1 + b2) / ((p1 + p2) * 1e-3) / 1e9 / peak})
+        del bufs
+        torch.cuda.empty_cache()
+    last = res[-1]
+    out = _base(last["n_params"] / (last["step_ms"] * 1e-3) / 1e9, last["step_ms"], steps, args.warmup,
+                "clipped stage-2 step split into its two passes (CUDA events), flat parameters, grads N(0,1e-3)",
+                {"stage": 2, "bucket_elems": 1 << 24})
+    out["points"] = res
+    out["roofline"] = {"bound": "hbm", "kernel": "k_reduce_staged (pass 1) / k_finalize + k_update (pass 2)",
+                       "achieved": last["step_frac"] * peak, "peak": peak, "peak_kind": kind, "unit": "GB/s",
+                       "frac": last["step_frac"], "traffic": None}
+    return out
+
+
 # ---------------------------------------------------------------------------
 def leg_offload(args):
     """The headline workload with the fp32 optimizer state (w, m, v and their
@@ -837,4 +906,5 @@ def leg_gather(args):
     return out
 
 
-LEGS = {1: leg_cfg1, 3: leg_cfg3, 4: leg_cfg4, 5: leg_cfg5, 6: leg_offload, 7: leg_pa, 8: leg_gather}
+LEGS = {1: leg_cfg1, 3: leg_cfg3, 4: leg_cfg4, 5: leg_cfg5, 6: leg_offload, 7: leg_pa, 8: leg_gather,
+        9: leg_pass_split}
