@@ -986,7 +986,7 @@ def main():
                          "fetcher run")
     ap.add_argument("--layer-elems", type=int, default=1 << 24, help="--config 8: elements per layer")
     ap.add_argument("--n-layers", type=int, default=2, help="--config 8: layers")
-    ap.add_argument("--ranks", type=int, default=None, help="--config 5, 9: N_d of a single point")
+    ap.add_argument("--ranks", type=int, default=None, help="--config 5, 9: N_d of a single point; --config 8: N_d")
     ap.add_argument("--optimizer", default="adam", choices=sorted(OPTIMIZERS),
                     help="optimizer of the headline step (with --headline-only)")
     ap.add_argument("--dtype", default=None, choices=["fp16", "bf16", "fp32"],

@@ -860,14 +860,14 @@ def leg_pa(args):
 # ---------------------------------------------------------------------------
 def leg_gather(args):
     """Stage-3 layer gathers alone: a model of --n-layers layers of
-    --layer-elems elements each, N_d = 64 owner shards, every call gathering
-    one layer (in turn) into 64 destination buffers.  The case the k_gather
-    ncu summary captures (small enough for a profiler: 2 x 2^24 elements
-    hold about 4.4 GB of device memory)."""
+    --layer-elems elements each, N_d = 64 owner shards (--ranks: another
+    N_d), every call gathering one layer (in turn) into N_d destination
+    buffers.  The case the k_gather ncu summary captures (small enough for a
+    profiler: 2 x 2^24 elements hold about 4.4 GB of device memory)."""
     import torch
 
     import zero_sharded_mixed_bucket_gb300 as zg
-    N, le, nl = 64, args.layer_elems, args.n_layers
+    N, le, nl = args.ranks or 64, args.layer_elems, args.n_layers
     layers = [le] * nl
     n = le * nl
     dev = torch.device("cuda", 0)
@@ -896,11 +896,12 @@ def leg_gather(args):
     ms = sum(times) / steps
     bpe = 2 + 2 * N
     out = _base(le / (ms * 1e-3) / 1e9, ms, steps, args.warmup,
-                "stage-3 layer gather alone: %d layers of %d elements, N_d=64 owner shards, 64 destination buffers"
-                % (nl, le), {"n_params": n, "n_ranks": N, "stage": 3, "layer_elems": le}, dtype="u16")
+                "stage-3 layer gather alone: %d layers of %d elements, N_d=%d owner shards, %d destination buffers"
+                % (nl, le, N, N), {"n_params": n, "n_ranks": N, "stage": 3, "layer_elems": le}, dtype="u16")
     out["unit"] = "Gelements/s"
-    out["metric"] = "stage-3 layer gather: elements gathered per second into all 64 destinations"
-    out["roofline"] = _roofline(le * bpe, ms, "k_gather (chunk by chunk, destination by destination, 64 destinations)")
+    out["metric"] = "stage-3 layer gather: elements gathered per second into all %d destinations" % N
+    out["roofline"] = _roofline(le * bpe, ms, "k_gather (chunk by chunk, destination by destination, %d destinations)"
+                                % N)
     out["bytes_per_element"] = bpe
     out["l2"] = "each call writes %.1f GB: far larger than L2" % (le * 2 * N / 1e9)
     return out

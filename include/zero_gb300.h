@@ -351,11 +351,11 @@ zero_status_t zero_step_buckets(const zero_config_t* cfg, const zero_plan_t* pla
  * buffers dst[d] (capacity max_layer_elems; element j = flat index
  * layer_start + j).  The parameter all-gather that runs before a layer's
  * forward and again before its backward (ZeRO visual reading, communication
- * accounting; "ZeRO：大模型训练的内存优化革命" 3.1.3).  n_dst 1..64.  With 8
- * or more destinations, and the layer's shards, in device memory the layer
- * is written 2 MB chunk by chunk, destination by destination (the chunk's
- * source stays in L2); otherwise each value is read once and stored to
- * every destination. */
+ * accounting; "ZeRO：大模型训练的内存优化革命" 3.1.3).  n_dst 1..64.  With the
+ * destinations and the layer's shards in device memory the layer is written
+ * 2 MB chunk by chunk, destination by destination (the chunk's source stays
+ * in L2); otherwise each value is read once and stored to every
+ * destination. */
 zero_status_t zero_gather_layer(const zero_config_t* cfg, const zero_plan_t* plan, int32_t layer,
                                 void* const* param_shards, void* const* dst, int32_t n_dst, void* stream);
 

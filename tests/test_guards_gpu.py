@@ -135,7 +135,7 @@ def test_bucket_staging_gather_and_fetch_stay_inside():
     shards = [x.ptr() for x in every[N:2 * N]]
     dst = [Guarded(plan.max_layer_elems, torch.int16) for _ in range(9)]
     for l in range(len(layers)):
-        zg.zero_gather_layer(cfg, plan, l, shards, [d.ptr() for d in dst[:2]], s)   # direct stores
+        zg.zero_gather_layer(cfg, plan, l, shards, [d.ptr() for d in dst[:2]], s)   # chunked, 2 destinations
         zg.zero_gather_layer(cfg, plan, l, shards, [d.ptr() for d in dst], s)       # chunked, destination by destination
     cap = 4008 + 2056
     pool = [Guarded(cap, torch.int16) for _ in range(2)]

@@ -1,8 +1,8 @@
 """P_a (partitioned activation checkpoints) on the GPU against the oracle, bit
 for bit: partition of every rank's replica into its slice, all-gather into
-one or many destinations (direct stores below 8, or with the slices in
-host memory; from 8, chunk by chunk, destination by destination), slices in
-device memory or in pinned host memory
+one or many destinations (chunk by chunk, destination by destination; with
+the slices in host memory, each value read once and stored to every
+destination), slices in device memory or in pinned host memory
 (P_a+cpu), ragged sizes, 16-bit and binary32 activations, guard regions."""
 import numpy as np
 import pytest

@@ -341,9 +341,8 @@ def test_deterministic_repeat():
 @pytest.mark.parametrize("A,n_dst", [(8, 3), (2048, 3), (8, 8), (2048, 17)])
 def test_gather_layers(A, n_dst):
     """Layers with unaligned starts, ragged ends and several 8192-unit
-    segments, shards smaller than a segment; fewer than 8 destinations take
-    the direct-store kernel, 8 or more the chunked one (destination by
-    destination)."""
+    segments, shards smaller than a segment, 3 to 17 destinations (the
+    chunked kernel, destination by destination)."""
     layers = [1001, 4096, 7, 20_000, 3333]
     n = sum(layers)
     N = 6

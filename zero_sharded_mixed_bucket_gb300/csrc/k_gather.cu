@@ -21,9 +21,9 @@ namespace {
 
 constexpr int kG = 8;                 // units per 16-byte group
 
-// Few destinations: each thread copies its 16-byte group straight to every
-// destination (for one destination this is a copy and measured 5.1 TB/s,
-// against 4.0 through shared memory and a single bulk copy per tile).
+// Destinations or shards in host memory: each thread reads its 16-byte
+// group once and stores it to every destination (each value crosses the
+// host link once).
 __global__ void __launch_bounds__(kThreads) k_gather_direct(const __grid_constant__ GatherArgs a)
 {
     const int64_t ngroups = (a.len + kG - 1) / kG;
@@ -58,10 +58,7 @@ __global__ void __launch_bounds__(kThreads) k_gather_direct(const __grid_constan
     }
 }
 
-// Destinations from which k_gather is used.
-constexpr int kChunkMinDst = 8;
-
-// Eight or more destinations.  The layer is cut into chunks of kChunk units
+// The layer is cut into chunks of kChunk units
 // (2 MB) and each chunk into segments of kSeg units (16 KB); a block copies
 // one segment of one chunk to one destination -- blockIdx.x the segment,
 // blockIdx.y the destination, blockIdx.z the chunk -- with 16-byte loads (L2)
@@ -77,6 +74,10 @@ constexpr int kChunkMinDst = 8;
 // chunks of 2-4 MB measured the same, 8 MB 2 % less, 16 MB 12 % less.  Eight
 // blocks per SM (32 registers): with the owner found by a 64-bit division
 // per group, or at 4 blocks per SM, the same order reached only 6.3-6.5.
+// Fewer destinations too, against k_gather_direct (201 M / 2^24-unit
+// layers, of the copy bandwidth): 1 destination 0.97 / 0.62 against 0.82 /
+// 0.56, 2: 0.99 / 0.67 against 0.92 / 0.72, 4: 1.00 / 0.73 against 0.84 /
+// 0.67, 7: 1.00 / 0.73 against 0.86 / 0.72.
 constexpr int kSegThreads = 256;
 constexpr int kPer = 4;                                            // groups per thread
 constexpr int64_t kSeg = (int64_t)kSegThreads * kPer * kG;         // 8192 units
@@ -178,7 +179,7 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s)
     // the first): only for sources, as well as destinations, in this GPU's
     // memory; a source in host memory would cross the host link n_dst times
     const int o_first = owner_of_host(a.start, a.shard), o_last = owner_of_host(a.start + a.len - 1, a.shard);
-    if (a.n_dst < kChunkMinDst || !device_resident(const_cast<void* const*>(a.dst), a.n_dst, s) ||
+    if (!device_resident(const_cast<void* const*>(a.dst), a.n_dst, s) ||
         !device_resident(const_cast<void* const*>(a.shards) + o_first, o_last - o_first + 1, s)) {
         const int grid = grid_for((const void*)k_gather_direct, (a.len + kG - 1) / kG);
         k_gather_direct<<<grid, kThreads, 0, s>>>(a);
