@@ -68,6 +68,10 @@ def test_gpu_arm_line():
     assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
     assert r["traffic"] is None or (r["traffic"] > 0 and r["traffic_source"]["summary"])
     assert 0.5 < r["share_of_step_bytes"] < 0.7
+    # the gather mostly writes: beside the copy bandwidth, the write-only
+    # ceiling measured on the same GPU, which the gather cannot pass by much
+    w = r["write_only_ceiling"]
+    assert w["gbs"] > 0 and w["frac"] == pytest.approx(r["achieved"] / w["gbs"]) and w["frac"] < 1.1
     assert d["step_roofline"]["bytes_per_param"] == 414
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
