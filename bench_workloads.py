@@ -393,7 +393,7 @@ def leg_cfg3(args):
                            cuda_stream=s.cuda_stream)
         adam = zg.zero_adam_t(max_grad_norm=0.0, **ADAM)
         state = zg.zero_state_t(t=0, loss_scale=1024.0, min_loss_scale=1.0, dynamic=1, growth_interval=0)
-        walls, skipped, scales, skipped_bytes = [], 0, [], []
+        walls, skipped, scales, skipped_bytes, moved = [], 0, [], [], []
         for k in range(steps):
             step_no = k + 1
             S = state.loss_scale
@@ -411,10 +411,12 @@ def leg_cfg3(args):
             walls.append(w0.elapsed_time(w1))
             skipped += res.skipped
             scales.append(res.new_loss_scale)
+            moved.append(res.hbm_bytes)
             if res.skipped:
                 skipped_bytes.append(res.hbm_bytes)
         ms = sum(walls) / len(walls)
         runs[run] = {"ms_per_step": ms, "value": n / (ms * 1e-3) / 1e9, "steps": steps, "skipped": skipped,
+                     "hbm_gbs": sum(moved) / (sum(walls) * 1e-3) / 1e9,
                      "loss_scales": scales, "t": state.t,
                      "hbm_bytes_per_clean_step": plan.hbm_bytes_fused,
                      "hbm_bytes_per_skipped_step": (sum(skipped_bytes) / len(skipped_bytes)) if skipped_bytes
@@ -427,6 +429,11 @@ def leg_cfg3(args):
                 {"n_params": n, "n_ranks": N, "stage": 2, "bucket_elems": B, "injection": "value: odd steps only; "
                  "runs.literal: every step (12 infs over 1.24e10 gradient elements)"})
     out["runs"] = runs
+    peak, kind = bench.measured_peak_hbm()
+    out["roofline"] = {"bound": "hbm", "kernel": "k_fused<stage 2, fp16, adam> + k_restore (skipped steps)",
+                       "achieved": main["hbm_gbs"], "peak": peak, "peak_kind": kind, "unit": "GB/s",
+                       "frac": main["hbm_gbs"] / peak, "traffic": None,
+                       "bytes": "the library's count of what each step moved (hbm_bytes), over the steps' time"}
     out["note"] = ("bucket kernels that start after the step's flag is raised do nothing; a skipped step then "
                    "restores the parameters of the window the other kernels wrote (cast of the unchanged master "
                    "weights to every rank); hbm_bytes_per_skipped_step is the library's count of what moved; step "
