@@ -540,22 +540,33 @@ __device__ __forceinline__ void sumsq_group_bf16(const H16<8>& h, int win_lo, U1
         // multiply-add per value, no group maximum, one add at a constant
         // shift.  Subnormals (e = 0, first >= 1) and inf and NaN (e = 255,
         // first <= 222) always lie outside it.
-        const int fbase = first + 9;
+        // Two values per 32-bit word at once: with m = |x|'s 15 bits, bit 15
+        // of m + (0x8000 - lim) is set iff m >= lim (no carry between the
+        // halves, m < 0x8000), which tests both ends of the window and
+        // m != 0; M = f | 0x80 for both halves in one operation (in the
+        // window the values are normal), and the shift is PTX shl, whose
+        // shift counts of 32 or more give 0, so a zero (e = 0, shift count
+        // 0 - fbase, wrapped) adds nothing.  tests/test_bf16_window_bits.py checks
+        // this against the value-by-value form for every 16-bit pattern.
+        const uint32_t fbase = (uint32_t)(first + 9);                       // 10..231
+        const uint32_t k_hi = (0x8000u - ((fbase + 23u) << 7)) * 0x00010001u;
+        const uint32_t k_lo = (0x8000u - (fbase << 7)) * 0x00010001u;
         unsigned long long b = 0ull;
         uint32_t outside = 0;
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            const uint32_t w = h.w[j >> 1];
-            const uint32_t e = (j & 1) ? __umulhi(w & 0x7f800000u, 1u << 9) : __umulhi(w & 0x00007f80u, 1u << 25);
-            const uint32_t f = (j & 1) ? __umulhi(w & 0x007f0000u, 1u << 16) : (w & 0x0000007fu);
-            const uint32_t hid = min(e, 1u);
-            const uint32_t M = f + hid * 0x80u;
-            const uint32_t d = e + 1u - hid - (uint32_t)fbase;   // e - fbase for e >= 1
-            outside |= d > 22u ? M : 0u;                          // a nonzero value outside the window
-            const uint32_t X = M << (d & 31u);
-            asm("mad.wide.u32 %0, %1, %1, %0;" : "+l"(b) : "r"(X));
+        for (int p = 0; p < 4; p++) {
+            const uint32_t w = h.w[p];
+            const uint32_t mag = w & 0x7fff7fffu;
+            outside |= (mag + k_hi) | ((mag + 0x7fff7fffu) & ~(mag + k_lo));
+            const uint32_t m2 = (w & 0x007f007fu) | 0x00800080u;
+            const uint32_t e2 = (w >> 7) & 0x00ff00ffu;
+            uint32_t x0, x1;
+            asm("shl.b32 %0, %1, %2;" : "=r"(x0) : "r"(m2 & 0xffffu), "r"((e2 & 0xffu) - fbase));
+            asm("shl.b32 %0, %1, %2;" : "=r"(x1) : "r"(m2 >> 16), "r"((e2 >> 16) - fbase));
+            asm("mad.wide.u32 %0, %1, %1, %0;" : "+l"(b) : "r"(x0));
+            asm("mad.wide.u32 %0, %1, %1, %0;" : "+l"(b) : "r"(x1));
         }
-        if (!outside) {
+        if (!(outside & 0x80008000u)) {
             u128_add(acc, b << 18, b >> 46);
             return;
         }
