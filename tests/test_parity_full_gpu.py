@@ -11,6 +11,9 @@ recomputes from the host generator (plus properties that hold at any size).
     sets, device-state protocol, two gathers per layer).
   * 2^31 flat params, N_d = 32, bf16, clipping path with c < 1, staged
     gradients; the exact norm over all 2^31 reduced values.
+  * 2^28 flat params, N_d = 2, fp16 and bf16, clipping: pass 1 on the
+    staged kernel (packed sums, the bfloat16 window tested two values per
+    word); the exact norm over all 2^28 reduced values.
 """
 import numpy as np
 import pytest
@@ -255,4 +258,53 @@ def test_sweep_2p31_n32_bf16_clip_path():
         assert np.array_equal(as_u32(_at(gm, idx)), as_u32(m))
         assert np.array_equal(as_u32(_at(gv, idx)), as_u32(v))
         for r in (0, 13, 31):
+            assert np.array_equal(as_u16(_at(bufs.params16[r], idx)), p16)
+
+
+@pytest.mark.parametrize("dtype", [oracle.FP16, oracle.BF16])
+def test_sweep_2p28_n2_clip_staged_pass1(dtype):
+    """Two ranks, 2^28 parameters resident in HBM, clipping at 1.0 with the
+    gradient spread set so that c < 1: the exact norm over all 2^28 reduced
+    values (the oracle's exponent bins of the GPU's reduced gradient), the
+    clip coefficient from it, and sampled elements of the reduced gradient,
+    state and both ranks' parameters against the oracle, two steps."""
+    n, N, B = 1 << 28, 2, 1 << 24
+    s = torch.cuda.current_stream()
+    dt = zg.ZERO_BF16 if dtype == oracle.BF16 else zg.ZERO_FP16
+    cfg = zg.Config(n, N, 2, B, 0, None, dt)
+    plan = zg.zero_plan(cfg)
+    bufs = zg.DeviceBuffers(cfg, plan, device="cuda", shadow=False)
+    synth.dev_normal32(bufs.w[0].data_ptr(), n, 0.02, seed=0, stream=synth.STREAM_WEIGHT, cuda_stream=s.cuda_stream)
+    max_norm, sigma = 1.0, 2e-4        # norm of the mean gradient about sqrt(2^28 / 2) * 2e-4 = 2.3
+    adam = zg.zero_adam_t(max_grad_norm=max_norm, **ADAM)
+    state = zg.zero_state_t(t=0, loss_scale=1.0, min_loss_scale=1.0)
+    idx = _samples(n, [0, n - 1, B - 1, B, n // 2])
+    w = synth.host_normal32_at(idx, 0.02, seed=0, stream=synth.STREAM_WEIGHT)
+    m, v = np.zeros_like(w), np.zeros_like(w)
+    inv = oracle.inv_scale(1.0, N)
+    for step in (1, 2):
+        for r in range(N):
+            synth.dev_normal16(bufs.grads[r].data_ptr(), n, dt, sigma, seed=0, stream=synth.STREAM_GRAD, step=step,
+                               rank=r, cuda_stream=s.cuda_stream)
+        res = zg.zero_step_stage2(cfg, plan, bufs, adam, state, s)
+        torch.cuda.synchronize()
+        assert res.overflow == 0 and res.path == 1 and res.t == step
+        h_all = bufs.reduced[:n].cpu().numpy().view(np.uint16)
+        norm = oracle.grad_norm(float(oracle.sumsq_fraction(h_all, dtype)), inv)
+        del h_all
+        assert res.grad_norm == norm, (res.grad_norm, norm)
+        c = oracle.clip_coef(norm, max_norm)
+        assert 0.0 < c < 1.0 and res.clip_coef == c
+        grads = [synth.host_normal16_at(idx, dtype, sigma, seed=0, stream=synth.STREAM_GRAD, step=step, rank=r)
+                 for r in range(N)]
+        h, flag = oracle.reduce(grads, dtype)
+        assert flag == 0
+        assert np.array_equal(as_u16(_at(bufs.reduced, idx)), h)
+        hyper = oracle.make_hyper(inv=inv, clip=c, t=step, **ADAM)
+        p16 = oracle.adam(h, dtype, hyper, w, m, v)
+        gw, gm, gv = bufs.state()
+        assert np.array_equal(as_u32(_at(gw, idx)), as_u32(w))
+        assert np.array_equal(as_u32(_at(gm, idx)), as_u32(m))
+        assert np.array_equal(as_u32(_at(gv, idx)), as_u32(v))
+        for r in range(N):
             assert np.array_equal(as_u16(_at(bufs.params16[r], idx)), p16)
